@@ -1,0 +1,232 @@
+/*
+ * dv.h — C ABI of libdv, the KV-cache buffered copy for one GB300 GPU.
+ *
+ * The operations follow "DejaVu: KV-Cache Streaming for Fast, Fault-Tolerant
+ * Generative LLM Serving" (Strati et al., ICML 2024):
+ *
+ *   dv_kv_pack       Table 1 "gather" and §3 "Buffered copies" (Fig 7a): the
+ *                    many small, non-contiguous K/V slices of a cache that is
+ *                    preallocated at the maximum sequence length (Fig 6) are
+ *                    gathered into one contiguous buffer in GPU memory.
+ *   dv_kv_unpack     Table 1 "scatter" / stream_in: the inverse, a contiguous
+ *                    buffer split back into the same slices.
+ *   dv_swap_out/in   §3 "Microbatch swapping" (Fig 9): the used part of a
+ *                    microbatch's cache moved to pinned host memory and back;
+ *                    Table 1 flush/fetch are the contiguous copies inside.
+ *   dv_stream_layer  §3 "Layer-by-layer prompt cache streaming" (Fig 7b): the
+ *                    pack of layer l+1 overlaps the device-to-host copy of
+ *                    layer l, on two streams ordered by events.
+ *   dv_replica_*     §3 "Fault detection and recovery" (Fig 10) on one GPU:
+ *                    per-step decode deltas (§3 "Token computation and
+ *                    streaming parallelization", Fig 7c) appended to a
+ *                    host-side replica, and the restore of a cache from it.
+ *
+ * Cache layout (the FasterTransformer-style layout the pages build on).  Per
+ * layer, with x = 16 / elem_bytes elements per 16-byte chunk:
+ *   K: [batch][num_heads][head_dim / x][max_seq][x]   (x-interleaved keys)
+ *   V: [batch][num_heads][max_seq][head_dim]
+ * Layer l starts at element l * layer_stride_elems of k_base (and v_base).
+ *
+ * Staging (packed) order, the same for every call:
+ *   [layer l0..l1)[K, then V][sequence b][head h][token t in [s_b, e_b)][d]
+ * with d in logical order (0..head_dim-1).  The size is
+ *   2 * (l1 - l0) * num_heads * head_dim * elem_bytes * sum_b (e_b - s_b)
+ * bytes; for a full cache (all layers, all ranges [0, max_seq)) this is the
+ * capacity formula 2*B*S*H*D*P*N of the KV-cache capacity page.  Each
+ * layer's slab is contiguous, so packing layers one at a time lays down the
+ * same bytes as one pack of all of them.
+ *
+ * Conventions shared by every call:
+ *  - Ranges: seq_start / seq_end are HOST arrays of `batch` int32 values,
+ *    read during the call only; 0 <= s_b <= e_b <= max_seq; an empty range is
+ *    legal (a finished sequence).  Layer range: 0 <= l0 <= l1 <= num_layers.
+ *  - Ownership: the caller allocates every buffer.  The library allocates no
+ *    device or host memory except the small streamer and replica handles.
+ *  - Memory kinds: k_base / v_base and `staging` are device memory of the
+ *    current device.  A pack destination or unpack source may be device
+ *    memory or pinned (page-locked, mapped) host memory; for host memory the
+ *    kernel reads or writes it directly over the host link (zero copy).
+ *  - Alignment: k_base, v_base, buffers and layer_stride_elems * elem_bytes
+ *    must be multiples of 16 bytes (DV_ERR_MISALIGNED); head_dim must be a
+ *    multiple of x (DV_ERR_UNSUPPORTED).  batch <= DV_MAX_BATCH.
+ *  - Asynchrony: every call validates all arguments first and enqueues
+ *    nothing when it fails.  On success the work is enqueued on the given
+ *    stream(s) and the call returns; buffers must stay alive and unmodified
+ *    until the stream reaches that point.  A launch failure returns
+ *    DV_ERR_CUDA.  No call blocks except dv_streamer_wait and the
+ *    synchronous helpers marked as such.
+ *  - Errors: every call returns a dv_status; dv_last_error() gives a
+ *    message for the calling thread's most recent failure.
+ *  - Threads: calls on distinct handles may run concurrently; a streamer or
+ *    replica handle must not be used by two threads at once.
+ */
+#ifndef DV_H_
+#define DV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DV_ABI_VERSION 1
+#define DV_MAX_BATCH 1024
+
+/* A CUDA stream (cudaStream_t / CUstream); NULL is the legacy default
+ * stream. */
+typedef struct CUstream_st* dv_stream;
+
+typedef enum {
+  DV_OK = 0,
+  DV_ERR_INVALID_ARG = 1,      /* null pointer, bad geometry, wrong memory kind */
+  DV_ERR_RANGE = 2,            /* a layer or token range outside the cache */
+  DV_ERR_BUFFER_TOO_SMALL = 3, /* destination / source / staging too small */
+  DV_ERR_MISALIGNED = 4,       /* a pointer or stride not 16-byte aligned */
+  DV_ERR_CUDA = 5,             /* a CUDA runtime call or launch failed */
+  DV_ERR_TIMEOUT = 6,          /* reserved for bounded waits */
+  DV_ERR_UNSUPPORTED = 7       /* a geometry this build does not handle */
+} dv_status;
+
+/* Cache geometry and base pointers; owned by the caller. */
+typedef struct {
+  int32_t num_layers;         /* resident layers N */
+  int32_t batch;              /* sequences B */
+  int32_t num_heads;          /* H */
+  int32_t head_dim;           /* D */
+  int32_t max_seq;            /* S, token slots per sequence */
+  int32_t elem_bytes;         /* P: 1, 2 (fp16 / bf16) or 4 */
+  int64_t layer_stride_elems; /* 0 = batch*num_heads*head_dim*max_seq */
+  void* k_base;               /* device pointer, K of layer 0 */
+  void* v_base;               /* device pointer, V of layer 0 */
+} dv_cache;
+
+/* Kernel choice for dv_kv_pack_variant / dv_kv_unpack_variant (testing and
+ * tuning; the plain calls use DV_VARIANT_AUTO). */
+typedef enum {
+  DV_VARIANT_AUTO = 0, /* tile kernel for long ranges, flat kernel otherwise */
+  DV_VARIANT_FLAT = 1, /* one 16-byte chunk per thread, staging order */
+  DV_VARIANT_TILE = 2  /* token tiles; K transposed through shared memory */
+} dv_variant;
+
+int32_t dv_abi_version(void);
+const char* dv_status_string(dv_status status);
+/* Message for the calling thread's most recent failed call ("" if none). */
+const char* dv_last_error(void);
+
+/* Bytes from `ptr` to the end of the CUDA allocation that holds it, as the
+ * driver reports it; every call checks the buffers it is given against this
+ * extent when the driver knows it.  DV_ERR_UNSUPPORTED when the driver cannot
+ * tell (then calls rely on the sizes the caller passes). */
+dv_status dv_allocation_extent(const void* ptr, size_t* bytes_after);
+
+/* Bytes the staging buffer of (l0, l1, ranges) takes (see the size formula
+ * above).  Host only; enqueues nothing.  Pointers in `cache` are not read. */
+dv_status dv_staging_bytes(const dv_cache* cache, int32_t l0, int32_t l1,
+                           const int32_t* seq_start, const int32_t* seq_end, size_t* bytes);
+
+/* Gather (Table 1; Fig 7a).  Writes the staging bytes of (l0, l1, ranges)
+ * to `dst` (device memory, or pinned host memory written directly).
+ * DV_ERR_BUFFER_TOO_SMALL if dst_bytes is less than dv_staging_bytes.
+ * dst may be NULL when that size is 0. */
+dv_status dv_kv_pack(const dv_cache* cache, int32_t l0, int32_t l1, const int32_t* seq_start,
+                     const int32_t* seq_end, void* dst, size_t dst_bytes, dv_stream stream);
+
+/* Scatter (Table 1).  Reads staging bytes from `src` (device memory or
+ * pinned host memory) and writes exactly the selected K/V slices; every other
+ * byte of the cache is left as it was. */
+dv_status dv_kv_unpack(const dv_cache* cache, int32_t l0, int32_t l1, const int32_t* seq_start,
+                       const int32_t* seq_end, const void* src, size_t src_bytes,
+                       dv_stream stream);
+
+dv_status dv_kv_pack_variant(const dv_cache* cache, int32_t l0, int32_t l1,
+                             const int32_t* seq_start, const int32_t* seq_end, void* dst,
+                             size_t dst_bytes, dv_stream stream, int32_t variant);
+dv_status dv_kv_unpack_variant(const dv_cache* cache, int32_t l0, int32_t l1,
+                               const int32_t* seq_start, const int32_t* seq_end,
+                               const void* src, size_t src_bytes, dv_stream stream,
+                               int32_t variant);
+
+/* Swap-out (§3 microbatch swapping, Fig 9; Table 1 flush).  Leaves the
+ * staging bytes of (l0, l1, ranges) in `host_dst` (pinned host memory,
+ * host_bytes at least dv_staging_bytes).
+ *  - staging == NULL: fused path, the pack kernel stores straight into
+ *    host_dst over the host link (one launch, no device buffer).
+ *  - staging != NULL: staged path, groups of whole layers are packed into
+ *    `staging` (device, staging_bytes >= one layer's slab) and copied to
+ *    the host with cudaMemcpyAsync, all in order on `stream`. */
+dv_status dv_swap_out(const dv_cache* cache, int32_t l0, int32_t l1, const int32_t* seq_start,
+                      const int32_t* seq_end, void* host_dst, size_t host_bytes, void* staging,
+                      size_t staging_bytes, dv_stream stream);
+
+/* Swap-in (§3 microbatch swapping; Table 1 fetch + scatter).  The inverse of
+ * dv_swap_out: host_src holds staging bytes; staging == NULL unpacks straight
+ * from host memory, otherwise layer groups go host -> staging -> cache. */
+dv_status dv_swap_in(const dv_cache* cache, int32_t l0, int32_t l1, const int32_t* seq_start,
+                     const int32_t* seq_end, const void* host_src, size_t host_bytes,
+                     void* staging, size_t staging_bytes, dv_stream stream);
+
+/* ---- layer-by-layer streaming (§3, Fig 7b) ------------------------------ */
+
+/* Owns two events per slot; borrows the slots and streams. */
+typedef struct dv_streamer dv_streamer;
+
+/* slot0 / slot1: device buffers of slot_bytes each (16-byte aligned), used
+ * alternately.  Packs run on pack_stream, copies on copy_stream (two
+ * different streams overlap the pack of layer l+1 with the copy of layer l;
+ * one stream serialises them). */
+dv_status dv_streamer_create(dv_streamer** out, void* slot0, void* slot1, size_t slot_bytes,
+                             dv_stream pack_stream, dv_stream copy_stream);
+
+/* Packs layer `layer` of the ranges into the next slot on the pack stream
+ * (after the slot's previous copy has finished) and copies it, on the copy
+ * stream, to host_dst + (layer - l0) * slab, where slab is this layer's
+ * staging size: host_dst is the base of the buffer of the whole layer range
+ * [l0, ...) streamed with the same ranges, so the layers land in the order
+ * of one dv_kv_pack over that range.  host_dst_bytes is that buffer's size. */
+dv_status dv_stream_layer(dv_streamer* streamer, const dv_cache* cache, int32_t layer,
+                          const int32_t* seq_start, const int32_t* seq_end, void* host_dst,
+                          size_t host_dst_bytes, int32_t l0);
+
+/* Blocks the calling thread until every copy issued so far has finished. */
+dv_status dv_streamer_wait(dv_streamer* streamer);
+
+/* Releases the handle (its events are released once pending work ends). */
+void dv_streamer_destroy(dv_streamer* streamer);
+
+/* ---- host-side replica of a cache (§3 state replication, Fig 10) -------- */
+
+/* A log of records in a caller-owned pinned host arena.  Each record holds
+ * the staging bytes of (l0, l1, ranges) and is tagged with a step number;
+ * the first record is normally a snapshot of the used prefixes and the rest
+ * one-token decode deltas. */
+typedef struct dv_replica dv_replica;
+
+dv_status dv_replica_create(dv_replica** out, void* host_arena, size_t arena_bytes,
+                            int32_t batch);
+
+/* Appends the staging bytes of (l0, l1, ranges) of `cache` as a record
+ * tagged `step` (steps must not decrease), by dv_swap_out (fused when
+ * staging is NULL).  DV_ERR_BUFFER_TOO_SMALL when the arena is full. */
+dv_status dv_replica_append(dv_replica* replica, const dv_cache* cache, int32_t l0, int32_t l1,
+                            const int32_t* seq_start, const int32_t* seq_end, int64_t step,
+                            void* staging, size_t staging_bytes, dv_stream stream);
+
+/* Unpacks every record with step < upto_step (all records if upto_step < 0),
+ * in append order, into `cache` by dv_swap_in.  The cache must have the
+ * geometry of the appended records. */
+dv_status dv_replica_restore(const dv_replica* replica, const dv_cache* cache, int64_t upto_step,
+                             void* staging, size_t staging_bytes, dv_stream stream);
+
+/* Drops every record with step >= step (the acknowledged prefix is kept). */
+dv_status dv_replica_truncate(dv_replica* replica, int64_t step);
+
+dv_status dv_replica_info(const dv_replica* replica, int64_t* num_records, size_t* bytes_used);
+
+void dv_replica_destroy(dv_replica* replica);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* DV_H_ */

@@ -1,0 +1,69 @@
+"""Builds libdv.so (the copy library) in-tree with nvcc for sm_103a.
+
+    python kv_cache_streaming_gb300/build.py
+
+(run it as a script, or load it by path: importing the package itself loads
+the library this file builds).
+
+Translation units compile in parallel; the result is
+``kv_cache_streaming_gb300/libdv.so``.  The CUDA runtime is linked
+statically; the driver is reached through the runtime, so the library also
+loads (for symbol checks) on a machine without a GPU driver.
+"""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+from pathlib import Path
+
+PKG = Path(__file__).resolve().parent
+ROOT = PKG.parent
+CSRC = PKG / "csrc"
+OBJ = PKG / "_build"
+LIB = PKG / "libdv.so"
+SOURCES = ["dv_api.cu", "dv_kernels.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and Path(cand).exists():
+            return cand
+    raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libdv")
+
+
+def _compile(src: str) -> Path:
+    out = OBJ / (Path(src).stem + ".o")
+    cmd = [nvcc(), *ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
+           "-Xcompiler", "-Wall", "-I", str(ROOT / "include"), "-c", str(CSRC / src), "-o", str(out)]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def _stale(target: Path, deps) -> bool:
+    if not target.exists():
+        return True
+    t = target.stat().st_mtime
+    return any(Path(d).stat().st_mtime > t for d in deps)
+
+
+def build(force: bool = False) -> Path:
+    deps = [CSRC / s for s in SOURCES] + [CSRC / "dv_plan.h", ROOT / "include" / "dv.h",
+                                          Path(__file__)]
+    if not force and not _stale(LIB, deps):
+        return LIB
+    OBJ.mkdir(exist_ok=True)
+    with ThreadPoolExecutor(len(SOURCES)) as ex:
+        objs = list(ex.map(_compile, SOURCES))
+    tmp = LIB.with_suffix(f".{os.getpid()}.tmp")
+    subprocess.run([nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", str(tmp),
+                    *map(str, objs)], check=True)
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv))

@@ -1,0 +1,56 @@
+// Internal to libdv: a validated copy plan and the kernel launchers.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace dv {
+
+constexpr int kMaxBatch = 1024;   // == DV_MAX_BATCH
+constexpr int kSmallBatch = 32;   // kernels with 32-entry range tables
+constexpr int kThreads = 256;     // threads per CTA of every copy kernel
+
+// Everything a pack / unpack launch needs, validated on the host.  Sizes in
+// 16-byte chunks: one chunk is x = 16 / P consecutive elements of a K row or
+// of a V row, the unit every kernel moves.
+struct Plan {
+  int32_t L, B, H, D, S, P;
+  int32_t C;                 // chunks per token of one head: D * P / 16
+  int64_t layer_chunks;      // layer stride of K and V
+  int32_t l0, l1;
+  int32_t seq_start[kMaxBatch];
+  int32_t seq_len[kMaxBatch];
+  int32_t tok_pre[kMaxBatch + 1];  // tok_pre[b] = sum of seq_len[0..b)
+  int64_t tokens;            // T = tok_pre[B]
+  int32_t max_len;
+  int32_t active;            // sequences with a non-empty range
+  int64_t lkv_chunks;        // chunks of one (layer, K|V) slab: H * T * C
+  int64_t bytes;             // staging bytes: 2 * (l1 - l0) * lkv_chunks * 16
+  void* k;                   // device-visible K / V bases
+  void* v;
+};
+
+// Re-targets `p` to the layer sub-range [la, lb) (inside [p.l0, p.l1)).
+inline void restrict_layers(Plan& p, int32_t la, int32_t lb) {
+  p.l0 = la;
+  p.l1 = lb;
+  p.bytes = 2 * (int64_t)(lb - la) * p.lkv_chunks * 16;
+}
+
+// Bytes of one layer's slab of the staging buffer.
+inline int64_t layer_slab_bytes(const Plan& p) { return 2 * p.lkv_chunks * 16; }
+
+enum Variant { kAuto = 0, kFlat = 1, kTile = 2 };
+
+// Kernel choice of kAuto (the tile kernel pays off once ranges are long).
+bool auto_uses_tile(const Plan& p);
+// Whether the tile kernel handles this geometry (C <= 64).
+bool tile_supported(const Plan& p);
+
+// `stg` is the device-visible address of the staging bytes (device memory or
+// mapped pinned host memory).  Both return cudaSuccess without launching
+// when the plan moves nothing.
+cudaError_t launch_pack(const Plan& p, void* stg, cudaStream_t stream, int variant);
+cudaError_t launch_unpack(const Plan& p, const void* stg, cudaStream_t stream, int variant);
+
+}  // namespace dv

@@ -1,0 +1,313 @@
+"""ctypes binding of libdv (``include/dv.h``): argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does no
+copy work of its own.  Buffers may be given as torch tensors (device or
+pinned host; their ``data_ptr()`` and byte size are used) or as
+``(address, nbytes)`` pairs.  Streams may be ``torch.cuda.Stream`` objects,
+raw ``cudaStream_t`` integers, or ``None`` for torch's current stream.
+A status other than DV_OK raises ``DvError`` with the library's message.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import numpy as np
+
+PKG = Path(__file__).resolve().parent
+library_path = PKG / "libdv.so"
+
+DV_MAX_BATCH = 1024
+(DV_OK, DV_ERR_INVALID_ARG, DV_ERR_RANGE, DV_ERR_BUFFER_TOO_SMALL, DV_ERR_MISALIGNED,
+ DV_ERR_CUDA, DV_ERR_TIMEOUT, DV_ERR_UNSUPPORTED) = range(8)
+DV_VARIANT_AUTO, DV_VARIANT_FLAT, DV_VARIANT_TILE = 0, 1, 2
+
+if not library_path.exists():
+    raise ImportError(f"{library_path} is missing: build it with "
+                      "`python -m kv_cache_streaming_gb300.build` (needs nvcc)")
+lib = ctypes.CDLL(str(library_path))
+
+
+class dv_cache(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("batch", ctypes.c_int32),
+                ("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("max_seq", ctypes.c_int32), ("elem_bytes", ctypes.c_int32),
+                ("layer_stride_elems", ctypes.c_int64),
+                ("k_base", ctypes.c_void_p), ("v_base", ctypes.c_void_p)]
+
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_I32P = ctypes.POINTER(ctypes.c_int32)
+_CP = ctypes.POINTER(dv_cache)
+_RANGE = [_CP, _I32, _I32, _I32P, _I32P]
+
+
+def _sig(name, args, res=ctypes.c_int):
+    fn = getattr(lib, name)
+    fn.argtypes = args
+    fn.restype = res
+    return fn
+
+
+_abi = _sig("dv_abi_version", [], _I32)
+_status_string = _sig("dv_status_string", [ctypes.c_int], ctypes.c_char_p)
+_last_error = _sig("dv_last_error", [], ctypes.c_char_p)
+_staging_bytes = _sig("dv_staging_bytes", _RANGE + [ctypes.POINTER(_SZ)])
+_extent = _sig("dv_allocation_extent", [_P, ctypes.POINTER(_SZ)])
+_pack = _sig("dv_kv_pack_variant", _RANGE + [_P, _SZ, _P, _I32])
+_unpack = _sig("dv_kv_unpack_variant", _RANGE + [_P, _SZ, _P, _I32])
+_swap_out = _sig("dv_swap_out", _RANGE + [_P, _SZ, _P, _SZ, _P])
+_swap_in = _sig("dv_swap_in", _RANGE + [_P, _SZ, _P, _SZ, _P])
+_streamer_create = _sig("dv_streamer_create", [ctypes.POINTER(_P), _P, _P, _SZ, _P, _P])
+_stream_layer = _sig("dv_stream_layer", [_P, _CP, _I32, _I32P, _I32P, _P, _SZ, _I32])
+_streamer_wait = _sig("dv_streamer_wait", [_P])
+_streamer_destroy = _sig("dv_streamer_destroy", [_P], None)
+_replica_create = _sig("dv_replica_create", [ctypes.POINTER(_P), _P, _SZ, _I32])
+_replica_append = _sig("dv_replica_append", [_P] + _RANGE + [_I64, _P, _SZ, _P])
+_replica_restore = _sig("dv_replica_restore", [_P, _CP, _I64, _P, _SZ, _P])
+_replica_truncate = _sig("dv_replica_truncate", [_P, _I64])
+_replica_info = _sig("dv_replica_info", [_P, ctypes.POINTER(_I64), ctypes.POINTER(_SZ)])
+_replica_destroy = _sig("dv_replica_destroy", [_P], None)
+
+
+class DvError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_status_string(status).decode()}: {message}")
+        self.status = status
+
+
+def _check(status: int) -> None:
+    if status != DV_OK:
+        raise DvError(status, _last_error().decode(errors="replace"))
+
+
+def dv_abi_version() -> int:
+    return _abi()
+
+
+# ---- marshalling helpers -------------------------------------------------------
+
+def _buf(x, nbytes=None):
+    """(address, nbytes) of a tensor, a pair, or None."""
+    if x is None:
+        return None, 0
+    if isinstance(x, tuple):
+        return int(x[0]), int(x[1] if nbytes is None else nbytes)
+    if hasattr(x, "data_ptr"):
+        n = x.numel() * x.element_size()
+        return x.data_ptr(), int(n if nbytes is None else nbytes)
+    raise TypeError(f"cannot use {type(x).__name__} as a buffer")
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _ranges(seq_start, seq_end):
+    s = np.ascontiguousarray(seq_start, dtype=np.int32)
+    e = np.ascontiguousarray(seq_end, dtype=np.int32)
+    return s, e, s.ctypes.data_as(_I32P), e.ctypes.data_as(_I32P)
+
+
+class Cache:
+    """Geometry plus K/V base addresses of one cache (layout in ``dv.h``).
+
+    ``k`` and ``v`` are device tensors (any dtype; only their addresses are
+    used) or raw addresses.  ``layer_stride_elems`` 0 means layers are packed
+    densely."""
+
+    def __init__(self, num_layers, batch, num_heads, head_dim, max_seq, elem_bytes, k, v,
+                 layer_stride_elems=0):
+        self.k, self.v = k, v  # keep the tensors alive
+        kp = k.data_ptr() if hasattr(k, "data_ptr") else int(k)
+        vp = v.data_ptr() if hasattr(v, "data_ptr") else int(v)
+        self.c = dv_cache(num_layers, batch, num_heads, head_dim, max_seq, elem_bytes,
+                          layer_stride_elems, kp, vp)
+        self.ref = ctypes.byref(self.c)
+
+    @classmethod
+    def from_geometry(cls, g, k, v):
+        return cls(g.num_layers, g.batch, g.num_heads, g.head_dim, g.max_seq, g.elem_bytes,
+                   k, v, g.layer_stride_elems)
+
+    @property
+    def num_layers(self):
+        return self.c.num_layers
+
+    @property
+    def batch(self):
+        return self.c.batch
+
+
+# ---- entry points --------------------------------------------------------------
+
+def dv_allocation_extent(ptr):
+    """Bytes from ``ptr`` (tensor or address) to the end of its CUDA
+    allocation, or None when the driver cannot tell."""
+    addr = ptr.data_ptr() if hasattr(ptr, "data_ptr") else int(ptr)
+    out = _SZ(0)
+    st = _extent(addr, ctypes.byref(out))
+    if st == DV_ERR_UNSUPPORTED:
+        return None
+    _check(st)
+    return out.value
+
+
+def dv_staging_bytes(cache: Cache, l0, l1, seq_start, seq_end) -> int:
+    s, e, sp, ep = _ranges(seq_start, seq_end)
+    out = _SZ(0)
+    _check(_staging_bytes(cache.ref, l0, l1, sp, ep, ctypes.byref(out)))
+    return out.value
+
+
+def dv_kv_pack(cache: Cache, l0, l1, seq_start, seq_end, dst, stream=None,
+               variant=DV_VARIANT_AUTO, dst_bytes=None) -> None:
+    s, e, sp, ep = _ranges(seq_start, seq_end)
+    d, n = _buf(dst, dst_bytes)
+    _check(_pack(cache.ref, l0, l1, sp, ep, d, n, _stream(stream), variant))
+
+
+def dv_kv_unpack(cache: Cache, l0, l1, seq_start, seq_end, src, stream=None,
+                 variant=DV_VARIANT_AUTO, src_bytes=None) -> None:
+    s, e, sp, ep = _ranges(seq_start, seq_end)
+    d, n = _buf(src, src_bytes)
+    _check(_unpack(cache.ref, l0, l1, sp, ep, d, n, _stream(stream), variant))
+
+
+def dv_swap_out(cache: Cache, l0, l1, seq_start, seq_end, host_dst, staging=None,
+                stream=None) -> None:
+    s, e, sp, ep = _ranges(seq_start, seq_end)
+    h, hn = _buf(host_dst)
+    st, sn = _buf(staging)
+    _check(_swap_out(cache.ref, l0, l1, sp, ep, h, hn, st, sn, _stream(stream)))
+
+
+def dv_swap_in(cache: Cache, l0, l1, seq_start, seq_end, host_src, staging=None,
+               stream=None) -> None:
+    s, e, sp, ep = _ranges(seq_start, seq_end)
+    h, hn = _buf(host_src)
+    st, sn = _buf(staging)
+    _check(_swap_in(cache.ref, l0, l1, sp, ep, h, hn, st, sn, _stream(stream)))
+
+
+class Streamer:
+    """Handle of ``dv_streamer`` (two slots, pack and copy streams)."""
+
+    def __init__(self, slot0, slot1, pack_stream=None, copy_stream=None):
+        a0, n0 = _buf(slot0)
+        a1, n1 = _buf(slot1)
+        self._keep = (slot0, slot1, pack_stream, copy_stream)
+        h = _P()
+        _check(_streamer_create(ctypes.byref(h), a0, a1, min(n0, n1), _stream(pack_stream),
+                                _stream(copy_stream)))
+        self.h = h
+
+    def stream_layer(self, cache: Cache, layer, seq_start, seq_end, host_dst, l0=0):
+        s, e, sp, ep = _ranges(seq_start, seq_end)
+        d, n = _buf(host_dst)
+        _check(_stream_layer(self.h, cache.ref, layer, sp, ep, d, n, l0))
+
+    def wait(self):
+        _check(_streamer_wait(self.h))
+
+    def close(self):
+        if self.h:
+            _streamer_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def dv_streamer_create(slot0, slot1, pack_stream=None, copy_stream=None) -> Streamer:
+    return Streamer(slot0, slot1, pack_stream, copy_stream)
+
+
+def dv_stream_layer(streamer: Streamer, cache: Cache, layer, seq_start, seq_end, host_dst,
+                    l0=0) -> None:
+    streamer.stream_layer(cache, layer, seq_start, seq_end, host_dst, l0)
+
+
+def dv_streamer_wait(streamer: Streamer) -> None:
+    streamer.wait()
+
+
+def dv_streamer_destroy(streamer: Streamer) -> None:
+    streamer.close()
+
+
+class Replica:
+    """Handle of ``dv_replica``: a record log in a pinned host arena."""
+
+    def __init__(self, host_arena, batch):
+        a, n = _buf(host_arena)
+        self._keep = host_arena
+        h = _P()
+        _check(_replica_create(ctypes.byref(h), a, n, batch))
+        self.h = h
+
+    def append(self, cache: Cache, l0, l1, seq_start, seq_end, step, staging=None, stream=None):
+        s, e, sp, ep = _ranges(seq_start, seq_end)
+        st, sn = _buf(staging)
+        _check(_replica_append(self.h, cache.ref, l0, l1, sp, ep, step, st, sn, _stream(stream)))
+
+    def restore(self, cache: Cache, upto_step=-1, staging=None, stream=None):
+        st, sn = _buf(staging)
+        _check(_replica_restore(self.h, cache.ref, upto_step, st, sn, _stream(stream)))
+
+    def truncate(self, step):
+        _check(_replica_truncate(self.h, step))
+
+    def info(self):
+        n = _I64(0)
+        b = _SZ(0)
+        _check(_replica_info(self.h, ctypes.byref(n), ctypes.byref(b)))
+        return n.value, b.value
+
+    def close(self):
+        if self.h:
+            _replica_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def dv_replica_create(host_arena, batch) -> Replica:
+    return Replica(host_arena, batch)
+
+
+def dv_replica_append(replica: Replica, cache: Cache, l0, l1, seq_start, seq_end, step,
+                      staging=None, stream=None) -> None:
+    replica.append(cache, l0, l1, seq_start, seq_end, step, staging, stream)
+
+
+def dv_replica_restore(replica: Replica, cache: Cache, upto_step=-1, staging=None,
+                       stream=None) -> None:
+    replica.restore(cache, upto_step, staging, stream)
+
+
+def dv_replica_truncate(replica: Replica, step) -> None:
+    replica.truncate(step)
+
+
+def dv_replica_info(replica: Replica):
+    return replica.info()
+
+
+def dv_replica_destroy(replica: Replica) -> None:
+    replica.close()

@@ -57,9 +57,17 @@ def stream_base(seed: int, kv: int) -> int:
 
 
 def _words(base: int, word_index: np.ndarray) -> np.ndarray:
-    n = np.asarray(word_index, dtype=np.uint64)
+    z = np.array(word_index, dtype=np.uint64)  # a fresh array, updated in place
     with np.errstate(over="ignore"):
-        return mix64(np.uint64(base) + (n + np.uint64(1)) * np.uint64(GAMMA))
+        z += np.uint64(1)
+        z *= np.uint64(GAMMA)
+        z += np.uint64(base)
+        z ^= z >> np.uint64(30)
+        z *= np.uint64(_MUL1)
+        z ^= z >> np.uint64(27)
+        z *= np.uint64(_MUL2)
+        z ^= z >> np.uint64(31)
+    return z
 
 
 def _make_finite(elems: np.ndarray, kind: str) -> np.ndarray:
@@ -88,9 +96,11 @@ def fill_bytes(seed: int, kv: int, nbytes: int, kind: str = "fp16") -> np.ndarra
         out[8 * w0: 8 * w1] = words.view(np.uint8) if words.dtype.byteorder in "=<" else \
             words.astype("<u8").view(np.uint8)
     if kind in FINITE_MASKS:
-        esize = FINITE_MASKS[kind][2]
+        emask, ebit, esize = FINITE_MASKS[kind]
         view = out.view(_UINT[esize])
-        view[:] = _make_finite(view, kind)
+        t = view.dtype.type
+        bad = (view & t(emask)) == t(emask)
+        view[bad] &= t(~ebit & ((1 << (8 * esize)) - 1))
     return out
 
 

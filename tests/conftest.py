@@ -8,3 +8,16 @@ if str(ROOT) not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a)")
+    # Build (when missing or stale) the copy library, the GPU input generator
+    # and the oracle before any test module imports them.
+    import importlib.util
+    from synth import build as synth_build
+    import oracle
+    # load the build script by path: importing the package loads libdv.so
+    spec = importlib.util.spec_from_file_location(
+        "_dv_build", ROOT / "kv_cache_streaming_gb300" / "build.py")
+    dv_build = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(dv_build)
+    dv_build.build()
+    synth_build.build()
+    oracle.load()

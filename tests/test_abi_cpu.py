@@ -1,0 +1,96 @@
+"""The C ABI without a GPU: the library loads, exports what dv.h declares,
+and its host-side planning and validation behave (CPU)."""
+import re
+from pathlib import Path
+
+import numpy as np
+import pytest
+
+import kv_cache_streaming_gb300 as dv  # noqa: E402
+import oracle  # noqa: E402
+from synth.configs import Geometry, GEOMETRIES  # noqa: E402
+from tests import oracle_pins as P  # noqa: E402
+
+HEADER = Path(__file__).resolve().parent.parent / "include" / "dv.h"
+
+
+def declared_functions():
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dv_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert len(names) >= 20
+    for name in names:
+        assert hasattr(dv.lib, name), name
+
+
+def test_abi_version():
+    assert dv.dv_abi_version() == 1
+
+
+def _cache(g):
+    # addresses are never dereferenced by the host-only calls below
+    return dv.Cache.from_geometry(g, 0x1000, 0x2000)
+
+
+def test_staging_bytes_matches_oracle():
+    orc = oracle.default()
+    rng = np.random.default_rng(4)
+    for g in GEOMETRIES + P.READING_GEOMS:
+        for _ in range(5):
+            s, e = P.random_ranges(g, rng)
+            l0 = int(rng.integers(0, g.num_layers + 1))
+            l1 = int(rng.integers(l0, g.num_layers + 1))
+            assert dv.dv_staging_bytes(_cache(g), l0, l1, s, e) == orc.staging_bytes(g, l0, l1, s, e)
+
+
+def test_full_cache_size_is_the_capacity_formula():
+    for g in GEOMETRIES:
+        s = np.zeros(g.batch, np.int32)
+        e = np.full(g.batch, g.max_seq, np.int32)
+        want = 2 * g.batch * g.max_seq * g.num_heads * g.head_dim * g.elem_bytes * g.num_layers
+        assert dv.dv_staging_bytes(_cache(g), 0, g.num_layers, s, e) == want
+
+
+def _status(fn):
+    with pytest.raises(dv.DvError) as ei:
+        fn()
+    return ei.value.status
+
+
+def test_validation_errors():
+    g = Geometry("v", 2, 2, 2, 64, 16, 2, "raw")
+    c = _cache(g)
+    ok_s, ok_e = np.zeros(2, np.int32), np.full(2, 4, np.int32)
+    st = lambda f: _status(f)  # noqa: E731
+    assert st(lambda: dv.dv_staging_bytes(c, 0, 3, ok_s, ok_e)) == dv.DV_ERR_RANGE
+    assert st(lambda: dv.dv_staging_bytes(c, 2, 1, ok_s, ok_e)) == dv.DV_ERR_RANGE
+    assert st(lambda: dv.dv_staging_bytes(c, 0, 2, [5, 0], [4, 4])) == dv.DV_ERR_RANGE
+    assert st(lambda: dv.dv_staging_bytes(c, 0, 2, [0, 0], [17, 4])) == dv.DV_ERR_RANGE
+    assert st(lambda: dv.dv_staging_bytes(c, 0, 2, [-1, 0], [3, 4])) == dv.DV_ERR_RANGE
+    bad = dv.Cache(2, 2, 2, 60, 16, 2, 0x1000, 0x2000)  # head_dim not a multiple of 8
+    assert st(lambda: dv.dv_staging_bytes(bad, 0, 2, ok_s, ok_e)) == dv.DV_ERR_UNSUPPORTED
+    bad = dv.Cache(2, 2, 2, 64, 16, 3, 0x1000, 0x2000)
+    assert st(lambda: dv.dv_staging_bytes(bad, 0, 2, ok_s, ok_e)) == dv.DV_ERR_INVALID_ARG
+    bad = dv.Cache(2, 2, 2, 64, 16, 2, 0x1000, 0x2000, layer_stride_elems=100)
+    assert st(lambda: dv.dv_staging_bytes(bad, 0, 2, ok_s, ok_e)) == dv.DV_ERR_INVALID_ARG
+    bad = dv.Cache(2, 2, 2, 64, 16, 2, 0x1000, 0x2000, layer_stride_elems=2 * 2 * 64 * 16 + 4)
+    assert st(lambda: dv.dv_staging_bytes(bad, 0, 2, ok_s, ok_e)) == dv.DV_ERR_MISALIGNED
+    big = dv.Cache(1, dv.DV_MAX_BATCH + 1, 1, 8, 4, 2, 0x1000, 0x2000)
+    n = dv.DV_MAX_BATCH + 1
+    assert st(lambda: dv.dv_staging_bytes(big, 0, 1, np.zeros(n), np.ones(n))) == \
+        dv.DV_ERR_UNSUPPORTED
+    need = dv.dv_staging_bytes(c, 0, 2, ok_s, ok_e)
+    # too-small destination / source is caught before any pointer is touched
+    assert st(lambda: dv.dv_kv_pack(c, 0, 2, ok_s, ok_e, (0x3000, need - 16), stream=0)) == \
+        dv.DV_ERR_BUFFER_TOO_SMALL
+    assert st(lambda: dv.dv_kv_unpack(c, 0, 2, ok_s, ok_e, (0x3000, need - 16), stream=0)) == \
+        dv.DV_ERR_BUFFER_TOO_SMALL
+    assert st(lambda: dv.dv_kv_pack(c, 0, 2, ok_s, ok_e, (0x3000, need), stream=0,
+                                    variant=7)) == dv.DV_ERR_INVALID_ARG
+    # an empty pack enqueues nothing and needs no buffer
+    dv.dv_kv_pack(c, 1, 1, ok_s, ok_e, None, stream=0)
+    dv.dv_kv_pack(c, 0, 2, ok_s, ok_s, None, stream=0)

@@ -1,0 +1,258 @@
+"""Parity of the CUDA path with the oracle, byte for byte, on seeded inputs
+small enough for the oracle (several tiles, ragged tails, empty ranges)."""
+import numpy as np
+import pytest
+import torch
+
+import kv_cache_streaming_gb300 as dv
+import oracle
+import synth
+from synth.configs import Geometry, TINY, seed_of, tiny_ranges
+from tests import gpu_helpers as H
+from tests import oracle_pins as P
+
+pytestmark = pytest.mark.gpu
+ORC = oracle.default()
+VARIANTS = [dv.DV_VARIANT_AUTO, dv.DV_VARIANT_FLAT, dv.DV_VARIANT_TILE]
+
+GEOMS = [
+    Geometry("c16", 3, 5, 3, 128, 300, 2, "fp16"),      # C = 16, 32-token tiles
+    Geometry("c8", 2, 4, 5, 64, 200, 2, "bf16"),        # C = 8, 64-token tiles
+    Geometry("c12", 2, 3, 2, 96, 100, 2, "fp16"),       # C = 12, generic kernels
+    Geometry("p1", 2, 3, 2, 128, 64, 1, "raw"),         # 1-byte elements, x = 16
+    Geometry("p4", 2, 3, 2, 64, 64, 4, "fp32"),         # 4-byte elements, x = 4
+    Geometry("pad", 3, 2, 2, 128, 50, 2, "fp16", layer_stride_elems=2 * 2 * 128 * 50 + 64),
+    Geometry("b40", 1, 40, 2, 64, 32, 2, "fp16"),       # batch > 32: 1024-entry tables
+]
+
+
+def range_sets(g, rng):
+    B, S = g.batch, g.max_seq
+    out = [("full", np.zeros(B, np.int32), np.full(B, S, np.int32)),
+           ("empty", np.zeros(B, np.int32), np.zeros(B, np.int32))]
+    pos = rng.integers(0, S, size=B).astype(np.int32)
+    e = pos + 1
+    e[::3] = pos[::3]  # some finished sequences
+    out.append(("decode", pos, e.astype(np.int32)))
+    for i in range(3):
+        s, e = P.random_ranges(g, rng)
+        out.append((f"rand{i}", s, e))
+    return out
+
+
+def check_pack_unpack(g, cache, kh, vh, l0, l1, s, e, variant):
+    n = ORC.staging_bytes(g, l0, l1, s, e)
+    dst = H.device_bytes(n + 64, fill=0xEE)
+    dv.dv_kv_pack(cache, l0, l1, s, e, dst, variant=variant)
+    got = H.to_np(dst)
+    want = ORC.pack(g, kh, vh, l0, l1, s, e)
+    assert np.array_equal(got[:n], want), (g.name, l0, l1, s, e, variant)
+    assert (got[n:] == 0xEE).all()  # nothing written past the staging bytes
+    # unpack into a sentinel cache: exactly the selected slices change
+    back = H.device_cache(g, fill=0x5A)
+    dv.dv_kv_unpack(back, l0, l1, s, e, dst, variant=variant, src_bytes=n)
+    kw = np.full(g.tensor_bytes, 0x5A, np.uint8)
+    vw = np.full(g.tensor_bytes, 0x5A, np.uint8)
+    ORC.unpack(g, kw, vw, l0, l1, s, e, want)
+    assert np.array_equal(H.to_np(back.k), kw)
+    assert np.array_equal(H.to_np(back.v), vw)
+
+
+def test_gpu_fill_matches_host_generator():
+    for g in (TINY, GEOMS[1], GEOMS[4]):
+        c = H.device_cache(g, fill="synth", seed=99)
+        kh, vh = H.host_cache(g, 99)
+        assert np.array_equal(H.to_np(c.k), kh) and np.array_equal(H.to_np(c.v), vh)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_tiny_workload(variant):
+    """Tiny cache: prompt [0,37), then the decode token at 37; unpack into a
+    zeroed cache."""
+    g, seed = TINY, seed_of(1)
+    kh, vh = H.host_cache(g, seed)
+    cache = H.device_cache(g, fill=(kh, vh))
+    (ps, pe), (ds, de) = tiny_ranges()
+    for s, e in ((ps, pe), (ds, de)):
+        n = ORC.staging_bytes(g, 0, g.num_layers, s, e)
+        dst = H.device_bytes(n)
+        dv.dv_kv_pack(cache, 0, g.num_layers, s, e, dst, variant=variant)
+        want = ORC.pack(g, kh, vh, 0, g.num_layers, s, e)
+        assert np.array_equal(H.to_np(dst)[:n], want)
+        z = H.device_cache(g, fill="zero")
+        dv.dv_kv_unpack(z, 0, g.num_layers, s, e, dst, variant=variant, src_bytes=n)
+        kw, vw = np.zeros_like(kh), np.zeros_like(vh)
+        ORC.unpack(g, kw, vw, 0, g.num_layers, s, e, want)
+        assert np.array_equal(H.to_np(z.k), kw) and np.array_equal(H.to_np(z.v), vw)
+
+
+@pytest.mark.parametrize("g", GEOMS, ids=lambda g: g.name)
+def test_pack_unpack_geometries(g):
+    rng = np.random.default_rng(abs(hash(g.name)) % 2**32)
+    kh, vh = H.host_cache(g, 1234)
+    cache = H.device_cache(g, fill=(kh, vh))
+    for name, s, e in range_sets(g, rng):
+        for l0, l1 in ((0, g.num_layers), (g.num_layers - 1, g.num_layers)):
+            for variant in VARIANTS:
+                check_pack_unpack(g, cache, kh, vh, l0, l1, s, e, variant)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_pack_to_and_unpack_from_pinned_host(variant):
+    g = GEOMS[0]
+    rng = np.random.default_rng(8)
+    kh, vh = H.host_cache(g, 77)
+    cache = H.device_cache(g, fill=(kh, vh))
+    s, e = P.random_ranges(g, rng)
+    n = ORC.staging_bytes(g, 0, g.num_layers, s, e)
+    host = H.pinned(n)
+    dv.dv_kv_pack(cache, 0, g.num_layers, s, e, host, variant=variant)
+    torch.cuda.synchronize()
+    want = ORC.pack(g, kh, vh, 0, g.num_layers, s, e)
+    assert np.array_equal(host.numpy()[:n], want)
+    back = H.device_cache(g, fill=0x11)
+    dv.dv_kv_unpack(back, 0, g.num_layers, s, e, host, variant=variant)
+    kw = np.full_like(kh, 0x11)
+    vw = np.full_like(vh, 0x11)
+    ORC.unpack(g, kw, vw, 0, g.num_layers, s, e, want)
+    assert np.array_equal(H.to_np(back.k), kw) and np.array_equal(H.to_np(back.v), vw)
+
+
+@pytest.mark.parametrize("staged", [False, True])
+def test_swap_out_and_in(staged):
+    g = Geometry("swap", 5, 4, 3, 128, 256, 2, "fp16")
+    rng = np.random.default_rng(9)
+    kh, vh = H.host_cache(g, 5)
+    cache = H.device_cache(g, fill=(kh, vh))
+    s = np.zeros(g.batch, np.int32)
+    e = rng.integers(1, g.max_seq + 1, size=g.batch).astype(np.int32)
+    n = ORC.staging_bytes(g, 0, g.num_layers, s, e)
+    slab = n // g.num_layers
+    staging = H.device_bytes(2 * slab + 16) if staged else None  # 2 layers per group
+    host = H.pinned(n)
+    dv.dv_swap_out(cache, 0, g.num_layers, s, e, host, staging=staging)
+    torch.cuda.synchronize()
+    want = ORC.swap_out(g, kh, vh, 0, g.num_layers, s, e)
+    assert np.array_equal(host.numpy()[:n], want)
+    fresh = H.device_cache(g, fill="zero")
+    dv.dv_swap_in(fresh, 0, g.num_layers, s, e, host, staging=staging)
+    kw, vw = np.zeros_like(kh), np.zeros_like(vh)
+    ORC.unpack(g, kw, vw, 0, g.num_layers, s, e, want)
+    assert np.array_equal(H.to_np(fresh.k), kw) and np.array_equal(H.to_np(fresh.v), vw)
+
+
+def test_stream_layers_matches_oracle_and_swap_out():
+    g = Geometry("stream", 6, 3, 4, 64, 128, 2, "fp16")
+    kh, vh = H.host_cache(g, 6)
+    cache = H.device_cache(g, fill=(kh, vh))
+    s = np.zeros(g.batch, np.int32)
+    e = np.array([100, 128, 7], np.int32)
+    n = ORC.staging_bytes(g, 0, g.num_layers, s, e)
+    slab = n // g.num_layers
+    slots = (H.device_bytes(slab), H.device_bytes(slab))
+    pack_stream, copy_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    host = H.pinned(n, fill=0)
+    st = dv.Streamer(slots[0], slots[1], pack_stream, copy_stream)
+    torch.cuda.synchronize()
+    for layer in range(g.num_layers):
+        st.stream_layer(cache, layer, s, e, host, l0=0)
+    st.wait()
+    want = ORC.stream_layers(g, kh, vh, 0, g.num_layers, s, e)
+    assert np.array_equal(host.numpy()[:n], want)
+    assert np.array_equal(want, ORC.swap_out(g, kh, vh, 0, g.num_layers, s, e))
+    st.close()
+
+
+@pytest.mark.parametrize("staged", [False, True])
+def test_replica_snapshot_deltas_restore_truncate(staged):
+    g = Geometry("rep", 3, 4, 2, 128, 64, 2, "bf16")
+    kh, vh = H.host_cache(g, 12)
+    cache = H.device_cache(g, fill=(kh, vh))
+    len0 = np.array([5, 20, 1, 33], np.int32)
+    zero = np.zeros(g.batch, np.int32)
+    steps = 6
+    total = ORC.staging_bytes(g, 0, g.num_layers, zero, len0 + steps)
+    arena = H.pinned(total + 4096)
+    staging = H.device_bytes(total) if staged else None
+    rep = dv.Replica(arena, g.batch)
+    rep.append(cache, 0, g.num_layers, zero, len0, step=0, staging=staging)
+    pos = len0.copy()
+    records = [(0, g.num_layers, zero, len0.copy())]
+    for k in range(1, steps + 1):
+        act = np.array([1, 1, 1 if k < 3 else 0, 1], np.int32)  # sequence 2 finishes
+        rep.append(cache, 0, g.num_layers, pos, pos + act, step=k, staging=staging)
+        records.append((0, g.num_layers, pos.copy(), (pos + act).copy()))
+        pos = pos + act
+    torch.cuda.synchronize()
+    nrec, used = rep.info()
+    assert nrec == steps + 1
+    assert used == sum(ORC.staging_bytes(g, a, b, s, e) for a, b, s, e in records)
+    # the arena holds the records end to end
+    want_arena = np.concatenate([ORC.pack(g, kh, vh, a, b, s, e) for a, b, s, e in records])
+    assert np.array_equal(arena.numpy()[:used], want_arena)
+    # restore everything into a zeroed cache = the live cache on [0, pos)
+    z = H.device_cache(g, fill="zero")
+    rep.restore(z, staging=staging)
+    kw, vw = ORC.restore(g, [(a, b, s, e, ORC.pack(g, kh, vh, a, b, s, e))
+                             for a, b, s, e in records])
+    assert np.array_equal(H.to_np(z.k), kw) and np.array_equal(H.to_np(z.v), vw)
+    # acknowledged prefix: truncate at step 4 keeps steps 0..3 only
+    rep.truncate(4)
+    assert rep.info()[0] == 4
+    z2 = H.device_cache(g, fill="zero")
+    rep.restore(z2, staging=staging)
+    kw, vw = ORC.restore(g, [(a, b, s, e, ORC.pack(g, kh, vh, a, b, s, e))
+                             for a, b, s, e in records[:4]])
+    assert np.array_equal(H.to_np(z2.k), kw) and np.array_equal(H.to_np(z2.v), vw)
+    rep.close()
+
+
+def _status(fn):
+    with pytest.raises(dv.DvError) as ei:
+        fn()
+    return ei.value.status
+
+
+def test_errors_with_real_buffers_enqueue_nothing():
+    g = Geometry("err", 2, 2, 2, 64, 32, 2, "fp16")
+    cache = H.device_cache(g, fill=0x33)
+    s, e = np.zeros(2, np.int32), np.full(2, 32, np.int32)
+    n = ORC.staging_bytes(g, 0, 2, s, e)
+    dst = H.device_bytes(n + 64, fill=0x44)
+    # misaligned destination
+    assert _status(lambda: dv.dv_kv_pack(cache, 0, 2, s, e, (dst.data_ptr() + 8, n))) == \
+        dv.DV_ERR_MISALIGNED
+    # pageable host memory is refused
+    pageable = np.zeros(n + 64, np.uint8)
+    assert _status(lambda: dv.dv_kv_pack(cache, 0, 2, s, e, (pageable.ctypes.data, n))) == \
+        dv.DV_ERR_INVALID_ARG
+    # A claimed size past the end of the allocation is refused by the driver
+    # range check.  Exercised only when the library itself reports, before the
+    # call, an extent shorter than the claim: the call that follows is then
+    # refused on the host and no kernel can run out of bounds.
+    gb = Geometry("err2", 2, 2, 2, 128, 2048, 2, "fp16")
+    cb = H.device_cache(gb, fill=0x33)
+    sb, eb = np.zeros(2, np.int32), np.full(2, 2048, np.int32)
+    nb = ORC.staging_bytes(gb, 0, 2, sb, eb)
+    small = H.device_bytes(1 << 20)
+    ext = dv.dv_allocation_extent(small)
+    if ext is not None and ext < nb:
+        assert _status(lambda: dv.dv_kv_pack(cb, 0, 2, sb, eb, (small.data_ptr(), nb))) == \
+            dv.DV_ERR_BUFFER_TOO_SMALL
+    huge_layers = 1 << 20
+    ext_k = dv.dv_allocation_extent(cb.k)
+    lay = gb.tensor_bytes // gb.num_layers
+    if ext_k is not None and ext_k < huge_layers * lay:
+        big = dv.Cache(huge_layers, 2, 2, 128, 2048, 2, cb.k, cb.v)
+        assert _status(lambda: dv.dv_kv_pack(big, huge_layers - 1, huge_layers, sb, eb,
+                                             (dst.data_ptr(), nb // 2))) == \
+            dv.DV_ERR_BUFFER_TOO_SMALL
+    # staging smaller than one layer slab
+    host = H.pinned(n)
+    tiny_stg = H.device_bytes(n // 4)
+    assert _status(lambda: dv.dv_swap_out(cache, 0, 2, s, e, host, staging=tiny_stg)) == \
+        dv.DV_ERR_BUFFER_TOO_SMALL
+    # swap to device memory instead of pinned host memory is refused
+    assert _status(lambda: dv.dv_swap_out(cache, 0, 2, s, e, dst)) == dv.DV_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert (H.to_np(dst) == 0x44).all()  # no failed call wrote anything
