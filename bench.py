@@ -51,6 +51,10 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-swap", action="store_true", help="skip the swap / link section")
+    ap.add_argument("--kernel-case", default=None,
+                    choices=["tile-pack", "tile-unpack", "flat-pack", "flat-unpack"],
+                    help="run one kernel of the step on an 8-layer cache of the workload's "
+                         "shape, 5 launches, and exit (a small case for profilers)")
     return ap.parse_args()
 
 
@@ -471,9 +475,40 @@ def run_mine(args):
     print(json.dumps(line), flush=True)
 
 
+def run_kernel_case(case):
+    """One kernel of the step on the first 8 layers of the workload's cache
+    (inputs larger than L2, under 1 GB on the device), launched 5 times."""
+    from dataclasses import replace
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import kv_cache_streaming_gb300 as dv
+    from synth import gpu as synth_gpu
+    torch.cuda.set_device(0)
+    g = replace(GPT2, num_layers=8)
+    k = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+    v = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+    synth_gpu.fill_cache(g, k, v, seed_of(2))
+    cache = dv.Cache.from_geometry(g, k, v)
+    (ps, pe), deltas = gpt2_ranges()
+    s, e = (ps, pe) if case.startswith("tile") else deltas[0]
+    n = dv.dv_staging_bytes(cache, 0, g.num_layers, s, e)
+    stg = torch.empty(n, dtype=torch.uint8, device="cuda")
+    dv.dv_kv_pack(cache, 0, g.num_layers, s, e, stg)
+    for _ in range(5):
+        if case.endswith("-pack"):
+            dv.dv_kv_pack(cache, 0, g.num_layers, s, e, stg)
+        else:
+            dv.dv_kv_unpack(cache, 0, g.num_layers, s, e, stg)
+    torch.cuda.synchronize()
+    print(f"{case}: 5 launches of {2 * n} algorithmic bytes each")
+
+
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.kernel_case:
+        run_kernel_case(args.kernel_case)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_mine(args)
