@@ -166,6 +166,41 @@ dv_status dv_swap_in(const dv_cache* cache, int32_t l0, int32_t l1, const int32_
                      const int32_t* seq_end, const void* host_src, size_t host_bytes,
                      void* staging, size_t staging_bytes, dv_stream stream);
 
+/* ---- swap-out without allocation ------------------------------------------ */
+
+/* Size of the device buffer built into libdv for dv_swap_out_noalloc. */
+#define DV_NOALLOC_STAGING_BYTES 67108864 /* 64 MiB */
+
+/* The paper has no counterpart to this call.  It is dv_swap_out on the
+ * staged path, but the staging buffer is built into the library, so the
+ * caller allocates nothing on the device.  It is meant for callers that
+ * cannot call cudaMalloc: a host that embeds libdv but owns no device
+ * allocator (it only receives the cache and host pointers from elsewhere), a
+ * serving process whose device memory is owned entirely by another allocator
+ * (a framework's caching allocator holding the whole budget, where an extra
+ * cudaMalloc fails or fragments it), or a latency-critical loop that must not
+ * take the device-wide synchronisation cudaMalloc can cause.
+ *
+ * Limits and behaviour:
+ *  - The buffer is DV_NOALLOC_STAGING_BYTES (64 MiB) of device memory that
+ *    every GPU loading libdv holds until the process exits.  Layers are
+ *    packed into it in groups and copied to host_dst, as on dv_swap_out's
+ *    staged path, so the whole swap may be larger; one layer of the ranges
+ *    larger than 64 MiB is refused with DV_ERR_BUFFER_TOO_SMALL before
+ *    anything is enqueued.
+ *  - The first call on a device looks up the buffer's device address on the
+ *    current device (cudaGetSymbolAddress); make that first call on each
+ *    device before any stream capture.
+ *  - All calls share the one buffer, which keeps the last call's bytes
+ *    (nothing in it needs to start at zero: each group is packed in full
+ *    before it is copied).  Calls whose work overlaps on the GPU (on
+ *    different streams, or from different threads without ordering) race on
+ *    it and corrupt each other's output: order them on one stream.
+ *  - Arguments, validation and errors are those of dv_swap_out. */
+dv_status dv_swap_out_noalloc(const dv_cache* cache, int32_t l0, int32_t l1,
+                              const int32_t* seq_start, const int32_t* seq_end, void* host_dst,
+                              size_t host_bytes, dv_stream stream);
+
 /* ---- layer-by-layer streaming (§3, Fig 7b) ------------------------------ */
 
 /* Owns two events per slot; borrows the slots and streams. */

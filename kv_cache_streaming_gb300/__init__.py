@@ -18,6 +18,7 @@ from .dv import (  # noqa: F401
     DV_VARIANT_AUTO, DV_VARIANT_FLAT, DV_VARIANT_TILE,
     DvError, Cache, Streamer, Replica, lib, library_path,
     dv_abi_version, dv_allocation_extent, dv_staging_bytes, dv_kv_pack, dv_kv_unpack, dv_swap_out, dv_swap_in,
+    dv_swap_out_noalloc, DV_NOALLOC_STAGING_BYTES,
     dv_streamer_create, dv_stream_layer, dv_streamer_wait, dv_streamer_destroy,
     dv_replica_create, dv_replica_append, dv_replica_restore, dv_replica_truncate,
     dv_replica_info, dv_replica_destroy,

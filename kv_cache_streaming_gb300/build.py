@@ -24,7 +24,7 @@ ROOT = PKG.parent
 CSRC = PKG / "csrc"
 OBJ = PKG / "_build"
 LIB = PKG / "libdv.so"
-SOURCES = ["dv_api.cu", "dv_kernels.cu"]
+SOURCES = ["dv_api.cu", "dv_kernels.cu", "dv_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -297,6 +297,18 @@ dv_status do_swap(Dir dir, const dv_cache* c, int32_t l0, int32_t l1, const int3
 
 }  // namespace
 
+namespace dv {
+dv_status set_error(dv_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+}  // namespace dv
+
 // ---- streamer ----------------------------------------------------------------
 
 struct dv_streamer {

@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "../../include/dv.h"
+
 namespace dv {
 
 constexpr int kMaxBatch = 1024;   // == DV_MAX_BATCH
@@ -52,5 +54,8 @@ bool tile_supported(const Plan& p);
 // when the plan moves nothing.
 cudaError_t launch_pack(const Plan& p, void* stg, cudaStream_t stream, int variant);
 cudaError_t launch_unpack(const Plan& p, const void* stg, cudaStream_t stream, int variant);
+
+// Records a message for dv_last_error() on the calling thread; returns `st`.
+dv_status set_error(dv_status st, const char* fmt, ...);
 
 }  // namespace dv

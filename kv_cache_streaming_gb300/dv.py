@@ -61,6 +61,8 @@ _pack = _sig("dv_kv_pack_variant", _RANGE + [_P, _SZ, _P, _I32])
 _unpack = _sig("dv_kv_unpack_variant", _RANGE + [_P, _SZ, _P, _I32])
 _swap_out = _sig("dv_swap_out", _RANGE + [_P, _SZ, _P, _SZ, _P])
 _swap_in = _sig("dv_swap_in", _RANGE + [_P, _SZ, _P, _SZ, _P])
+_swap_out_noalloc = _sig("dv_swap_out_noalloc", _RANGE + [_P, _SZ, _P])
+DV_NOALLOC_STAGING_BYTES = 64 << 20
 _streamer_create = _sig("dv_streamer_create", [ctypes.POINTER(_P), _P, _P, _SZ, _P, _P])
 _stream_layer = _sig("dv_stream_layer", [_P, _CP, _I32, _I32P, _I32P, _P, _SZ, _I32])
 _streamer_wait = _sig("dv_streamer_wait", [_P])
@@ -196,6 +198,15 @@ def dv_swap_in(cache: Cache, l0, l1, seq_start, seq_end, host_src, staging=None,
     h, hn = _buf(host_src)
     st, sn = _buf(staging)
     _check(_swap_in(cache.ref, l0, l1, sp, ep, h, hn, st, sn, _stream(stream)))
+
+
+def dv_swap_out_noalloc(cache: Cache, l0, l1, seq_start, seq_end, host_dst,
+                        stream=None) -> None:
+    """dv_swap_out through libdv's built-in 64 MiB staging buffer (no
+    allocation by the caller); see dv.h for the limits."""
+    s, e, sp, ep = _ranges(seq_start, seq_end)
+    h, hn = _buf(host_dst)
+    _check(_swap_out_noalloc(cache.ref, l0, l1, sp, ep, h, hn, _stream(stream)))
 
 
 class Streamer:
