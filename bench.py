@@ -41,7 +41,7 @@ METRIC = "KV pack/unpack GB/s (bytes read + written, HBM-resident step)"
 UNIT = "GB/s"
 WORKLOAD = ("gpt2-1.5b-shaped KV cache L48 B8 H25 D64 S1024 fp16: prompt [0,1000) packed "
             "layer by layer + 24 one-token decode deltas, all unpacked into a second cache")
-L2_NOTE = "inputs larger than L2: 5.03 GB moved per step"
+L2_NOTE = "inputs larger than L2: 10.07 GB read + written per step"
 
 
 def parse_args():
@@ -52,7 +52,7 @@ def parse_args():
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-swap", action="store_true", help="skip the swap / link section")
     ap.add_argument("--kernel-case", default=None,
-                    choices=["tile-pack", "tile-unpack", "flat-pack", "flat-unpack"],
+                    choices=["tile-pack", "tile-unpack", "delta-pack", "delta-unpack"],
                     help="run one kernel of the step on an 8-layer cache of the workload's "
                          "shape, 5 launches, and exit (a small case for profilers)")
     return ap.parse_args()
@@ -237,22 +237,33 @@ class Bench:
         self.bytes_per_step = 2 * 2 * (L * self.slab + GPT2_DECODE_STEPS * self.dsz)
         self.launches_per_step = 2 * (L + GPT2_DECODE_STEPS)
         self.stream = torch.cuda.Stream()
+        self.stream_b = torch.cuda.Stream()
+        self.events = [torch.cuda.Event() for _ in range(L + GPT2_DECODE_STEPS)]
 
     # one step, all buffers in HBM
-    def device_step(self, stream):
+    def device_step(self, stream, two_streams=True):
+        """Packs on `stream`; each unpack waits for its own pack only (an event),
+        on a second stream when `two_streams`, so that the two sides of the
+        transfer overlap the way a sender and a receiver do."""
         dv, g = self.dv, self.g
         sp, dp = self.stg.data_ptr(), self.dstg.data_ptr()
-        for l in range(g.num_layers):
+        sb = self.stream_b if two_streams else stream
+        L = g.num_layers
+        for l in range(L):
             dv.dv_kv_pack(self.cache, l, l + 1, self.ps, self.pe, (sp + l * self.slab, self.slab),
                           stream)
+            self.events[l].record(stream)
         for k, (s, e) in enumerate(self.deltas):
-            dv.dv_kv_pack(self.cache, 0, g.num_layers, s, e, (dp + k * self.dsz, self.dsz), stream)
-        for l in range(g.num_layers):
+            dv.dv_kv_pack(self.cache, 0, L, s, e, (dp + k * self.dsz, self.dsz), stream)
+            self.events[L + k].record(stream)
+        for l in range(L):
+            sb.wait_event(self.events[l])
             dv.dv_kv_unpack(self.cache_b, l, l + 1, self.ps, self.pe,
-                            (sp + l * self.slab, self.slab), stream)
+                            (sp + l * self.slab, self.slab), sb)
         for k, (s, e) in enumerate(self.deltas):
-            dv.dv_kv_unpack(self.cache_b, 0, g.num_layers, s, e, (dp + k * self.dsz, self.dsz),
-                            stream)
+            sb.wait_event(self.events[L + k])
+            dv.dv_kv_unpack(self.cache_b, 0, L, s, e, (dp + k * self.dsz, self.dsz), sb)
+        stream.wait_stream(sb)
 
     def capture(self):
         torch = self.torch
@@ -262,7 +273,26 @@ class Bench:
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph, stream=self.stream, capture_error_mode="relaxed"):
             self.device_step(self.stream)
+        self.graph_serial = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph_serial, stream=self.stream, capture_error_mode="relaxed"):
+            self.device_step(self.stream, two_streams=False)
         torch.cuda.synchronize()
+
+    def timed_serial(self, steps=50):
+        """The same step with every launch on one stream, for reference."""
+        torch = self.torch
+        for _ in range(3):
+            self.graph_serial.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            for _ in range(steps):
+                self.graph_serial.replay()
+            e1.record(self.stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / steps
 
     def timed_value(self, steps, warmup, world):
         torch = self.torch
@@ -300,11 +330,11 @@ class Bench:
                 lambda l: dv.dv_kv_unpack(self.cache_b, l, l + 1, self.ps, self.pe,
                                           (sp + l * self.slab, self.slab), s),
                 g.num_layers, 2 * self.slab),
-            "pack decode delta (flat kernel)": (
+            "pack decode delta (token kernel)": (
                 lambda k: dv.dv_kv_pack(self.cache, 0, g.num_layers, *self.deltas[k],
                                         (dp + k * self.dsz, self.dsz), s),
                 GPT2_DECODE_STEPS, 2 * self.dsz),
-            "unpack decode delta (flat kernel)": (
+            "unpack decode delta (token kernel)": (
                 lambda k: dv.dv_kv_unpack(self.cache_b, 0, g.num_layers, *self.deltas[k],
                                           (dp + k * self.dsz, self.dsz), s),
                 GPT2_DECODE_STEPS, 2 * self.dsz),
@@ -342,20 +372,30 @@ class Bench:
         self.slots = (torch.empty(self.slab, dtype=torch.uint8, device="cuda"),
                       torch.empty(self.slab, dtype=torch.uint8, device="cuda"))
         self.copy_stream = torch.cuda.Stream()
+        self.in_stream = torch.cuda.Stream()
         self.streamer = dv.Streamer(self.slots[0], self.slots[1], self.stream, self.copy_stream)
         self.replica = dv.Replica(self.arena, g.batch)
 
     def e2e_step(self):
-        torch, dv, g = self.torch, self.dv, self.g
-        s = self.stream
+        """Layer by layer: the streamer packs layer l and copies it to pinned
+        host memory; as soon as that copy is done, layer l is swapped in from
+        the host into the second cache on a third stream, so host-to-device
+        traffic of layer l overlaps device-to-host traffic of layer l+1.  Then
+        the 24 deltas go to the host replica and are restored from it."""
+        dv, g = self.dv, self.g
+        s, si = self.stream, self.in_stream
+        hp = self.host_prompt.data_ptr()
         for l in range(g.num_layers):
             self.streamer.stream_layer(self.cache, l, self.ps, self.pe, self.host_prompt, l0=0)
+            si.wait_stream(self.copy_stream)
+            dv.dv_swap_in(self.cache_b, l, l + 1, self.ps, self.pe, (hp + l * self.slab, self.slab),
+                          stream=si)
         self.replica.truncate(0)
         for k, (a, b) in enumerate(self.deltas):
             self.replica.append(self.cache, 0, g.num_layers, a, b, step=k, stream=s)
-        s.wait_stream(self.copy_stream)
-        dv.dv_swap_in(self.cache_b, 0, g.num_layers, self.ps, self.pe, self.host_prompt, stream=s)
-        self.replica.restore(self.cache_b, stream=s)
+        si.wait_stream(s)
+        self.replica.restore(self.cache_b, stream=si)
+        s.wait_stream(si)
 
     def timed_e2e(self, steps, warmup, world):
         torch = self.torch
@@ -432,6 +472,7 @@ def run_mine(args):
     clk = clocks.stop()
     secs = max_over_ranks(secs, world)
     value = world * b.bytes_per_step * args.steps / secs / 1e9
+    serial = b.timed_serial()
     # kernel roofline, live
     kt = b.kernel_times()
     hbm_peak, peak_kind = peaks()
@@ -460,7 +501,10 @@ def run_mine(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "u16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "l2": L2_NOTE,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "timing": "CUDA-graph replay of the step, CUDA events on the launching stream",
+                   "timing": "CUDA-graph replay of the step (packs on one stream, each unpack "
+                             "after its pack on a second stream), CUDA events on the launching stream",
+                   "serial_step_ms": round(serial * 1e3, 4),
+                   "serial_value": round(b.bytes_per_step / serial / 1e9, 2),
                    "kernel_timing": "per launch kind: its launches of one step in a CUDA graph, L2 flushed before each replay, median of 5"},
         "roofline": {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1),
                      "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
@@ -473,8 +517,9 @@ def run_mine(args):
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "path": "dv_stream_layer x48 -> pinned host, dv_replica_append x24 (fused), "
-                        "dv_swap_in + dv_replica_restore (fused)"},
+                "path": "per layer: dv_stream_layer (pack + D2H) then dv_swap_in of that layer "
+                        "on a third stream (H2D overlaps the next layer's D2H); "
+                        "dv_replica_append x24 (fused) + dv_replica_restore (fused)"},
         "swap": swap,
         "gpu_launches": b.launches_per_step * args.steps,
         "clocks": clk,

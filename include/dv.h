@@ -104,9 +104,11 @@ typedef struct {
 /* Kernel choice for dv_kv_pack_variant / dv_kv_unpack_variant (testing and
  * tuning; the plain calls use DV_VARIANT_AUTO). */
 typedef enum {
-  DV_VARIANT_AUTO = 0, /* tile kernel for long ranges, flat kernel otherwise */
+  DV_VARIANT_AUTO = 0, /* token kernel when every range has at most one token, tile
+                          kernel for long ranges, flat kernel otherwise */
   DV_VARIANT_FLAT = 1, /* one 16-byte chunk per thread, staging order */
-  DV_VARIANT_TILE = 2  /* token tiles; K transposed through shared memory */
+  DV_VARIANT_TILE = 2, /* token tiles; K transposed through shared memory */
+  DV_VARIANT_TOKEN = 3 /* one-token ranges only (decode deltas): one chunk per thread */
 } dv_variant;
 
 int32_t dv_abi_version(void);

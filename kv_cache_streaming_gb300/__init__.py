@@ -15,7 +15,7 @@ been built (``python -m kv_cache_streaming_gb300.build``).
 from .dv import (  # noqa: F401
     DV_MAX_BATCH, DV_OK, DV_ERR_INVALID_ARG, DV_ERR_RANGE, DV_ERR_BUFFER_TOO_SMALL,
     DV_ERR_MISALIGNED, DV_ERR_CUDA, DV_ERR_TIMEOUT, DV_ERR_UNSUPPORTED,
-    DV_VARIANT_AUTO, DV_VARIANT_FLAT, DV_VARIANT_TILE,
+    DV_VARIANT_AUTO, DV_VARIANT_FLAT, DV_VARIANT_TILE, DV_VARIANT_TOKEN,
     DvError, Cache, Streamer, Replica, lib, library_path,
     dv_abi_version, dv_allocation_extent, dv_staging_bytes, dv_kv_pack, dv_kv_unpack, dv_swap_out, dv_swap_in,
     dv_swap_out_noalloc, DV_NOALLOC_STAGING_BYTES,

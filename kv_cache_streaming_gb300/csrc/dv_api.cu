@@ -183,11 +183,13 @@ dv_status resolve_cache(const dv_cache* c, dv::Plan* p) {
 }
 
 dv_status check_variant(const dv::Plan& p, int32_t variant) {
-  if (variant < dv::kAuto || variant > dv::kTile)
+  if (variant < dv::kAuto || variant > dv::kToken)
     return fail(DV_ERR_INVALID_ARG, "unknown variant %d", variant);
   if (variant == dv::kTile && !dv::tile_supported(p))
     return fail(DV_ERR_UNSUPPORTED, "tile kernel handles at most 64 chunks per token (got %d)",
                 p.C);
+  if (variant == dv::kToken && !dv::token_supported(p))
+    return fail(DV_ERR_UNSUPPORTED, "token kernel needs every range to hold at most one token");
   return DV_OK;
 }
 

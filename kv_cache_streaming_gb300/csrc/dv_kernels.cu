@@ -10,20 +10,28 @@
 // one V row.  Bytes are copied as bit patterns and never pass through
 // floating point.
 //
-// Two kernels, one data path each way:
-//  * flat_kernel: thread per staging chunk, in staging order, so stores (pack)
-//    or loads (unpack) of the staging side are fully coalesced.  Its cache-side
-//    accesses for K are one chunk per token row: right for one-token decode
-//    deltas, where no two chunks of a K row are adjacent anyway.
-//  * tile_kernel: one CTA per tile of up to TB tokens of one (layer, K|V,
-//    sequence, head).  A V tile is one contiguous run.  A K tile is C rows of
-//    TB contiguous chunks in the cache but TB rows of C chunks in staging; it
-//    is transposed through shared memory so that both the cache side (512
-//    contiguous bytes per warp along a row) and the staging side are
-//    coalesced.  The shared-memory row pitch is odd (C | 1 chunks) so that the
-//    column-wise accesses of 8 consecutive tokens fall in 8 distinct 16-byte
-//    bank groups.
-// Neither kernel waits on anything but __syncthreads.
+// Three kernels, each with a pack and an unpack form:
+//  * tile_kernel (long ranges): one CTA of 256 threads moves one tile, up to TB
+//    tokens of one (layer, K|V, sequence, head); TB * C = 1024 chunks (16 KiB)
+//    when C is 8 or 16, four in flight per thread.  A V tile is one contiguous
+//    run.  A K tile is C rows of TB contiguous chunks in the cache but TB rows
+//    of C chunks in staging; it is transposed through shared memory so that
+//    the cache side (512 contiguous bytes per warp instruction along a row)
+//    and the staging side are both coalesced.  The shared-memory row pitch is
+//    odd (C | 1 chunks), so the column-wise accesses of 8 consecutive tokens
+//    fall in 8 distinct 16-byte bank groups.  The grid is persistent (SMs x
+//    resident CTAs) and strides over the tiles in staging order, so at any
+//    moment the whole GPU works on neighbouring tiles.
+//  * token_kernel (every range at most one token: decode deltas): one chunk
+//    per thread, the record found with multiply-high divisions by host
+//    constants; no shared memory, no barrier.  A one-token K record is C
+//    isolated 16-byte chunks (S * 16 bytes apart) by the layout itself.
+//  * flat_kernel (anything else short): thread per staging chunk, in staging
+//    order, sequence found by binary search in shared memory.
+// All launches use programmatic dependent launch: a kernel waits for the grids
+// it depends on (griddepcontrol.wait) before touching memory, then lets the
+// next launch in the stream be scheduled.  Nothing waits on anything else
+// but __syncthreads.
 #include <atomic>
 #include <cstdint>
 
@@ -42,22 +50,48 @@ struct KParams {
   int64_t total;           // flat: chunks; tile: tiles
   int32_t l0, B, H, C, S;
   int32_t tiles_per_lkv;   // tile kernel: tiles per (layer, K|V) slab
+  uint64_t m_tpl;          // ceil(2^64 / tiles_per_lkv) (0 when it is 1)
+  uint64_t m_HT;           // ceil(2^64 / (H * T)) (0 when it is 1); flat kernel: of lkv_chunks
   int32_t seq_start[MAXB];
   int32_t seq_len[MAXB];
   int32_t tok_pre[MAXB + 1];
   int32_t tile_pre[MAXB + 1];  // tile kernel: H * sum of ceil(len / TB)
 };
 
+#ifndef DV_TILE_CPT
+#define DV_TILE_CPT 4  // 16-byte chunks each thread moves per tile
+#endif
+#ifndef DV_TILE_MIN_BLOCKS
+#define DV_TILE_MIN_BLOCKS 5  // resident CTAs per SM the tile kernel is compiled for
+#endif
+#ifndef DV_PDL
+#define DV_PDL 1  // programmatic dependent launch
+#endif
+
 constexpr int kFlatUnroll = 4;
-constexpr int kTileUnroll = 2;
+constexpr int kTileUnroll = DV_TILE_CPT;
 constexpr int kMaxTileC = 64;  // generic tile kernel: at most 64 chunks per token
 
 template <int LOG2C>
 struct TileShape {
-  // 512 chunks (8 KiB) per tile when C is a power of two we specialise.
-  static constexpr int LOG2TB = LOG2C >= 0 ? 9 - LOG2C : 5;
+  // kThreads * DV_TILE_CPT chunks per tile when C is a power of two we
+  // specialise (16 KiB for 4 chunks per thread); 32 tokens otherwise.
+  static constexpr int LOG2CH =
+      DV_TILE_CPT == 8 ? 11 : DV_TILE_CPT == 4 ? 10 : DV_TILE_CPT == 2 ? 9 : 8;
+  static constexpr int LOG2TB = LOG2C >= 0 ? LOG2CH - LOG2C : 5;
   static constexpr int TB = 1 << LOG2TB;
 };
+
+// Programmatic dependent launch: wait until the grids this launch depends on
+// have completed and their memory is visible, then let the next launch in the
+// stream be scheduled while this one runs (it still waits for this grid to
+// finish before it touches memory).  No-ops when launched without PDL.
+__device__ __forceinline__ void pdl_enter() {
+#if DV_PDL
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
 
@@ -73,12 +107,30 @@ __device__ __forceinline__ int find_seq(const Arr& pre, int B, int32_t key) {
   return lo;
 }
 
+// floor(n / d) for n < 2^31, with m = ceil(2^32 / d): n*m / 2^32 lies in
+// [n/d, n/d + 1/2), so its floor is the quotient or one more.
+__device__ __forceinline__ uint32_t div_by(uint32_t n, uint32_t d, uint64_t m) {
+  uint32_t q = (uint32_t)(((uint64_t)n * m) >> 32);
+  if ((uint64_t)q * d > n) --q;
+  return q;
+}
+
+// floor(n / d) for 0 <= n < 2^63 and 1 <= d < 2^32, with m = ceil(2^64 / d)
+// (m = 0 stands for d = 1): n*m / 2^64 lies in [n/d, n/d + 1/2).
+__device__ __forceinline__ uint64_t div64_by(uint64_t n, uint64_t d, uint64_t m) {
+  if (m == 0) return n;
+  uint64_t q = __umul64hi(n, m);
+  if (q * d > n) --q;
+  return q;
+}
+
 template <bool PACK, int MAXB, int LOG2C>
 __global__ void __launch_bounds__(kThreads)
 flat_kernel(const __grid_constant__ KParams<MAXB> p) {
   __shared__ int32_t s_rec_pre[MAXB + 1];  // first token record of each sequence
   __shared__ int32_t s_len[MAXB];
   __shared__ int32_t s_start[MAXB];
+  pdl_enter();
   for (int i = threadIdx.x; i <= p.B; i += kThreads) {
     s_rec_pre[i] = p.H * p.tok_pre[i];
     if (i < p.B) {
@@ -98,7 +150,7 @@ flat_kernel(const __grid_constant__ KParams<MAXB> p) {
       const int64_t g = base + u * kThreads;
       cptr[u] = nullptr;
       if (g < p.total) {
-        const int64_t lkv = g / p.lkv_chunks;
+        const int64_t lkv = (int64_t)div64_by((uint64_t)g, (uint64_t)p.lkv_chunks, p.m_HT);
         const int32_t r = (int32_t)(g - lkv * p.lkv_chunks);
         const int32_t rec = LOG2C >= 0 ? (r >> LOG2C) : r / C;  // (b, h, t) record
         const int32_t c = r - rec * C;
@@ -125,6 +177,49 @@ flat_kernel(const __grid_constant__ KParams<MAXB> p) {
   }
 }
 
+// ---- one-token ranges (decode deltas) ----------------------------------------
+
+template <int MAXB>
+struct TokParams {
+  uint4* k;
+  uint4* v;
+  uint4* stg;
+  int64_t layer_chunks;
+  uint32_t total;         // staging chunks
+  uint32_t AH;            // active sequences x heads: records per (layer, K|V)
+  uint64_t m_AH, m_H;     // ceil(2^32 / d) for d = AH, H
+  int32_t l0, H, C, S;
+  int32_t act_b[MAXB];    // sequence of the a-th non-empty range
+  int32_t act_t[MAXB];    // its one token
+};
+
+// Every non-empty range holds one token: staging chunk g is chunk c of record
+// (layer, K|V, a-th non-empty sequence, head).  One chunk per thread, no
+// shared memory, no barrier: the shortest chain from launch to the copy.
+template <bool PACK, int MAXB, int LOG2C>
+__global__ void __launch_bounds__(kThreads)
+token_kernel(const __grid_constant__ TokParams<MAXB> p) {
+  pdl_enter();
+  const uint32_t C = LOG2C >= 0 ? (1u << LOG2C) : (uint32_t)p.C;
+  for (uint32_t g = blockIdx.x * kThreads + threadIdx.x; g < p.total;
+       g += gridDim.x * kThreads) {
+    const uint32_t rec = LOG2C >= 0 ? (g >> LOG2C) : g / C;
+    const uint32_t c = g - rec * C;
+    const uint32_t lkv = div_by(rec, p.AH, p.m_AH);
+    const uint32_t rem = rec - lkv * p.AH;
+    const uint32_t a = div_by(rem, (uint32_t)p.H, p.m_H);
+    const uint32_t h = rem - a * p.H;
+    const int64_t b = p.act_b[a];
+    const int64_t t = p.act_t[a];
+    const int64_t l = p.l0 + (lkv >> 1);
+    const int64_t bh = b * p.H + h;
+    uint4* ptr = (lkv & 1) == 0 ? p.k + l * p.layer_chunks + ((bh * C + c) * p.S + t)
+                                : p.v + l * p.layer_chunks + ((bh * p.S + t) * C + c);
+    if (PACK) p.stg[g] = ld_stream(ptr);
+    else *ptr = ld_stream(p.stg + g);
+  }
+}
+
 // Contiguous run of `cnt` chunks between the cache and staging.
 template <bool PACK>
 __device__ __forceinline__ void copy_run(uint4* cache, uint4* stg, int cnt) {
@@ -147,7 +242,7 @@ __device__ __forceinline__ void copy_run(uint4* cache, uint4* stg, int cnt) {
 }
 
 template <bool PACK, int MAXB, int LOG2C>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, DV_TILE_MIN_BLOCKS)
 tile_kernel(const __grid_constant__ KParams<MAXB> p) {
   extern __shared__ uint4 smem[];  // TB rows of (C | 1) chunks
   constexpr int TB = TileShape<LOG2C>::TB;
@@ -155,9 +250,10 @@ tile_kernel(const __grid_constant__ KParams<MAXB> p) {
   const int32_t C = LOG2C >= 0 ? (1 << LOG2C) : p.C;
   const int32_t SROW = C | 1;
   const int32_t TC = TB * C;  // chunk slots of a full tile
+  pdl_enter();
   for (int64_t tile = blockIdx.x; tile < p.total; tile += gridDim.x) {
     // Uniform across the CTA: which (layer, K|V, sequence, head, token block).
-    const int64_t lkv = tile / p.tiles_per_lkv;
+    const int64_t lkv = (int64_t)div64_by((uint64_t)tile, (uint64_t)p.tiles_per_lkv, p.m_tpl);
     const int32_t r = (int32_t)(tile - lkv * p.tiles_per_lkv);
     const int b = find_seq(p.tile_pre, p.B, r);
     const int32_t len = p.seq_len[b];
@@ -166,19 +262,17 @@ tile_kernel(const __grid_constant__ KParams<MAXB> p) {
     const int32_t h = rr / nblk;
     const int32_t t0 = (rr - h * nblk) << LOG2TB;
     const int32_t n = min(TB, len - t0);  // tokens in this tile
+    uint4* stg = p.stg + lkv * p.lkv_chunks +
+                 ((int64_t)p.H * p.tok_pre[b] + (int64_t)h * len + t0) * C;
     const int32_t cnt = n * C;            // chunks in this tile
     const int64_t l = p.l0 + (lkv >> 1);
     const int64_t bh = (int64_t)b * p.H + h;
-    uint4* stg = p.stg + lkv * p.lkv_chunks +
-                 ((int64_t)p.H * p.tok_pre[b] + (int64_t)h * len + t0) * C;
     if (lkv & 1) {
       uint4* cv = p.v + l * p.layer_chunks + (bh * p.S + p.seq_start[b] + t0) * C;
       copy_run<PACK>(cv, stg, cnt);
-      continue;
-    }
-    // K: row c of this tile starts at ck + c * S.
-    uint4* ck = p.k + l * p.layer_chunks + bh * C * p.S + p.seq_start[b] + t0;
-    if (PACK) {
+    } else if (PACK) {
+      // K: row c of this tile starts at ck + c * S.
+      uint4* ck = p.k + l * p.layer_chunks + bh * C * p.S + p.seq_start[b] + t0;
       for (int q0 = threadIdx.x; q0 < TC; q0 += kThreads * kTileUnroll) {
         uint4 val[kTileUnroll];
 #pragma unroll
@@ -202,6 +296,7 @@ tile_kernel(const __grid_constant__ KParams<MAXB> p) {
       }
       __syncthreads();
     } else {
+      uint4* ck = p.k + l * p.layer_chunks + bh * C * p.S + p.seq_start[b] + t0;
       for (int q0 = threadIdx.x; q0 < cnt; q0 += kThreads * kTileUnroll) {
         uint4 val[kTileUnroll];
 #pragma unroll
@@ -260,6 +355,32 @@ int blocks_per_sm(Kernel kernel, size_t smem, std::atomic<int64_t>& cache) {
   return v;
 }
 
+// Launches `kernel` with programmatic stream serialisation allowed (when
+// DV_PDL), so that it is scheduled while the previous kernel in the stream
+// drains; the kernel's pdl_enter() keeps the ordering.
+template <typename Params>
+cudaError_t launch_kernel(void (*kernel)(Params), unsigned grid, size_t smem,
+                          cudaStream_t stream, const Params& kp) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = DV_PDL ? 1 : 0;
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, kp);
+  return err != cudaSuccess ? err : cudaGetLastError();
+}
+
+// ceil(2^64 / d) for d >= 2; 0 for d <= 1 (div64_by then returns n).
+inline uint64_t div64_magic(uint64_t d) {
+  if (d <= 1) return 0;
+  return (uint64_t)((((unsigned __int128)1 << 64) + d - 1) / d);
+}
+
 template <int MAXB>
 void fill_params(KParams<MAXB>& kp, const Plan& p, void* stg) {
   kp.k = static_cast<uint4*>(p.k);
@@ -287,12 +408,12 @@ cudaError_t run_flat(const Plan& p, void* stg, cudaStream_t stream) {
   fill_params(kp, p, stg);
   kp.total = 2 * (int64_t)(p.l1 - p.l0) * p.lkv_chunks;
   kp.tiles_per_lkv = 0;
+  kp.m_HT = div64_magic((uint64_t)p.lkv_chunks);  // the flat kernel divides by lkv_chunks
   const auto kernel = flat_kernel<PACK, MAXB, LOG2C>;
   const int64_t want = (kp.total + kThreads * kFlatUnroll - 1) / (kThreads * kFlatUnroll);
   const int64_t cap = (int64_t)sm_count() * blocks_per_sm(kernel, 0, occ_cache);
   const unsigned grid = (unsigned)(want < cap ? want : cap);
-  kernel<<<grid, kThreads, 0, stream>>>(kp);
-  return cudaGetLastError();
+  return launch_kernel(kernel, grid, 0, stream, kp);
 }
 
 template <bool PACK, int MAXB, int LOG2C>
@@ -308,17 +429,54 @@ cudaError_t run_tile(const Plan& p, void* stg, cudaStream_t stream) {
   }
   kp.tile_pre[p.B] = acc;
   kp.tiles_per_lkv = acc;
-  kp.total = 2 * (int64_t)(p.l1 - p.l0) * acc;
+  const int64_t tiles = 2 * (int64_t)(p.l1 - p.l0) * acc;
+  kp.total = tiles;
+  kp.m_tpl = div64_magic((uint64_t)kp.tiles_per_lkv);
   const size_t smem = (size_t)TB * (p.C | 1) * sizeof(uint4);
   const auto kernel = tile_kernel<PACK, MAXB, LOG2C>;
   const int64_t cap = (int64_t)sm_count() * blocks_per_sm(kernel, smem, occ_cache);
-  const unsigned grid = (unsigned)(kp.total < cap ? kp.total : cap);
-  kernel<<<grid, kThreads, smem, stream>>>(kp);
-  return cudaGetLastError();
+  const unsigned grid = (unsigned)(tiles < cap ? tiles : cap);
+  return launch_kernel(kernel, grid, smem, stream, kp);
+}
+
+inline uint64_t div_magic(uint32_t d) { return ((1ull << 32) + d - 1) / d; }
+
+template <bool PACK, int MAXB, int LOG2C>
+cudaError_t run_token(const Plan& p, void* stg, cudaStream_t stream) {
+  TokParams<MAXB> kp;
+  kp.k = static_cast<uint4*>(p.k);
+  kp.v = static_cast<uint4*>(p.v);
+  kp.stg = static_cast<uint4*>(stg);
+  kp.layer_chunks = p.layer_chunks;
+  int32_t a = 0;
+  for (int32_t b = 0; b < p.B; ++b) {
+    if (p.seq_len[b] == 0) continue;
+    kp.act_b[a] = b;
+    kp.act_t[a] = p.seq_start[b];
+    ++a;
+  }
+  kp.AH = (uint32_t)(a * p.H);
+  kp.m_AH = div_magic(kp.AH);
+  kp.m_H = div_magic((uint32_t)p.H);
+  kp.total = (uint32_t)(2 * (int64_t)(p.l1 - p.l0) * kp.AH * p.C);
+  kp.l0 = p.l0;
+  kp.H = p.H;
+  kp.C = p.C;
+  kp.S = p.S;
+  const auto kernel = token_kernel<PACK, MAXB, LOG2C>;
+  const unsigned want = (kp.total + kThreads - 1) / kThreads;
+  const unsigned cap = (unsigned)sm_count() * 8;
+  return launch_kernel(kernel, want < cap ? want : cap, 0, stream, kp);
 }
 
 template <bool PACK, int MAXB>
-cudaError_t dispatch_c(const Plan& p, void* stg, cudaStream_t stream, bool tile) {
+cudaError_t dispatch_c(const Plan& p, void* stg, cudaStream_t stream, int kind) {
+  if (kind == kToken) {
+    if (p.C == 8) return run_token<PACK, MAXB, 3>(p, stg, stream);
+    if (p.C == 16) return run_token<PACK, MAXB, 4>(p, stg, stream);
+    return run_token<PACK, MAXB, -1>(p, stg, stream);
+  }
+  const bool tile = kind == kTile;
   if (tile) {
     if (p.C == 8) return run_tile<PACK, MAXB, 3>(p, stg, stream);
     if (p.C == 16) return run_tile<PACK, MAXB, 4>(p, stg, stream);
@@ -332,14 +490,19 @@ cudaError_t dispatch_c(const Plan& p, void* stg, cudaStream_t stream, bool tile)
 template <bool PACK>
 cudaError_t launch(const Plan& p, void* stg, cudaStream_t stream, int variant) {
   if (p.bytes == 0) return cudaSuccess;
-  const bool tile = variant == kTile || (variant == kAuto && auto_uses_tile(p));
-  if (p.B <= kSmallBatch) return dispatch_c<PACK, kSmallBatch>(p, stg, stream, tile);
-  return dispatch_c<PACK, kMaxBatch>(p, stg, stream, tile);
+  int kind = variant;
+  if (variant == kAuto) kind = token_supported(p) ? kToken : auto_uses_tile(p) ? kTile : kFlat;
+  if (p.B <= kSmallBatch) return dispatch_c<PACK, kSmallBatch>(p, stg, stream, kind);
+  return dispatch_c<PACK, kMaxBatch>(p, stg, stream, kind);
 }
 
 }  // namespace
 
 bool tile_supported(const Plan& p) { return p.C <= kMaxTileC; }
+
+bool token_supported(const Plan& p) {
+  return p.max_len <= 1 && 2 * (int64_t)(p.l1 - p.l0) * p.H * p.tokens * p.C < ((int64_t)1 << 31);
+}
 
 bool auto_uses_tile(const Plan& p) {
   if (!tile_supported(p) || p.active == 0) return false;

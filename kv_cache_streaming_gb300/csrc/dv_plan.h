@@ -42,12 +42,15 @@ inline void restrict_layers(Plan& p, int32_t la, int32_t lb) {
 // Bytes of one layer's slab of the staging buffer.
 inline int64_t layer_slab_bytes(const Plan& p) { return 2 * p.lkv_chunks * 16; }
 
-enum Variant { kAuto = 0, kFlat = 1, kTile = 2 };
+enum Variant { kAuto = 0, kFlat = 1, kTile = 2, kToken = 3 };
 
 // Kernel choice of kAuto (the tile kernel pays off once ranges are long).
 bool auto_uses_tile(const Plan& p);
 // Whether the tile kernel handles this geometry (C <= 64).
 bool tile_supported(const Plan& p);
+// Whether the one-token kernel handles these ranges (every range at most one
+// token long; fewer than 2^31 staging chunks).
+bool token_supported(const Plan& p);
 
 // `stg` is the device-visible address of the staging bytes (device memory or
 // mapped pinned host memory).  Both return cudaSuccess without launching

@@ -20,7 +20,7 @@ library_path = PKG / "libdv.so"
 DV_MAX_BATCH = 1024
 (DV_OK, DV_ERR_INVALID_ARG, DV_ERR_RANGE, DV_ERR_BUFFER_TOO_SMALL, DV_ERR_MISALIGNED,
  DV_ERR_CUDA, DV_ERR_TIMEOUT, DV_ERR_UNSUPPORTED) = range(8)
-DV_VARIANT_AUTO, DV_VARIANT_FLAT, DV_VARIANT_TILE = 0, 1, 2
+DV_VARIANT_AUTO, DV_VARIANT_FLAT, DV_VARIANT_TILE, DV_VARIANT_TOKEN = 0, 1, 2, 3
 
 if not library_path.exists():
     raise ImportError(f"{library_path} is missing: build it with "

@@ -40,6 +40,11 @@ def range_sets(g, rng):
     return out
 
 
+def variants_for(s, e):
+    one_token = (np.asarray(e) - np.asarray(s)).max() <= 1
+    return VARIANTS + ([dv.DV_VARIANT_TOKEN] if one_token else [])
+
+
 def check_pack_unpack(g, cache, kh, vh, l0, l1, s, e, variant):
     n = ORC.staging_bytes(g, l0, l1, s, e)
     dst = H.device_bytes(n + 64, fill=0xEE)
@@ -65,7 +70,7 @@ def test_gpu_fill_matches_host_generator():
         assert np.array_equal(H.to_np(c.k), kh) and np.array_equal(H.to_np(c.v), vh)
 
 
-@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("variant", VARIANTS + [dv.DV_VARIANT_TOKEN])
 def test_tiny_workload(variant):
     """Tiny cache: prompt [0,37), then the decode token at 37; unpack into a
     zeroed cache."""
@@ -74,6 +79,8 @@ def test_tiny_workload(variant):
     cache = H.device_cache(g, fill=(kh, vh))
     (ps, pe), (ds, de) = tiny_ranges()
     for s, e in ((ps, pe), (ds, de)):
+        if variant == dv.DV_VARIANT_TOKEN and (e - s).max() > 1:
+            continue
         n = ORC.staging_bytes(g, 0, g.num_layers, s, e)
         dst = H.device_bytes(n)
         dv.dv_kv_pack(cache, 0, g.num_layers, s, e, dst, variant=variant)
@@ -93,7 +100,7 @@ def test_pack_unpack_geometries(g):
     cache = H.device_cache(g, fill=(kh, vh))
     for name, s, e in range_sets(g, rng):
         for l0, l1 in ((0, g.num_layers), (g.num_layers - 1, g.num_layers)):
-            for variant in VARIANTS:
+            for variant in variants_for(s, e):
                 check_pack_unpack(g, cache, kh, vh, l0, l1, s, e, variant)
 
 
@@ -247,6 +254,9 @@ def test_errors_with_real_buffers_enqueue_nothing():
         assert _status(lambda: dv.dv_kv_pack(big, huge_layers - 1, huge_layers, sb, eb,
                                              (dst.data_ptr(), nb // 2))) == \
             dv.DV_ERR_BUFFER_TOO_SMALL
+    # the one-token kernel refuses longer ranges
+    assert _status(lambda: dv.dv_kv_pack(cache, 0, 2, s, e, dst,
+                                         variant=dv.DV_VARIANT_TOKEN)) == dv.DV_ERR_UNSUPPORTED
     # staging smaller than one layer slab
     host = H.pinned(n)
     tiny_stg = H.device_bytes(n // 4)
