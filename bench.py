@@ -58,6 +58,17 @@ def parse_args():
     return ap.parse_args()
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
+# tile kernels, from one ncu capture of an 8-layer launch of this workload's
+# shape (`--kernel-case tile-pack` / `tile-unpack`), scaled by 1/8 to one
+# layer (traffic grows with the tiles processed).  Set an entry to None when
+# the kernel changes, until it is captured again.
+TRAFFIC_PER_LAUNCH = {
+    "pack prompt layer (tile kernel)": (409.628928e6 + 351.752192e6) / 8,
+    "unpack prompt layer (tile kernel)": (409.681664e6 + 351.681536e6) / 8,
+}
+
+
 def peaks():
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
@@ -373,15 +384,18 @@ class Bench:
                       torch.empty(self.slab, dtype=torch.uint8, device="cuda"))
         self.copy_stream = torch.cuda.Stream()
         self.in_stream = torch.cuda.Stream()
+        self.in_staging = torch.empty(self.slab, dtype=torch.uint8, device="cuda")
         self.streamer = dv.Streamer(self.slots[0], self.slots[1], self.stream, self.copy_stream)
         self.replica = dv.Replica(self.arena, g.batch)
 
     def e2e_step(self):
         """Layer by layer: the streamer packs layer l and copies it to pinned
-        host memory; as soon as that copy is done, layer l is swapped in from
-        the host into the second cache on a third stream, so host-to-device
-        traffic of layer l overlaps device-to-host traffic of layer l+1.  Then
-        the 24 deltas go to the host replica and are restored from it."""
+        host memory (copy engine); as soon as that copy is done, layer l is
+        swapped in from the host into the second cache on a third stream,
+        staged through a device buffer so that a copy engine carries it too:
+        host-to-device traffic of layer l overlaps device-to-host traffic of
+        layer l+1 on the full-duplex link.  Then the 24 deltas go to the host
+        replica (fused pack into host memory) and are restored from it."""
         dv, g = self.dv, self.g
         s, si = self.stream, self.in_stream
         hp = self.host_prompt.data_ptr()
@@ -389,12 +403,12 @@ class Bench:
             self.streamer.stream_layer(self.cache, l, self.ps, self.pe, self.host_prompt, l0=0)
             si.wait_stream(self.copy_stream)
             dv.dv_swap_in(self.cache_b, l, l + 1, self.ps, self.pe, (hp + l * self.slab, self.slab),
-                          stream=si)
+                          staging=self.in_staging, stream=si)
         self.replica.truncate(0)
         for k, (a, b) in enumerate(self.deltas):
             self.replica.append(self.cache, 0, g.num_layers, a, b, step=k, stream=s)
         si.wait_stream(s)
-        self.replica.restore(self.cache_b, stream=si)
+        self.replica.restore(self.cache_b, staging=self.in_staging, stream=si)
         s.wait_stream(si)
 
     def timed_e2e(self, steps, warmup, world):
@@ -439,6 +453,19 @@ class Bench:
         res = {"payload_bytes": n}
         res["link_d2h_gbs"] = n / timed(lambda: host.copy_(dev, non_blocking=True)) / 1e9
         res["link_h2d_gbs"] = n / timed(lambda: dev.copy_(host, non_blocking=True)) / 1e9
+        host2 = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+        dev2 = torch.empty(n, dtype=torch.uint8, device="cuda")
+        s2 = torch.cuda.Stream()
+
+        def both():
+            s2.wait_stream(s)
+            host.copy_(dev, non_blocking=True)
+            with torch.cuda.stream(s2):
+                dev2.copy_(host2, non_blocking=True)
+            s.wait_stream(s2)
+
+        res["link_bidir_gbs"] = 2 * n / timed(both) / 1e9
+        del host2, dev2
         for name, stg in (("fused", None), ("staged", staging)):
             t_out = timed(lambda: dv.dv_swap_out(self.cache, 0, g.num_layers, zs, full, host,
                                                  staging=stg, stream=s))
@@ -508,7 +535,7 @@ def run_mine(args):
                    "kernel_timing": "per launch kind: its launches of one step in a CUDA graph, L2 flushed before each replay, median of 5"},
         "roofline": {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1),
                      "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                     "peak_kind": peak_kind, "traffic": None,
+                     "peak_kind": peak_kind, "traffic": TRAFFIC_PER_LAUNCH.get(name),
                      "algorithmic_bytes_per_launch": nbytes,
                      "avg_launch_us": round(t_launch * 1e6, 2)},
         "kernels": [{"kernel": n_, "avg_launch_us": round(t * 1e6, 2),
@@ -517,9 +544,10 @@ def run_mine(args):
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "path": "per layer: dv_stream_layer (pack + D2H) then dv_swap_in of that layer "
-                        "on a third stream (H2D overlaps the next layer's D2H); "
-                        "dv_replica_append x24 (fused) + dv_replica_restore (fused)"},
+                "path": "per layer: dv_stream_layer (pack + D2H copy) then dv_swap_in of that "
+                        "layer (H2D copy + unpack) on a third stream, overlapping the next "
+                        "layer's D2H; dv_replica_append x24 (fused) + dv_replica_restore "
+                        "(staged)"},
         "swap": swap,
         "gpu_launches": b.launches_per_step * args.steps,
         "clocks": clk,
