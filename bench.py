@@ -79,7 +79,9 @@ def peaks():
 
 # ---- distributed plumbing (one process per GPU; no data-path collective) ------
 
-def dist_init(n):
+def dist_init(backend=None):
+    """(rank, world, local_rank) from the torchrun environment; joins the
+    process group (NCCL on GPUs, gloo when asked) when world > 1."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if world <= 1:
         return 0, 1, 0
@@ -87,8 +89,12 @@ def dist_init(n):
     import torch.distributed as td
     rank = int(os.environ["RANK"])
     local = int(os.environ.get("LOCAL_RANK", rank))
-    torch.cuda.set_device(local)
-    td.init_process_group("nccl", device_id=torch.device("cuda", local))
+    backend = backend or "nccl"
+    if backend == "nccl":
+        torch.cuda.set_device(local)
+        td.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        td.init_process_group(backend)
     return rank, world, local
 
 
@@ -99,13 +105,21 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """The largest `x` over all ranks (the slowest rank's time)."""
     if world <= 1:
         return x
     import torch
     import torch.distributed as td
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if td.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     td.all_reduce(t, op=td.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(bytes_per_step, steps, max_secs, world):
+    """GB/s of all ranks together: every rank moves the same bytes per step
+    (weak scaling), timed by the slowest rank."""
+    return world * bytes_per_step * steps / max_secs / 1e9
 
 
 # ---- clocks ------------------------------------------------------------------
@@ -483,7 +497,7 @@ class Bench:
 
 def run_mine(args):
     import torch
-    rank, world, local = dist_init(args.gpus)
+    rank, world, local = dist_init()
     if world == 1:
         torch.cuda.set_device(0)
     import __graft_entry__
@@ -498,7 +512,7 @@ def run_mine(args):
     secs = b.timed_value(args.steps, max(args.warmup, 3), world)
     clk = clocks.stop()
     secs = max_over_ranks(secs, world)
-    value = world * b.bytes_per_step * args.steps / secs / 1e9
+    value = whole_job_rate(b.bytes_per_step, args.steps, secs, world)
     serial = b.timed_serial()
     # kernel roofline, live
     kt = b.kernel_times()
@@ -510,7 +524,7 @@ def run_mine(args):
     b.setup_e2e()
     e2e_steps = max(3, min(args.steps, 10))
     e2e_secs = max_over_ranks(b.timed_e2e(e2e_steps, 2, world), world)
-    e2e_value = world * b.bytes_per_step * e2e_steps / e2e_secs / 1e9
+    e2e_value = whole_job_rate(b.bytes_per_step, e2e_steps, e2e_secs, world)
     h2d = d2h = b.g.num_layers * b.slab + GPT2_DECODE_STEPS * b.dsz
     swap = None if args.no_swap else b.swap_section()
     cpu = None
