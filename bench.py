@@ -495,6 +495,59 @@ class Bench:
         return {k: (round(v, 3) if isinstance(v, float) else v) for k, v in res.items()}
 
 
+def naive_vs_buffered(torch, dv, reps=3):
+    """The pages' one microbenchmark claim (buffered copy vs many small copies,
+    §5.1, Fig 11) on GB300: one decode step's delta moved to pinned host memory
+    (a) with one copy call per contiguous region (dv_naive_gather) and (b) as
+    one pack into device staging plus one copy (the buffered copy), for the
+    GPT2-1.5B-shaped cache and one OPT-66B-stage microbatch.  Wall time of the
+    calls plus the stream, median of `reps`."""
+    from synth.configs import OPT66B_STAGE, opt66b_microbatches
+    from synth import gpu as synth_gpu
+    out = {}
+    s = torch.cuda.Stream()
+    for name, g, pos in (("gpt2-1.5b delta", GPT2, np.full(GPT2.batch, GPT2_PROMPT, np.int32)),
+                         ("opt-66b-stage delta", OPT66B_STAGE, opt66b_microbatches()[0][0])):
+        k = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+        v = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+        synth_gpu.fill_cache(g, k, v, seed_of(4))
+        cache = dv.Cache.from_geometry(g, k, v)
+        e = pos + 1
+        n = dv.dv_staging_bytes(cache, 0, g.num_layers, pos, e)
+        host_a = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+        host_b = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+        stg = torch.empty(n, dtype=torch.uint8, device="cuda")
+        torch.cuda.synchronize()
+
+        def naive():
+            return dv.dv_naive_gather(cache, 0, g.num_layers, pos, e, host_a, stream=s)
+
+        def buffered():
+            dv.dv_kv_pack(cache, 0, g.num_layers, pos, e, stg, stream=s)
+            with torch.cuda.stream(s):
+                host_b.copy_(stg, non_blocking=True)
+
+        def wall(fn):
+            ts = []
+            for _ in range(reps + 1):
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                fn()
+                s.synchronize()
+                ts.append(time.perf_counter() - t0)
+            return statistics.median(ts[1:])
+
+        calls = naive()
+        t_naive, t_buf = wall(naive), wall(buffered)
+        same = bool(torch.equal(host_a, host_b))
+        out[name] = {"bytes": n, "naive_copies": calls, "naive_ms": round(t_naive * 1e3, 3),
+                     "buffered_ms": round(t_buf * 1e3, 4),
+                     "speedup": round(t_naive / t_buf, 1), "same_bytes": same}
+        del k, v, cache, host_a, host_b, stg
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_mine(args):
     import torch
     rank, world, local = dist_init()
@@ -527,6 +580,7 @@ def run_mine(args):
     e2e_value = whole_job_rate(b.bytes_per_step, e2e_steps, e2e_secs, world)
     h2d = d2h = b.g.num_layers * b.slab + GPT2_DECODE_STEPS * b.dsz
     swap = None if args.no_swap else b.swap_section()
+    naive = None if args.no_swap else naive_vs_buffered(b.torch, b.dv)
     cpu = None
     if rank == 0:
         smp = OracleSample(8)
@@ -563,6 +617,7 @@ def run_mine(args):
                         "layer's D2H; dv_replica_append x24 (fused) + dv_replica_restore "
                         "(staged)"},
         "swap": swap,
+        "naive_vs_buffered": naive,
         "gpu_launches": b.launches_per_step * args.steps,
         "clocks": clk,
     }

@@ -149,6 +149,18 @@ dv_status dv_kv_unpack_variant(const dv_cache* cache, int32_t l0, int32_t l1,
                                const void* src, size_t src_bytes, dv_stream stream,
                                int32_t variant);
 
+/* The naive transfer the pages measure buffered copies against (§5.1, Fig 11:
+ * "many cudaMemcpy calls" for the small non-contiguous regions): the same bytes
+ * as dv_kv_pack written to `dst` (device or pinned host memory) with one
+ * cudaMemcpyAsync per contiguous V run and one cudaMemcpy2DAsync per K token
+ * (when a range holds fewer tokens than C = head_dim*elem_bytes/16) or per K
+ * chunk row (otherwise), and no kernel.  It exists to be timed against
+ * dv_kv_pack plus one copy; *num_copies (may be NULL) receives the number of
+ * copy calls it enqueued. */
+dv_status dv_naive_gather(const dv_cache* cache, int32_t l0, int32_t l1,
+                          const int32_t* seq_start, const int32_t* seq_end, void* dst,
+                          size_t dst_bytes, dv_stream stream, int64_t* num_copies);
+
 /* Swap-out (§3 microbatch swapping, Fig 9; Table 1 flush).  Leaves the
  * staging bytes of (l0, l1, ranges) in `host_dst` (pinned host memory,
  * host_bytes at least dv_staging_bytes).

@@ -410,6 +410,61 @@ dv_status dv_kv_unpack_variant(const dv_cache* cache, int32_t l0, int32_t l1,
   return do_unpack(cache, l0, l1, seq_start, seq_end, src, src_bytes, stream, variant);
 }
 
+dv_status dv_naive_gather(const dv_cache* cache, int32_t l0, int32_t l1,
+                          const int32_t* seq_start, const int32_t* seq_end, void* dst,
+                          size_t dst_bytes, dv_stream stream, int64_t* num_copies) {
+  if (num_copies) *num_copies = 0;
+  dv::Plan p;
+  dv_status st = plan_ranges(cache, l0, l1, seq_start, seq_end, &p);
+  if (st != DV_OK) return st;
+  if (p.bytes == 0) return DV_OK;
+  if (dst_bytes < (size_t)p.bytes)
+    return fail(DV_ERR_BUFFER_TOO_SMALL, "gather needs %lld bytes, dst has %zu",
+                (long long)p.bytes, dst_bytes);
+  if ((st = resolve_cache(cache, &p)) != DV_OK) return st;
+  void* d = nullptr;
+  if ((st = resolve(dst, (size_t)p.bytes, true, "dst", &d)) != DV_OK) return st;
+  const int64_t row = (int64_t)p.D * p.P;  // bytes of one token of one head
+  const int64_t S16 = (int64_t)p.S * 16;
+  const uint8_t* kb = static_cast<const uint8_t*>(p.k);
+  const uint8_t* vb = static_cast<const uint8_t*>(p.v);
+  uint8_t* out = static_cast<uint8_t*>(dst);
+  int64_t off = 0, calls = 0;
+  cudaError_t err = cudaSuccess;
+  for (int64_t l = l0; l < l1 && err == cudaSuccess; ++l)
+    for (int kv = 0; kv < 2 && err == cudaSuccess; ++kv)
+      for (int64_t b = 0; b < p.B && err == cudaSuccess; ++b) {
+        const int64_t len = p.seq_len[b];
+        for (int64_t h = 0; h < p.H && len > 0 && err == cudaSuccess; ++h) {
+          const int64_t bh = b * p.H + h;
+          if (kv == 1) {  // one contiguous run
+            const uint8_t* src = vb + (l * p.layer_chunks * 16) + (bh * p.S + p.seq_start[b]) * row;
+            err = cudaMemcpyAsync(out + off, src, (size_t)(len * row), cudaMemcpyDefault, stream);
+            ++calls;
+          } else if (len < p.C) {  // per token: C chunks S*16 bytes apart -> C contiguous
+            for (int64_t t = 0; t < len && err == cudaSuccess; ++t) {
+              const uint8_t* src =
+                  kb + (l * p.layer_chunks + bh * p.C * p.S + p.seq_start[b] + t) * 16;
+              err = cudaMemcpy2DAsync(out + off + t * row, 16, src, (size_t)S16, 16, (size_t)p.C,
+                                      cudaMemcpyDefault, stream);
+              ++calls;
+            }
+          } else {  // per chunk row: len contiguous chunks -> every C-th chunk
+            for (int64_t c = 0; c < p.C && err == cudaSuccess; ++c) {
+              const uint8_t* src =
+                  kb + (l * p.layer_chunks + (bh * p.C + c) * p.S + p.seq_start[b]) * 16;
+              err = cudaMemcpy2DAsync(out + off + c * 16, (size_t)row, src, 16, 16, (size_t)len,
+                                      cudaMemcpyDefault, stream);
+              ++calls;
+            }
+          }
+          off += len * row;
+        }
+      }
+  if (num_copies) *num_copies = calls;
+  return err == cudaSuccess ? DV_OK : cuda_fail(err, "naive gather copy");
+}
+
 dv_status dv_swap_out(const dv_cache* cache, int32_t l0, int32_t l1, const int32_t* seq_start,
                       const int32_t* seq_end, void* host_dst, size_t host_bytes, void* staging,
                       size_t staging_bytes, dv_stream stream) {

@@ -62,6 +62,7 @@ _unpack = _sig("dv_kv_unpack_variant", _RANGE + [_P, _SZ, _P, _I32])
 _swap_out = _sig("dv_swap_out", _RANGE + [_P, _SZ, _P, _SZ, _P])
 _swap_in = _sig("dv_swap_in", _RANGE + [_P, _SZ, _P, _SZ, _P])
 _swap_out_noalloc = _sig("dv_swap_out_noalloc", _RANGE + [_P, _SZ, _P])
+_naive_gather = _sig("dv_naive_gather", _RANGE + [_P, _SZ, _P, ctypes.POINTER(_I64)])
 DV_NOALLOC_STAGING_BYTES = 64 << 20
 _streamer_create = _sig("dv_streamer_create", [ctypes.POINTER(_P), _P, _P, _SZ, _P, _P])
 _stream_layer = _sig("dv_stream_layer", [_P, _CP, _I32, _I32P, _I32P, _P, _SZ, _I32])
@@ -182,6 +183,16 @@ def dv_kv_unpack(cache: Cache, l0, l1, seq_start, seq_end, src, stream=None,
     s, e, sp, ep = _ranges(seq_start, seq_end)
     d, n = _buf(src, src_bytes)
     _check(_unpack(cache.ref, l0, l1, sp, ep, d, n, _stream(stream), variant))
+
+
+def dv_naive_gather(cache: Cache, l0, l1, seq_start, seq_end, dst, stream=None,
+                    dst_bytes=None) -> int:
+    """The per-region copy baseline; returns the number of copies enqueued."""
+    s, e, sp, ep = _ranges(seq_start, seq_end)
+    d, n = _buf(dst, dst_bytes)
+    calls = _I64(0)
+    _check(_naive_gather(cache.ref, l0, l1, sp, ep, d, n, _stream(stream), ctypes.byref(calls)))
+    return calls.value
 
 
 def dv_swap_out(cache: Cache, l0, l1, seq_start, seq_end, host_dst, staging=None,

@@ -266,3 +266,25 @@ def test_errors_with_real_buffers_enqueue_nothing():
     assert _status(lambda: dv.dv_swap_out(cache, 0, 2, s, e, dst)) == dv.DV_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert (H.to_np(dst) == 0x44).all()  # no failed call wrote anything
+
+
+def test_naive_gather_matches_the_pack():
+    """The per-region copy baseline writes the staging bytes of the pack, for
+    ranges shorter than C (per-token copies) and longer (per-row copies), to
+    device memory and to pinned host memory."""
+    g = Geometry("naive", 3, 3, 2, 128, 64, 2, "fp16")  # C = 16
+    kh, vh = H.host_cache(g, 41)
+    cache = H.device_cache(g, fill=(kh, vh))
+    cases = [(np.array([5, 0, 9], np.int32), np.array([6, 0, 12], np.int32)),   # < C tokens
+             (np.array([0, 3, 10], np.int32), np.array([40, 64, 30], np.int32))]  # >= C tokens
+    for s, e in cases:
+        n = ORC.staging_bytes(g, 0, g.num_layers, s, e)
+        want = ORC.pack(g, kh, vh, 0, g.num_layers, s, e)
+        dst = H.device_bytes(n)
+        calls = dv.dv_naive_gather(cache, 0, g.num_layers, s, e, dst)
+        assert calls > 0
+        assert np.array_equal(H.to_np(dst)[:n], want)
+        host = H.pinned(n)
+        dv.dv_naive_gather(cache, 0, g.num_layers, s, e, host)
+        torch.cuda.synchronize()
+        assert np.array_equal(host.numpy()[:n], want)
