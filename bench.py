@@ -548,6 +548,92 @@ def naive_vs_buffered(torch, dv, reps=3):
     return out
 
 
+class DecodeStreaming:
+    """Decode steps with the step's delta streamed to a host replica (§3 "Token
+    computation and streaming parallelization", Fig 7c).  A decode step is a
+    stand-in compute (a full read of the cache's K and V, as attention reads
+    them, reduced on the device) followed by the decode write of the new token
+    (an unpack of a seeded one-token buffer).  The delta of step i is packed
+    straight into pinned host memory, either on the compute stream after the
+    step ("inline") or on a side stream that waits only for step i's write
+    ("overlapped"), so that it runs while step i+1 computes.  Each mode's
+    `steps` decode steps are one CUDA graph."""
+
+    def __init__(self, torch, dv, steps=GPT2_DECODE_STEPS):
+        from synth import gpu as synth_gpu
+        self.torch, self.dv, self.steps = torch, dv, steps
+        g = self.g = GPT2
+        self.k = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+        self.v = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+        synth_gpu.fill_cache(g, self.k, self.v, seed_of(2))
+        self.cache = dv.Cache.from_geometry(g, self.k, self.v)
+        (_, _), self.deltas = gpt2_ranges()
+        self.dsz = dv.dv_staging_bytes(self.cache, 0, g.num_layers, *self.deltas[0])
+        self.tokens = torch.empty(steps * self.dsz, dtype=torch.uint8, device="cuda")
+        synth_gpu.fill_tensor(self.tokens, 777, 0, g.kind)
+        self.host = torch.empty(steps * self.dsz, dtype=torch.uint8, pin_memory=True)
+        self.acc = torch.zeros(1, dtype=torch.int64, device="cuda")
+        self.kv32 = (self.k.view(torch.int32), self.v.view(torch.int32))
+        self.s_side = torch.cuda.Stream()
+        self.events = [torch.cuda.Event() for _ in range(steps)]
+
+    def _compute_and_write(self, i, s):
+        torch, dv, g = self.torch, self.dv, self.g
+        self.acc += self.kv32[0].sum(dtype=torch.int64) + self.kv32[1].sum(dtype=torch.int64)
+        a, b = self.deltas[i]
+        tok = self.tokens[i * self.dsz:(i + 1) * self.dsz]
+        dv.dv_kv_unpack(self.cache, 0, g.num_layers, a, b, tok, stream=s)
+
+    def run(self, mode, s):
+        """Enqueues `steps` decode steps on stream `s` (inside a capture or not)."""
+        dv, g = self.dv, self.g
+        hp = self.host.data_ptr()
+        for i in range(self.steps):
+            self._compute_and_write(i, s)
+            a, b = self.deltas[i]
+            dst = (hp + i * self.dsz, self.dsz)
+            if mode == "inline":
+                dv.dv_kv_pack(self.cache, 0, g.num_layers, a, b, dst, stream=s)
+            elif mode == "overlapped":
+                self.events[i].record(s)
+                self.s_side.wait_event(self.events[i])
+                dv.dv_kv_pack(self.cache, 0, g.num_layers, a, b, dst, stream=self.s_side)
+        if mode == "overlapped":
+            s.wait_stream(self.s_side)
+
+    def measure(self, reps=5):
+        torch = self.torch
+        s = torch.cuda.Stream()
+        out = {}
+        for mode in ("compute_only", "inline", "overlapped"):
+            with torch.cuda.stream(s):
+                self.run(mode, s)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=s, capture_error_mode="relaxed"):
+                self.run(mode, s)
+            ts = []
+            with torch.cuda.stream(s):
+                for r in range(reps + 1):
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(s)
+                    graph.replay()
+                    b.record(s)
+                    torch.cuda.synchronize()
+                    if r:
+                        ts.append(a.elapsed_time(b))
+            out[mode] = statistics.median(ts) / self.steps
+            del graph
+        same = bool(torch.equal(self.host.cuda(), self.tokens))
+        base = out["compute_only"]
+        return {"steps": self.steps, "delta_bytes": self.dsz,
+                "step_ms": {k: round(v, 4) for k, v in out.items()},
+                "overhead_inline": round(out["inline"] / base - 1, 4),
+                "overhead_overlapped": round(out["overlapped"] / base - 1, 4),
+                "replica_equals_written_tokens": same}
+
+
 def run_mine(args):
     import torch
     rank, world, local = dist_init()
@@ -581,6 +667,7 @@ def run_mine(args):
     h2d = d2h = b.g.num_layers * b.slab + GPT2_DECODE_STEPS * b.dsz
     swap = None if args.no_swap else b.swap_section()
     naive = None if args.no_swap else naive_vs_buffered(b.torch, b.dv)
+    streaming = None if args.no_swap else DecodeStreaming(b.torch, b.dv).measure()
     cpu = None
     if rank == 0:
         smp = OracleSample(8)
@@ -618,6 +705,7 @@ def run_mine(args):
                         "(staged)"},
         "swap": swap,
         "naive_vs_buffered": naive,
+        "decode_streaming": streaming,
         "gpu_launches": b.launches_per_step * args.steps,
         "clocks": clk,
     }
