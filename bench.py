@@ -634,6 +634,191 @@ class DecodeStreaming:
                 "replica_equals_written_tokens": same}
 
 
+class MicrobatchSwapping:
+    """Microbatch swapping on the OPT-66B-stage workload (§3 "Microbatch
+    swapping", Fig 9): N = 4 microbatches share the GPU; each microbatch's
+    cache lives in a host replica (a snapshot of its prompt cache plus one
+    record per decode step: the swap-out is delta-only).  A round processes
+    the microbatches in turn: swap-in (restore snapshot + deltas into a device
+    slot, copy engine + unpack), a stand-in compute (a read of the used bytes
+    of the slot, as attention reads them) and the decode write of one token
+    per active sequence, then the swap-out of that token (a one-token pack
+    straight into the replica).
+      serial: one device slot, everything in order on one stream.
+      double: two slots (the pages' 2*M); while microbatch x computes in one
+              slot, the other slot takes x-1's swap-out and then x+1's
+              swap-in on a second, high-priority stream, ordered by events."""
+
+    def __init__(self, torch, dv, rounds=3, keep_refs=False):
+        from synth import gpu as synth_gpu
+        from synth.configs import OPT66B_STAGE, opt66b_microbatches
+        self.torch, self.dv, self.rounds = torch, dv, rounds
+        g = self.g = OPT66B_STAGE
+        self.synth_gpu = synth_gpu
+        self.mbs = opt66b_microbatches()
+        self.N = len(self.mbs)
+        L = g.num_layers
+        self.zs = np.zeros(g.batch, np.int32)
+        self.slots = [dv.Cache.from_geometry(
+            g, torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda"),
+            torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")) for _ in range(2)]
+        self.per_token = dv.dv_staging_bytes(self.slots[0], 0, L, self.zs,
+                                             np.ones(g.batch, np.int32)) // g.batch
+        self.staging = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+        self.refs = []
+        self.replicas, self.arenas, self.lens, self.seeds = [], [], [], []
+        for m, (p, o) in enumerate(self.mbs):
+            seed = seed_of(4) * 10 + m
+            cap = int((p.sum() + g.batch * rounds) * self.per_token)
+            arena = torch.empty(cap, dtype=torch.uint8, pin_memory=True)
+            rep = dv.Replica(arena, g.batch)
+            slot = self.slots[0]
+            synth_gpu.fill_cache(g, slot.k, slot.v, seed)
+            rep.append(slot, 0, L, self.zs, p, step=0)  # the prompt cache arrives
+            if keep_refs:
+                k2 = slot.k.clone()
+                v2 = slot.v.clone()
+                self.refs.append(dv.Cache.from_geometry(g, k2, v2))
+            torch.cuda.synchronize()
+            self.arenas.append(arena)
+            self.replicas.append(rep)
+            self.lens.append(p.copy())
+            self.seeds.append(seed)
+        self.step_no = [1] * self.N
+        self.tok = torch.empty(g.batch * self.per_token, dtype=torch.uint8, device="cuda")
+        self.acc = torch.zeros(1, dtype=torch.int64, device="cuda")
+
+    def _compute_and_write(self, m, slot, s):
+        """Stand-in compute on stream s, then the decode write of microbatch m's
+        next token into `slot` and the delta appended to its replica."""
+        torch, dv, g = self.torch, self.dv, self.g
+        p, o = self.mbs[m]
+        ln = self.lens[m]
+        used = int(ln.sum()) * self.per_token  # bytes a decode step would read
+        with torch.cuda.stream(s):
+            self.acc += slot.k[:used // 2].view(torch.int32).sum(dtype=torch.int64)
+            self.acc += slot.v[:used // 2].view(torch.int32).sum(dtype=torch.int64)
+        act = ((ln - p) < o).astype(np.int32)
+        nt = dv.dv_staging_bytes(slot, 0, g.num_layers, ln, ln + act)
+        if nt:
+            tok = self.tok[:nt]
+            with torch.cuda.stream(s):
+                self.synth_gpu.fill_tensor(tok, 1000 * m + self.step_no[m], 0, g.kind, s)
+            dv.dv_kv_unpack(slot, 0, g.num_layers, ln, ln + act, tok, stream=s)
+            if self.refs:
+                dv.dv_kv_unpack(self.refs[m], 0, g.num_layers, ln, ln + act, tok, stream=s)
+        return act
+
+    def run(self, mode, s, s2=None):
+        """`rounds` rounds over the N microbatches; returns the seconds taken."""
+        torch, dv, g = self.torch, self.dv, self.g
+        L = g.num_layers
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        if mode == "serial":
+            slot = self.slots[0]
+            for _ in range(self.rounds):
+                for m in range(self.N):
+                    self.replicas[m].restore(slot, staging=self.staging, stream=s)
+                    act = self._compute_and_write(m, slot, s)
+                    ln = self.lens[m]
+                    self.replicas[m].append(slot, 0, L, ln, ln + act, step=self.step_no[m],
+                                            stream=s)
+                    self.lens[m] = ln + act
+                    self.step_no[m] += 1
+        else:
+            ready = [torch.cuda.Event() for _ in range(2)]
+            done = [torch.cuda.Event() for _ in range(2)]
+            order = [m for _ in range(self.rounds) for m in range(self.N)]
+            # prefetch the first microbatch into slot 0
+            self.replicas[order[0]].restore(self.slots[0], staging=self.staging, stream=s2)
+            ready[0].record(s2)
+            for i, m in enumerate(order):
+                sl = i % 2
+                slot = self.slots[sl]
+                s.wait_event(ready[sl])
+                act = self._compute_and_write(m, slot, s)
+                done[sl].record(s)
+                if i + 1 < len(order):  # the next microbatch comes in on the other slot
+                    nxt = order[i + 1]
+                    self.replicas[nxt].restore(self.slots[1 - sl], staging=self.staging,
+                                               stream=s2)
+                    ready[1 - sl].record(s2)
+                # swap-out of this microbatch's step: its token, into its replica
+                s2.wait_event(done[sl])
+                ln = self.lens[m]
+                self.replicas[m].append(slot, 0, L, ln, ln + act, step=self.step_no[m],
+                                        stream=s2)
+                self.lens[m] = ln + act
+                self.step_no[m] += 1
+                # the slot is refilled two microbatches later, after this append
+            s.wait_stream(s2)
+        torch.cuda.synchronize()
+        return time.perf_counter() - t0
+
+    def check(self):
+        """Each replica restored into a zeroed slot equals the reference cache on
+        the used prefix (needs keep_refs)."""
+        torch, dv, g = self.torch, self.dv, self.g
+        L = g.num_layers
+        for m in range(self.N):
+            slot = self.slots[0]
+            slot.k.zero_()
+            slot.v.zero_()
+            self.replicas[m].restore(slot, staging=self.staging)
+            n = dv.dv_staging_bytes(slot, 0, L, self.zs, self.lens[m])
+            a = torch.empty(n, dtype=torch.uint8, device="cuda")
+            b = torch.empty(n, dtype=torch.uint8, device="cuda")
+            dv.dv_kv_pack(slot, 0, L, self.zs, self.lens[m], a)
+            dv.dv_kv_pack(self.refs[m], 0, L, self.zs, self.lens[m], b)
+            torch.cuda.synchronize()
+            if not torch.equal(a, b):
+                return False
+        return True
+
+    def reset(self):
+        """Back to the prompt caches: every replica keeps its snapshot only."""
+        for m, (p, o) in enumerate(self.mbs):
+            self.replicas[m].truncate(1)
+            self.lens[m] = p.copy()
+            self.step_no[m] = 1
+
+    def measure(self):
+        torch = self.torch
+        # the swap stream runs at high priority: its short unpack kernels then
+        # get SMs ahead of the compute, so its copy-engine pipeline never stalls
+        s, s2 = torch.cuda.Stream(), torch.cuda.Stream(priority=-1)
+        t_serial = self.run("serial", s)
+        self.reset()
+        t_double = self.run("double", s, s2)
+        steps = self.rounds * self.N
+        # the parts on their own: a swap-in (restore) and a compute + write
+        slot = self.slots[0]
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for m in range(self.N):
+            self.replicas[m].restore(slot, staging=self.staging, stream=s)
+        s.synchronize()
+        t_in = (time.perf_counter() - t0) / self.N
+        in_bytes = sum(r.info()[1] for r in self.replicas) / self.N
+        t0 = time.perf_counter()
+        for m in range(self.N):
+            used = int(self.lens[m].sum()) * self.per_token
+            with torch.cuda.stream(s):
+                self.acc += slot.k[:used // 2].view(torch.int32).sum(dtype=torch.int64)
+                self.acc += slot.v[:used // 2].view(torch.int32).sum(dtype=torch.int64)
+        s.synchronize()
+        t_comp = (time.perf_counter() - t0) / self.N
+        return {"microbatches": self.N, "rounds": self.rounds,
+                "ms_per_microbatch_step": {"serial": round(1e3 * t_serial / steps, 3),
+                                           "double": round(1e3 * t_double / steps, 3)},
+                "speedup_double": round(t_serial / t_double, 3),
+                "swap_in_ms": round(1e3 * t_in, 3), "swap_in_bytes": int(in_bytes),
+                "swap_in_gbs": round(in_bytes / t_in / 1e9, 1),
+                "compute_ms": round(1e3 * t_comp, 3),
+                "note": "the double schedule can hide at most min(swap-in, compute) per step"}
+
+
 def run_mine(args):
     import torch
     rank, world, local = dist_init()
@@ -668,6 +853,7 @@ def run_mine(args):
     swap = None if args.no_swap else b.swap_section()
     naive = None if args.no_swap else naive_vs_buffered(b.torch, b.dv)
     streaming = None if args.no_swap else DecodeStreaming(b.torch, b.dv).measure()
+    mb_swap = None if args.no_swap else MicrobatchSwapping(b.torch, b.dv).measure()
     cpu = None
     if rank == 0:
         smp = OracleSample(8)
@@ -706,6 +892,7 @@ def run_mine(args):
         "swap": swap,
         "naive_vs_buffered": naive,
         "decode_streaming": streaming,
+        "microbatch_swapping": mb_swap,
         "gpu_launches": b.launches_per_step * args.steps,
         "clocks": clk,
     }
