@@ -94,3 +94,15 @@ def test_validation_errors():
     # an empty pack enqueues nothing and needs no buffer
     dv.dv_kv_pack(c, 1, 1, ok_s, ok_e, None, stream=0)
     dv.dv_kv_pack(c, 0, 2, ok_s, ok_s, None, stream=0)
+
+
+def test_slab_beyond_32_bit_chunk_indexing_is_refused():
+    """One (layer, K|V) slab must stay under 2^31 16-byte chunks (32 GiB):
+    larger ranges are refused on the host, before any launch."""
+    g = Geometry("huge", 1, 1024, 128, 128, 1 << 17, 2, "fp16")
+    c = dv.Cache.from_geometry(g, 0x1000, 0x2000)
+    s = np.zeros(g.batch, np.int32)
+    e = np.full(g.batch, g.max_seq, np.int32)  # H * T * C = 128 * 2^27 * 16 = 2^38 chunks
+    assert _status(lambda: dv.dv_staging_bytes(c, 0, 1, s, e)) == dv.DV_ERR_UNSUPPORTED
+    e[:] = 1  # a one-token slab is fine
+    assert dv.dv_staging_bytes(c, 0, 1, s, e) == 2 * 1024 * 128 * 128 * 2

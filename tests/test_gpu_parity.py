@@ -23,6 +23,7 @@ GEOMS = [
     Geometry("p4", 2, 3, 2, 64, 64, 4, "fp32"),         # 4-byte elements, x = 4
     Geometry("pad", 3, 2, 2, 128, 50, 2, "fp16", layer_stride_elems=2 * 2 * 128 * 50 + 64),
     Geometry("b40", 1, 40, 2, 64, 32, 2, "fp16"),       # batch > 32: 1024-entry tables
+    Geometry("b1024", 2, 1024, 1, 64, 24, 2, "fp16"),   # the largest batch the ABI takes
 ]
 
 
