@@ -290,6 +290,18 @@ class Bench:
             dv.dv_kv_unpack(self.cache_b, 0, L, s, e, (dp + k * self.dsz, self.dsz), sb)
         stream.wait_stream(sb)
 
+    def verify(self):
+        """After the step (prompt [0,1000) + deltas 1000..1023 = every token of
+        every sequence), the second cache equals the first, byte for byte."""
+        torch = self.torch
+        torch.cuda.synchronize()
+        return bool(torch.equal(self.kb, self.k) and torch.equal(self.vb, self.v))
+
+    def clear_b(self):
+        self.kb.zero_()
+        self.vb.zero_()
+        self.torch.cuda.synchronize()
+
     def capture(self):
         torch = self.torch
         with torch.cuda.stream(self.stream):
@@ -837,6 +849,7 @@ def run_mine(args):
     clk = clocks.stop()
     secs = max_over_ranks(secs, world)
     value = whole_job_rate(b.bytes_per_step, args.steps, secs, world)
+    step_ok = b.verify()
     serial = b.timed_serial()
     # kernel roofline, live
     kt = b.kernel_times()
@@ -847,7 +860,9 @@ def run_mine(args):
     # e2e through the public API with host buffers
     b.setup_e2e()
     e2e_steps = max(3, min(args.steps, 10))
+    b.clear_b()
     e2e_secs = max_over_ranks(b.timed_e2e(e2e_steps, 2, world), world)
+    e2e_ok = b.verify()
     e2e_value = whole_job_rate(b.bytes_per_step, e2e_steps, e2e_secs, world)
     h2d = d2h = b.g.num_layers * b.slab + GPT2_DECODE_STEPS * b.dsz
     swap = None if args.no_swap else b.swap_section()
@@ -871,6 +886,7 @@ def run_mine(args):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "timing": "CUDA-graph replay of the step (packs on one stream, each unpack "
                              "after its pack on a second stream), CUDA events on the launching stream",
+                   "step_verified": step_ok,
                    "serial_step_ms": round(serial * 1e3, 4),
                    "serial_value": round(b.bytes_per_step / serial / 1e9, 2),
                    "kernel_timing": "per launch kind: its launches of one step in a CUDA graph, L2 flushed before each replay, median of 5"},
@@ -884,7 +900,7 @@ def run_mine(args):
                     for n_, t, nb, c in kt],
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "verified": e2e_ok,
                 "path": "per layer: dv_stream_layer (pack + D2H copy) then dv_swap_in of that "
                         "layer (H2D copy + unpack) on a third stream, overlapping the next "
                         "layer's D2H; dv_replica_append x24 (fused) + dv_replica_restore "
