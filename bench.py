@@ -865,10 +865,13 @@ def run_mine(args):
     e2e_ok = b.verify()
     e2e_value = whole_job_rate(b.bytes_per_step, e2e_steps, e2e_secs, world)
     h2d = d2h = b.g.num_layers * b.slab + GPT2_DECODE_STEPS * b.dsz
-    swap = None if args.no_swap else b.swap_section()
-    naive = None if args.no_swap else naive_vs_buffered(b.torch, b.dv)
-    streaming = None if args.no_swap else DecodeStreaming(b.torch, b.dv).measure()
-    mb_swap = None if args.no_swap else MicrobatchSwapping(b.torch, b.dv).measure()
+    # The sections below describe one GPU and only rank 0 prints them: the other
+    # ranks skip them (they would pin about 20 GB of host memory each).
+    extra = rank == 0 and not args.no_swap
+    swap = b.swap_section() if extra else None
+    naive = naive_vs_buffered(b.torch, b.dv) if extra else None
+    streaming = DecodeStreaming(b.torch, b.dv).measure() if extra else None
+    mb_swap = MicrobatchSwapping(b.torch, b.dv).measure() if extra else None
     cpu = None
     if rank == 0:
         smp = OracleSample(8)
