@@ -24,6 +24,10 @@ GEOMS = [
     Geometry("pad", 3, 2, 2, 128, 50, 2, "fp16", layer_stride_elems=2 * 2 * 128 * 50 + 64),
     Geometry("b40", 1, 40, 2, 64, 32, 2, "fp16"),       # batch > 32: 1024-entry tables
     Geometry("b1024", 2, 1024, 1, 64, 24, 2, "fp16"),   # the largest batch the ABI takes
+    Geometry("c1", 2, 3, 2, 8, 70, 2, "fp16"),          # C = 1: one chunk per token
+    Geometry("c5", 2, 3, 2, 40, 90, 2, "fp16"),         # odd C
+    Geometry("c64", 2, 2, 2, 512, 40, 2, "fp16"),       # the largest C the tile kernel takes
+    Geometry("c128", 1, 2, 2, 1024, 20, 2, "fp16"),     # beyond it: flat kernel only
 ]
 
 
@@ -41,9 +45,12 @@ def range_sets(g, rng):
     return out
 
 
-def variants_for(s, e):
+def variants_for(s, e, g=None):
     one_token = (np.asarray(e) - np.asarray(s)).max() <= 1
-    return VARIANTS + ([dv.DV_VARIANT_TOKEN] if one_token else [])
+    base = VARIANTS
+    if g is not None and g.head_dim * g.elem_bytes // 16 > 64:  # no tile kernel for C > 64
+        base = [dv.DV_VARIANT_AUTO, dv.DV_VARIANT_FLAT]
+    return base + ([dv.DV_VARIANT_TOKEN] if one_token else [])
 
 
 def check_pack_unpack(g, cache, kh, vh, l0, l1, s, e, variant):
@@ -101,7 +108,7 @@ def test_pack_unpack_geometries(g):
     cache = H.device_cache(g, fill=(kh, vh))
     for name, s, e in range_sets(g, rng):
         for l0, l1 in ((0, g.num_layers), (g.num_layers - 1, g.num_layers)):
-            for variant in variants_for(s, e):
+            for variant in variants_for(s, e, g):
                 check_pack_unpack(g, cache, kh, vh, l0, l1, s, e, variant)
 
 
@@ -255,6 +262,14 @@ def test_errors_with_real_buffers_enqueue_nothing():
         assert _status(lambda: dv.dv_kv_pack(big, huge_layers - 1, huge_layers, sb, eb,
                                              (dst.data_ptr(), nb // 2))) == \
             dv.DV_ERR_BUFFER_TOO_SMALL
+    # the tile kernel refuses more than 64 chunks per token
+    wide = Geometry("wide", 1, 2, 1, 1024, 8, 2, "fp16")
+    cw = H.device_cache(wide, fill=0x33)
+    sw, ew = np.zeros(2, np.int32), np.full(2, 8, np.int32)
+    nw = ORC.staging_bytes(wide, 0, 1, sw, ew)
+    dw = H.device_bytes(nw)
+    assert _status(lambda: dv.dv_kv_pack(cw, 0, 1, sw, ew, dw, variant=dv.DV_VARIANT_TILE)) == \
+        dv.DV_ERR_UNSUPPORTED
     # the one-token kernel refuses longer ranges
     assert _status(lambda: dv.dv_kv_pack(cache, 0, 2, s, e, dst,
                                          variant=dv.DV_VARIANT_TOKEN)) == dv.DV_ERR_UNSUPPORTED
