@@ -116,6 +116,15 @@ const char* dv_status_string(dv_status status);
 /* Message for the calling thread's most recent failed call ("" if none). */
 const char* dv_last_error(void);
 
+/* Debugging.  A checked build of the library (built with DV_CHECKED=1, file
+ * libdv_checked.so) checks every global access of its kernels against the
+ * extents the host validated; an access outside them is skipped and the
+ * first one is recorded (nothing traps).  dv_debug_fault waits for the device,
+ * returns that record in *fault (0: none; else bit 63 set, bits 56..62 the
+ * kernel site, bits 0..55 the chunk index relative to the buffer) and clears
+ * it.  In the regular build it returns DV_ERR_UNSUPPORTED. */
+dv_status dv_debug_fault(uint64_t* fault);
+
 /* Bytes from `ptr` to the end of the CUDA allocation that holds it, as the
  * driver reports it; every call checks the buffers it is given against this
  * extent when the driver knows it.  DV_ERR_UNSUPPORTED when the driver cannot

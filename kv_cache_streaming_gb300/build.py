@@ -24,6 +24,7 @@ ROOT = PKG.parent
 CSRC = PKG / "csrc"
 OBJ = PKG / "_build"
 LIB = PKG / "libdv.so"
+LIB_CHECKED = PKG / "libdv_checked.so"  # device-side bounds checks (debugging)
 SOURCES = ["dv_api.cu", "dv_kernels.cu", "dv_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -35,10 +36,13 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libdv")
 
 
-def _compile(src: str) -> Path:
-    out = OBJ / (Path(src).stem + ".o")
+def _compile(src: str, checked: bool) -> Path:
+    out_dir = OBJ / ("checked" if checked else "release")
+    out = out_dir / (Path(src).stem + ".o")
+    defs = ["-DDV_CHECKED=1"] if checked else []
     cmd = [nvcc(), *ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
-           "-Xcompiler", "-Wall", "-I", str(ROOT / "include"), "-c", str(CSRC / src), "-o", str(out)]
+           "-Xcompiler", "-Wall", *defs, "-I", str(ROOT / "include"), "-c", str(CSRC / src),
+           "-o", str(out)]
     subprocess.run(cmd, check=True)
     return out
 
@@ -50,20 +54,22 @@ def _stale(target: Path, deps) -> bool:
     return any(Path(d).stat().st_mtime > t for d in deps)
 
 
-def build(force: bool = False) -> Path:
+def build(force: bool = False, checked: bool = False) -> Path:
+    """Builds libdv.so, or with `checked` the bounds-checked libdv_checked.so."""
+    lib = LIB_CHECKED if checked else LIB
     deps = [CSRC / s for s in SOURCES] + [CSRC / "dv_plan.h", ROOT / "include" / "dv.h",
                                           Path(__file__)]
-    if not force and not _stale(LIB, deps):
-        return LIB
-    OBJ.mkdir(exist_ok=True)
+    if not force and not _stale(lib, deps):
+        return lib
+    (OBJ / ("checked" if checked else "release")).mkdir(parents=True, exist_ok=True)
     with ThreadPoolExecutor(len(SOURCES)) as ex:
-        objs = list(ex.map(_compile, SOURCES))
-    tmp = LIB.with_suffix(f".{os.getpid()}.tmp")
+        objs = list(ex.map(lambda src: _compile(src, checked), SOURCES))
+    tmp = lib.with_suffix(f".{os.getpid()}.tmp")
     subprocess.run([nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", str(tmp),
                     *map(str, objs)], check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv))
+    print(build(force="--force" in sys.argv, checked="--checked" in sys.argv))

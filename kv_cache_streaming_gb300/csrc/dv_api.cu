@@ -364,6 +364,15 @@ const char* dv_status_string(dv_status st) {
 
 const char* dv_last_error(void) { return g_last_error.c_str(); }
 
+dv_status dv_debug_fault(uint64_t* fault) {
+  if (!fault) return fail(DV_ERR_INVALID_ARG, "fault is NULL");
+  *fault = 0;
+  if (!dv::checked_build())
+    return fail(DV_ERR_UNSUPPORTED, "this libdv was built without device-side bounds checks");
+  const cudaError_t err = dv::read_fault(fault);
+  return err == cudaSuccess ? DV_OK : cuda_fail(err, "reading the fault record");
+}
+
 dv_status dv_allocation_extent(const void* ptr, size_t* bytes_after) {
   if (!ptr || !bytes_after) return fail(DV_ERR_INVALID_ARG, "ptr / bytes_after is NULL");
   CUdeviceptr base = 0;

@@ -48,6 +48,7 @@ struct KParams {
   int64_t layer_chunks;    // layer stride
   int64_t lkv_chunks;      // chunks per (layer, K|V) slab of staging
   int64_t total;           // flat: chunks; tile: tiles
+  int64_t k_lim, v_lim, stg_lim;  // checked builds: extents (chunks) the host validated
   int32_t l0, B, H, C, S;
   int32_t tiles_per_lkv;   // tile kernel: tiles per (layer, K|V) slab
   uint64_t m_tpl;          // ceil(2^64 / tiles_per_lkv) (0 when it is 1)
@@ -94,6 +95,34 @@ __device__ __forceinline__ void pdl_enter() {
 }
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
+
+#ifndef DV_CHECKED
+#define DV_CHECKED 0  // 1: every global access is checked against the host-validated extents
+#endif
+
+#if DV_CHECKED
+// First access outside its buffer since the last read: bit 63 set, bits 56..62
+// the site, bits 0..55 the chunk index relative to the buffer.  The access is
+// skipped; nothing traps.
+__device__ unsigned long long g_dv_fault;
+
+__device__ __forceinline__ bool in_bounds(const uint4* ptr, const uint4* base, int64_t lim,
+                                          int site) {
+  const int64_t i = ptr - base;
+  if (i >= 0 && i < lim) return true;
+  const unsigned long long code = (1ull << 63) | ((unsigned long long)(site & 0x7f) << 56) |
+                                  ((unsigned long long)i & 0x00FFFFFFFFFFFFFFull);
+  atomicCAS(&g_dv_fault, 0ull, code);
+  return false;
+}
+#define DV_OK_K(ptr, site) in_bounds((ptr), p.k, p.k_lim, (site))
+#define DV_OK_V(ptr, site) in_bounds((ptr), p.v, p.v_lim, (site))
+#define DV_OK_S(ptr, site) in_bounds((ptr), p.stg, p.stg_lim, (site))
+#else
+#define DV_OK_K(ptr, site) true
+#define DV_OK_V(ptr, site) true
+#define DV_OK_S(ptr, site) true
+#endif
 
 // Largest b in [0, B) with pre[b] <= key (pre ascending).  With key inside
 // [pre[b], pre[b+1]) of a non-empty b, that is b itself.
@@ -163,13 +192,16 @@ flat_kernel(const __grid_constant__ KParams<MAXB> p) {
         const int64_t bh = (int64_t)b * p.H + h;
         cptr[u] = (lkv & 1) == 0 ? p.k + l * p.layer_chunks + ((bh * C + c) * p.S + t)
                                  : p.v + l * p.layer_chunks + ((bh * p.S + t) * C + c);
-        val[u] = PACK ? ld_stream(cptr[u]) : ld_stream(p.stg + g);
+        const bool ok = ((lkv & 1) == 0 ? DV_OK_K(cptr[u], 1) : DV_OK_V(cptr[u], 2)) &&
+                        DV_OK_S(p.stg + g, 3);
+        if (!ok) cptr[u] = nullptr;
+        else val[u] = PACK ? ld_stream(cptr[u]) : ld_stream(p.stg + g);
       }
     }
 #pragma unroll
     for (int u = 0; u < kFlatUnroll; ++u) {
       const int64_t g = base + u * kThreads;
-      if (g < p.total) {
+      if (g < p.total && cptr[u]) {
         if (PACK) p.stg[g] = val[u];
         else *cptr[u] = val[u];
       }
@@ -185,6 +217,7 @@ struct TokParams {
   uint4* v;
   uint4* stg;
   int64_t layer_chunks;
+  int64_t k_lim, v_lim, stg_lim;  // checked builds: extents (chunks) the host validated
   uint32_t total;         // staging chunks
   uint32_t AH;            // active sequences x heads: records per (layer, K|V)
   uint64_t m_AH, m_H;     // ceil(2^32 / d) for d = AH, H
@@ -215,25 +248,29 @@ token_kernel(const __grid_constant__ TokParams<MAXB> p) {
     const int64_t bh = b * p.H + h;
     uint4* ptr = (lkv & 1) == 0 ? p.k + l * p.layer_chunks + ((bh * C + c) * p.S + t)
                                 : p.v + l * p.layer_chunks + ((bh * p.S + t) * C + c);
+    if (!(((lkv & 1) == 0 ? DV_OK_K(ptr, 11) : DV_OK_V(ptr, 12)) && DV_OK_S(p.stg + g, 13)))
+      continue;
     if (PACK) p.stg[g] = ld_stream(ptr);
     else *ptr = ld_stream(p.stg + g);
   }
 }
 
-// Contiguous run of `cnt` chunks between the cache and staging.
-template <bool PACK>
-__device__ __forceinline__ void copy_run(uint4* cache, uint4* stg, int cnt) {
+// Contiguous run of `cnt` chunks between the V cache and staging.
+template <bool PACK, typename Params>
+__device__ __forceinline__ void copy_run(const Params& p, uint4* cache, uint4* stg, int cnt) {
   for (int q0 = threadIdx.x; q0 < cnt; q0 += kThreads * kTileUnroll) {
     uint4 val[kTileUnroll];
+    bool ok[kTileUnroll];
 #pragma unroll
     for (int u = 0; u < kTileUnroll; ++u) {
       const int q = q0 + u * kThreads;
-      if (q < cnt) val[u] = PACK ? ld_stream(cache + q) : ld_stream(stg + q);
+      ok[u] = q < cnt && DV_OK_V(cache + q, 21) && DV_OK_S(stg + q, 22);
+      if (ok[u]) val[u] = PACK ? ld_stream(cache + q) : ld_stream(stg + q);
     }
 #pragma unroll
     for (int u = 0; u < kTileUnroll; ++u) {
       const int q = q0 + u * kThreads;
-      if (q < cnt) {
+      if (ok[u]) {
         if (PACK) stg[q] = val[u];
         else cache[q] = val[u];
       }
@@ -269,7 +306,7 @@ tile_kernel(const __grid_constant__ KParams<MAXB> p) {
     const int64_t bh = (int64_t)b * p.H + h;
     if (lkv & 1) {
       uint4* cv = p.v + l * p.layer_chunks + (bh * p.S + p.seq_start[b] + t0) * C;
-      copy_run<PACK>(cv, stg, cnt);
+      copy_run<PACK>(p, cv, stg, cnt);
     } else if (PACK) {
       // K: row c of this tile starts at ck + c * S.
       uint4* ck = p.k + l * p.layer_chunks + bh * C * p.S + p.seq_start[b] + t0;
@@ -279,7 +316,8 @@ tile_kernel(const __grid_constant__ KParams<MAXB> p) {
         for (int u = 0; u < kTileUnroll; ++u) {
           const int q = q0 + u * kThreads;
           const int c = q >> LOG2TB, t = q & (TB - 1);
-          if (q < TC && t < n) val[u] = ld_stream(ck + (int64_t)c * p.S + t);
+          if (q < TC && t < n && DV_OK_K(ck + (int64_t)c * p.S + t, 31))
+            val[u] = ld_stream(ck + (int64_t)c * p.S + t);
         }
 #pragma unroll
         for (int u = 0; u < kTileUnroll; ++u) {
@@ -292,7 +330,7 @@ tile_kernel(const __grid_constant__ KParams<MAXB> p) {
       for (int q = threadIdx.x; q < cnt; q += kThreads) {
         const int t = LOG2C >= 0 ? q >> LOG2C : q / C;
         const int c = q - t * C;
-        stg[q] = smem[t * SROW + c];
+        if (DV_OK_S(stg + q, 32)) stg[q] = smem[t * SROW + c];
       }
       __syncthreads();
     } else {
@@ -302,7 +340,7 @@ tile_kernel(const __grid_constant__ KParams<MAXB> p) {
 #pragma unroll
         for (int u = 0; u < kTileUnroll; ++u) {
           const int q = q0 + u * kThreads;
-          if (q < cnt) val[u] = ld_stream(stg + q);
+          if (q < cnt && DV_OK_S(stg + q, 33)) val[u] = ld_stream(stg + q);
         }
 #pragma unroll
         for (int u = 0; u < kTileUnroll; ++u) {
@@ -317,7 +355,8 @@ tile_kernel(const __grid_constant__ KParams<MAXB> p) {
       __syncthreads();
       for (int q = threadIdx.x; q < TC; q += kThreads) {
         const int c = q >> LOG2TB, t = q & (TB - 1);
-        if (t < n) ck[(int64_t)c * p.S + t] = smem[t * SROW + c];
+        if (t < n && DV_OK_K(ck + (int64_t)c * p.S + t, 34))
+          ck[(int64_t)c * p.S + t] = smem[t * SROW + c];
       }
       __syncthreads();
     }
@@ -381,8 +420,17 @@ inline uint64_t div64_magic(uint64_t d) {
   return (uint64_t)((((unsigned __int128)1 << 64) + d - 1) / d);
 }
 
+// Chunks of K (and of V) the host validated from the base pointer: layers
+// [0, l1) at the layer stride, the last one dense.
+inline int64_t cache_limit(const Plan& p) {
+  const int64_t dense = (int64_t)p.B * p.H * p.D * p.S * p.P / 16;
+  return p.l1 > 0 ? (int64_t)(p.l1 - 1) * p.layer_chunks + dense : 0;
+}
+
 template <int MAXB>
 void fill_params(KParams<MAXB>& kp, const Plan& p, void* stg) {
+  kp.k_lim = kp.v_lim = cache_limit(p);
+  kp.stg_lim = p.bytes / 16;
   kp.k = static_cast<uint4*>(p.k);
   kp.v = static_cast<uint4*>(p.v);
   kp.stg = static_cast<uint4*>(stg);
@@ -448,6 +496,8 @@ cudaError_t run_token(const Plan& p, void* stg, cudaStream_t stream) {
   kp.v = static_cast<uint4*>(p.v);
   kp.stg = static_cast<uint4*>(stg);
   kp.layer_chunks = p.layer_chunks;
+  kp.k_lim = kp.v_lim = cache_limit(p);
+  kp.stg_lim = p.bytes / 16;
   int32_t a = 0;
   for (int32_t b = 0; b < p.B; ++b) {
     if (p.seq_len[b] == 0) continue;
@@ -507,6 +557,23 @@ bool token_supported(const Plan& p) {
 bool auto_uses_tile(const Plan& p) {
   if (!tile_supported(p) || p.active == 0) return false;
   return p.tokens >= (int64_t)16 * p.active;  // mean range length >= 16 tokens
+}
+
+bool checked_build() { return DV_CHECKED != 0; }
+
+cudaError_t read_fault(uint64_t* out) {
+#if DV_CHECKED
+  unsigned long long v = 0;
+  cudaError_t err = cudaMemcpyFromSymbol(&v, g_dv_fault, sizeof(v));
+  if (err != cudaSuccess) return err;
+  const unsigned long long zero = 0;
+  err = cudaMemcpyToSymbol(g_dv_fault, &zero, sizeof(zero));
+  *out = v;
+  return err;
+#else
+  *out = 0;
+  return cudaSuccess;
+#endif
 }
 
 cudaError_t launch_pack(const Plan& p, void* stg, cudaStream_t stream, int variant) {

@@ -58,6 +58,12 @@ bool token_supported(const Plan& p);
 cudaError_t launch_pack(const Plan& p, void* stg, cudaStream_t stream, int variant);
 cudaError_t launch_unpack(const Plan& p, const void* stg, cudaStream_t stream, int variant);
 
+// Whether this library was built with device-side bounds checks, and the
+// first out-of-bounds access they recorded since the last call (0 if none;
+// the record is cleared).  Synchronous.
+bool checked_build();
+cudaError_t read_fault(uint64_t* out);
+
 // Records a message for dv_last_error() on the calling thread; returns `st`.
 dv_status set_error(dv_status st, const char* fmt, ...);
 

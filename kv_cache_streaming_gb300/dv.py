@@ -10,12 +10,15 @@ A status other than DV_OK raises ``DvError`` with the library's message.
 from __future__ import annotations
 
 import ctypes
+import os
 from pathlib import Path
 
 import numpy as np
 
 PKG = Path(__file__).resolve().parent
-library_path = PKG / "libdv.so"
+# DV_LIBRARY=checked loads the bounds-checked debugging build instead.
+library_path = PKG / ("libdv_checked.so" if os.environ.get("DV_LIBRARY") == "checked"
+                      else "libdv.so")
 
 DV_MAX_BATCH = 1024
 (DV_OK, DV_ERR_INVALID_ARG, DV_ERR_RANGE, DV_ERR_BUFFER_TOO_SMALL, DV_ERR_MISALIGNED,
@@ -57,6 +60,7 @@ _status_string = _sig("dv_status_string", [ctypes.c_int], ctypes.c_char_p)
 _last_error = _sig("dv_last_error", [], ctypes.c_char_p)
 _staging_bytes = _sig("dv_staging_bytes", _RANGE + [ctypes.POINTER(_SZ)])
 _extent = _sig("dv_allocation_extent", [_P, ctypes.POINTER(_SZ)])
+_debug_fault = _sig("dv_debug_fault", [ctypes.POINTER(ctypes.c_uint64)])
 _pack = _sig("dv_kv_pack_variant", _RANGE + [_P, _SZ, _P, _I32])
 _unpack = _sig("dv_kv_unpack_variant", _RANGE + [_P, _SZ, _P, _I32])
 _swap_out = _sig("dv_swap_out", _RANGE + [_P, _SZ, _P, _SZ, _P])
@@ -151,6 +155,17 @@ class Cache:
 
 
 # ---- entry points --------------------------------------------------------------
+
+def dv_debug_fault():
+    """The first out-of-bounds access the checked build recorded (0: none), or
+    None for the regular build.  Waits for the device and clears the record."""
+    out = ctypes.c_uint64(0)
+    st = _debug_fault(ctypes.byref(out))
+    if st == DV_ERR_UNSUPPORTED:
+        return None
+    _check(st)
+    return out.value
+
 
 def dv_allocation_extent(ptr):
     """Bytes from ``ptr`` (tensor or address) to the end of its CUDA
