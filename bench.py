@@ -410,7 +410,9 @@ class Bench:
                       torch.empty(self.slab, dtype=torch.uint8, device="cuda"))
         self.copy_stream = torch.cuda.Stream()
         self.in_stream = torch.cuda.Stream()
+        self.in_stream2 = torch.cuda.Stream()
         self.in_staging = torch.empty(self.slab, dtype=torch.uint8, device="cuda")
+        self.in_staging2 = torch.empty(self.slab, dtype=torch.uint8, device="cuda")
         self.streamer = dv.Streamer(self.slots[0], self.slots[1], self.stream, self.copy_stream)
         self.replica = dv.Replica(self.arena, g.batch)
 
@@ -423,18 +425,23 @@ class Bench:
         layer l+1 on the full-duplex link.  Then the 24 deltas go to the host
         replica (fused pack into host memory) and are restored from it."""
         dv, g = self.dv, self.g
-        s, si = self.stream, self.in_stream
+        s = self.stream
+        ins = (self.in_stream, self.in_stream2)
+        stgs = (self.in_staging, self.in_staging2)
         hp = self.host_prompt.data_ptr()
         for l in range(g.num_layers):
             self.streamer.stream_layer(self.cache, l, self.ps, self.pe, self.host_prompt, l0=0)
+            si = ins[l % 2]  # two swap-in streams: layer l's unpack overlaps l+1's copy
             si.wait_stream(self.copy_stream)
             dv.dv_swap_in(self.cache_b, l, l + 1, self.ps, self.pe, (hp + l * self.slab, self.slab),
-                          staging=self.in_staging, stream=si)
+                          staging=stgs[l % 2], stream=si)
         self.replica.truncate(0)
         for k, (a, b) in enumerate(self.deltas):
             self.replica.append(self.cache, 0, g.num_layers, a, b, step=k, stream=s)
+        si = ins[0]
         si.wait_stream(s)
-        self.replica.restore(self.cache_b, staging=self.in_staging, stream=si)
+        si.wait_stream(ins[1])
+        self.replica.restore(self.cache_b, staging=stgs[0], stream=si)
         s.wait_stream(si)
 
     def timed_e2e(self, steps, warmup, world):
