@@ -1,0 +1,52 @@
+/* Calls libdv from plain C with no GPU work: staging sizes (the capacity
+ * formula 2*B*S*H*D*P*N for a full cache), and the validation errors that are
+ * decided on the host.  Exit status 0 when every check holds. */
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "dv.h"
+
+static int failures = 0;
+#define CHECK(cond)                                                   \
+  do {                                                                \
+    if (!(cond)) {                                                    \
+      fprintf(stderr, "check failed at line %d: %s\n", __LINE__, #cond); \
+      ++failures;                                                     \
+    }                                                                 \
+  } while (0)
+
+int main(void) {
+  CHECK(dv_abi_version() == DV_ABI_VERSION);
+  int32_t s[8], e[8];
+  for (int b = 0; b < 8; ++b) {
+    s[b] = 0;
+    e[b] = 1024;
+  }
+  dv_cache c;
+  memset(&c, 0, sizeof(c));
+  c.num_layers = 48;
+  c.batch = 8;
+  c.num_heads = 25;
+  c.head_dim = 64;
+  c.max_seq = 1024;
+  c.elem_bytes = 2;
+  c.k_base = (void*)0x1000;
+  c.v_base = (void*)0x2000;
+  size_t bytes = 0;
+  CHECK(dv_staging_bytes(&c, 0, 48, s, e, &bytes) == DV_OK);
+  CHECK(bytes == (size_t)2 * 8 * 1024 * 25 * 64 * 2 * 48);
+  e[3] = 1025; /* past max_seq */
+  CHECK(dv_staging_bytes(&c, 0, 48, s, e, &bytes) == DV_ERR_RANGE);
+  CHECK(strlen(dv_last_error()) > 0);
+  e[3] = 1024;
+  CHECK(dv_staging_bytes(&c, 0, 49, s, e, &bytes) == DV_ERR_RANGE);
+  c.head_dim = 60; /* not a multiple of x = 8 */
+  CHECK(dv_staging_bytes(&c, 0, 48, s, e, &bytes) == DV_ERR_UNSUPPORTED);
+  c.head_dim = 64;
+  CHECK(dv_kv_pack(&c, 0, 48, s, e, (void*)0x3000, 16, NULL) == DV_ERR_BUFFER_TOO_SMALL);
+  CHECK(dv_kv_pack(NULL, 0, 48, s, e, (void*)0x3000, 16, NULL) == DV_ERR_INVALID_ARG);
+  CHECK(strcmp(dv_status_string(DV_ERR_MISALIGNED), "DV_ERR_MISALIGNED") == 0);
+  if (failures == 0) printf("abi_host: all checks passed\n");
+  return failures == 0 ? 0 : 1;
+}
