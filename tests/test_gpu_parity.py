@@ -304,3 +304,35 @@ def test_naive_gather_matches_the_pack():
         dv.dv_naive_gather(cache, 0, g.num_layers, s, e, host)
         torch.cuda.synchronize()
         assert np.array_equal(host.numpy()[:n], want)
+
+
+def test_replica_compaction():
+    """Compaction: the snapshot + deltas of a replica replaced by one snapshot of
+    the used prefix (truncate to nothing, append the prefix); the compacted
+    replica restores the same cache and takes only the prefix's bytes."""
+    g = Geometry("compact", 2, 3, 2, 64, 40, 2, "fp16")
+    kh, vh = H.host_cache(g, 57)
+    cache = H.device_cache(g, fill=(kh, vh))
+    zero = np.zeros(g.batch, np.int32)
+    pos = np.array([4, 9, 2], np.int32)
+    arena = H.pinned(ORC.staging_bytes(g, 0, g.num_layers, zero, pos + 5) + 4096)
+    rep = dv.Replica(arena, g.batch)
+    rep.append(cache, 0, g.num_layers, zero, pos, step=0)
+    for k in range(1, 6):
+        rep.append(cache, 0, g.num_layers, pos, pos + 1, step=k)
+        pos = pos + 1
+    before = H.device_cache(g, fill="zero")
+    rep.restore(before)
+    rep.truncate(0)  # compaction: the whole log is replaced ...
+    assert rep.info() == (0, 0)
+    rep.append(before, 0, g.num_layers, zero, pos, step=5)  # ... by one snapshot of the prefix
+    after = H.device_cache(g, fill="zero")
+    rep.restore(after)
+    torch.cuda.synchronize()
+    assert rep.info() == (1, ORC.staging_bytes(g, 0, g.num_layers, zero, pos))
+    assert torch.equal(before.k, after.k) and torch.equal(before.v, after.v)
+    mk, mv = P.selected_mask(g, 0, g.num_layers, zero, pos)
+    kw = np.where(np.repeat(mk, 2), kh, 0).astype(np.uint8)
+    vw = np.where(np.repeat(mv, 2), vh, 0).astype(np.uint8)
+    assert np.array_equal(H.to_np(after.k), kw) and np.array_equal(H.to_np(after.v), vw)
+    rep.close()
