@@ -105,7 +105,9 @@ typedef struct {
  * tuning; the plain calls use DV_VARIANT_AUTO). */
 typedef enum {
   DV_VARIANT_AUTO = 0, /* token kernel when every range has at most one token, tile
-                          kernel for long ranges, flat kernel otherwise */
+                          kernel when the mean range holds at least 384 16-byte chunks
+                          per head (e.g. 48 tokens at head_dim 64, fp16), flat
+                          kernel otherwise */
   DV_VARIANT_FLAT = 1, /* one 16-byte chunk per thread, staging order */
   DV_VARIANT_TILE = 2, /* token tiles; K transposed through shared memory */
   DV_VARIANT_TOKEN = 3 /* one-token ranges only (decode deltas): one chunk per thread */

@@ -556,7 +556,11 @@ bool token_supported(const Plan& p) {
 
 bool auto_uses_tile(const Plan& p) {
   if (!tile_supported(p) || p.active == 0) return false;
-  return p.tokens >= (int64_t)16 * p.active;  // mean range length >= 16 tokens
+  // Tiles pay once a (layer, K|V, sequence, head) run holds about 384 chunks
+  // (6 KiB) on average: measured on GB300, the flat kernel wins below (e.g.
+  // 40 tokens for head_dim 64, 24 for head_dim 128 in fp16), the tile kernel
+  // above.
+  return p.tokens * p.C >= (int64_t)384 * p.active;
 }
 
 bool checked_build() { return DV_CHECKED != 0; }
