@@ -104,13 +104,14 @@ typedef struct {
 /* Kernel choice for dv_kv_pack_variant / dv_kv_unpack_variant (testing and
  * tuning; the plain calls use DV_VARIANT_AUTO). */
 typedef enum {
-  DV_VARIANT_AUTO = 0, /* token kernel when every range has at most one token, tile
-                          kernel when the mean range holds at least 384 16-byte chunks
-                          per head (e.g. 48 tokens at head_dim 64, fp16), flat
-                          kernel otherwise */
+  DV_VARIANT_AUTO = 0, /* equal-length ranges (e.g. one-token decode deltas): the
+                          token kernel below 640 16-byte chunks per head and range
+                          (80 tokens at head_dim 64, fp16), the tile kernel above;
+                          ragged ranges: the flat kernel below a mean of 384 chunks,
+                          the tile kernel above */
   DV_VARIANT_FLAT = 1, /* one 16-byte chunk per thread, staging order */
   DV_VARIANT_TILE = 2, /* token tiles; K transposed through shared memory */
-  DV_VARIANT_TOKEN = 3 /* one-token ranges only (decode deltas): one chunk per thread */
+  DV_VARIANT_TOKEN = 3 /* every non-empty range equally long: one chunk per thread */
 } dv_variant;
 
 int32_t dv_abi_version(void);

@@ -91,7 +91,7 @@ dv_status plan_ranges(const dv_cache* c, int32_t l0, int32_t l1, const int32_t* 
   p->l0 = l0;
   p->l1 = l1;
   int64_t acc = 0;
-  int32_t mx = 0, act = 0;
+  int32_t mx = 0, mn = 0, act = 0;
   for (int32_t b = 0; b < c->batch; ++b) {
     if (s[b] < 0 || s[b] > e[b] || e[b] > c->max_seq)
       return fail(DV_ERR_RANGE, "sequence %d range [%d,%d) outside [0,%d]", b, s[b], e[b],
@@ -102,11 +102,13 @@ dv_status plan_ranges(const dv_cache* c, int32_t l0, int32_t l1, const int32_t* 
     p->tok_pre[b] = (int32_t)acc;
     acc += len;
     if (len > mx) mx = len;
+    if (len > 0 && (mn == 0 || len < mn)) mn = len;
     if (len > 0) ++act;
   }
   p->tok_pre[c->batch] = (int32_t)acc;
   p->tokens = acc;
   p->max_len = mx;
+  p->min_len = mn;
   p->active = act;
   p->lkv_chunks = (int64_t)p->H * acc * p->C;
   if (p->lkv_chunks >= (int64_t)1 << 31)
@@ -189,7 +191,7 @@ dv_status check_variant(const dv::Plan& p, int32_t variant) {
     return fail(DV_ERR_UNSUPPORTED, "tile kernel handles at most 64 chunks per token (got %d)",
                 p.C);
   if (variant == dv::kToken && !dv::token_supported(p))
-    return fail(DV_ERR_UNSUPPORTED, "token kernel needs every range to hold at most one token");
+    return fail(DV_ERR_UNSUPPORTED, "token kernel needs every non-empty range to be equally long");
   return DV_OK;
 }
 

@@ -219,16 +219,18 @@ struct TokParams {
   int64_t layer_chunks;
   int64_t k_lim, v_lim, stg_lim;  // checked builds: extents (chunks) the host validated
   uint32_t total;         // staging chunks
-  uint32_t AH;            // active sequences x heads: records per (layer, K|V)
-  uint64_t m_AH, m_H;     // ceil(2^32 / d) for d = AH, H
+  uint32_t AH;            // active sequences x heads: runs per (layer, K|V)
+  uint32_t n;             // tokens of every non-empty range
+  uint64_t m_AH, m_H, m_n;  // ceil(2^32 / d) for d = AH, H, n
   int32_t l0, H, C, S;
   int32_t act_b[MAXB];    // sequence of the a-th non-empty range
   int32_t act_t[MAXB];    // its one token
 };
 
-// Every non-empty range holds one token: staging chunk g is chunk c of record
-// (layer, K|V, a-th non-empty sequence, head).  One chunk per thread, no
-// shared memory, no barrier: the shortest chain from launch to the copy.
+// Every non-empty range holds the same n tokens (n = 1: decode deltas):
+// staging chunk g is chunk c of token j of run (layer, K|V, a-th non-empty
+// sequence, head).  One chunk per thread, no shared memory, no barrier: the
+// shortest chain from launch to the copy.
 template <bool PACK, int MAXB, int LOG2C>
 __global__ void __launch_bounds__(kThreads)
 token_kernel(const __grid_constant__ TokParams<MAXB> p) {
@@ -238,12 +240,14 @@ token_kernel(const __grid_constant__ TokParams<MAXB> p) {
        g += gridDim.x * kThreads) {
     const uint32_t rec = LOG2C >= 0 ? (g >> LOG2C) : g / C;
     const uint32_t c = g - rec * C;
-    const uint32_t lkv = div_by(rec, p.AH, p.m_AH);
-    const uint32_t rem = rec - lkv * p.AH;
+    const uint32_t run = div_by(rec, p.n, p.m_n);
+    const uint32_t j = rec - run * p.n;
+    const uint32_t lkv = div_by(run, p.AH, p.m_AH);
+    const uint32_t rem = run - lkv * p.AH;
     const uint32_t a = div_by(rem, (uint32_t)p.H, p.m_H);
     const uint32_t h = rem - a * p.H;
     const int64_t b = p.act_b[a];
-    const int64_t t = p.act_t[a];
+    const int64_t t = p.act_t[a] + j;
     const int64_t l = p.l0 + (lkv >> 1);
     const int64_t bh = b * p.H + h;
     uint4* ptr = (lkv & 1) == 0 ? p.k + l * p.layer_chunks + ((bh * C + c) * p.S + t)
@@ -506,9 +510,11 @@ cudaError_t run_token(const Plan& p, void* stg, cudaStream_t stream) {
     ++a;
   }
   kp.AH = (uint32_t)(a * p.H);
+  kp.n = (uint32_t)p.max_len;
   kp.m_AH = div_magic(kp.AH);
   kp.m_H = div_magic((uint32_t)p.H);
-  kp.total = (uint32_t)(2 * (int64_t)(p.l1 - p.l0) * kp.AH * p.C);
+  kp.m_n = div_magic(kp.n);
+  kp.total = (uint32_t)(2 * (int64_t)(p.l1 - p.l0) * kp.AH * kp.n * p.C);
   kp.l0 = p.l0;
   kp.H = p.H;
   kp.C = p.C;
@@ -541,7 +547,7 @@ template <bool PACK>
 cudaError_t launch(const Plan& p, void* stg, cudaStream_t stream, int variant) {
   if (p.bytes == 0) return cudaSuccess;
   int kind = variant;
-  if (variant == kAuto) kind = token_supported(p) ? kToken : auto_uses_tile(p) ? kTile : kFlat;
+  if (variant == kAuto) kind = auto_kind(p);
   if (p.B <= kSmallBatch) return dispatch_c<PACK, kSmallBatch>(p, stg, stream, kind);
   return dispatch_c<PACK, kMaxBatch>(p, stg, stream, kind);
 }
@@ -551,7 +557,18 @@ cudaError_t launch(const Plan& p, void* stg, cudaStream_t stream, int variant) {
 bool tile_supported(const Plan& p) { return p.C <= kMaxTileC; }
 
 bool token_supported(const Plan& p) {
-  return p.max_len <= 1 && 2 * (int64_t)(p.l1 - p.l0) * p.H * p.tokens * p.C < ((int64_t)1 << 31);
+  return p.active > 0 && p.min_len == p.max_len &&
+         2 * (int64_t)(p.l1 - p.l0) * p.H * p.tokens * p.C < ((int64_t)1 << 31);
+}
+
+int auto_kind(const Plan& p) {
+  // Equal-length ranges: the token kernel up to about 640 chunks per run
+  // (measured on GB300: between 64 and 96 tokens at head_dim 64, between 32
+  // and 48 at 128 in fp16), the tile kernel beyond.  Ragged ranges: the flat
+  // kernel below the tile kernel's crossover.
+  if (token_supported(p))
+    return tile_supported(p) && (int64_t)p.max_len * p.C >= 640 ? kTile : kToken;
+  return auto_uses_tile(p) ? kTile : kFlat;
 }
 
 bool auto_uses_tile(const Plan& p) {

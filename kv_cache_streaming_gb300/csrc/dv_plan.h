@@ -25,6 +25,7 @@ struct Plan {
   int32_t tok_pre[kMaxBatch + 1];  // tok_pre[b] = sum of seq_len[0..b)
   int64_t tokens;            // T = tok_pre[B]
   int32_t max_len;
+  int32_t min_len;           // shortest non-empty range (0 when all are empty)
   int32_t active;            // sequences with a non-empty range
   int64_t lkv_chunks;        // chunks of one (layer, K|V) slab: H * T * C
   int64_t bytes;             // staging bytes: 2 * (l1 - l0) * lkv_chunks * 16
@@ -44,12 +45,14 @@ inline int64_t layer_slab_bytes(const Plan& p) { return 2 * p.lkv_chunks * 16; }
 
 enum Variant { kAuto = 0, kFlat = 1, kTile = 2, kToken = 3 };
 
-// Kernel choice of kAuto (the tile kernel pays off once ranges are long).
+// Kernel choice of kAuto.
+int auto_kind(const Plan& p);
+// For ragged ranges: whether the tile kernel beats the flat kernel.
 bool auto_uses_tile(const Plan& p);
 // Whether the tile kernel handles this geometry (C <= 64).
 bool tile_supported(const Plan& p);
-// Whether the one-token kernel handles these ranges (every range at most one
-// token long; fewer than 2^31 staging chunks).
+// Whether the token kernel handles these ranges (every non-empty range the
+// same length; fewer than 2^31 staging chunks).
 bool token_supported(const Plan& p);
 
 // `stg` is the device-visible address of the staging bytes (device memory or

@@ -39,6 +39,11 @@ def range_sets(g, rng):
     e = pos + 1
     e[::3] = pos[::3]  # some finished sequences
     out.append(("decode", pos, e.astype(np.int32)))
+    n = min(3, S)  # a few equal-length ranges (multi-token deltas)
+    pos = rng.integers(0, S - n + 1, size=B).astype(np.int32)
+    e = pos + n
+    e[1::3] = pos[1::3]
+    out.append(("multi", pos, e.astype(np.int32)))
     for i in range(3):
         s, e = P.random_ranges(g, rng)
         out.append((f"rand{i}", s, e))
@@ -46,7 +51,8 @@ def range_sets(g, rng):
 
 
 def variants_for(s, e, g=None):
-    one_token = (np.asarray(e) - np.asarray(s)).max() <= 1
+    lens = (np.asarray(e) - np.asarray(s))
+    one_token = lens.max() > 0 and len(set(lens[lens > 0].tolist())) == 1  # equal lengths
     base = VARIANTS
     if g is not None and g.head_dim * g.elem_bytes // 16 > 64:  # no tile kernel for C > 64
         base = [dv.DV_VARIANT_AUTO, dv.DV_VARIANT_FLAT]
@@ -87,8 +93,6 @@ def test_tiny_workload(variant):
     cache = H.device_cache(g, fill=(kh, vh))
     (ps, pe), (ds, de) = tiny_ranges()
     for s, e in ((ps, pe), (ds, de)):
-        if variant == dv.DV_VARIANT_TOKEN and (e - s).max() > 1:
-            continue
         n = ORC.staging_bytes(g, 0, g.num_layers, s, e)
         dst = H.device_bytes(n)
         dv.dv_kv_pack(cache, 0, g.num_layers, s, e, dst, variant=variant)
@@ -270,8 +274,8 @@ def test_errors_with_real_buffers_enqueue_nothing():
     dw = H.device_bytes(nw)
     assert _status(lambda: dv.dv_kv_pack(cw, 0, 1, sw, ew, dw, variant=dv.DV_VARIANT_TILE)) == \
         dv.DV_ERR_UNSUPPORTED
-    # the one-token kernel refuses longer ranges
-    assert _status(lambda: dv.dv_kv_pack(cache, 0, 2, s, e, dst,
+    # the token kernel refuses ranges of different lengths
+    assert _status(lambda: dv.dv_kv_pack(cache, 0, 2, s, np.array([32, 16], np.int32), dst,
                                          variant=dv.DV_VARIANT_TOKEN)) == dv.DV_ERR_UNSUPPORTED
     # staging smaller than one layer slab
     host = H.pinned(n)
