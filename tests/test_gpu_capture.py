@@ -1,0 +1,54 @@
+"""The pack and unpack calls inside a CUDA graph captured in torch's default
+(global) capture mode, as a serving engine captures its decode step: the
+replayed graph moves the same bytes as the eager calls."""
+import numpy as np
+import pytest
+import torch
+
+import kv_cache_streaming_gb300 as dv
+import oracle
+from synth.configs import Geometry
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+ORC = oracle.default()
+
+
+def test_pack_unpack_in_a_globally_captured_graph():
+    g = Geometry("cap", 4, 4, 8, 128, 256, 2, "fp16")
+    kh, vh = H.host_cache(g, 91)
+    cache = H.device_cache(g, fill=(kh, vh))
+    back = H.device_cache(g, fill="zero")
+    pos = np.array([10, 200, 0, 77], np.int32)
+    e1 = pos + np.array([1, 1, 0, 1], np.int32)          # a decode delta (token kernel)
+    s2 = np.zeros(g.batch, np.int32)
+    e2 = np.array([100, 256, 3, 64], np.int32)           # ragged prefixes (tile / flat)
+    n1 = ORC.staging_bytes(g, 0, g.num_layers, pos, e1)
+    n2 = ORC.staging_bytes(g, 0, g.num_layers, s2, e2)
+    b1, b2 = H.device_bytes(n1), H.device_bytes(n2)
+    host = H.pinned(n1)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):  # eager once (first-use set-up happens here)
+        dv.dv_kv_pack(cache, 0, g.num_layers, pos, e1, b1, stream=s)
+        dv.dv_kv_pack(cache, 0, g.num_layers, s2, e2, b2, stream=s)
+    torch.cuda.synchronize()
+    b1.zero_()
+    b2.zero_()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):  # default capture_error_mode="global"
+        dv.dv_kv_pack(cache, 0, g.num_layers, pos, e1, b1, stream=s)
+        dv.dv_kv_pack(cache, 0, g.num_layers, s2, e2, b2, stream=s)
+        dv.dv_kv_pack(cache, 0, g.num_layers, pos, e1, host, stream=s)  # zero copy to host
+        dv.dv_kv_unpack(back, 0, g.num_layers, s2, e2, b2, stream=s)
+        dv.dv_kv_unpack(back, 0, g.num_layers, pos, e1, b1, stream=s)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(H.to_np(b1)[:n1], ORC.pack(g, kh, vh, 0, g.num_layers, pos, e1))
+    assert np.array_equal(H.to_np(b2)[:n2], ORC.pack(g, kh, vh, 0, g.num_layers, s2, e2))
+    assert np.array_equal(host.numpy()[:n1], H.to_np(b1)[:n1])
+    kw, vw = np.zeros_like(kh), np.zeros_like(vh)
+    ORC.unpack(g, kw, vw, 0, g.num_layers, s2, e2, ORC.pack(g, kh, vh, 0, g.num_layers, s2, e2))
+    ORC.unpack(g, kw, vw, 0, g.num_layers, pos, e1, ORC.pack(g, kh, vh, 0, g.num_layers, pos, e1))
+    assert np.array_equal(H.to_np(back.k), kw) and np.array_equal(H.to_np(back.v), vw)
