@@ -838,6 +838,124 @@ class MicrobatchSwapping:
                 "note": "the double schedule can hide at most min(swap-in, compute) per step"}
 
 
+def workload_section(torch, dv):
+    """The other workloads' operations on their full sizes (seeded caches, the
+    same calls the parity tests check), as payload GB/s; one timed run each
+    after a warm-up of the same call."""
+    from synth.configs import TINY, OPT13B, BLOOM_STAGE, tiny_ranges, opt13b_lengths, \
+        bloom_lengths, BLOOM_DECODE_STEPS
+    from synth import gpu as synth_gpu
+    s = torch.cuda.Stream()
+    out = {}
+
+    def cache_of(g, seed):
+        k = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+        v = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+        synth_gpu.fill_cache(g, k, v, seed)
+        return dv.Cache.from_geometry(g, k, v)
+
+    def timed(fn, reps=3):
+        ts = []
+        for _ in range(reps + 1):
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s):
+                a.record(s)
+                fn()
+                b.record(s)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) / 1e3)
+        return statistics.median(ts[1:])
+
+    # workload 1: tiny cache, prompt [0,37) and the decode token (latency)
+    c = cache_of(TINY, seed_of(1))
+    (ps, pe), (ds, de) = tiny_ranges()
+    buf = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    L = TINY.num_layers
+    def graph_us(fn, n=20):
+        """GPU time per call: n calls captured in one graph, replayed."""
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s, capture_error_mode="relaxed"):
+            for _ in range(n):
+                fn()
+        t = timed(graph.replay)
+        del graph
+        return round(1e6 * t / n, 2)
+
+    def host_us(fn, n=200):
+        """Host time per call (argument checks and the launch), eager."""
+        with torch.cuda.stream(s):
+            fn()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(n):
+                fn()
+            t1 = time.perf_counter()
+        torch.cuda.synchronize()
+        return round(1e6 * (t1 - t0) / n, 2)
+
+    pp = lambda: dv.dv_kv_pack(c, 0, L, ps, pe, buf, s)  # noqa: E731
+    pt = lambda: dv.dv_kv_pack(c, 0, L, ds, de, buf, s)  # noqa: E731
+    up = lambda: dv.dv_kv_unpack(c, 0, L, ps, pe, buf, s)  # noqa: E731
+    out["tiny"] = {"pack_prompt_gpu_us": graph_us(pp), "pack_token_gpu_us": graph_us(pt),
+                   "unpack_prompt_gpu_us": graph_us(up), "host_us_per_call": host_us(pt)}
+    del c, buf
+    # workload 3: OPT-13B swap-out / swap-in of the used prefixes
+    g = OPT13B
+    c = cache_of(g, seed_of(3))
+    lens = opt13b_lengths()
+    zs = np.zeros(g.batch, np.int32)
+    n = dv.dv_staging_bytes(c, 0, g.num_layers, zs, lens)
+    host = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    stg = torch.empty(4 * (n // g.num_layers), dtype=torch.uint8, device="cuda")
+    res = {"payload_bytes": n}
+    for name, st in (("fused", None), ("staged", stg)):
+        res[f"out_{name}_gbs"] = round(n / timed(lambda: dv.dv_swap_out(
+            c, 0, g.num_layers, zs, lens, host, staging=st, stream=s)) / 1e9, 1)
+        res[f"in_{name}_gbs"] = round(n / timed(lambda: dv.dv_swap_in(
+            c, 0, g.num_layers, zs, lens, host, staging=st, stream=s)) / 1e9, 1)
+    out["opt-13b swap"] = res
+    del c, host, stg
+    torch.cuda.empty_cache()
+    # workload 5: BLOOM stage, snapshot + 256 one-token deltas to a replica, restore
+    g = BLOOM_STAGE
+    c = cache_of(g, seed_of(5))
+    len0 = bloom_lengths()
+    zs = np.zeros(g.batch, np.int32)
+    total = dv.dv_staging_bytes(c, 0, g.num_layers, zs, len0 + BLOOM_DECODE_STEPS)
+    arena = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    rep = dv.Replica(arena, g.batch)
+    snap = dv.dv_staging_bytes(c, 0, g.num_layers, zs, len0)
+
+    def append_all():
+        rep.truncate(0)
+        rep.append(c, 0, g.num_layers, zs, len0, step=0, stream=s)
+        pos = len0.copy()
+        for k in range(1, BLOOM_DECODE_STEPS + 1):
+            rep.append(c, 0, g.num_layers, pos, pos + 1, step=k, stream=s)
+            pos = pos + 1
+
+    t_app = timed(append_all, reps=1)
+    back = cache_of(g, 0)
+    t_res = timed(lambda: rep.restore(back, stream=s), reps=1)
+    out["bloom-176b-stage replica"] = {
+        "records": BLOOM_DECODE_STEPS + 1, "bytes": total, "snapshot_bytes": snap,
+        "append_gbs": round(total / t_app / 1e9, 1), "restore_gbs": round(total / t_res / 1e9, 1),
+        "delta_append_us": None}
+    # one delta on its own (the per-step replication cost)
+    pos = len0 + BLOOM_DECODE_STEPS - 1
+    rep.truncate(BLOOM_DECODE_STEPS)
+    t_one = timed(lambda: (rep.truncate(BLOOM_DECODE_STEPS),
+                           rep.append(c, 0, g.num_layers, pos, pos + 1, step=BLOOM_DECODE_STEPS,
+                                      stream=s)))
+    out["bloom-176b-stage replica"]["delta_append_us"] = round(1e6 * t_one, 1)
+    rep.close()
+    del c, back, arena
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_mine(args):
     import torch
     rank, world, local = dist_init()
@@ -879,6 +997,8 @@ def run_mine(args):
     naive = naive_vs_buffered(b.torch, b.dv) if extra else None
     streaming = DecodeStreaming(b.torch, b.dv).measure() if extra else None
     mb_swap = MicrobatchSwapping(b.torch, b.dv).measure() if extra else None
+    b.torch.cuda.empty_cache()
+    workloads = workload_section(b.torch, b.dv) if extra else None
     cpu = None
     if rank == 0:
         smp = OracleSample(8)
@@ -919,6 +1039,7 @@ def run_mine(args):
         "naive_vs_buffered": naive,
         "decode_streaming": streaming,
         "microbatch_swapping": mb_swap,
+        "workloads": workloads,
         "gpu_launches": b.launches_per_step * args.steps,
         "clocks": clk,
     }
