@@ -26,8 +26,10 @@
 //    per thread, the record found with multiply-high divisions by host
 //    constants; no shared memory, no barrier.  A one-token K record is C
 //    isolated 16-byte chunks (S * 16 bytes apart) by the layout itself.
-//  * flat_kernel (anything else short): thread per staging chunk, in staging
-//    order, sequence found by binary search in shared memory.
+//  * flat_kernel (ragged short ranges): thread per staging chunk, in staging
+//    order; the sequence by binary search over the prefix table passed by
+//    value, head and token by a multiply-high division with the sequence's
+//    host constant; no shared memory, no barrier.
 // All launches use programmatic dependent launch: a kernel waits for the grids
 // it depends on (griddepcontrol.wait) before touching memory, then lets the
 // next launch in the stream be scheduled.  Nothing waits on anything else
@@ -57,6 +59,7 @@ struct KParams {
   int32_t seq_len[MAXB];
   int32_t tok_pre[MAXB + 1];
   int32_t tile_pre[MAXB + 1];  // tile kernel: H * sum of ceil(len / TB)
+  uint32_t m_len[MAXB];        // flat kernel: ceil(2^32 / seq_len[b]), 0 for length 1
 };
 
 #ifndef DV_TILE_CPT
@@ -156,18 +159,7 @@ __device__ __forceinline__ uint64_t div64_by(uint64_t n, uint64_t d, uint64_t m)
 template <bool PACK, int MAXB, int LOG2C>
 __global__ void __launch_bounds__(kThreads)
 flat_kernel(const __grid_constant__ KParams<MAXB> p) {
-  __shared__ int32_t s_rec_pre[MAXB + 1];  // first token record of each sequence
-  __shared__ int32_t s_len[MAXB];
-  __shared__ int32_t s_start[MAXB];
   pdl_enter();
-  for (int i = threadIdx.x; i <= p.B; i += kThreads) {
-    s_rec_pre[i] = p.H * p.tok_pre[i];
-    if (i < p.B) {
-      s_len[i] = p.seq_len[i];
-      s_start[i] = p.seq_start[i];
-    }
-  }
-  __syncthreads();
   const int32_t C = LOG2C >= 0 ? (1 << LOG2C) : p.C;
   const int64_t step = (int64_t)gridDim.x * (kThreads * kFlatUnroll);
   for (int64_t base = (int64_t)blockIdx.x * (kThreads * kFlatUnroll) + threadIdx.x;
@@ -181,13 +173,19 @@ flat_kernel(const __grid_constant__ KParams<MAXB> p) {
       if (g < p.total) {
         const int64_t lkv = (int64_t)div64_by((uint64_t)g, (uint64_t)p.lkv_chunks, p.m_HT);
         const int32_t r = (int32_t)(g - lkv * p.lkv_chunks);
-        const int32_t rec = LOG2C >= 0 ? (r >> LOG2C) : r / C;  // (b, h, t) record
+        const int32_t rec = LOG2C >= 0 ? (r >> LOG2C) : r / C;
         const int32_t c = r - rec * C;
-        const int b = find_seq(s_rec_pre, p.B, rec);
-        const int32_t rr = rec - s_rec_pre[b];
-        const int32_t len = s_len[b];
-        const int32_t h = rr / len;
-        const int64_t t = s_start[b] + (rr - h * len);
+        int lo = 0, hi = p.B - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (p.H * p.tok_pre[mid] <= rec) lo = mid; else hi = mid - 1;
+        }
+        const int b = lo;
+        const int32_t rr = rec - p.H * p.tok_pre[b];
+        const int32_t len = p.seq_len[b];
+        const int32_t h = p.m_len[b] ? (int32_t)div_by((uint32_t)rr, (uint32_t)len, p.m_len[b])
+                                     : rr;
+        const int64_t t = p.seq_start[b] + (rr - h * len);
         const int64_t l = p.l0 + (lkv >> 1);
         const int64_t bh = (int64_t)b * p.H + h;
         cptr[u] = (lkv & 1) == 0 ? p.k + l * p.layer_chunks + ((bh * C + c) * p.S + t)
@@ -418,6 +416,8 @@ cudaError_t launch_kernel(void (*kernel)(Params), unsigned grid, size_t smem,
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 
+inline uint64_t div_magic(uint32_t d) { return ((1ull << 32) + d - 1) / d; }
+
 // ceil(2^64 / d) for d >= 2; 0 for d <= 1 (div64_by then returns n).
 inline uint64_t div64_magic(uint64_t d) {
   if (d <= 1) return 0;
@@ -461,6 +461,8 @@ cudaError_t run_flat(const Plan& p, void* stg, cudaStream_t stream) {
   kp.total = 2 * (int64_t)(p.l1 - p.l0) * p.lkv_chunks;
   kp.tiles_per_lkv = 0;
   kp.m_HT = div64_magic((uint64_t)p.lkv_chunks);  // the flat kernel divides by lkv_chunks
+  for (int b = 0; b < p.B; ++b)
+    kp.m_len[b] = p.seq_len[b] > 1 ? (uint32_t)div_magic((uint32_t)p.seq_len[b]) : 0u;
   const auto kernel = flat_kernel<PACK, MAXB, LOG2C>;
   const int64_t want = (kp.total + kThreads * kFlatUnroll - 1) / (kThreads * kFlatUnroll);
   const int64_t cap = (int64_t)sm_count() * blocks_per_sm(kernel, 0, occ_cache);
@@ -490,8 +492,6 @@ cudaError_t run_tile(const Plan& p, void* stg, cudaStream_t stream) {
   const unsigned grid = (unsigned)(tiles < cap ? tiles : cap);
   return launch_kernel(kernel, grid, smem, stream, kp);
 }
-
-inline uint64_t div_magic(uint32_t d) { return ((1ull << 32) + d - 1) / d; }
 
 template <bool PACK, int MAXB, int LOG2C>
 cudaError_t run_token(const Plan& p, void* stg, cudaStream_t stream) {
