@@ -43,7 +43,7 @@ _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
 _I64 = ctypes.c_int64
 _SZ = ctypes.c_size_t
-_I32P = ctypes.POINTER(ctypes.c_int32)
+_I32P = _P  # int32 host arrays, passed by address
 _CP = ctypes.POINTER(dv_cache)
 _RANGE = [_CP, _I32, _I32, _I32P, _I32P]
 
@@ -118,10 +118,26 @@ def _stream(s):
     return s.cuda_stream
 
 
-def _ranges(seq_start, seq_end):
-    s = np.ascontiguousarray(seq_start, dtype=np.int32)
-    e = np.ascontiguousarray(seq_end, dtype=np.int32)
-    return s, e, s.ctypes.data_as(_I32P), e.ctypes.data_as(_I32P)
+def _addr(a):
+    """Address of a contiguous int32 numpy array's data (the cheapest route
+    through ctypes; read-only arrays are copied first)."""
+    try:
+        return ctypes.addressof(ctypes.c_int32.from_buffer(a)), a
+    except (TypeError, ValueError):
+        a = a.copy()
+        return ctypes.addressof(ctypes.c_int32.from_buffer(a)), a
+
+
+def _ranges(seq_start, seq_end, batch):
+    """int32 copies (or views) of the ranges and their addresses; the library
+    reads exactly `batch` entries of each, so shorter arrays are refused."""
+    s = np.ascontiguousarray(seq_start, dtype=np.int32).reshape(-1)
+    e = np.ascontiguousarray(seq_end, dtype=np.int32).reshape(-1)
+    if s.size != batch or e.size != batch:
+        raise ValueError(f"seq_start / seq_end need {batch} entries (got {s.size}, {e.size})")
+    sp, s = _addr(s)
+    ep, e = _addr(e)
+    return s, e, sp, ep
 
 
 class Cache:
@@ -180,7 +196,7 @@ def dv_allocation_extent(ptr):
 
 
 def dv_staging_bytes(cache: Cache, l0, l1, seq_start, seq_end) -> int:
-    s, e, sp, ep = _ranges(seq_start, seq_end)
+    s, e, sp, ep = _ranges(seq_start, seq_end, cache.c.batch)
     out = _SZ(0)
     _check(_staging_bytes(cache.ref, l0, l1, sp, ep, ctypes.byref(out)))
     return out.value
@@ -188,14 +204,14 @@ def dv_staging_bytes(cache: Cache, l0, l1, seq_start, seq_end) -> int:
 
 def dv_kv_pack(cache: Cache, l0, l1, seq_start, seq_end, dst, stream=None,
                variant=DV_VARIANT_AUTO, dst_bytes=None) -> None:
-    s, e, sp, ep = _ranges(seq_start, seq_end)
+    s, e, sp, ep = _ranges(seq_start, seq_end, cache.c.batch)
     d, n = _buf(dst, dst_bytes)
     _check(_pack(cache.ref, l0, l1, sp, ep, d, n, _stream(stream), variant))
 
 
 def dv_kv_unpack(cache: Cache, l0, l1, seq_start, seq_end, src, stream=None,
                  variant=DV_VARIANT_AUTO, src_bytes=None) -> None:
-    s, e, sp, ep = _ranges(seq_start, seq_end)
+    s, e, sp, ep = _ranges(seq_start, seq_end, cache.c.batch)
     d, n = _buf(src, src_bytes)
     _check(_unpack(cache.ref, l0, l1, sp, ep, d, n, _stream(stream), variant))
 
@@ -203,7 +219,7 @@ def dv_kv_unpack(cache: Cache, l0, l1, seq_start, seq_end, src, stream=None,
 def dv_naive_gather(cache: Cache, l0, l1, seq_start, seq_end, dst, stream=None,
                     dst_bytes=None) -> int:
     """The per-region copy baseline; returns the number of copies enqueued."""
-    s, e, sp, ep = _ranges(seq_start, seq_end)
+    s, e, sp, ep = _ranges(seq_start, seq_end, cache.c.batch)
     d, n = _buf(dst, dst_bytes)
     calls = _I64(0)
     _check(_naive_gather(cache.ref, l0, l1, sp, ep, d, n, _stream(stream), ctypes.byref(calls)))
@@ -212,7 +228,7 @@ def dv_naive_gather(cache: Cache, l0, l1, seq_start, seq_end, dst, stream=None,
 
 def dv_swap_out(cache: Cache, l0, l1, seq_start, seq_end, host_dst, staging=None,
                 stream=None) -> None:
-    s, e, sp, ep = _ranges(seq_start, seq_end)
+    s, e, sp, ep = _ranges(seq_start, seq_end, cache.c.batch)
     h, hn = _buf(host_dst)
     st, sn = _buf(staging)
     _check(_swap_out(cache.ref, l0, l1, sp, ep, h, hn, st, sn, _stream(stream)))
@@ -220,7 +236,7 @@ def dv_swap_out(cache: Cache, l0, l1, seq_start, seq_end, host_dst, staging=None
 
 def dv_swap_in(cache: Cache, l0, l1, seq_start, seq_end, host_src, staging=None,
                stream=None) -> None:
-    s, e, sp, ep = _ranges(seq_start, seq_end)
+    s, e, sp, ep = _ranges(seq_start, seq_end, cache.c.batch)
     h, hn = _buf(host_src)
     st, sn = _buf(staging)
     _check(_swap_in(cache.ref, l0, l1, sp, ep, h, hn, st, sn, _stream(stream)))
@@ -230,7 +246,7 @@ def dv_swap_out_noalloc(cache: Cache, l0, l1, seq_start, seq_end, host_dst,
                         stream=None) -> None:
     """dv_swap_out through libdv's built-in 64 MiB staging buffer (no
     allocation by the caller); see dv.h for the limits."""
-    s, e, sp, ep = _ranges(seq_start, seq_end)
+    s, e, sp, ep = _ranges(seq_start, seq_end, cache.c.batch)
     h, hn = _buf(host_dst)
     _check(_swap_out_noalloc(cache.ref, l0, l1, sp, ep, h, hn, _stream(stream)))
 
@@ -248,7 +264,7 @@ class Streamer:
         self.h = h
 
     def stream_layer(self, cache: Cache, layer, seq_start, seq_end, host_dst, l0=0):
-        s, e, sp, ep = _ranges(seq_start, seq_end)
+        s, e, sp, ep = _ranges(seq_start, seq_end, cache.c.batch)
         d, n = _buf(host_dst)
         _check(_stream_layer(self.h, cache.ref, layer, sp, ep, d, n, l0))
 
@@ -295,7 +311,7 @@ class Replica:
         self.h = h
 
     def append(self, cache: Cache, l0, l1, seq_start, seq_end, step, staging=None, stream=None):
-        s, e, sp, ep = _ranges(seq_start, seq_end)
+        s, e, sp, ep = _ranges(seq_start, seq_end, cache.c.batch)
         st, sn = _buf(staging)
         _check(_replica_append(self.h, cache.ref, l0, l1, sp, ep, step, st, sn, _stream(stream)))
 

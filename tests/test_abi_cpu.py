@@ -106,3 +106,17 @@ def test_slab_beyond_32_bit_chunk_indexing_is_refused():
     assert _status(lambda: dv.dv_staging_bytes(c, 0, 1, s, e)) == dv.DV_ERR_UNSUPPORTED
     e[:] = 1  # a one-token slab is fine
     assert dv.dv_staging_bytes(c, 0, 1, s, e) == 2 * 1024 * 128 * 128 * 2
+
+
+def test_binding_refuses_ranges_of_the_wrong_length():
+    """The library reads `batch` entries of each range array: the binding
+    refuses shorter or longer arrays before calling it."""
+    g = Geometry("v", 2, 4, 2, 64, 16, 2, "raw")
+    c = _cache(g)
+    with pytest.raises(ValueError):
+        dv.dv_staging_bytes(c, 0, 2, [0, 0], [1, 1])
+    with pytest.raises(ValueError):
+        dv.dv_kv_pack(c, 0, 2, np.zeros(5), np.ones(5), (0x3000, 1 << 20), stream=0)
+    ro = np.zeros(4, np.int32)
+    ro.setflags(write=False)  # read-only arrays are accepted (copied)
+    assert dv.dv_staging_bytes(c, 0, 2, ro, ro + 3) == 2 * 2 * 2 * 64 * 2 * 12
