@@ -45,7 +45,10 @@
  *  - Memory kinds: k_base / v_base and `staging` are device memory of the
  *    current device.  A pack destination or unpack source may be device
  *    memory or pinned (page-locked, mapped) host memory; for host memory the
- *    kernel reads or writes it directly over the host link (zero copy).
+ *    kernel reads or writes it directly over the host link (zero copy) with a
+ *    small grid (32 CTAs by default, the environment variable DV_HOST_CTAS
+ *    overrides it, 0 for none), enough for the link, so that other kernels
+ *    keep the rest of the GPU.
  *  - Alignment: k_base, v_base, buffers and layer_stride_elems * elem_bytes
  *    must be multiples of 16 bytes (DV_ERR_MISALIGNED); head_dim must be a
  *    multiple of x (DV_ERR_UNSUPPORTED).  batch <= DV_MAX_BATCH.

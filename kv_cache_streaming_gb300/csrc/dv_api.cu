@@ -117,12 +117,15 @@ dv_status plan_ranges(const dv_cache* c, int32_t l0, int32_t l1, const int32_t* 
   p->bytes = 2 * (int64_t)(l1 - l0) * p->lkv_chunks * 16;
   p->k = c->k_base;
   p->v = c->v_base;
+  p->host_side = false;
   return DV_OK;
 }
 
 // Device-visible address of `ptr` after checking its memory kind; when the
 // driver knows the allocation, also that [ptr, ptr + need) lies inside it.
-dv_status resolve(const void* ptr, size_t need, bool allow_host, const char* what, void** dev) {
+dv_status resolve(const void* ptr, size_t need, bool allow_host, const char* what, void** dev,
+                  bool* is_host = nullptr) {
+  if (is_host) *is_host = false;
   if (!ptr) return fail(DV_ERR_INVALID_ARG, "%s is NULL", what);
   if (!aligned16(ptr)) return fail(DV_ERR_MISALIGNED, "%s %p is not 16-byte aligned", what, ptr);
   cudaPointerAttributes a;
@@ -150,6 +153,7 @@ dv_status resolve(const void* ptr, size_t need, bool allow_host, const char* wha
       if (!a.devicePointer)
         return fail(DV_ERR_INVALID_ARG, "%s: pinned host memory not mapped for the device", what);
       *dev = a.devicePointer;
+      if (is_host) *is_host = true;
       break;
     default:
       return fail(DV_ERR_INVALID_ARG, "%s is not CUDA-registered memory (pageable host memory "
@@ -207,7 +211,7 @@ dv_status do_pack(const dv_cache* c, int32_t l0, int32_t l1, const int32_t* s, c
                 dst_bytes);
   if ((st = resolve_cache(c, &p)) != DV_OK) return st;
   void* d = nullptr;
-  if ((st = resolve(dst, (size_t)p.bytes, true, "dst", &d)) != DV_OK) return st;
+  if ((st = resolve(dst, (size_t)p.bytes, true, "dst", &d, &p.host_side)) != DV_OK) return st;
   const cudaError_t err = dv::launch_pack(p, d, stream, variant);
   return err == cudaSuccess ? DV_OK : cuda_fail(err, "pack launch");
 }
@@ -225,7 +229,7 @@ dv_status do_unpack(const dv_cache* c, int32_t l0, int32_t l1, const int32_t* s,
                 (long long)p.bytes, src_bytes);
   if ((st = resolve_cache(c, &p)) != DV_OK) return st;
   void* d = nullptr;
-  if ((st = resolve(src, (size_t)p.bytes, true, "src", &d)) != DV_OK) return st;
+  if ((st = resolve(src, (size_t)p.bytes, true, "src", &d, &p.host_side)) != DV_OK) return st;
   const cudaError_t err = dv::launch_unpack(p, d, stream, variant);
   return err == cudaSuccess ? DV_OK : cuda_fail(err, "unpack launch");
 }
@@ -264,6 +268,7 @@ dv_status do_swap(Dir dir, const dv_cache* c, int32_t l0, int32_t l1, const int3
     return st;
   cudaError_t err;
   if (!staging) {  // fused: the kernel touches host memory directly
+    p.host_side = true;
     err = dir == Dir::kOut ? dv::launch_pack(p, host_dev, stream, dv::kAuto)
                            : dv::launch_unpack(p, host_dev, stream, dv::kAuto);
     return err == cudaSuccess ? DV_OK : cuda_fail(err, "fused swap launch");

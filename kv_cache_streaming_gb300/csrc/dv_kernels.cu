@@ -36,6 +36,7 @@
 // but __syncthreads.
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 
 #include "dv_plan.h"
 
@@ -418,6 +419,30 @@ cudaError_t launch_kernel(void (*kernel)(Params), unsigned grid, size_t smem,
 
 inline uint64_t div_magic(uint32_t d) { return ((1ull << 32) + d - 1) / d; }
 
+// Grid cap for a transfer whose staging side is (mapped) host memory: it is
+// bound by the host link, so it keeps to a few CTAs and leaves the rest of
+// the GPU to other work.  32 CTAs of 256 threads carry the full link (193 /
+// 211 GB/s each way on the GB300 measured) and let a concurrent compute
+// kernel run nearly unslowed; the whole GPU would serialise it.  The
+// environment variable DV_HOST_CTAS, read once, overrides the count (0: no
+// cap) for hosts with a faster link.
+int64_t host_ctas() {
+  static const int64_t v = [] {
+    const char* e = std::getenv("DV_HOST_CTAS");
+    if (!e || !*e) return (int64_t)32;
+    const long x = std::strtol(e, nullptr, 10);
+    return (int64_t)(x > 0 ? x : 0);
+  }();
+  return v;
+}
+
+// `per_cta` scales the count by the bytes a CTA keeps in flight relative to
+// a tile CTA's 16 KiB (the token kernel keeps 4 KiB, so it gets 4x the CTAs).
+inline int64_t host_cap(const Plan& p, int64_t cap, int64_t per_cta = 1) {
+  const int64_t h = host_ctas() * per_cta;
+  return (h > 0 && p.host_side && cap > h) ? h : cap;
+}
+
 // ceil(2^64 / d) for d >= 2; 0 for d <= 1 (div64_by then returns n).
 inline uint64_t div64_magic(uint64_t d) {
   if (d <= 1) return 0;
@@ -465,7 +490,7 @@ cudaError_t run_flat(const Plan& p, void* stg, cudaStream_t stream) {
     kp.m_len[b] = p.seq_len[b] > 1 ? (uint32_t)div_magic((uint32_t)p.seq_len[b]) : 0u;
   const auto kernel = flat_kernel<PACK, MAXB, LOG2C>;
   const int64_t want = (kp.total + kThreads * kFlatUnroll - 1) / (kThreads * kFlatUnroll);
-  const int64_t cap = (int64_t)sm_count() * blocks_per_sm(kernel, 0, occ_cache);
+  const int64_t cap = host_cap(p, (int64_t)sm_count() * blocks_per_sm(kernel, 0, occ_cache));
   const unsigned grid = (unsigned)(want < cap ? want : cap);
   return launch_kernel(kernel, grid, 0, stream, kp);
 }
@@ -488,7 +513,7 @@ cudaError_t run_tile(const Plan& p, void* stg, cudaStream_t stream) {
   kp.m_tpl = div64_magic((uint64_t)kp.tiles_per_lkv);
   const size_t smem = (size_t)TB * (p.C | 1) * sizeof(uint4);
   const auto kernel = tile_kernel<PACK, MAXB, LOG2C>;
-  const int64_t cap = (int64_t)sm_count() * blocks_per_sm(kernel, smem, occ_cache);
+  const int64_t cap = host_cap(p, (int64_t)sm_count() * blocks_per_sm(kernel, smem, occ_cache));
   const unsigned grid = (unsigned)(tiles < cap ? tiles : cap);
   return launch_kernel(kernel, grid, smem, stream, kp);
 }
@@ -521,7 +546,7 @@ cudaError_t run_token(const Plan& p, void* stg, cudaStream_t stream) {
   kp.S = p.S;
   const auto kernel = token_kernel<PACK, MAXB, LOG2C>;
   const unsigned want = (kp.total + kThreads - 1) / kThreads;
-  const unsigned cap = (unsigned)sm_count() * 8;
+  const unsigned cap = (unsigned)host_cap(p, (int64_t)sm_count() * 8, 4);
   return launch_kernel(kernel, want < cap ? want : cap, 0, stream, kp);
 }
 

@@ -31,6 +31,7 @@ struct Plan {
   int64_t bytes;             // staging bytes: 2 * (l1 - l0) * lkv_chunks * 16
   void* k;                   // device-visible K / V bases
   void* v;
+  bool host_side;            // the staging bytes are in (mapped) host memory
 };
 
 // Re-targets `p` to the layer sub-range [la, lb) (inside [p.l0, p.l1)).
