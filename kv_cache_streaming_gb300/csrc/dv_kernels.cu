@@ -22,10 +22,11 @@
 //    fall in 8 distinct 16-byte bank groups.  The grid is persistent (SMs x
 //    resident CTAs) and strides over the tiles in staging order, so at any
 //    moment the whole GPU works on neighbouring tiles.
-//  * token_kernel (every range at most one token: decode deltas): one chunk
-//    per thread, the record found with multiply-high divisions by host
-//    constants; no shared memory, no barrier.  A one-token K record is C
-//    isolated 16-byte chunks (S * 16 bytes apart) by the layout itself.
+//  * token_kernel (every non-empty range of one common length: one-token
+//    decode deltas, multi-token deltas): one chunk per thread, its run and
+//    token found with multiply-high divisions by host constants; no shared
+//    memory, no barrier.  A one-token K record is C isolated 16-byte chunks
+//    (S * 16 bytes apart) by the layout itself.
 //  * flat_kernel (ragged short ranges): thread per staging chunk, in staging
 //    order; the sequence by binary search over the prefix table passed by
 //    value, head and token by a multiply-high division with the sequence's
@@ -33,7 +34,8 @@
 // All launches use programmatic dependent launch: a kernel waits for the grids
 // it depends on (griddepcontrol.wait) before touching memory, then lets the
 // next launch in the stream be scheduled.  Nothing waits on anything else
-// but __syncthreads.
+// but __syncthreads.  A launch whose staging side is host memory keeps to a
+// small grid (see host_ctas) and leaves the rest of the GPU to other work.
 #include <atomic>
 #include <cstdint>
 #include <cstdlib>
@@ -55,7 +57,7 @@ struct KParams {
   int32_t l0, B, H, C, S;
   int32_t tiles_per_lkv;   // tile kernel: tiles per (layer, K|V) slab
   uint64_t m_tpl;          // ceil(2^64 / tiles_per_lkv) (0 when it is 1)
-  uint64_t m_HT;           // ceil(2^64 / (H * T)) (0 when it is 1); flat kernel: of lkv_chunks
+  uint64_t m_lkv;          // flat kernel: ceil(2^64 / lkv_chunks) (0 when it is 1)
   int32_t seq_start[MAXB];
   int32_t seq_len[MAXB];
   int32_t tok_pre[MAXB + 1];
@@ -172,7 +174,7 @@ flat_kernel(const __grid_constant__ KParams<MAXB> p) {
       const int64_t g = base + u * kThreads;
       cptr[u] = nullptr;
       if (g < p.total) {
-        const int64_t lkv = (int64_t)div64_by((uint64_t)g, (uint64_t)p.lkv_chunks, p.m_HT);
+        const int64_t lkv = (int64_t)div64_by((uint64_t)g, (uint64_t)p.lkv_chunks, p.m_lkv);
         const int32_t r = (int32_t)(g - lkv * p.lkv_chunks);
         const int32_t rec = LOG2C >= 0 ? (r >> LOG2C) : r / C;
         const int32_t c = r - rec * C;
@@ -485,7 +487,7 @@ cudaError_t run_flat(const Plan& p, void* stg, cudaStream_t stream) {
   fill_params(kp, p, stg);
   kp.total = 2 * (int64_t)(p.l1 - p.l0) * p.lkv_chunks;
   kp.tiles_per_lkv = 0;
-  kp.m_HT = div64_magic((uint64_t)p.lkv_chunks);  // the flat kernel divides by lkv_chunks
+  kp.m_lkv = div64_magic((uint64_t)p.lkv_chunks);  // the flat kernel divides by lkv_chunks
   for (int b = 0; b < p.B; ++b)
     kp.m_len[b] = p.seq_len[b] > 1 ? (uint32_t)div_magic((uint32_t)p.seq_len[b]) : 0u;
   const auto kernel = flat_kernel<PACK, MAXB, LOG2C>;
