@@ -441,7 +441,7 @@ class Bench:
         si = ins[0]
         si.wait_stream(s)
         si.wait_stream(ins[1])
-        self.replica.restore(self.cache_b, staging=stgs[0], stream=si)
+        self.replica.restore_batched(self.cache_b, staging=stgs[0], stream=si)
         s.wait_stream(si)
 
     def timed_e2e(self, steps, warmup, world):
@@ -738,7 +738,7 @@ class MicrobatchSwapping:
             slot = self.slots[0]
             for _ in range(self.rounds):
                 for m in range(self.N):
-                    self.replicas[m].restore(slot, staging=self.staging, stream=s)
+                    self.replicas[m].restore_batched(slot, staging=self.staging, stream=s)
                     act = self._compute_and_write(m, slot, s)
                     ln = self.lens[m]
                     self.replicas[m].append(slot, 0, L, ln, ln + act, step=self.step_no[m],
@@ -750,7 +750,8 @@ class MicrobatchSwapping:
             done = [torch.cuda.Event() for _ in range(2)]
             order = [m for _ in range(self.rounds) for m in range(self.N)]
             # prefetch the first microbatch into slot 0
-            self.replicas[order[0]].restore(self.slots[0], staging=self.staging, stream=s2)
+            self.replicas[order[0]].restore_batched(self.slots[0], staging=self.staging,
+                                                    stream=s2)
             ready[0].record(s2)
             for i, m in enumerate(order):
                 sl = i % 2
@@ -760,8 +761,8 @@ class MicrobatchSwapping:
                 done[sl].record(s)
                 if i + 1 < len(order):  # the next microbatch comes in on the other slot
                     nxt = order[i + 1]
-                    self.replicas[nxt].restore(self.slots[1 - sl], staging=self.staging,
-                                               stream=s2)
+                    self.replicas[nxt].restore_batched(self.slots[1 - sl], staging=self.staging,
+                                                       stream=s2)
                     ready[1 - sl].record(s2)
                 # swap-out of this microbatch's step: its token, into its replica
                 s2.wait_event(done[sl])
@@ -816,7 +817,7 @@ class MicrobatchSwapping:
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for m in range(self.N):
-            self.replicas[m].restore(slot, staging=self.staging, stream=s)
+            self.replicas[m].restore_batched(slot, staging=self.staging, stream=s)
         s.synchronize()
         t_in = (time.perf_counter() - t0) / self.N
         in_bytes = sum(r.info()[1] for r in self.replicas) / self.N
@@ -842,7 +843,7 @@ def workload_section(torch, dv):
     """The other workloads' operations on their full sizes (seeded caches, the
     same calls the parity tests check), as payload GB/s; one timed run each
     after a warm-up of the same call."""
-    from synth.configs import TINY, OPT13B, BLOOM_STAGE, tiny_ranges, opt13b_lengths, \
+    from synth.configs import TINY, GPT2, OPT13B, BLOOM_STAGE, tiny_ranges, opt13b_lengths, \
         bloom_lengths, BLOOM_DECODE_STEPS
     from synth import gpu as synth_gpu
     s = torch.cuda.Stream()
@@ -900,7 +901,69 @@ def workload_section(torch, dv):
     up = lambda: dv.dv_kv_unpack(c, 0, L, ps, pe, buf, s)  # noqa: E731
     out["tiny"] = {"pack_prompt_gpu_us": graph_us(pp), "pack_token_gpu_us": graph_us(pt),
                    "unpack_prompt_gpu_us": graph_us(up), "host_us_per_call": host_us(pt)}
-    del c, buf
+
+    def restore_pair(g, c, rep, staging=None, reps=3):
+        """One replica restored record by record and record-batched into two
+        caches of the same initial content: times (CUDA events on the stream,
+        host submission included) and whether the results agree."""
+        a = cache_of(g, 0)
+        b = cache_of(g, 0)
+        t_rec = timed(lambda: rep.restore(a, staging=staging, stream=s), reps)
+        t_bat = timed(lambda: rep.restore_batched(b, staging=staging, stream=s), reps)
+        torch.cuda.synchronize()
+        same = bool(torch.equal(a.k, b.k) and torch.equal(a.v, b.v))
+        del a, b
+        return t_rec, t_bat, same
+
+    # restore of a snapshot + decode deltas, record by record vs batched
+    rb = {}
+    nd = 64
+    zs = np.zeros(TINY.batch, np.int32)
+    arena = torch.empty(dv.dv_staging_bytes(c, 0, L, zs, pe + nd) + 4096, dtype=torch.uint8,
+                        pin_memory=True)
+    rep = dv.Replica(arena, TINY.batch)
+    rep.append(c, 0, L, ps, pe, step=0, stream=s)
+    for k in range(nd):
+        rep.append(c, 0, L, pe + k, pe + k + 1, step=k + 1, stream=s)
+    t_rec, t_bat, same = restore_pair(TINY, c, rep)
+    rb["tiny: [0,37) + 64 one-token deltas, fused"] = {
+        "records": nd + 1, "per_record_us": round(1e6 * t_rec, 1),
+        "batched_us": round(1e6 * t_bat, 1), "speedup": round(t_rec / t_bat, 2),
+        "same_result": same}
+    rep.close()
+    del c, buf, arena
+    g = GPT2
+    c = cache_of(g, seed_of(2))
+    zs = np.zeros(g.batch, np.int32)
+    p0 = np.full(g.batch, 1000, np.int32)
+    nd = 24
+    arena = torch.empty(dv.dv_staging_bytes(c, 0, g.num_layers, zs, p0 + nd), dtype=torch.uint8,
+                        pin_memory=True)
+    rep = dv.Replica(arena, g.batch)
+    rep.append(c, 0, g.num_layers, zs, p0, step=0, stream=s)
+    for k in range(nd):
+        rep.append(c, 0, g.num_layers, p0 + k, p0 + k + 1, step=k + 1, stream=s)
+    stg = torch.empty(dv.dv_staging_bytes(c, 0, 1, zs, p0), dtype=torch.uint8, device="cuda")
+    for name, st in (("fused", None), ("staged (one-layer staging buffer)", stg)):
+        t_rec, t_bat, same = restore_pair(g, c, rep, staging=st)
+        rb[f"gpt2-1.5b: [0,1000) + 24 one-token deltas, {name}"] = {
+            "records": nd + 1, "bytes": rep.info()[1], "per_record_ms": round(1e3 * t_rec, 3),
+            "batched_ms": round(1e3 * t_bat, 3), "speedup": round(t_rec / t_bat, 3),
+            "same_result": same}
+    # the deltas alone (the swap-in of delta-only swapping, snapshot elsewhere)
+    rep.truncate(0)
+    for k in range(nd):
+        rep.append(c, 0, g.num_layers, p0 + k, p0 + k + 1, step=k + 1, stream=s)
+    for name, st in (("fused", None), ("staged (one-layer staging buffer)", stg)):
+        t_rec, t_bat, same = restore_pair(g, c, rep, staging=st)
+        rb[f"gpt2-1.5b: 24 one-token deltas only, {name}"] = {
+            "records": nd, "bytes": rep.info()[1], "per_record_us": round(1e6 * t_rec, 1),
+            "batched_us": round(1e6 * t_bat, 1), "speedup": round(t_rec / t_bat, 3),
+            "same_result": same}
+    out["restore_batched"] = rb
+    rep.close()
+    del c, arena, stg
+    torch.cuda.empty_cache()
     # workload 3: OPT-13B swap-out / swap-in of the used prefixes
     g = OPT13B
     c = cache_of(g, seed_of(3))
@@ -939,10 +1002,11 @@ def workload_section(torch, dv):
     t_app = timed(append_all, reps=1)
     back = cache_of(g, 0)
     t_res = timed(lambda: rep.restore(back, stream=s), reps=1)
+    t_bat = timed(lambda: rep.restore_batched(back, stream=s), reps=1)
     out["bloom-176b-stage replica"] = {
         "records": BLOOM_DECODE_STEPS + 1, "bytes": total, "snapshot_bytes": snap,
         "append_gbs": round(total / t_app / 1e9, 1), "restore_gbs": round(total / t_res / 1e9, 1),
-        "delta_append_us": None}
+        "restore_batched_gbs": round(total / t_bat / 1e9, 1), "delta_append_us": None}
     # one delta on its own (the per-step replication cost)
     pos = len0 + BLOOM_DECODE_STEPS - 1
     rep.truncate(BLOOM_DECODE_STEPS)
@@ -1033,8 +1097,8 @@ def run_mine(args):
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps, "verified": e2e_ok,
                 "path": "per layer: dv_stream_layer (pack + D2H copy) then dv_swap_in of that "
                         "layer (H2D copy + unpack) on a third stream, overlapping the next "
-                        "layer's D2H; dv_replica_append x24 (fused) + dv_replica_restore "
-                        "(staged)"},
+                        "layer's D2H; dv_replica_append x24 (fused) + "
+                        "dv_replica_restore_batched (staged)"},
         "swap": swap,
         "naive_vs_buffered": naive,
         "decode_streaming": streaming,

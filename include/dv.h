@@ -282,6 +282,27 @@ dv_status dv_replica_append(dv_replica* replica, const dv_cache* cache, int32_t 
 dv_status dv_replica_restore(const dv_replica* replica, const dv_cache* cache, int64_t upto_step,
                              void* staging, size_t staging_bytes, dv_stream stream);
 
+/* The restore of dv_replica_restore with the records batched: every record
+ * whose ranges are long enough for the tile kernel (normally the snapshot) is
+ * unpacked by itself, as by dv_swap_in; the others (the decode deltas) go
+ * into as few launches of one record-batched unpack kernel as its kernel
+ * parameters allow (up to 128 records per launch; at batch 32, 72 records).
+ * This is the restore of the pages' delta-only swapping: swap-in = snapshot +
+ * every delta (§3 "Microbatch swapping", Fig 9, with the replication log of
+ * "Fault detection and recovery", Fig 10), with one launch for the deltas
+ * instead of one per step.  A launch takes consecutive records whose writes
+ * to the cache are disjoint; where a record overwrites what an earlier record
+ * of the run wrote, a new launch starts, so the result equals dv_replica_restore
+ * (append order) for any log.  staging == NULL: the kernel reads the records
+ * straight from the arena (mapped pinned memory).  Otherwise each launch's
+ * records go to `staging` with one host-to-device copy first (consecutive
+ * records up to staging_bytes; a record larger than staging_bytes is restored
+ * by itself through dv_swap_in's layer groups).  Validates every record before
+ * enqueuing anything; same errors as dv_replica_restore. */
+dv_status dv_replica_restore_batched(const dv_replica* replica, const dv_cache* cache,
+                                     int64_t upto_step, void* staging, size_t staging_bytes,
+                                     dv_stream stream);
+
 /* Drops every record with step >= step (the acknowledged prefix is kept). */
 dv_status dv_replica_truncate(dv_replica* replica, int64_t step);
 

@@ -20,6 +20,7 @@ from .dv import (  # noqa: F401
     dv_abi_version, dv_allocation_extent, dv_debug_fault, dv_staging_bytes, dv_kv_pack, dv_kv_unpack, dv_naive_gather, dv_swap_out, dv_swap_in,
     dv_swap_out_noalloc, DV_NOALLOC_STAGING_BYTES,
     dv_streamer_create, dv_stream_layer, dv_streamer_wait, dv_streamer_destroy,
-    dv_replica_create, dv_replica_append, dv_replica_restore, dv_replica_truncate,
+    dv_replica_create, dv_replica_append, dv_replica_restore, dv_replica_restore_batched,
+    dv_replica_truncate,
     dv_replica_info, dv_replica_destroy,
 )

@@ -679,6 +679,108 @@ dv_status dv_replica_restore(const dv_replica* r, const dv_cache* cache, int64_t
   return DV_OK;
 }
 
+dv_status dv_replica_restore_batched(const dv_replica* r, const dv_cache* cache,
+                                    int64_t upto_step, void* staging, size_t staging_bytes,
+                                    dv_stream stream) {
+  if (!r) return fail(DV_ERR_INVALID_ARG, "replica is NULL");
+  if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
+  if (cache->batch != r->batch)
+    return fail(DV_ERR_INVALID_ARG, "cache batch %d differs from the replica's %d", cache->batch,
+                r->batch);
+  // Validate every record against this cache before enqueuing anything, and
+  // sort them into long-range records (unpacked one by one with the tile
+  // kernel, as dv_swap_in would) and the rest (batched).
+  std::vector<const Record*> todo;
+  std::vector<dv::RecordRanges> recs;
+  std::vector<char> alone;
+  int32_t l_end = 0;
+  size_t total = 0;
+  try {
+    dv::Plan q;
+    for (const Record& rec : r->records) {
+      if (upto_step >= 0 && rec.step >= upto_step) break;
+      const int32_t* s = r->ranges.data() + rec.ranges;
+      dv_status st = plan_ranges(cache, rec.l0, rec.l1, s, s + r->batch, &q);
+      if (st != DV_OK) return st;
+      if ((size_t)q.bytes != rec.bytes)
+        return fail(DV_ERR_INVALID_ARG, "record of step %lld does not match this cache geometry",
+                    (long long)rec.step);
+      if (rec.bytes == 0) continue;
+      const bool by_itself =
+          dv::auto_kind(q) == dv::kTile || (staging && rec.bytes > staging_bytes);
+      if (by_itself && staging && staging_bytes < (size_t)dv::layer_slab_bytes(q))
+        return fail(DV_ERR_BUFFER_TOO_SMALL, "staging of %zu bytes holds less than one layer "
+                    "slab (%lld bytes) of the record of step %lld", staging_bytes,
+                    (long long)dv::layer_slab_bytes(q), (long long)rec.step);
+      todo.push_back(&rec);
+      recs.push_back(dv::RecordRanges{rec.l0, rec.l1, s, s + r->batch});
+      alone.push_back(by_itself);
+      if (rec.l1 > l_end) l_end = rec.l1;
+      total += rec.bytes;
+    }
+  } catch (...) {
+    return fail(DV_ERR_INVALID_ARG, "out of host memory for the restore plan");
+  }
+  const int n = (int)todo.size();
+  if (n == 0) return DV_OK;
+  dv::Plan base;
+  {
+    std::vector<int32_t> zero((size_t)r->batch, 0);
+    dv_status st = plan_ranges(cache, 0, l_end, zero.data(), zero.data(), &base);
+    if (st != DV_OK) return st;
+    if ((st = resolve_cache(cache, &base)) != DV_OK) return st;
+  }
+  void* arena_dev = nullptr;
+  void* stg = nullptr;
+  if (!staging) {
+    dv_status st = check_host(r->arena, "replica arena", &arena_dev);
+    if (st != DV_OK) return st;
+    base.host_side = true;
+  } else {
+    const dv_status st =
+        resolve(staging, total < staging_bytes ? total : staging_bytes, false, "staging", &stg);
+    if (st != DV_OK) return st;
+  }
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  int i = 0;
+  while (i < n) {
+    const Record& first = *todo[i];
+    if (alone[i]) {
+      const int32_t* s = r->ranges.data() + first.ranges;
+      const dv_status st = dv_swap_in(cache, first.l0, first.l1, s, s + r->batch,
+                                      r->arena + first.offset, first.bytes, staging,
+                                      staging_bytes, stream);
+      if (st != DV_OK) return st;
+      ++i;
+      continue;
+    }
+    int run = 0;
+    while (i + run < n && !alone[i + run]) ++run;
+    int k = dv::records_per_launch(base, recs.data() + i, run);
+    size_t bytes = 0;
+    for (int j = 0; j < k; ++j) {
+      if (staging && bytes + todo[i + j]->bytes > staging_bytes) {
+        k = j;
+        break;
+      }
+      bytes += todo[i + j]->bytes;
+    }
+    cudaError_t err;
+    if (staging) {
+      if ((err = cudaMemcpyAsync(stg, r->arena + first.offset, bytes, cudaMemcpyHostToDevice,
+                                 cs)) != cudaSuccess)
+        return cuda_fail(err, "restore copy");
+      err = dv::launch_unpack_records(base, recs.data() + i, k, stg, cs);
+    } else {
+      err = dv::launch_unpack_records(base, recs.data() + i, k,
+                                      static_cast<uint8_t*>(arena_dev) + first.offset, cs);
+    }
+    if (err != cudaSuccess) return cuda_fail(err, "batched restore launch");
+    i += k;
+  }
+  return DV_OK;
+}
+
 dv_status dv_replica_truncate(dv_replica* r, int64_t step) {
   if (!r) return fail(DV_ERR_INVALID_ARG, "replica is NULL");
   size_t keep = 0;

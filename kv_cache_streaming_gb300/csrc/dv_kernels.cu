@@ -37,8 +37,10 @@
 // but __syncthreads.  A launch whose staging side is host memory keeps to a
 // small grid (see host_ctas) and leaves the rest of the GPU to other work.
 #include <atomic>
+#include <climits>
 #include <cstdint>
 #include <cstdlib>
+#include <vector>
 
 #include "dv_plan.h"
 
@@ -257,6 +259,97 @@ token_kernel(const __grid_constant__ TokParams<MAXB> p) {
       continue;
     if (PACK) p.stg[g] = ld_stream(ptr);
     else *ptr = ld_stream(p.stg + g);
+  }
+}
+
+// ---- batched unpack of log records (replica restore) -------------------------
+
+#ifndef DV_REC_HOST_SCALE
+#define DV_REC_HOST_SCALE 2  // host-memory launches: CTAs relative to a tile launch's (64)
+#endif
+
+constexpr int kRecMax = 128;     // records one launch takes at most (a power of two)
+constexpr int kRecWords = 7000;  // int32 words of range tables one launch carries
+
+// Records whose staging bytes lie back to back in `stg` (device memory or
+// mapped host memory), each with its own layer range and token ranges.
+struct RecParams {
+  uint4* k;
+  uint4* v;
+  uint4* stg;              // the records' bytes, back to back (read only)
+  int64_t layer_chunks;
+  int64_t total;           // chunks of all records
+  int64_t k_lim, v_lim, stg_lim;  // checked builds: extents (chunks) the host validated
+  int32_t B, H, C, S;
+  int32_t nrec;
+  int64_t rec_pre[kRecMax + 1];  // first chunk of record r in stg
+  int64_t rec_lkv[kRecMax];      // chunks of one (layer, K|V) slab of record r: H * T_r * C
+  uint64_t rec_m[kRecMax];       // ceil(2^64 / rec_lkv[r]) (0 when it is 1)
+  int32_t rec_l0[kRecMax];
+  int32_t rec_tab[kRecMax];      // first word of record r's table in `words`
+  int32_t words[kRecWords];      // per record: seq_start[B], tok_pre[B + 1], m_len[B]
+};
+static_assert(sizeof(RecParams) <= 32764, "kernel parameters are limited to 32764 bytes");
+
+// The flat kernel with one more level: chunk g of the launch belongs to the
+// record whose first chunk is the last one at or below g, and inside that
+// record it is addressed exactly as the flat kernel addresses a staging chunk
+// (staging order [layer][K|V][sequence][head][token][chunk]).  Records of one
+// launch write disjoint parts of the cache (the host splits launches where
+// they would not), so their order inside a launch does not matter.
+template <int LOG2C>
+__global__ void __launch_bounds__(kThreads)
+record_unpack_kernel(const __grid_constant__ RecParams p) {
+  pdl_enter();
+  const int32_t C = LOG2C >= 0 ? (1 << LOG2C) : p.C;
+  const int64_t step = (int64_t)gridDim.x * (kThreads * kFlatUnroll);
+  for (int64_t base = (int64_t)blockIdx.x * (kThreads * kFlatUnroll) + threadIdx.x;
+       base < p.total; base += step) {
+    // The source is read in order: issue every load first, so that the
+    // address arithmetic below runs while they are in flight (the source is
+    // often host memory, a long round trip).
+    uint4 val[kFlatUnroll];
+    bool ok[kFlatUnroll];
+#pragma unroll
+    for (int u = 0; u < kFlatUnroll; ++u) {
+      const int64_t g = base + u * kThreads;
+      ok[u] = g < p.total && DV_OK_S(p.stg + g, 33);
+      if (ok[u]) val[u] = ld_stream(p.stg + g);
+    }
+#pragma unroll
+    for (int u = 0; u < kFlatUnroll; ++u) {
+      if (!ok[u]) continue;
+      const int64_t g = base + u * kThreads;
+      // Fixed-depth searches without branches, so that the four chunks'
+      // lookups can overlap: the last record starting at or before g ...
+      int r = 0;
+#pragma unroll
+      for (int half = kRecMax / 2; half > 0; half >>= 1)
+        if (r + half < p.nrec && p.rec_pre[r + half] <= g) r += half;
+      const int64_t q = g - p.rec_pre[r];
+      const int64_t lkv = (int64_t)div64_by((uint64_t)q, (uint64_t)p.rec_lkv[r], p.rec_m[r]);
+      const int32_t w = (int32_t)(q - lkv * p.rec_lkv[r]);
+      const int32_t rec = LOG2C >= 0 ? (w >> LOG2C) : w / C;
+      const int32_t c = w - rec * C;
+      const int32_t tab = p.rec_tab[r];
+      const int32_t pre = tab + p.B;           // tok_pre of the record
+      // ... and the last sequence of that record whose run starts at or
+      // before the chunk's token-head (a non-empty one, as in find_seq).
+      int b = 0;
+#pragma unroll
+      for (int half = kMaxBatch / 2; half > 0; half >>= 1)
+        if (b + half < p.B && p.H * p.words[pre + b + half] <= rec) b += half;
+      const int32_t rr = rec - p.H * p.words[pre + b];
+      const int32_t len = p.words[pre + b + 1] - p.words[pre + b];
+      const uint32_t m = (uint32_t)p.words[pre + p.B + 1 + b];
+      const int32_t h = m ? (int32_t)div_by((uint32_t)rr, (uint32_t)len, m) : rr;
+      const int64_t t = p.words[tab + b] + (rr - h * len);
+      const int64_t l = p.rec_l0[r] + (lkv >> 1);
+      const int64_t bh = (int64_t)b * p.H + h;
+      uint4* ptr = (lkv & 1) == 0 ? p.k + l * p.layer_chunks + ((bh * C + c) * p.S + t)
+                                  : p.v + l * p.layer_chunks + ((bh * p.S + t) * C + c);
+      if ((lkv & 1) == 0 ? DV_OK_K(ptr, 31) : DV_OK_V(ptr, 32)) *ptr = val[u];
+    }
   }
 }
 
@@ -579,6 +672,78 @@ cudaError_t launch(const Plan& p, void* stg, cudaStream_t stream, int variant) {
   return dispatch_c<PACK, kMaxBatch>(p, stg, stream, kind);
 }
 
+template <int LOG2C>
+cudaError_t run_records(const Plan& cache, const RecordRanges* recs, int n, const void* src,
+                        cudaStream_t stream) {
+  static std::atomic<int64_t> occ_cache{0};
+  static thread_local RecParams kp;  // 32 KB: kept off the stack
+  const int32_t B = cache.B;
+  if (n > kRecMax || (int64_t)n * (3 * B + 1) > kRecWords) return cudaErrorInvalidValue;
+  kp.k = static_cast<uint4*>(cache.k);
+  kp.v = static_cast<uint4*>(cache.v);
+  kp.stg = static_cast<uint4*>(const_cast<void*>(src));
+  kp.layer_chunks = cache.layer_chunks;
+  kp.k_lim = kp.v_lim = cache_limit(cache);
+  kp.B = B;
+  kp.H = cache.H;
+  kp.C = cache.C;
+  kp.S = cache.S;
+  kp.nrec = n;
+  int64_t chunk = 0;
+  int32_t word = 0;
+  for (int r = 0; r < n; ++r) {
+    const RecordRanges& rec = recs[r];
+    kp.rec_pre[r] = chunk;
+    kp.rec_tab[r] = word;
+    kp.rec_l0[r] = rec.l0;
+    int32_t* start = kp.words + word;
+    int32_t* pre = start + B;
+    int32_t* mlen = pre + B + 1;
+    int64_t tokens = 0;
+    for (int32_t b = 0; b < B; ++b) {
+      const int32_t len = rec.end[b] > rec.start[b] ? rec.end[b] - rec.start[b] : 0;
+      start[b] = rec.start[b];
+      pre[b] = (int32_t)tokens;
+      mlen[b] = len > 1 ? (int32_t)(uint32_t)div_magic((uint32_t)len) : 0;
+      tokens += len;
+    }
+    pre[B] = (int32_t)tokens;
+    const int64_t lkv = (int64_t)cache.H * tokens * cache.C;
+    kp.rec_lkv[r] = lkv;
+    kp.rec_m[r] = div64_magic((uint64_t)lkv);
+    chunk += 2 * (int64_t)(rec.l1 - rec.l0) * lkv;
+    word += 3 * B + 1;
+  }
+  kp.rec_pre[n] = chunk;
+  kp.total = chunk;
+  kp.stg_lim = chunk;
+  if (chunk == 0) return cudaSuccess;
+  const auto kernel = record_unpack_kernel<LOG2C>;
+  const int64_t want = (chunk + kThreads * kFlatUnroll - 1) / (kThreads * kFlatUnroll);
+  const int64_t cap = host_cap(cache, (int64_t)sm_count() * blocks_per_sm(kernel, 0, occ_cache),
+                               DV_REC_HOST_SCALE);
+  const unsigned grid = (unsigned)(want < cap ? want : cap);
+  return launch_kernel(kernel, grid, 0, stream, kp);
+}
+
+// Whether record k writes a part of the cache that one of recs[0, k) writes:
+// their layer ranges meet and, for some sequence, so do their token ranges.
+// `lo` / `hi` hold the hull of the token ranges of recs[0, k) per sequence.
+bool overlaps_earlier(const RecordRanges* recs, int k, int32_t B, const int32_t* lo,
+                      const int32_t* hi) {
+  const RecordRanges& x = recs[k];
+  for (int32_t b = 0; b < B; ++b) {
+    const int32_t s = x.start[b], e = x.end[b];
+    if (s >= e || s >= hi[b] || e <= lo[b]) continue;
+    for (int j = 0; j < k; ++j) {
+      const RecordRanges& y = recs[j];
+      if (y.l0 >= x.l1 || x.l0 >= y.l1) continue;
+      if (y.start[b] < y.end[b] && y.start[b] < e && s < y.end[b]) return true;
+    }
+  }
+  return false;
+}
+
 }  // namespace
 
 bool tile_supported(const Plan& p) { return p.C <= kMaxTileC; }
@@ -630,6 +795,33 @@ cudaError_t launch_pack(const Plan& p, void* stg, cudaStream_t stream, int varia
 
 cudaError_t launch_unpack(const Plan& p, const void* stg, cudaStream_t stream, int variant) {
   return launch<false>(p, const_cast<void*>(stg), stream, variant);
+}
+
+int records_per_launch(const Plan& cache, const RecordRanges* recs, int n) {
+  if (n <= 0) return 0;
+  const int32_t B = cache.B;
+  int limit = kRecWords / (3 * B + 1);
+  if (limit > kRecMax) limit = kRecMax;
+  if (limit > n) limit = n;
+  std::vector<int32_t> lo(B, INT32_MAX), hi(B, INT32_MIN);
+  int k = 0;
+  for (; k < limit; ++k) {
+    if (k > 0 && overlaps_earlier(recs, k, B, lo.data(), hi.data())) break;
+    for (int32_t b = 0; b < B; ++b) {
+      if (recs[k].start[b] >= recs[k].end[b]) continue;
+      if (recs[k].start[b] < lo[b]) lo[b] = recs[k].start[b];
+      if (recs[k].end[b] > hi[b]) hi[b] = recs[k].end[b];
+    }
+  }
+  return k;
+}
+
+cudaError_t launch_unpack_records(const Plan& cache, const RecordRanges* recs, int n,
+                                  const void* src, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  if (cache.C == 8) return run_records<3>(cache, recs, n, src, stream);
+  if (cache.C == 16) return run_records<4>(cache, recs, n, src, stream);
+  return run_records<-1>(cache, recs, n, src, stream);
 }
 
 }  // namespace dv

@@ -62,6 +62,26 @@ bool token_supported(const Plan& p);
 cudaError_t launch_pack(const Plan& p, void* stg, cudaStream_t stream, int variant);
 cudaError_t launch_unpack(const Plan& p, const void* stg, cudaStream_t stream, int variant);
 
+// One record of a log: layers [l0, l1) and per-sequence token ranges
+// [start[b], end[b]) (B entries each, validated), whose staging bytes follow
+// the previous record's in the source buffer.
+struct RecordRanges {
+  int32_t l0, l1;
+  const int32_t* start;
+  const int32_t* end;
+};
+
+// How many of recs[0, n), from the first, one launch_unpack_records call
+// takes: consecutive records whose writes to the cache are pairwise disjoint
+// and whose range tables fit in the kernel parameters (at least 1 for n > 0).
+int records_per_launch(const Plan& cache, const RecordRanges* recs, int n);
+
+// Unpacks recs[0, n) (n at most records_per_launch) from `src` into the cache
+// of `cache` (its k, v, geometry, l1 covering every record, host_side) in one
+// launch.
+cudaError_t launch_unpack_records(const Plan& cache, const RecordRanges* recs, int n,
+                                  const void* src, cudaStream_t stream);
+
 // Whether this library was built with device-side bounds checks, and the
 // first out-of-bounds access they recorded since the last call (0 if none;
 // the record is cleared).  Synchronous.

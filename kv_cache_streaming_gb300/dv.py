@@ -75,6 +75,7 @@ _streamer_destroy = _sig("dv_streamer_destroy", [_P], None)
 _replica_create = _sig("dv_replica_create", [ctypes.POINTER(_P), _P, _SZ, _I32])
 _replica_append = _sig("dv_replica_append", [_P] + _RANGE + [_I64, _P, _SZ, _P])
 _replica_restore = _sig("dv_replica_restore", [_P, _CP, _I64, _P, _SZ, _P])
+_replica_restore_batched = _sig("dv_replica_restore_batched", [_P, _CP, _I64, _P, _SZ, _P])
 _replica_truncate = _sig("dv_replica_truncate", [_P, _I64])
 _replica_info = _sig("dv_replica_info", [_P, ctypes.POINTER(_I64), ctypes.POINTER(_SZ)])
 _replica_destroy = _sig("dv_replica_destroy", [_P], None)
@@ -319,6 +320,10 @@ class Replica:
         st, sn = _buf(staging)
         _check(_replica_restore(self.h, cache.ref, upto_step, st, sn, _stream(stream)))
 
+    def restore_batched(self, cache: Cache, upto_step=-1, staging=None, stream=None):
+        st, sn = _buf(staging)
+        _check(_replica_restore_batched(self.h, cache.ref, upto_step, st, sn, _stream(stream)))
+
     def truncate(self, step):
         _check(_replica_truncate(self.h, step))
 
@@ -352,6 +357,11 @@ def dv_replica_append(replica: Replica, cache: Cache, l0, l1, seq_start, seq_end
 def dv_replica_restore(replica: Replica, cache: Cache, upto_step=-1, staging=None,
                        stream=None) -> None:
     replica.restore(cache, upto_step, staging, stream)
+
+
+def dv_replica_restore_batched(replica: Replica, cache: Cache, upto_step=-1, staging=None,
+                               stream=None) -> None:
+    replica.restore_batched(cache, upto_step, staging, stream)
 
 
 def dv_replica_truncate(replica: Replica, step) -> None:

@@ -1,0 +1,202 @@
+"""Parity of the record-batched restore (dv_replica_restore_batched) with the
+oracle's in-order restore of the same log: a snapshot and many decode deltas
+in few launches, records with their own layer ranges, records that rewrite
+what earlier records wrote (later wins), empty records, more records than one
+launch takes, batch 1024, fused and staged, upto_step, and the errors."""
+import numpy as np
+import pytest
+import torch
+
+import kv_cache_streaming_gb300 as dv
+import oracle
+from synth.configs import Geometry
+from tests import gpu_helpers as H
+from tests import oracle_pins as P
+
+pytestmark = pytest.mark.gpu
+ORC = oracle.default()
+
+GEOMS = [
+    Geometry("c16", 3, 5, 3, 128, 300, 2, "fp16"),
+    Geometry("c8", 2, 4, 5, 64, 200, 2, "bf16"),
+    Geometry("c5", 2, 3, 2, 40, 90, 2, "fp16"),      # odd C: generic kernel
+    Geometry("p1", 2, 3, 2, 128, 64, 1, "raw"),
+    Geometry("p4", 2, 3, 2, 64, 64, 4, "fp32"),
+    Geometry("pad", 3, 2, 2, 128, 50, 2, "fp16", layer_stride_elems=2 * 2 * 128 * 50 + 64),
+    Geometry("b40", 1, 40, 2, 64, 32, 2, "fp16"),    # batch > 32
+]
+
+
+class Log:
+    """A live cache and a replica of it; `records` mirrors the log for the
+    oracle: (l0, l1, s, e, the bytes the oracle packs from the live cache as
+    it was at the append)."""
+
+    def __init__(self, g, seed, capacity):
+        self.g = g
+        self.seed = seed
+        self.kh, self.vh = H.host_cache(g, seed)
+        self.cache = H.device_cache(g, fill=(self.kh, self.vh))
+        self.arena = H.pinned(capacity + 4096)
+        self.rep = dv.Replica(self.arena, g.batch)
+        self.records = []
+
+    def rewrite(self, salt):
+        """New content for the whole live cache (a later record over the same
+        slices then carries different bytes)."""
+        self.kh, self.vh = H.host_cache(self.g, self.seed * 7919 + salt)
+        self.cache.k.copy_(torch.from_numpy(self.kh))
+        self.cache.v.copy_(torch.from_numpy(self.vh))
+
+    def append(self, l0, l1, s, e):
+        s = np.asarray(s, np.int32)
+        e = np.asarray(e, np.int32)
+        step = len(self.records)
+        self.rep.append(self.cache, l0, l1, s, e, step=step)
+        self.records.append((l0, l1, s.copy(), e.copy(),
+                             ORC.pack(self.g, self.kh, self.vh, l0, l1, s, e)))
+
+    def check(self, staging_bytes=None, upto=-1, batched=True):
+        torch.cuda.synchronize()
+        g = self.g
+        z = H.device_cache(g, fill="zero")
+        staging = H.device_bytes(staging_bytes) if staging_bytes else None
+        if batched:
+            self.rep.restore_batched(z, upto_step=upto, staging=staging)
+        else:
+            self.rep.restore(z, upto_step=upto, staging=staging)
+        recs = self.records if upto < 0 else self.records[:upto]
+        kw, vw = ORC.restore(g, recs)
+        assert np.array_equal(H.to_np(z.k), kw), (g.name, staging_bytes, upto)
+        assert np.array_equal(H.to_np(z.v), vw), (g.name, staging_bytes, upto)
+
+
+def min_staging(log):
+    """The smallest staging buffer a staged restore of the log accepts: the
+    largest layer slab of any record."""
+    slab = max(d.size // (l1 - l0) for l0, l1, _, _, d in log.records if d.size)
+    return (slab + 15) // 16 * 16
+
+
+def standard_log(g, seed):
+    """Snapshot of ragged prefixes, then decode deltas (some sequences
+    finish), a ragged multi-token record, an empty record, records over part
+    of the layers, and records that rewrite earlier slices."""
+    rng = np.random.default_rng(seed)
+    B, S, L = g.batch, g.max_seq, g.num_layers
+    zero = np.zeros(B, np.int32)
+    pos = rng.integers(S // 4, S // 2, size=B).astype(np.int32)
+    full = ORC.staging_bytes(g, 0, L, zero, np.full(B, S, np.int32))
+    log = Log(g, seed, 4 * full)
+    log.append(0, L, zero, pos)                               # snapshot
+    live = np.ones(B, bool)
+    for k in range(12):                                       # one-token deltas
+        if k == 5:
+            live[::3] = False
+        act = np.where(live & (pos < S), 1, 0).astype(np.int32)
+        log.append(0, L, pos, pos + act)
+        pos = pos + act
+    n = np.minimum(rng.integers(0, 4, size=B), S - pos).astype(np.int32)
+    log.append(0, L, pos, pos + n)                            # ragged multi-token
+    pos = pos + n
+    log.append(0, L, pos, pos)                                # empty record
+    a = np.maximum(pos - 3, 0).astype(np.int32)
+    log.append(0, 1, a, pos)                                  # first layer only ...
+    if L > 1:
+        log.append(1, L, a, pos)                              # ... the others: disjoint
+    log.rewrite(1)
+    b = np.maximum(pos - 2, 0).astype(np.int32)
+    log.append(0, L, b, pos)                                  # overwrites the last two
+    log.rewrite(2)
+    s, e = P.random_ranges(g, rng)
+    log.append(0, L, s, e)                                    # random ranges over all
+    log.rewrite(3)
+    log.append(L - 1, L, zero, np.minimum(pos, S).astype(np.int32))  # last layer again
+    return log
+
+
+@pytest.mark.parametrize("g", GEOMS, ids=lambda g: g.name)
+def test_batched_restore_matches_oracle(g):
+    log = standard_log(g, 101)
+    log.check()                                   # fused
+    log.check(staging_bytes=log.rep.info()[1])    # staged, everything fits
+    log.check(upto=7)                             # snapshot + first deltas only
+    log.check(batched=False)                      # the per-record restore agrees
+
+
+def test_staging_smaller_than_the_log():
+    """Staged: launches cut where the staging buffer is full; a record larger
+    than the staging buffer (the snapshot here) is restored by itself in layer
+    groups."""
+    g = GEOMS[0]
+    log = standard_log(g, 202)
+    snap = log.records[0][4].size
+    slab = min_staging(log)
+    assert slab < snap
+    for stg in (slab, slab + 16, 3 * slab // 2 // 16 * 16, max(snap, slab), 2 * snap):
+        log.check(staging_bytes=stg)
+
+
+def test_many_records_several_launches():
+    """More one-token records than one launch takes (128 at batch 2), the
+    staged form with a buffer that holds 50 of them."""
+    g = Geometry("many", 2, 2, 2, 64, 400, 2, "fp16")
+    zero = np.zeros(2, np.int32)
+    log = Log(g, 303, ORC.staging_bytes(g, 0, 2, zero, np.full(2, 400, np.int32)))
+    pos = np.array([3, 0], np.int32)
+    log.append(0, 2, zero, pos)
+    for k in range(300):
+        act = np.array([1, 1 if k % 5 else 0], np.int32)
+        log.append(0, 2, pos, pos + act)
+        pos = pos + act
+    one = ORC.staging_bytes(g, 0, 2, pos, pos + 1)
+    log.check()
+    log.check(staging_bytes=50 * one)
+    log.check(staging_bytes=log.rep.info()[1])
+
+
+def test_batch_1024_two_records_per_launch():
+    g = Geometry("b1024", 2, 1024, 1, 64, 24, 2, "fp16")
+    rng = np.random.default_rng(404)
+    zero = np.zeros(g.batch, np.int32)
+    log = Log(g, 404, 3 * ORC.staging_bytes(g, 0, 2, zero, np.full(g.batch, 24, np.int32)))
+    pos = rng.integers(0, 12, size=g.batch).astype(np.int32)
+    log.append(0, 2, zero, pos)
+    for k in range(7):
+        act = (rng.random(g.batch) < 0.8).astype(np.int32)
+        log.append(0, 2, pos, pos + act)
+        pos = pos + act
+    log.rewrite(5)
+    log.append(0, 2, np.maximum(pos - 1, 0).astype(np.int32), pos)
+    log.check()
+    log.check(staging_bytes=max(min_staging(log), log.rep.info()[1] // 3 // 16 * 16))
+
+
+def test_overlapping_deltas_later_wins():
+    """Every record rewrites the same token of every sequence with new bytes:
+    no two records can share a launch, and the last one must win."""
+    g = Geometry("same", 2, 3, 2, 128, 16, 2, "bf16")
+    pos = np.array([4, 9, 15], np.int32)
+    log = Log(g, 505, 16 * ORC.staging_bytes(g, 0, 2, pos, pos + 1))
+    for k in range(10):
+        log.rewrite(10 + k)
+        log.append(0, 2, pos, pos + 1)
+    log.check()
+    log.check(staging_bytes=ORC.staging_bytes(g, 0, 2, pos, pos + 1))
+
+
+def test_errors_enqueue_nothing():
+    g = GEOMS[0]
+    log = standard_log(g, 606)
+    torch.cuda.synchronize()
+    z = H.device_cache(g, fill="zero")
+    with pytest.raises(dv.DvError) as ei:       # a record larger than staging needs a slab
+        log.rep.restore_batched(z, staging=H.device_bytes(min_staging(log) - 16))
+    assert ei.value.status == dv.DV_ERR_BUFFER_TOO_SMALL
+    other = Geometry("other", 3, 5, 2, 128, 300, 2, "fp16")  # records do not fit this cache
+    zo = H.device_cache(other, fill="zero")
+    with pytest.raises(dv.DvError) as ei:
+        log.rep.restore_batched(zo)
+    assert ei.value.status == dv.DV_ERR_INVALID_ARG
+    assert not H.to_np(z.k).any() and not H.to_np(z.v).any()
+    assert not H.to_np(zo.k).any() and not H.to_np(zo.v).any()
