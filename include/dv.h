@@ -46,9 +46,11 @@
  *    current device.  A pack destination or unpack source may be device
  *    memory or pinned (page-locked, mapped) host memory; for host memory the
  *    kernel reads or writes it directly over the host link (zero copy) with a
- *    small grid (32 CTAs by default, the environment variable DV_HOST_CTAS
- *    overrides it, 0 for none), enough for the link, so that other kernels
- *    keep the rest of the GPU.
+ *    small grid (32 CTAs by default for the tile kernel, 64 for the kernels
+ *    that look up every chunk's address, 128 for the one-chunk-per-thread
+ *    token kernel; the environment variable DV_HOST_CTAS overrides the base
+ *    32, 0 for none), enough for the link, so that other kernels keep the
+ *    rest of the GPU.
  *  - Alignment: k_base, v_base, buffers and layer_stride_elems * elem_bytes
  *    must be multiples of 16 bytes (DV_ERR_MISALIGNED); head_dim must be a
  *    multiple of x (DV_ERR_UNSUPPORTED).  batch <= DV_MAX_BATCH.

@@ -73,6 +73,10 @@ struct KParams {
 #ifndef DV_TILE_MIN_BLOCKS
 #define DV_TILE_MIN_BLOCKS 5  // resident CTAs per SM the tile kernel is compiled for
 #endif
+#ifndef DV_LOOKUP_HOST_SCALE
+#define DV_LOOKUP_HOST_SCALE 2  // flat / record kernels on host memory: CTAs per tile-kernel CTA
+#endif
+
 #ifndef DV_PDL
 #define DV_PDL 1  // programmatic dependent launch
 #endif
@@ -171,46 +175,53 @@ flat_kernel(const __grid_constant__ KParams<MAXB> p) {
        base < p.total; base += step) {
     uint4 val[kFlatUnroll];
     uint4* cptr[kFlatUnroll];
+    bool ok[kFlatUnroll];
+    // Unpack reads staging in order: those loads go first, and the lookups
+    // below run while they are in flight (staging is often host memory).
+#pragma unroll
+    for (int u = 0; u < kFlatUnroll; ++u) {
+      const int64_t g = base + u * kThreads;
+      ok[u] = g < p.total && DV_OK_S(p.stg + g, 3);
+      if (!PACK && ok[u]) val[u] = ld_stream(p.stg + g);
+    }
 #pragma unroll
     for (int u = 0; u < kFlatUnroll; ++u) {
       const int64_t g = base + u * kThreads;
       cptr[u] = nullptr;
-      if (g < p.total) {
-        const int64_t lkv = (int64_t)div64_by((uint64_t)g, (uint64_t)p.lkv_chunks, p.m_lkv);
-        const int32_t r = (int32_t)(g - lkv * p.lkv_chunks);
-        const int32_t rec = LOG2C >= 0 ? (r >> LOG2C) : r / C;
-        const int32_t c = r - rec * C;
-        int lo = 0, hi = p.B - 1;
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (p.H * p.tok_pre[mid] <= rec) lo = mid; else hi = mid - 1;
-        }
-        const int b = lo;
-        const int32_t rr = rec - p.H * p.tok_pre[b];
-        const int32_t len = p.seq_len[b];
-        const int32_t h = p.m_len[b] ? (int32_t)div_by((uint32_t)rr, (uint32_t)len, p.m_len[b])
-                                     : rr;
-        const int64_t t = p.seq_start[b] + (rr - h * len);
-        const int64_t l = p.l0 + (lkv >> 1);
-        const int64_t bh = (int64_t)b * p.H + h;
-        cptr[u] = (lkv & 1) == 0 ? p.k + l * p.layer_chunks + ((bh * C + c) * p.S + t)
-                                 : p.v + l * p.layer_chunks + ((bh * p.S + t) * C + c);
-        const bool ok = ((lkv & 1) == 0 ? DV_OK_K(cptr[u], 1) : DV_OK_V(cptr[u], 2)) &&
-                        DV_OK_S(p.stg + g, 3);
-        if (!ok) cptr[u] = nullptr;
-        else val[u] = PACK ? ld_stream(cptr[u]) : ld_stream(p.stg + g);
-      }
+      if (!ok[u]) continue;
+      const int64_t lkv = (int64_t)div64_by((uint64_t)g, (uint64_t)p.lkv_chunks, p.m_lkv);
+      const int32_t r = (int32_t)(g - lkv * p.lkv_chunks);
+      const int32_t rec = LOG2C >= 0 ? (r >> LOG2C) : r / C;
+      const int32_t c = r - rec * C;
+      // The last sequence whose run starts at or before this token-head (a
+      // non-empty one, as in find_seq): a fixed-depth search without
+      // branches, so that the four chunks' lookups overlap.
+      int b = 0;
+#pragma unroll
+      for (int half = MAXB / 2; half > 0; half >>= 1)
+        if (b + half < p.B && p.H * p.tok_pre[b + half] <= rec) b += half;
+      const int32_t rr = rec - p.H * p.tok_pre[b];
+      const int32_t len = p.seq_len[b];
+      const int32_t h = p.m_len[b] ? (int32_t)div_by((uint32_t)rr, (uint32_t)len, p.m_len[b])
+                                   : rr;
+      const int64_t t = p.seq_start[b] + (rr - h * len);
+      const int64_t l = p.l0 + (lkv >> 1);
+      const int64_t bh = (int64_t)b * p.H + h;
+      uint4* ptr = (lkv & 1) == 0 ? p.k + l * p.layer_chunks + ((bh * C + c) * p.S + t)
+                                  : p.v + l * p.layer_chunks + ((bh * p.S + t) * C + c);
+      if (!((lkv & 1) == 0 ? DV_OK_K(ptr, 1) : DV_OK_V(ptr, 2))) continue;
+      cptr[u] = ptr;
+      if (PACK) val[u] = ld_stream(ptr);
     }
 #pragma unroll
     for (int u = 0; u < kFlatUnroll; ++u) {
-      const int64_t g = base + u * kThreads;
-      if (g < p.total && cptr[u]) {
-        if (PACK) p.stg[g] = val[u];
-        else *cptr[u] = val[u];
-      }
+      if (!cptr[u]) continue;
+      if (PACK) p.stg[base + u * kThreads] = val[u];
+      else *cptr[u] = val[u];
     }
   }
 }
+
 
 // ---- one-token ranges (decode deltas) ----------------------------------------
 
@@ -263,10 +274,6 @@ token_kernel(const __grid_constant__ TokParams<MAXB> p) {
 }
 
 // ---- batched unpack of log records (replica restore) -------------------------
-
-#ifndef DV_REC_HOST_SCALE
-#define DV_REC_HOST_SCALE 2  // host-memory launches: CTAs relative to a tile launch's (64)
-#endif
 
 constexpr int kRecMax = 128;     // records one launch takes at most (a power of two)
 constexpr int kRecWords = 7000;  // int32 words of range tables one launch carries
@@ -531,8 +538,10 @@ int64_t host_ctas() {
   return v;
 }
 
-// `per_cta` scales the count by the bytes a CTA keeps in flight relative to
-// a tile CTA's 16 KiB (the token kernel keeps 4 KiB, so it gets 4x the CTAs).
+// `per_cta` scales the count for kernels whose CTAs keep fewer bytes in flight
+// than a tile CTA's 16 KiB (the token kernel keeps 4 KiB: 4x the CTAs) or
+// spend longer between loads on address lookups (flat and record kernels:
+// 2x; at 1x they carried 70-85% of the link).
 inline int64_t host_cap(const Plan& p, int64_t cap, int64_t per_cta = 1) {
   const int64_t h = host_ctas() * per_cta;
   return (h > 0 && p.host_side && cap > h) ? h : cap;
@@ -585,7 +594,8 @@ cudaError_t run_flat(const Plan& p, void* stg, cudaStream_t stream) {
     kp.m_len[b] = p.seq_len[b] > 1 ? (uint32_t)div_magic((uint32_t)p.seq_len[b]) : 0u;
   const auto kernel = flat_kernel<PACK, MAXB, LOG2C>;
   const int64_t want = (kp.total + kThreads * kFlatUnroll - 1) / (kThreads * kFlatUnroll);
-  const int64_t cap = host_cap(p, (int64_t)sm_count() * blocks_per_sm(kernel, 0, occ_cache));
+  const int64_t cap = host_cap(p, (int64_t)sm_count() * blocks_per_sm(kernel, 0, occ_cache),
+                               DV_LOOKUP_HOST_SCALE);
   const unsigned grid = (unsigned)(want < cap ? want : cap);
   return launch_kernel(kernel, grid, 0, stream, kp);
 }
@@ -721,7 +731,7 @@ cudaError_t run_records(const Plan& cache, const RecordRanges* recs, int n, cons
   const auto kernel = record_unpack_kernel<LOG2C>;
   const int64_t want = (chunk + kThreads * kFlatUnroll - 1) / (kThreads * kFlatUnroll);
   const int64_t cap = host_cap(cache, (int64_t)sm_count() * blocks_per_sm(kernel, 0, occ_cache),
-                               DV_REC_HOST_SCALE);
+                               DV_LOOKUP_HOST_SCALE);
   const unsigned grid = (unsigned)(want < cap ? want : cap);
   return launch_kernel(kernel, grid, 0, stream, kp);
 }
