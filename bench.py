@@ -52,9 +52,12 @@ def parse_args():
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-swap", action="store_true", help="skip the swap / link section")
     ap.add_argument("--kernel-case", default=None,
-                    choices=["tile-pack", "tile-unpack", "delta-pack", "delta-unpack"],
+                    choices=["tile-pack", "tile-unpack", "delta-pack", "delta-unpack",
+                             "record-restore"],
                     help="run one kernel of the step on an 8-layer cache of the workload's "
-                         "shape, 5 launches, and exit (a small case for profilers)")
+                         "shape, 5 launches, and exit (a small case for profilers); "
+                         "record-restore: 5 staged batched restores of 96 decode deltas of "
+                         "the whole cache, one record-kernel launch each")
     return ap.parse_args()
 
 
@@ -173,49 +176,77 @@ class ClockSampler:
 
 # ---- the reference arm: the CPU oracle on a bounded sample --------------------
 
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 class OracleSample:
     """The oracle on layers [0, nl) of the workload: per-layer prompt packs,
     the 24 deltas of those layers, and the unpacks into a zeroed cache (the
-    same operations as the GPU step, on a bounded number of layers)."""
+    same operations as the GPU step, on a bounded number of layers).  With
+    `threads` > 1 the layers are dealt out to that many threads; the oracle's
+    C functions run without the interpreter lock, so each thread has a core."""
 
-    def __init__(self, nl):
+    def __init__(self, nl, threads=1):
+        from concurrent.futures import ThreadPoolExecutor
         from dataclasses import replace
         import oracle
         import synth
         self.nl = nl
+        self.threads = max(1, min(threads, nl))
         self.g = replace(GPT2, num_layers=nl)
         seed = seed_of(2)
         self.kh = synth.fill_bytes(seed, 0, self.g.tensor_bytes, self.g.kind)
         self.vh = synth.fill_bytes(seed, 1, self.g.tensor_bytes, self.g.kind)
         self.orc = oracle.default()
         (self.ps, self.pe), self.deltas = gpt2_ranges()
-        self.desc = (f"layers 0..{nl - 1} of the 48 (prompt packs, 24 deltas, unpacks), "
-                     "single-thread C loop nest")
+        self.pool = ThreadPoolExecutor(self.threads) if self.threads > 1 else None
+        how = ("single-thread C loop nest" if self.threads == 1 else
+               f"C loop nest, layers dealt to {self.threads} threads")
+        self.desc = f"layers 0..{nl - 1} of the 48 (prompt packs, 24 deltas, unpacks), {how}"
+
+    def _layers(self, layers, kz, vz):
+        g, orc = self.g, self.orc
+        moved = 0
+        for l in layers:
+            slab = orc.pack(g, self.kh, self.vh, l, l + 1, self.ps, self.pe)
+            dels = [orc.pack(g, self.kh, self.vh, l, l + 1, s, e) for s, e in self.deltas]
+            orc.unpack(g, kz, vz, l, l + 1, self.ps, self.pe, slab)
+            for (s, e), d in zip(self.deltas, dels):
+                orc.unpack(g, kz, vz, l, l + 1, s, e, d)
+            moved += 2 * 2 * (slab.size + sum(d.size for d in dels))
+        return moved
 
     def step(self):
         """Returns (bytes read + written, seconds)."""
-        g, orc, nl = self.g, self.orc, self.nl
         kz = np.zeros_like(self.kh)
         vz = np.zeros_like(self.vh)
+        parts = [list(range(i, self.nl, self.threads)) for i in range(self.threads)]
         t0 = time.perf_counter()
-        slabs = [orc.pack(g, self.kh, self.vh, l, l + 1, self.ps, self.pe) for l in range(nl)]
-        dels = [orc.pack(g, self.kh, self.vh, 0, nl, s, e) for s, e in self.deltas]
-        for l in range(nl):
-            orc.unpack(g, kz, vz, l, l + 1, self.ps, self.pe, slabs[l])
-        for (s, e), d in zip(self.deltas, dels):
-            orc.unpack(g, kz, vz, 0, nl, s, e, d)
+        if self.pool is None:
+            moved = self._layers(parts[0], kz, vz)
+        else:
+            moved = sum(self.pool.map(lambda p: self._layers(p, kz, vz), parts))
         dt = time.perf_counter() - t0
-        moved = 2 * 2 * (sum(x.size for x in slabs) + sum(x.size for x in dels))
         return moved, dt
+
+    def close(self):
+        if self.pool is not None:
+            self.pool.shutdown()
 
 
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    # about 0.4 s of oracle work per layer: keep the whole run near two minutes
-    nl = int(max(1, min(8, 120.0 / (0.4 * (args.steps + args.warmup)))))
-    smp = OracleSample(nl)
+    # About 0.2 s of oracle work per layer and core: each step gives every host
+    # core the same number of layers, sized to keep the whole run near two minutes.
+    cores = host_cores()
+    per_core = int(max(1, min(4, 120.0 / (0.2 * (args.steps + args.warmup)))))
+    smp = OracleSample(min(GPT2.num_layers, cores * per_core), threads=cores)
     for _ in range(args.warmup):
         smp.step()
     moved = secs = 0.0
@@ -229,10 +260,11 @@ def run_reference(args):
             "ms_per_step": round(1e3 * secs / max(args.steps, 1), 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "u16", "data": "synthetic",
             "config": {"workload": WORKLOAD, "l2": "n/a (CPU)", "parallelism": "replicas"},
-            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1,
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": smp.threads,
                              "kind": "oracle", "sample": smp.desc},
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+    smp.close()
     print(json.dumps(line), flush=True)
 
 
@@ -1065,10 +1097,17 @@ def run_mine(args):
     workloads = workload_section(b.torch, b.dv) if extra else None
     cpu = None
     if rank == 0:
-        smp = OracleSample(8)
+        cores = host_cores()
+        smp = OracleSample(min(GPT2.num_layers, 2 * cores), threads=cores)
         moved, dt = smp.step()
-        cpu = {"value": round(moved / dt / 1e9, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": smp.desc + f", {dt:.1f} s"}
+        smp.close()
+        one = OracleSample(4)
+        moved1, dt1 = one.step()
+        cpu = {"value": round(moved / dt / 1e9, 3), "unit": UNIT, "cores": smp.threads,
+               "kind": "oracle", "sample": smp.desc + f", {dt:.1f} s",
+               "single_thread": {"value": round(moved1 / dt1 / 1e9, 3), "cores": 1,
+                                 "sample": one.desc + f", {dt1:.1f} s"}}
+        del smp, one
     if rank != 0:
         return
     line = {
@@ -1120,6 +1159,9 @@ def run_kernel_case(case):
     import kv_cache_streaming_gb300 as dv
     from synth import gpu as synth_gpu
     torch.cuda.set_device(0)
+    if case == "record-restore":
+        run_record_case(torch, dv, synth_gpu)
+        return
     g = replace(GPT2, num_layers=8)
     k = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
     v = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
@@ -1137,6 +1179,40 @@ def run_kernel_case(case):
             dv.dv_kv_unpack(cache, 0, g.num_layers, s, e, stg)
     torch.cuda.synchronize()
     print(f"{case}: 5 launches of {2 * n} algorithmic bytes each")
+
+
+def run_record_case(torch, dv, synth_gpu):
+    """A replica of 96 one-token decode deltas (positions 928..1023) of the
+    workload's cache, 236 MB (more than L2), restored 5 times through a device
+    staging buffer: each restore is one host-to-device copy and one launch of
+    the record kernel (96 records of batch 8 fit one launch)."""
+    g = GPT2
+    k = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+    v = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+    synth_gpu.fill_cache(g, k, v, seed_of(2))
+    cache = dv.Cache.from_geometry(g, k, v)
+    back = dv.Cache.from_geometry(g, torch.zeros_like(k), torch.zeros_like(v))
+    p0, nd = 928, 96
+    pos = np.full(g.batch, p0, np.int32)
+    one = dv.dv_staging_bytes(cache, 0, g.num_layers, pos, pos + 1)
+    arena = torch.empty(nd * one, dtype=torch.uint8, pin_memory=True)
+    rep = dv.Replica(arena, g.batch)
+    for i in range(nd):
+        rep.append(cache, 0, g.num_layers, pos + i, pos + i + 1, step=i)
+    stg = torch.empty(nd * one, dtype=torch.uint8, device="cuda")
+    for _ in range(5):
+        rep.restore_batched(back, staging=stg)
+    torch.cuda.synchronize()
+    n = dv.dv_staging_bytes(cache, 0, g.num_layers, pos, pos + nd)
+    a = torch.empty(n, dtype=torch.uint8, device="cuda")
+    b = torch.empty(n, dtype=torch.uint8, device="cuda")
+    dv.dv_kv_pack(cache, 0, g.num_layers, pos, pos + nd, a)
+    dv.dv_kv_pack(back, 0, g.num_layers, pos, pos + nd, b)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b), "restored slices differ from the source cache"
+    rep.close()
+    print(f"record-restore: 5 launches of {2 * nd * one} algorithmic bytes each "
+          f"({nd} records, {n} bytes of cache slices)")
 
 
 def main():
