@@ -477,18 +477,22 @@ class Bench:
         s.wait_stream(si)
 
     def timed_e2e(self, steps, warmup, world):
+        """Seconds of each of `steps` end-to-end steps, every step timed from an
+        idle GPU to its last copy (the host link is shared with other tenants
+        of the machine: the median step is the robust figure)."""
         torch = self.torch
         for _ in range(warmup):
             self.e2e_step()
         torch.cuda.synchronize()
         barrier(world)
-        t0 = time.perf_counter()
+        ts = []
         for _ in range(steps):
+            t0 = time.perf_counter()
             self.e2e_step()
-        torch.cuda.synchronize()
-        dt = time.perf_counter() - t0
+            torch.cuda.synchronize()
+            ts.append(time.perf_counter() - t0)
         barrier(world)
-        return dt
+        return ts
 
     # swap section: used cache to pinned host and back, against the link peak
     def swap_section(self, reps=3):
@@ -700,7 +704,7 @@ class MicrobatchSwapping:
               slot, the other slot takes x-1's swap-out and then x+1's
               swap-in on a second, high-priority stream, ordered by events."""
 
-    def __init__(self, torch, dv, rounds=3, keep_refs=False):
+    def __init__(self, torch, dv, rounds=8, keep_refs=False):
         from synth import gpu as synth_gpu
         from synth.configs import OPT66B_STAGE, opt66b_microbatches
         self.torch, self.dv, self.rounds = torch, dv, rounds
@@ -720,7 +724,7 @@ class MicrobatchSwapping:
         self.replicas, self.arenas, self.lens, self.seeds = [], [], [], []
         for m, (p, o) in enumerate(self.mbs):
             seed = seed_of(4) * 10 + m
-            cap = int((p.sum() + g.batch * rounds) * self.per_token)
+            cap = int((p.sum() + g.batch * (rounds + 1)) * self.per_token)  # + per_op's
             arena = torch.empty(cap, dtype=torch.uint8, pin_memory=True)
             rep = dv.Replica(arena, g.batch)
             slot = self.slots[0]
@@ -861,14 +865,62 @@ class MicrobatchSwapping:
                 self.acc += slot.v[:used // 2].view(torch.int32).sum(dtype=torch.int64)
         s.synchronize()
         t_comp = (time.perf_counter() - t0) / self.N
+        ops = self.per_op(s)
         return {"microbatches": self.N, "rounds": self.rounds,
                 "ms_per_microbatch_step": {"serial": round(1e3 * t_serial / steps, 3),
                                            "double": round(1e3 * t_double / steps, 3)},
                 "speedup_double": round(t_serial / t_double, 3),
                 "swap_in_ms": round(1e3 * t_in, 3), "swap_in_bytes": int(in_bytes),
                 "swap_in_gbs": round(in_bytes / t_in / 1e9, 1),
-                "compute_ms": round(1e3 * t_comp, 3),
+                "compute_ms": round(1e3 * t_comp, 3), "per_op": ops,
                 "note": "the double schedule can hide at most min(swap-in, compute) per step"}
+
+    def per_op(self, s):
+        """Each operation of a microbatch step on its own, payload GB/s (CUDA
+        events on `s`, median over the microbatches): the delta append (the
+        swap-out of delta-only swapping, fused into the pinned replica), and
+        the swap-out / swap-in of a microbatch's whole used prefix (fused, the
+        full-prefix reading of a swap)."""
+        torch, dv, g = self.torch, self.dv, self.g
+        L = g.num_layers
+        slot = self.slots[0]
+        big = max(dv.dv_staging_bytes(slot, 0, L, self.zs, ln) for ln in self.lens)
+        host = torch.empty(big, dtype=torch.uint8, pin_memory=True)
+
+        def ev_time(fn):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(s)
+            fn()
+            b.record(s)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / 1e3
+
+        app, out, inn = [], [], []
+        for m in range(self.N):
+            ln = self.lens[m]
+            rep = self.replicas[m]
+            nt = dv.dv_staging_bytes(slot, 0, L, ln, ln + 1)
+            for _ in range(2):  # the first of each is a warm-up
+                t = ev_time(lambda: rep.append(slot, 0, L, ln, ln + 1, step=self.step_no[m],
+                                               stream=s))
+                rep.truncate(self.step_no[m])
+            app.append((nt, t))
+            n = dv.dv_staging_bytes(slot, 0, L, self.zs, ln)
+            for _ in range(2):
+                to = ev_time(lambda: dv.dv_swap_out(slot, 0, L, self.zs, ln, host, stream=s))
+                ti = ev_time(lambda: dv.dv_swap_in(slot, 0, L, self.zs, ln, host, stream=s))
+            out.append((n, to))
+            inn.append((n, ti))
+        del host
+        med = lambda xs: statistics.median(b / t / 1e9 for b, t in xs)  # noqa: E731
+        return {"delta_append_gbs": round(med(app), 1),
+                "delta_append_us": round(1e6 * statistics.median(t for _, t in app), 1),
+                "delta_bytes": int(statistics.median(b for b, _ in app)),
+                "prefix_swap_out_gbs": round(med(out), 1),
+                "prefix_swap_in_gbs": round(med(inn), 1),
+                "prefix_bytes": int(statistics.median(b for b, _ in out))}
 
 
 def workload_section(torch, dv):
@@ -1080,11 +1132,14 @@ def run_mine(args):
     achieved = nbytes / t_launch / 1e9
     # e2e through the public API with host buffers
     b.setup_e2e()
-    e2e_steps = max(3, min(args.steps, 10))
+    e2e_steps = max(3, min(args.steps, 20))
     b.clear_b()
-    e2e_secs = max_over_ranks(b.timed_e2e(e2e_steps, 2, world), world)
+    e2e_ts = b.timed_e2e(e2e_steps, 2, world)
     e2e_ok = b.verify()
-    e2e_value = whole_job_rate(b.bytes_per_step, e2e_steps, e2e_secs, world)
+    e2e_med = max_over_ranks(statistics.median(e2e_ts), world)
+    e2e_value = whole_job_rate(b.bytes_per_step, 1, e2e_med, world)
+    e2e_all = whole_job_rate(b.bytes_per_step, e2e_steps, max_over_ranks(sum(e2e_ts), world),
+                             world)
     h2d = d2h = b.g.num_layers * b.slab + GPT2_DECODE_STEPS * b.dsz
     # The sections below describe one GPU and only rank 0 prints them: the other
     # ranks skip them (they would pin about 20 GB of host memory each).
@@ -1134,6 +1189,9 @@ def run_mine(args):
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps, "verified": e2e_ok,
+                "timing": "median step (each step synchronised); over all steps: "
+                          f"{e2e_all:.1f} GB/s, slowest step {max(e2e_ts) * 1e3:.2f} ms, "
+                          f"fastest {min(e2e_ts) * 1e3:.2f} ms",
                 "path": "per layer: dv_stream_layer (pack + D2H copy) then dv_swap_in of that "
                         "layer (H2D copy + unpack) on a third stream, overlapping the next "
                         "layer's D2H; dv_replica_append x24 (fused) + "

@@ -52,3 +52,49 @@ def test_pack_unpack_in_a_globally_captured_graph():
     ORC.unpack(g, kw, vw, 0, g.num_layers, s2, e2, ORC.pack(g, kh, vh, 0, g.num_layers, s2, e2))
     ORC.unpack(g, kw, vw, 0, g.num_layers, pos, e1, ORC.pack(g, kh, vh, 0, g.num_layers, pos, e1))
     assert np.array_equal(H.to_np(back.k), kw) and np.array_equal(H.to_np(back.v), vw)
+
+
+def test_batched_restore_in_a_globally_captured_graph():
+    """dv_replica_restore_batched, fused and staged, captured in global mode:
+    each replay restores the snapshot + deltas the oracle's in-order restore
+    gives."""
+    g = Geometry("caprep", 3, 5, 4, 128, 128, 2, "bf16")
+    kh, vh = H.host_cache(g, 93)
+    cache = H.device_cache(g, fill=(kh, vh))
+    zero = np.zeros(g.batch, np.int32)
+    pos = np.array([70, 5, 33, 100, 64], np.int32)
+    full = ORC.staging_bytes(g, 0, g.num_layers, zero, np.full(g.batch, g.max_seq, np.int32))
+    arena = H.pinned(full)
+    rep = dv.Replica(arena, g.batch)
+    records = [(0, g.num_layers, zero, pos.copy())]
+    rep.append(cache, 0, g.num_layers, zero, pos, step=0)
+    for k in range(1, 9):
+        act = np.array([1, 1, 0 if k > 4 else 1, 1, 1], np.int32)
+        rep.append(cache, 0, g.num_layers, pos, pos + act, step=k)
+        records.append((0, g.num_layers, pos.copy(), (pos + act).copy()))
+        pos = pos + act
+    torch.cuda.synchronize()
+    kw, vw = ORC.restore(g, [(a, b, s_, e_, ORC.pack(g, kh, vh, a, b, s_, e_))
+                             for a, b, s_, e_ in records])
+    fused = H.device_cache(g, fill="zero")
+    staged = H.device_cache(g, fill="zero")
+    stg = H.device_bytes(rep.info()[1])
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):  # eager once
+        rep.restore_batched(fused, stream=s)
+        rep.restore_batched(staged, staging=stg, stream=s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        rep.restore_batched(fused, stream=s)
+        rep.restore_batched(staged, staging=stg, stream=s)
+    for _ in range(2):
+        for c in (fused, staged):
+            c.k.zero_()
+            c.v.zero_()
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        for c in (fused, staged):
+            assert np.array_equal(H.to_np(c.k), kw) and np.array_equal(H.to_np(c.v), vw)
+    rep.close()

@@ -188,4 +188,11 @@ def test_bloom_replica_256_steps_and_restore():
     rep.restore(back)
     torch.cuda.synchronize()
     H.assert_prefix_equal_rest_zero(g, back, cache, pos)
+    # the record-batched restore: the snapshot alone, the 256 deltas in 4
+    # launches of the record kernel (72 records per launch at batch 32)
+    back.k.zero_()
+    back.v.zero_()
+    rep.restore_batched(back)
+    torch.cuda.synchronize()
+    H.assert_prefix_equal_rest_zero(g, back, cache, pos)
     rep.close()
