@@ -165,63 +165,96 @@ __device__ __forceinline__ uint64_t div64_by(uint64_t n, uint64_t d, uint64_t m)
   return q;
 }
 
-template <bool PACK, int MAXB, int LOG2C>
-__global__ void __launch_bounds__(kThreads)
-flat_kernel(const __grid_constant__ KParams<MAXB> p) {
-  pdl_enter();
+// Addresses of the cache chunks of staging chunks base + u * kThreads
+// (u < kFlatUnroll); nullptr where there is none.  Reads only the kernel
+// parameters, so it may run before griddepcontrol.wait.
+template <int MAXB, int LOG2C>
+__device__ __forceinline__ void flat_lookup(const KParams<MAXB>& p, int64_t base,
+                                            uint4* (&cptr)[kFlatUnroll]) {
   const int32_t C = LOG2C >= 0 ? (1 << LOG2C) : p.C;
-  const int64_t step = (int64_t)gridDim.x * (kThreads * kFlatUnroll);
-  for (int64_t base = (int64_t)blockIdx.x * (kThreads * kFlatUnroll) + threadIdx.x;
-       base < p.total; base += step) {
-    uint4 val[kFlatUnroll];
-    uint4* cptr[kFlatUnroll];
-    bool ok[kFlatUnroll];
-    // Unpack reads staging in order: those loads go first, and the lookups
-    // below run while they are in flight (staging is often host memory).
 #pragma unroll
-    for (int u = 0; u < kFlatUnroll; ++u) {
-      const int64_t g = base + u * kThreads;
-      ok[u] = g < p.total && DV_OK_S(p.stg + g, 3);
-      if (!PACK && ok[u]) val[u] = ld_stream(p.stg + g);
-    }
+  for (int u = 0; u < kFlatUnroll; ++u) {
+    const int64_t g = base + u * kThreads;
+    cptr[u] = nullptr;
+    if (g >= p.total || !DV_OK_S(p.stg + g, 3)) continue;
+    const int64_t lkv = (int64_t)div64_by((uint64_t)g, (uint64_t)p.lkv_chunks, p.m_lkv);
+    const int32_t r = (int32_t)(g - lkv * p.lkv_chunks);
+    const int32_t rec = LOG2C >= 0 ? (r >> LOG2C) : r / C;
+    const int32_t c = r - rec * C;
+    // The last sequence whose run starts at or before this token-head (a
+    // non-empty one, as in find_seq): a fixed-depth search without branches,
+    // so that the four chunks' lookups overlap.
+    int b = 0;
 #pragma unroll
-    for (int u = 0; u < kFlatUnroll; ++u) {
-      const int64_t g = base + u * kThreads;
-      cptr[u] = nullptr;
-      if (!ok[u]) continue;
-      const int64_t lkv = (int64_t)div64_by((uint64_t)g, (uint64_t)p.lkv_chunks, p.m_lkv);
-      const int32_t r = (int32_t)(g - lkv * p.lkv_chunks);
-      const int32_t rec = LOG2C >= 0 ? (r >> LOG2C) : r / C;
-      const int32_t c = r - rec * C;
-      // The last sequence whose run starts at or before this token-head (a
-      // non-empty one, as in find_seq): a fixed-depth search without
-      // branches, so that the four chunks' lookups overlap.
-      int b = 0;
-#pragma unroll
-      for (int half = MAXB / 2; half > 0; half >>= 1)
-        if (b + half < p.B && p.H * p.tok_pre[b + half] <= rec) b += half;
-      const int32_t rr = rec - p.H * p.tok_pre[b];
-      const int32_t len = p.seq_len[b];
-      const int32_t h = p.m_len[b] ? (int32_t)div_by((uint32_t)rr, (uint32_t)len, p.m_len[b])
-                                   : rr;
-      const int64_t t = p.seq_start[b] + (rr - h * len);
-      const int64_t l = p.l0 + (lkv >> 1);
-      const int64_t bh = (int64_t)b * p.H + h;
-      uint4* ptr = (lkv & 1) == 0 ? p.k + l * p.layer_chunks + ((bh * C + c) * p.S + t)
-                                  : p.v + l * p.layer_chunks + ((bh * p.S + t) * C + c);
-      if (!((lkv & 1) == 0 ? DV_OK_K(ptr, 1) : DV_OK_V(ptr, 2))) continue;
-      cptr[u] = ptr;
-      if (PACK) val[u] = ld_stream(ptr);
-    }
-#pragma unroll
-    for (int u = 0; u < kFlatUnroll; ++u) {
-      if (!cptr[u]) continue;
-      if (PACK) p.stg[base + u * kThreads] = val[u];
-      else *cptr[u] = val[u];
-    }
+    for (int half = MAXB / 2; half > 0; half >>= 1)
+      if (b + half < p.B && p.H * p.tok_pre[b + half] <= rec) b += half;
+    const int32_t rr = rec - p.H * p.tok_pre[b];
+    const int32_t len = p.seq_len[b];
+    const int32_t h = p.m_len[b] ? (int32_t)div_by((uint32_t)rr, (uint32_t)len, p.m_len[b])
+                                 : rr;
+    const int64_t t = p.seq_start[b] + (rr - h * len);
+    const int64_t l = p.l0 + (lkv >> 1);
+    const int64_t bh = (int64_t)b * p.H + h;
+    uint4* ptr = (lkv & 1) == 0 ? p.k + l * p.layer_chunks + ((bh * C + c) * p.S + t)
+                                : p.v + l * p.layer_chunks + ((bh * p.S + t) * C + c);
+    if ((lkv & 1) == 0 ? DV_OK_K(ptr, 1) : DV_OK_V(ptr, 2)) cptr[u] = ptr;
   }
 }
 
+// One unpack round whose staging loads are issued before its addresses are
+// known: `cptr` is looked up (when `lookup`) while the loads are in flight.
+template <int MAXB, int LOG2C, typename Params, typename Lookup>
+__device__ __forceinline__ void unpack_round(const Params& p, int64_t base,
+                                             uint4* (&cptr)[kFlatUnroll], bool lookup,
+                                             Lookup&& find) {
+  uint4 val[kFlatUnroll];
+#pragma unroll
+  for (int u = 0; u < kFlatUnroll; ++u) {
+    const int64_t g = base + u * kThreads;
+    if (g < p.total && DV_OK_S(p.stg + g, 3)) val[u] = ld_stream(p.stg + g);
+  }
+  if (lookup) find(base, cptr);
+#pragma unroll
+  for (int u = 0; u < kFlatUnroll; ++u)
+    if (cptr[u]) *cptr[u] = val[u];
+}
+
+// Each thread moves kFlatUnroll chunks per round, kThreads apart.  The first
+// round's addresses are looked up before the wait for the preceding grid.
+// Pack: each later round's addresses are looked up while the previous
+// round's loads are in flight.  Unpack reads staging in order: each round's
+// staging loads go first, and its lookups run while they are in flight.
+template <bool PACK, int MAXB, int LOG2C>
+__global__ void __launch_bounds__(kThreads, 5)
+flat_kernel(const __grid_constant__ KParams<MAXB> p) {
+  const int64_t step = (int64_t)gridDim.x * (kThreads * kFlatUnroll);
+  int64_t base = (int64_t)blockIdx.x * (kThreads * kFlatUnroll) + threadIdx.x;
+  uint4* cptr[kFlatUnroll];
+  flat_lookup<MAXB, LOG2C>(p, base, cptr);
+  pdl_enter();
+  if (PACK) {
+    for (; base < p.total; base += step) {
+      uint4 val[kFlatUnroll];
+#pragma unroll
+      for (int u = 0; u < kFlatUnroll; ++u)
+        if (cptr[u]) val[u] = ld_stream(cptr[u]);
+      uint4* next[kFlatUnroll];
+      flat_lookup<MAXB, LOG2C>(p, base + step, next);
+#pragma unroll
+      for (int u = 0; u < kFlatUnroll; ++u) {
+        if (cptr[u]) p.stg[base + u * kThreads] = val[u];
+        cptr[u] = next[u];
+      }
+    }
+  } else {
+    const auto find = [&p](int64_t b, uint4* (&c)[kFlatUnroll]) {
+      flat_lookup<MAXB, LOG2C>(p, b, c);
+    };
+    if (base < p.total) unpack_round<MAXB, LOG2C>(p, base, cptr, false, find);
+    for (base += step; base < p.total; base += step)
+      unpack_round<MAXB, LOG2C>(p, base, cptr, true, find);
+  }
+}
 
 // ---- one-token ranges (decode deltas) ----------------------------------------
 
@@ -241,35 +274,47 @@ struct TokParams {
   int32_t act_t[MAXB];    // its one token
 };
 
+// Address of the cache chunk of staging chunk g (nullptr if there is none);
+// parameters only, so it may run before griddepcontrol.wait.
+template <int MAXB, int LOG2C>
+__device__ __forceinline__ uint4* token_lookup(const TokParams<MAXB>& p, uint32_t g) {
+  if (g >= p.total || !DV_OK_S(p.stg + g, 13)) return nullptr;
+  const uint32_t C = LOG2C >= 0 ? (1u << LOG2C) : (uint32_t)p.C;
+  const uint32_t rec = LOG2C >= 0 ? (g >> LOG2C) : g / C;
+  const uint32_t c = g - rec * C;
+  const uint32_t run = div_by(rec, p.n, p.m_n);
+  const uint32_t j = rec - run * p.n;
+  const uint32_t lkv = div_by(run, p.AH, p.m_AH);
+  const uint32_t rem = run - lkv * p.AH;
+  const uint32_t a = div_by(rem, (uint32_t)p.H, p.m_H);
+  const uint32_t h = rem - a * p.H;
+  const int64_t b = p.act_b[a];
+  const int64_t t = p.act_t[a] + j;
+  const int64_t l = p.l0 + (lkv >> 1);
+  const int64_t bh = b * p.H + h;
+  uint4* ptr = (lkv & 1) == 0 ? p.k + l * p.layer_chunks + ((bh * C + c) * p.S + t)
+                              : p.v + l * p.layer_chunks + ((bh * p.S + t) * C + c);
+  return ((lkv & 1) == 0 ? DV_OK_K(ptr, 11) : DV_OK_V(ptr, 12)) ? ptr : nullptr;
+}
+
 // Every non-empty range holds the same n tokens (n = 1: decode deltas):
 // staging chunk g is chunk c of token j of run (layer, K|V, a-th non-empty
 // sequence, head).  One chunk per thread, no shared memory, no barrier: the
-// shortest chain from launch to the copy.
+// shortest chain from launch to the copy.  The first address is computed
+// before the wait for the preceding grid, so only the copy is left after it.
 template <bool PACK, int MAXB, int LOG2C>
 __global__ void __launch_bounds__(kThreads)
 token_kernel(const __grid_constant__ TokParams<MAXB> p) {
+  const uint32_t stride = gridDim.x * kThreads;
+  uint32_t g = blockIdx.x * kThreads + threadIdx.x;
+  uint4* ptr = token_lookup<MAXB, LOG2C>(p, g);
   pdl_enter();
-  const uint32_t C = LOG2C >= 0 ? (1u << LOG2C) : (uint32_t)p.C;
-  for (uint32_t g = blockIdx.x * kThreads + threadIdx.x; g < p.total;
-       g += gridDim.x * kThreads) {
-    const uint32_t rec = LOG2C >= 0 ? (g >> LOG2C) : g / C;
-    const uint32_t c = g - rec * C;
-    const uint32_t run = div_by(rec, p.n, p.m_n);
-    const uint32_t j = rec - run * p.n;
-    const uint32_t lkv = div_by(run, p.AH, p.m_AH);
-    const uint32_t rem = run - lkv * p.AH;
-    const uint32_t a = div_by(rem, (uint32_t)p.H, p.m_H);
-    const uint32_t h = rem - a * p.H;
-    const int64_t b = p.act_b[a];
-    const int64_t t = p.act_t[a] + j;
-    const int64_t l = p.l0 + (lkv >> 1);
-    const int64_t bh = b * p.H + h;
-    uint4* ptr = (lkv & 1) == 0 ? p.k + l * p.layer_chunks + ((bh * C + c) * p.S + t)
-                                : p.v + l * p.layer_chunks + ((bh * p.S + t) * C + c);
-    if (!(((lkv & 1) == 0 ? DV_OK_K(ptr, 11) : DV_OK_V(ptr, 12)) && DV_OK_S(p.stg + g, 13)))
-      continue;
-    if (PACK) p.stg[g] = ld_stream(ptr);
-    else *ptr = ld_stream(p.stg + g);
+  for (; g < p.total; g += stride) {
+    if (ptr) {
+      if (PACK) p.stg[g] = ld_stream(ptr);
+      else *ptr = ld_stream(p.stg + g);
+    }
+    ptr = token_lookup<MAXB, LOG2C>(p, g + stride);
   }
 }
 
@@ -298,66 +343,69 @@ struct RecParams {
 };
 static_assert(sizeof(RecParams) <= 32764, "kernel parameters are limited to 32764 bytes");
 
-// The flat kernel with one more level: chunk g of the launch belongs to the
-// record whose first chunk is the last one at or below g, and inside that
-// record it is addressed exactly as the flat kernel addresses a staging chunk
-// (staging order [layer][K|V][sequence][head][token][chunk]).  Records of one
-// launch write disjoint parts of the cache (the host splits launches where
-// they would not), so their order inside a launch does not matter.
+// Cache addresses of launch chunks base + u * kThreads (nullptr where there is
+// none); parameters only, so it may run before griddepcontrol.wait.
+template <int LOG2C>
+__device__ __forceinline__ void record_lookup(const RecParams& p, int64_t base,
+                                              uint4* (&cptr)[kFlatUnroll]) {
+  const int32_t C = LOG2C >= 0 ? (1 << LOG2C) : p.C;
+#pragma unroll
+  for (int u = 0; u < kFlatUnroll; ++u) {
+    const int64_t g = base + u * kThreads;
+    cptr[u] = nullptr;
+    if (g >= p.total || !DV_OK_S(p.stg + g, 33)) continue;
+    // Fixed-depth searches without branches, so that the four chunks'
+    // lookups overlap: the last record starting at or before g ...
+    int r = 0;
+#pragma unroll
+    for (int half = kRecMax / 2; half > 0; half >>= 1)
+      if (r + half < p.nrec && p.rec_pre[r + half] <= g) r += half;
+    const int64_t q = g - p.rec_pre[r];
+    const int64_t lkv = (int64_t)div64_by((uint64_t)q, (uint64_t)p.rec_lkv[r], p.rec_m[r]);
+    const int32_t w = (int32_t)(q - lkv * p.rec_lkv[r]);
+    const int32_t rec = LOG2C >= 0 ? (w >> LOG2C) : w / C;
+    const int32_t c = w - rec * C;
+    const int32_t tab = p.rec_tab[r];
+    const int32_t pre = tab + p.B;           // tok_pre of the record
+    // ... and the last sequence of that record whose run starts at or
+    // before the chunk's token-head (a non-empty one, as in find_seq).
+    int b = 0;
+#pragma unroll
+    for (int half = kMaxBatch / 2; half > 0; half >>= 1)
+      if (b + half < p.B && p.H * p.words[pre + b + half] <= rec) b += half;
+    const int32_t rr = rec - p.H * p.words[pre + b];
+    const int32_t len = p.words[pre + b + 1] - p.words[pre + b];
+    const uint32_t m = (uint32_t)p.words[pre + p.B + 1 + b];
+    const int32_t h = m ? (int32_t)div_by((uint32_t)rr, (uint32_t)len, m) : rr;
+    const int64_t t = p.words[tab + b] + (rr - h * len);
+    const int64_t l = p.rec_l0[r] + (lkv >> 1);
+    const int64_t bh = (int64_t)b * p.H + h;
+    uint4* ptr = (lkv & 1) == 0 ? p.k + l * p.layer_chunks + ((bh * C + c) * p.S + t)
+                                : p.v + l * p.layer_chunks + ((bh * p.S + t) * C + c);
+    if ((lkv & 1) == 0 ? DV_OK_K(ptr, 31) : DV_OK_V(ptr, 32)) cptr[u] = ptr;
+  }
+}
+
+// The flat kernel's unpack with one more level: chunk g of the launch belongs
+// to the record whose first chunk is the last one at or below g, and inside
+// that record it is addressed exactly as the flat kernel addresses a staging
+// chunk (staging order [layer][K|V][sequence][head][token][chunk]).  Records
+// of one launch write disjoint parts of the cache (the host splits launches
+// where they would not), so their order inside a launch does not matter.
+// The source is read in order (often from host memory, a long round trip):
+// each round's loads go first and its lookups run while they are in flight.
 template <int LOG2C>
 __global__ void __launch_bounds__(kThreads)
 record_unpack_kernel(const __grid_constant__ RecParams p) {
-  pdl_enter();
-  const int32_t C = LOG2C >= 0 ? (1 << LOG2C) : p.C;
   const int64_t step = (int64_t)gridDim.x * (kThreads * kFlatUnroll);
-  for (int64_t base = (int64_t)blockIdx.x * (kThreads * kFlatUnroll) + threadIdx.x;
-       base < p.total; base += step) {
-    // The source is read in order: issue every load first, so that the
-    // address arithmetic below runs while they are in flight (the source is
-    // often host memory, a long round trip).
-    uint4 val[kFlatUnroll];
-    bool ok[kFlatUnroll];
-#pragma unroll
-    for (int u = 0; u < kFlatUnroll; ++u) {
-      const int64_t g = base + u * kThreads;
-      ok[u] = g < p.total && DV_OK_S(p.stg + g, 33);
-      if (ok[u]) val[u] = ld_stream(p.stg + g);
-    }
-#pragma unroll
-    for (int u = 0; u < kFlatUnroll; ++u) {
-      if (!ok[u]) continue;
-      const int64_t g = base + u * kThreads;
-      // Fixed-depth searches without branches, so that the four chunks'
-      // lookups can overlap: the last record starting at or before g ...
-      int r = 0;
-#pragma unroll
-      for (int half = kRecMax / 2; half > 0; half >>= 1)
-        if (r + half < p.nrec && p.rec_pre[r + half] <= g) r += half;
-      const int64_t q = g - p.rec_pre[r];
-      const int64_t lkv = (int64_t)div64_by((uint64_t)q, (uint64_t)p.rec_lkv[r], p.rec_m[r]);
-      const int32_t w = (int32_t)(q - lkv * p.rec_lkv[r]);
-      const int32_t rec = LOG2C >= 0 ? (w >> LOG2C) : w / C;
-      const int32_t c = w - rec * C;
-      const int32_t tab = p.rec_tab[r];
-      const int32_t pre = tab + p.B;           // tok_pre of the record
-      // ... and the last sequence of that record whose run starts at or
-      // before the chunk's token-head (a non-empty one, as in find_seq).
-      int b = 0;
-#pragma unroll
-      for (int half = kMaxBatch / 2; half > 0; half >>= 1)
-        if (b + half < p.B && p.H * p.words[pre + b + half] <= rec) b += half;
-      const int32_t rr = rec - p.H * p.words[pre + b];
-      const int32_t len = p.words[pre + b + 1] - p.words[pre + b];
-      const uint32_t m = (uint32_t)p.words[pre + p.B + 1 + b];
-      const int32_t h = m ? (int32_t)div_by((uint32_t)rr, (uint32_t)len, m) : rr;
-      const int64_t t = p.words[tab + b] + (rr - h * len);
-      const int64_t l = p.rec_l0[r] + (lkv >> 1);
-      const int64_t bh = (int64_t)b * p.H + h;
-      uint4* ptr = (lkv & 1) == 0 ? p.k + l * p.layer_chunks + ((bh * C + c) * p.S + t)
-                                  : p.v + l * p.layer_chunks + ((bh * p.S + t) * C + c);
-      if ((lkv & 1) == 0 ? DV_OK_K(ptr, 31) : DV_OK_V(ptr, 32)) *ptr = val[u];
-    }
-  }
+  int64_t base = (int64_t)blockIdx.x * (kThreads * kFlatUnroll) + threadIdx.x;
+  uint4* cptr[kFlatUnroll];
+  record_lookup<LOG2C>(p, base, cptr);
+  pdl_enter();
+  const auto find = [&p](int64_t b, uint4* (&c)[kFlatUnroll]) { record_lookup<LOG2C>(p, b, c); };
+  if (base < p.total) unpack_round<0, LOG2C>(p, base, cptr, false, find);
+  for (base += step; base < p.total; base += step)
+    unpack_round<0, LOG2C>(p, base, cptr, true, find);
 }
 
 // Contiguous run of `cnt` chunks between the V cache and staging.
@@ -383,89 +431,122 @@ __device__ __forceinline__ void copy_run(const Params& p, uint4* cache, uint4* s
   }
 }
 
+// One tile, uniform across the CTA: its staging chunks, the cache chunk its
+// first token starts at (V: the start of the contiguous run; K: row 0, row c
+// at + c * S), its token count, and whether it is a V tile.
+struct TileJob {
+  uint4* stg;
+  uint4* cache;
+  int32_t n;
+  bool is_v;
+};
+
+template <int LOG2TB, int MAXB>
+__device__ __forceinline__ TileJob decode_tile(const KParams<MAXB>& p, int64_t tile, int32_t C) {
+  constexpr int TB = 1 << LOG2TB;
+  const int64_t lkv = (int64_t)div64_by((uint64_t)tile, (uint64_t)p.tiles_per_lkv, p.m_tpl);
+  const int32_t r = (int32_t)(tile - lkv * p.tiles_per_lkv);
+  const int b = find_seq(p.tile_pre, p.B, r);
+  const int32_t len = p.seq_len[b];
+  const int32_t nblk = (len + TB - 1) >> LOG2TB;
+  const int32_t rr = r - p.tile_pre[b];
+  const int32_t h = rr / nblk;
+  const int32_t t0 = (rr - h * nblk) << LOG2TB;
+  const int64_t l = p.l0 + (lkv >> 1);
+  const int64_t bh = (int64_t)b * p.H + h;
+  TileJob j;
+  j.n = min(TB, len - t0);
+  j.stg = p.stg + lkv * p.lkv_chunks + ((int64_t)p.H * p.tok_pre[b] + (int64_t)h * len + t0) * C;
+  j.is_v = (lkv & 1) != 0;
+  j.cache = j.is_v ? p.v + l * p.layer_chunks + (bh * p.S + p.seq_start[b] + t0) * C
+                   : p.k + l * p.layer_chunks + bh * C * p.S + p.seq_start[b] + t0;
+  return j;
+}
+
+// Moves one tile (see tile_kernel).
 template <bool PACK, int MAXB, int LOG2C>
-__global__ void __launch_bounds__(kThreads, DV_TILE_MIN_BLOCKS)
-tile_kernel(const __grid_constant__ KParams<MAXB> p) {
-  extern __shared__ uint4 smem[];  // TB rows of (C | 1) chunks
+__device__ __forceinline__ void copy_tile(const KParams<MAXB>& p, const TileJob& job,
+                                          uint4* smem) {
   constexpr int TB = TileShape<LOG2C>::TB;
   constexpr int LOG2TB = TileShape<LOG2C>::LOG2TB;
   const int32_t C = LOG2C >= 0 ? (1 << LOG2C) : p.C;
   const int32_t SROW = C | 1;
   const int32_t TC = TB * C;  // chunk slots of a full tile
-  pdl_enter();
-  for (int64_t tile = blockIdx.x; tile < p.total; tile += gridDim.x) {
-    // Uniform across the CTA: which (layer, K|V, sequence, head, token block).
-    const int64_t lkv = (int64_t)div64_by((uint64_t)tile, (uint64_t)p.tiles_per_lkv, p.m_tpl);
-    const int32_t r = (int32_t)(tile - lkv * p.tiles_per_lkv);
-    const int b = find_seq(p.tile_pre, p.B, r);
-    const int32_t len = p.seq_len[b];
-    const int32_t nblk = (len + TB - 1) >> LOG2TB;
-    const int32_t rr = r - p.tile_pre[b];
-    const int32_t h = rr / nblk;
-    const int32_t t0 = (rr - h * nblk) << LOG2TB;
-    const int32_t n = min(TB, len - t0);  // tokens in this tile
-    uint4* stg = p.stg + lkv * p.lkv_chunks +
-                 ((int64_t)p.H * p.tok_pre[b] + (int64_t)h * len + t0) * C;
-    const int32_t cnt = n * C;            // chunks in this tile
-    const int64_t l = p.l0 + (lkv >> 1);
-    const int64_t bh = (int64_t)b * p.H + h;
-    if (lkv & 1) {
-      uint4* cv = p.v + l * p.layer_chunks + (bh * p.S + p.seq_start[b] + t0) * C;
-      copy_run<PACK>(p, cv, stg, cnt);
-    } else if (PACK) {
-      // K: row c of this tile starts at ck + c * S.
-      uint4* ck = p.k + l * p.layer_chunks + bh * C * p.S + p.seq_start[b] + t0;
-      for (int q0 = threadIdx.x; q0 < TC; q0 += kThreads * kTileUnroll) {
-        uint4 val[kTileUnroll];
+  uint4* const stg = job.stg;
+  const int32_t n = job.n;
+  const int32_t cnt = n * C;            // chunks in this tile
+  if (job.is_v) {
+    copy_run<PACK>(p, job.cache, stg, cnt);
+  } else if (PACK) {
+    // K: row c of this tile starts at ck + c * S.
+    uint4* ck = job.cache;
+    for (int q0 = threadIdx.x; q0 < TC; q0 += kThreads * kTileUnroll) {
+      uint4 val[kTileUnroll];
 #pragma unroll
-        for (int u = 0; u < kTileUnroll; ++u) {
-          const int q = q0 + u * kThreads;
-          const int c = q >> LOG2TB, t = q & (TB - 1);
-          if (q < TC && t < n && DV_OK_K(ck + (int64_t)c * p.S + t, 31))
-            val[u] = ld_stream(ck + (int64_t)c * p.S + t);
-        }
-#pragma unroll
-        for (int u = 0; u < kTileUnroll; ++u) {
-          const int q = q0 + u * kThreads;
-          const int c = q >> LOG2TB, t = q & (TB - 1);
-          if (q < TC && t < n) smem[t * SROW + c] = val[u];
-        }
-      }
-      __syncthreads();
-      for (int q = threadIdx.x; q < cnt; q += kThreads) {
-        const int t = LOG2C >= 0 ? q >> LOG2C : q / C;
-        const int c = q - t * C;
-        if (DV_OK_S(stg + q, 32)) stg[q] = smem[t * SROW + c];
-      }
-      __syncthreads();
-    } else {
-      uint4* ck = p.k + l * p.layer_chunks + bh * C * p.S + p.seq_start[b] + t0;
-      for (int q0 = threadIdx.x; q0 < cnt; q0 += kThreads * kTileUnroll) {
-        uint4 val[kTileUnroll];
-#pragma unroll
-        for (int u = 0; u < kTileUnroll; ++u) {
-          const int q = q0 + u * kThreads;
-          if (q < cnt && DV_OK_S(stg + q, 33)) val[u] = ld_stream(stg + q);
-        }
-#pragma unroll
-        for (int u = 0; u < kTileUnroll; ++u) {
-          const int q = q0 + u * kThreads;
-          if (q < cnt) {
-            const int t = LOG2C >= 0 ? q >> LOG2C : q / C;
-            const int c = q - t * C;
-            smem[t * SROW + c] = val[u];
-          }
-        }
-      }
-      __syncthreads();
-      for (int q = threadIdx.x; q < TC; q += kThreads) {
+      for (int u = 0; u < kTileUnroll; ++u) {
+        const int q = q0 + u * kThreads;
         const int c = q >> LOG2TB, t = q & (TB - 1);
-        if (t < n && DV_OK_K(ck + (int64_t)c * p.S + t, 34))
-          ck[(int64_t)c * p.S + t] = smem[t * SROW + c];
+        if (q < TC && t < n && DV_OK_K(ck + (int64_t)c * p.S + t, 31))
+          val[u] = ld_stream(ck + (int64_t)c * p.S + t);
       }
-      __syncthreads();
+#pragma unroll
+      for (int u = 0; u < kTileUnroll; ++u) {
+        const int q = q0 + u * kThreads;
+        const int c = q >> LOG2TB, t = q & (TB - 1);
+        if (q < TC && t < n) smem[t * SROW + c] = val[u];
+      }
     }
+    __syncthreads();
+    for (int q = threadIdx.x; q < cnt; q += kThreads) {
+      const int t = LOG2C >= 0 ? q >> LOG2C : q / C;
+      const int c = q - t * C;
+      if (DV_OK_S(stg + q, 32)) stg[q] = smem[t * SROW + c];
+    }
+    __syncthreads();
+  } else {
+    uint4* ck = job.cache;
+    for (int q0 = threadIdx.x; q0 < cnt; q0 += kThreads * kTileUnroll) {
+      uint4 val[kTileUnroll];
+#pragma unroll
+      for (int u = 0; u < kTileUnroll; ++u) {
+        const int q = q0 + u * kThreads;
+        if (q < cnt && DV_OK_S(stg + q, 33)) val[u] = ld_stream(stg + q);
+      }
+#pragma unroll
+      for (int u = 0; u < kTileUnroll; ++u) {
+        const int q = q0 + u * kThreads;
+        if (q < cnt) {
+          const int t = LOG2C >= 0 ? q >> LOG2C : q / C;
+          const int c = q - t * C;
+          smem[t * SROW + c] = val[u];
+        }
+      }
+    }
+    __syncthreads();
+    for (int q = threadIdx.x; q < TC; q += kThreads) {
+      const int c = q >> LOG2TB, t = q & (TB - 1);
+      if (t < n && DV_OK_K(ck + (int64_t)c * p.S + t, 34))
+        ck[(int64_t)c * p.S + t] = smem[t * SROW + c];
+    }
+    __syncthreads();
   }
+}
+
+template <bool PACK, int MAXB, int LOG2C>
+__global__ void __launch_bounds__(kThreads, DV_TILE_MIN_BLOCKS)
+tile_kernel(const __grid_constant__ KParams<MAXB> p) {
+  extern __shared__ uint4 smem[];  // TB rows of (C | 1) chunks
+  constexpr int LOG2TB = TileShape<LOG2C>::LOG2TB;
+  const int32_t C = LOG2C >= 0 ? (1 << LOG2C) : p.C;
+  int64_t tile = blockIdx.x;
+  if (tile >= p.total) return;
+  // The first tile is decoded before the wait for the preceding grid (that
+  // reads only the kernel parameters), so its loads start right after it.
+  const TileJob first = decode_tile<LOG2TB>(p, tile, C);
+  pdl_enter();
+  copy_tile<PACK, MAXB, LOG2C>(p, first, smem);
+  for (tile += gridDim.x; tile < p.total; tile += gridDim.x)
+    copy_tile<PACK, MAXB, LOG2C>(p, decode_tile<LOG2TB>(p, tile, C), smem);
 }
 
 // ---- host side -------------------------------------------------------------
