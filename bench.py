@@ -67,8 +67,8 @@ def parse_args():
 # layer (traffic grows with the tiles processed).  Set an entry to None when
 # the kernel changes, until it is captured again.
 TRAFFIC_PER_LAUNCH = {
-    "pack prompt layer (tile kernel)": None,
-    "unpack prompt layer (tile kernel)": None,
+    "pack prompt layer (tile kernel)": (409.637632e6 + 351.859200e6) / 8,
+    "unpack prompt layer (tile kernel)": (409.633280e6 + 351.618816e6) / 8,
 }
 
 
