@@ -11,6 +11,7 @@ import torch
 
 import kv_cache_streaming_gb300 as dv
 import oracle
+import synth
 from synth import configs as C
 from synth import gpu as synth_gpu
 from tests import gpu_helpers as H
@@ -196,3 +197,36 @@ def test_bloom_replica_256_steps_and_restore():
     torch.cuda.synchronize()
     H.assert_prefix_equal_rest_zero(g, back, cache, pos)
     rep.close()
+
+
+def test_largest_launch_beyond_2_31_chunks():
+    """The whole BLOOM-stage cache ([0, 2048) of every sequence, all 14 layers:
+    52.6 GB of staging, 3.3e9 16-byte chunks, more than 2^31) in one pack
+    launch per kernel variant, and one unpack back into the zeroed cache:
+    sampled staging elements equal the oracle's, sampled cache elements the
+    generator's."""
+    g, seed = C.BLOOM_STAGE, C.seed_of(5)
+    rng = np.random.default_rng(55)
+    zs = np.zeros(g.batch, np.int32)
+    full = np.full(g.batch, g.max_seq, np.int32)
+    cache = H.device_cache(g, fill="synth", seed=seed)
+    n = dv.dv_staging_bytes(cache, 0, g.num_layers, zs, full)
+    assert n == 2 * g.tensor_bytes and n // 16 > 2 ** 31
+    stg = torch.empty(n, dtype=torch.uint8, device="cuda")
+    for variant in (dv.DV_VARIANT_AUTO, dv.DV_VARIANT_FLAT):
+        stg[-(1 << 20):].zero_()
+        dv.dv_kv_pack(cache, 0, g.num_layers, zs, full, stg, variant=variant)
+        torch.cuda.synchronize()
+        H.sampled_check(ORC, g, seed, stg, 0, g.num_layers, zs, full, rng)
+    cache.k.zero_()
+    cache.v.zero_()
+    dv.dv_kv_unpack(cache, 0, g.num_layers, zs, full, stg)
+    torch.cuda.synchronize()
+    del stg
+    view = {2: torch.int16}[g.elem_bytes]
+    for kv, t in ((0, cache.k), (1, cache.v)):
+        idx = np.unique(np.concatenate([rng.integers(0, g.tensor_elems, size=200_000),
+                                        np.array([0, g.tensor_elems - 1])]))
+        got = t.view(view)[torch.from_numpy(idx).cuda()].cpu().numpy().view(np.uint16)
+        want = synth.fill_elements(seed, kv, idx, g.elem_bytes, g.kind)
+        assert np.array_equal(got, want), f"{'KV'[kv]}: sampled elements differ after unpack"
