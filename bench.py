@@ -441,39 +441,38 @@ class Bench:
         self.slots = (torch.empty(self.slab, dtype=torch.uint8, device="cuda"),
                       torch.empty(self.slab, dtype=torch.uint8, device="cuda"))
         self.copy_stream = torch.cuda.Stream()
-        self.in_stream = torch.cuda.Stream()
-        self.in_stream2 = torch.cuda.Stream()
-        self.in_staging = torch.empty(self.slab, dtype=torch.uint8, device="cuda")
-        self.in_staging2 = torch.empty(self.slab, dtype=torch.uint8, device="cuda")
+        self.in_copy = torch.cuda.Stream()
+        self.in_unpack = torch.cuda.Stream()
+        self.in_slots = (torch.empty(self.slab, dtype=torch.uint8, device="cuda"),
+                         torch.empty(self.slab, dtype=torch.uint8, device="cuda"))
         self.streamer = dv.Streamer(self.slots[0], self.slots[1], self.stream, self.copy_stream)
+        self.fetcher = dv.Fetcher(self.in_slots[0], self.in_slots[1], self.in_copy,
+                                  self.in_unpack)
+        self.restore_staging = torch.empty(GPT2_DECODE_STEPS * self.dsz, dtype=torch.uint8,
+                                           device="cuda")
         self.replica = dv.Replica(self.arena, g.batch)
 
     def e2e_step(self):
         """Layer by layer: the streamer packs layer l and copies it to pinned
-        host memory (copy engine); as soon as that copy is done, layer l is
-        swapped in from the host into the second cache on a third stream,
-        staged through a device buffer so that a copy engine carries it too:
-        host-to-device traffic of layer l overlaps device-to-host traffic of
-        layer l+1 on the full-duplex link.  Then the 24 deltas go to the host
-        replica (fused pack into host memory) and are restored from it."""
-        dv, g = self.dv, self.g
+        host memory (copy engine); as soon as that copy is done, the fetcher
+        copies layer l back into one of its device slots (copy engine) and
+        unpacks it into the second cache on its own stream: host-to-device
+        traffic of layer l overlaps device-to-host traffic of layer l+1 on the
+        full-duplex link, and the unpack of layer l the copy of layer l+1.
+        Then the 24 deltas go to the host replica (fused pack into host
+        memory) and are restored from it (record-batched, staged)."""
+        g = self.g
         s = self.stream
-        ins = (self.in_stream, self.in_stream2)
-        stgs = (self.in_staging, self.in_staging2)
-        hp = self.host_prompt.data_ptr()
         for l in range(g.num_layers):
             self.streamer.stream_layer(self.cache, l, self.ps, self.pe, self.host_prompt, l0=0)
-            si = ins[l % 2]  # two swap-in streams: layer l's unpack overlaps l+1's copy
-            si.wait_stream(self.copy_stream)
-            dv.dv_swap_in(self.cache_b, l, l + 1, self.ps, self.pe, (hp + l * self.slab, self.slab),
-                          staging=stgs[l % 2], stream=si)
+            self.in_copy.wait_stream(self.copy_stream)  # layer l is in host memory
+            self.fetcher.fetch_layer(self.cache_b, l, self.ps, self.pe, self.host_prompt, l0=0)
         self.replica.truncate(0)
         for k, (a, b) in enumerate(self.deltas):
             self.replica.append(self.cache, 0, g.num_layers, a, b, step=k, stream=s)
-        si = ins[0]
+        si = self.in_unpack
         si.wait_stream(s)
-        si.wait_stream(ins[1])
-        self.replica.restore_batched(self.cache_b, staging=stgs[0], stream=si)
+        self.replica.restore_batched(self.cache_b, staging=self.restore_staging, stream=si)
         s.wait_stream(si)
 
     def timed_e2e(self, steps, warmup, world):
@@ -1192,9 +1191,9 @@ def run_mine(args):
                 "timing": "median step (each step synchronised); over all steps: "
                           f"{e2e_all:.1f} GB/s, slowest step {max(e2e_ts) * 1e3:.2f} ms, "
                           f"fastest {min(e2e_ts) * 1e3:.2f} ms",
-                "path": "per layer: dv_stream_layer (pack + D2H copy) then dv_swap_in of that "
-                        "layer (H2D copy + unpack) on a third stream, overlapping the next "
-                        "layer's D2H; dv_replica_append x24 (fused) + "
+                "path": "per layer: dv_stream_layer (pack + D2H copy) then dv_fetch_layer "
+                        "(H2D copy + unpack on the fetcher's two streams), overlapping the "
+                        "next layer's D2H; dv_replica_append x24 (fused) + "
                         "dv_replica_restore_batched (staged)"},
         "swap": swap,
         "naive_vs_buffered": naive,

@@ -16,6 +16,7 @@
  *   dv_stream_layer  §3 "Layer-by-layer prompt cache streaming" (Fig 7b): the
  *                    pack of layer l+1 overlaps the device-to-host copy of
  *                    layer l, on two streams ordered by events.
+ *   dv_fetch_layer   the receiving side of that stream (Table 1 stream_in).
  *   dv_replica_*     §3 "Fault detection and recovery" (Fig 10) on one GPU:
  *                    per-step decode deltas (§3 "Token computation and
  *                    streaming parallelization", Fig 7c) appended to a
@@ -259,6 +260,40 @@ dv_status dv_streamer_wait(dv_streamer* streamer);
 
 /* Releases the handle (its events are released once pending work ends). */
 void dv_streamer_destroy(dv_streamer* streamer);
+
+/* ---- layer-by-layer receive (§3, Fig 7b, the receiving side; Table 1
+ * stream_in) ------------------------------------------------------------- */
+
+/* The mirror image of dv_streamer: layer slabs come in from host memory
+ * through two device slots and are unpacked into a cache as they arrive.
+ * Owns two events per slot; borrows the slots and streams. */
+typedef struct dv_fetcher dv_fetcher;
+
+/* slot0 / slot1: device buffers of slot_bytes each (16-byte aligned), used
+ * alternately.  Host-to-device copies run on copy_stream, unpacks on
+ * unpack_stream (two different streams overlap the copy of layer l+1 with
+ * the unpack of layer l; one stream serialises them). */
+dv_status dv_fetcher_create(dv_fetcher** out, void* slot0, void* slot1, size_t slot_bytes,
+                            dv_stream copy_stream, dv_stream unpack_stream);
+
+/* Copies the slab of layer `layer` from host_src + (layer - l0) * slab, where
+ * slab is this layer's staging size (the layout dv_stream_layer and one
+ * dv_kv_pack over [l0, ...) produce with the same ranges), into the next
+ * slot on the copy stream (after that slot's previous unpack has finished),
+ * then unpacks it into `cache` on the unpack stream.  host_src: pinned host
+ * memory (or device memory) of host_src_bytes.  The caller orders the copy
+ * stream after whatever wrote host_src and the unpack stream after whatever
+ * last used the cache's slices; an event recorded on the unpack stream after
+ * the call marks the layer as present.  Errors as dv_stream_layer. */
+dv_status dv_fetch_layer(dv_fetcher* fetcher, const dv_cache* cache, int32_t layer,
+                         const int32_t* seq_start, const int32_t* seq_end, const void* host_src,
+                         size_t host_src_bytes, int32_t l0);
+
+/* Blocks the calling thread until every unpack issued so far has finished. */
+dv_status dv_fetcher_wait(dv_fetcher* fetcher);
+
+/* Releases the handle (its events are released once pending work ends). */
+void dv_fetcher_destroy(dv_fetcher* fetcher);
 
 /* ---- host-side replica of a cache (§3 state replication, Fig 10) -------- */
 

@@ -16,10 +16,11 @@ from .dv import (  # noqa: F401
     DV_MAX_BATCH, DV_OK, DV_ERR_INVALID_ARG, DV_ERR_RANGE, DV_ERR_BUFFER_TOO_SMALL,
     DV_ERR_MISALIGNED, DV_ERR_CUDA, DV_ERR_TIMEOUT, DV_ERR_UNSUPPORTED,
     DV_VARIANT_AUTO, DV_VARIANT_FLAT, DV_VARIANT_TILE, DV_VARIANT_TOKEN,
-    DvError, Cache, Streamer, Replica, lib, library_path,
+    DvError, Cache, Streamer, Fetcher, Replica, lib, library_path,
     dv_abi_version, dv_allocation_extent, dv_debug_fault, dv_staging_bytes, dv_kv_pack, dv_kv_unpack, dv_naive_gather, dv_swap_out, dv_swap_in,
     dv_swap_out_noalloc, DV_NOALLOC_STAGING_BYTES,
     dv_streamer_create, dv_stream_layer, dv_streamer_wait, dv_streamer_destroy,
+    dv_fetcher_create, dv_fetch_layer, dv_fetcher_wait, dv_fetcher_destroy,
     dv_replica_create, dv_replica_append, dv_replica_restore, dv_replica_restore_batched,
     dv_replica_truncate,
     dv_replica_info, dv_replica_destroy,

@@ -331,6 +331,17 @@ struct dv_streamer {
   int next;
 };
 
+struct dv_fetcher {
+  void* slot[2];
+  size_t slot_bytes;
+  cudaStream_t copy;
+  cudaStream_t unpack;
+  cudaEvent_t copied[2];
+  cudaEvent_t freed[2];
+  bool used[2];
+  int next;
+};
+
 // ---- replica -----------------------------------------------------------------
 
 namespace {
@@ -590,6 +601,106 @@ void dv_streamer_destroy(dv_streamer* h) {
   if (!h) return;
   cudaEventDestroy(h->packed[0]);
   cudaEventDestroy(h->packed[1]);
+  cudaEventDestroy(h->freed[0]);
+  cudaEventDestroy(h->freed[1]);
+  delete h;
+}
+
+dv_status dv_fetcher_create(dv_fetcher** out, void* slot0, void* slot1, size_t slot_bytes,
+                            dv_stream copy_stream, dv_stream unpack_stream) {
+  if (!out) return fail(DV_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  void* d0 = nullptr;
+  void* d1 = nullptr;
+  dv_status st = resolve(slot0, slot_bytes, false, "slot0", &d0);
+  if (st != DV_OK) return st;
+  if ((st = resolve(slot1, slot_bytes, false, "slot1", &d1)) != DV_OK) return st;
+  if (slot0 == slot1) return fail(DV_ERR_INVALID_ARG, "slot0 and slot1 must differ");
+  dv_fetcher* h = new (std::nothrow) dv_fetcher();
+  if (!h) return fail(DV_ERR_INVALID_ARG, "out of host memory for the fetcher handle");
+  h->slot[0] = d0;
+  h->slot[1] = d1;
+  h->slot_bytes = slot_bytes;
+  h->copy = copy_stream;
+  h->unpack = unpack_stream;
+  h->used[0] = h->used[1] = false;
+  h->next = 0;
+  int made = 0;
+  cudaError_t err = cudaSuccess;
+  cudaEvent_t* evs[4] = {&h->copied[0], &h->copied[1], &h->freed[0], &h->freed[1]};
+  for (; made < 4; ++made)
+    if ((err = cudaEventCreateWithFlags(evs[made], cudaEventDisableTiming)) != cudaSuccess) break;
+  if (made < 4) {
+    for (int i = 0; i < made; ++i) cudaEventDestroy(*evs[i]);
+    delete h;
+    return cuda_fail(err, "cudaEventCreateWithFlags");
+  }
+  *out = h;
+  return DV_OK;
+}
+
+dv_status dv_fetch_layer(dv_fetcher* h, const dv_cache* cache, int32_t layer,
+                         const int32_t* seq_start, const int32_t* seq_end, const void* host_src,
+                         size_t host_src_bytes, int32_t l0) {
+  if (!h) return fail(DV_ERR_INVALID_ARG, "fetcher is NULL");
+  if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
+  if (l0 < 0 || layer < l0)
+    return fail(DV_ERR_RANGE, "layer %d is before the streamed range start %d", layer, l0);
+  dv::Plan p;
+  dv_status st = plan_ranges(cache, layer, layer + 1, seq_start, seq_end, &p);
+  if (st != DV_OK) return st;
+  if (p.bytes == 0) return DV_OK;
+  if ((size_t)p.bytes > h->slot_bytes)
+    return fail(DV_ERR_BUFFER_TOO_SMALL, "layer slab of %lld bytes exceeds slot of %zu",
+                (long long)p.bytes, h->slot_bytes);
+  const size_t off = (size_t)(layer - l0) * (size_t)p.bytes;
+  if (!host_src) return fail(DV_ERR_INVALID_ARG, "host_src is NULL");
+  if (off + (size_t)p.bytes > host_src_bytes)
+    return fail(DV_ERR_BUFFER_TOO_SMALL, "layer %d lies at bytes [%zu,%zu) of a %zu-byte buffer",
+                layer, off, off + (size_t)p.bytes, host_src_bytes);
+  if ((st = resolve_cache(cache, &p)) != DV_OK) return st;
+  {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, host_src) != cudaSuccess ||
+        a.type == cudaMemoryTypeUnregistered) {
+      cudaGetLastError();
+      return fail(DV_ERR_INVALID_ARG, "host_src must be pinned host or device memory");
+    }
+  }
+  const int i = h->next;
+  cudaError_t err;
+  if (h->used[i] && (err = cudaStreamWaitEvent(h->copy, h->freed[i], 0)) != cudaSuccess)
+    return cuda_fail(err, "cudaStreamWaitEvent(slot free)");
+  if ((err = cudaMemcpyAsync(h->slot[i], static_cast<const uint8_t*>(host_src) + off,
+                             (size_t)p.bytes, cudaMemcpyDefault, h->copy)) != cudaSuccess)
+    return cuda_fail(err, "fetch_layer copy");
+  if ((err = cudaEventRecord(h->copied[i], h->copy)) != cudaSuccess)
+    return cuda_fail(err, "cudaEventRecord(copied)");
+  if ((err = cudaStreamWaitEvent(h->unpack, h->copied[i], 0)) != cudaSuccess)
+    return cuda_fail(err, "cudaStreamWaitEvent(copied)");
+  if ((err = dv::launch_unpack(p, h->slot[i], h->unpack, dv::kAuto)) != cudaSuccess)
+    return cuda_fail(err, "fetch_layer unpack launch");
+  if ((err = cudaEventRecord(h->freed[i], h->unpack)) != cudaSuccess)
+    return cuda_fail(err, "cudaEventRecord(freed)");
+  h->used[i] = true;
+  h->next = i ^ 1;
+  return DV_OK;
+}
+
+dv_status dv_fetcher_wait(dv_fetcher* h) {
+  if (!h) return fail(DV_ERR_INVALID_ARG, "fetcher is NULL");
+  for (int i = 0; i < 2; ++i) {
+    if (!h->used[i]) continue;
+    const cudaError_t err = cudaEventSynchronize(h->freed[i]);
+    if (err != cudaSuccess) return cuda_fail(err, "cudaEventSynchronize");
+  }
+  return DV_OK;
+}
+
+void dv_fetcher_destroy(dv_fetcher* h) {
+  if (!h) return;
+  cudaEventDestroy(h->copied[0]);
+  cudaEventDestroy(h->copied[1]);
   cudaEventDestroy(h->freed[0]);
   cudaEventDestroy(h->freed[1]);
   delete h;

@@ -72,6 +72,10 @@ _streamer_create = _sig("dv_streamer_create", [ctypes.POINTER(_P), _P, _P, _SZ, 
 _stream_layer = _sig("dv_stream_layer", [_P, _CP, _I32, _I32P, _I32P, _P, _SZ, _I32])
 _streamer_wait = _sig("dv_streamer_wait", [_P])
 _streamer_destroy = _sig("dv_streamer_destroy", [_P], None)
+_fetcher_create = _sig("dv_fetcher_create", [ctypes.POINTER(_P), _P, _P, _SZ, _P, _P])
+_fetch_layer = _sig("dv_fetch_layer", [_P, _CP, _I32, _I32P, _I32P, _P, _SZ, _I32])
+_fetcher_wait = _sig("dv_fetcher_wait", [_P])
+_fetcher_destroy = _sig("dv_fetcher_destroy", [_P], None)
 _replica_create = _sig("dv_replica_create", [ctypes.POINTER(_P), _P, _SZ, _I32])
 _replica_append = _sig("dv_replica_append", [_P] + _RANGE + [_I64, _P, _SZ, _P])
 _replica_restore = _sig("dv_replica_restore", [_P, _CP, _I64, _P, _SZ, _P])
@@ -299,6 +303,55 @@ def dv_streamer_wait(streamer: Streamer) -> None:
 
 def dv_streamer_destroy(streamer: Streamer) -> None:
     streamer.close()
+
+
+class Fetcher:
+    """Handle of ``dv_fetcher`` (two slots, copy and unpack streams)."""
+
+    def __init__(self, slot0, slot1, copy_stream=None, unpack_stream=None):
+        a0, n0 = _buf(slot0)
+        a1, n1 = _buf(slot1)
+        self._keep = (slot0, slot1, copy_stream, unpack_stream)
+        h = _P()
+        _check(_fetcher_create(ctypes.byref(h), a0, a1, min(n0, n1), _stream(copy_stream),
+                               _stream(unpack_stream)))
+        self.h = h
+
+    def fetch_layer(self, cache: Cache, layer, seq_start, seq_end, host_src, l0=0):
+        s, e, sp, ep = _ranges(seq_start, seq_end, cache.c.batch)
+        d, n = _buf(host_src)
+        _check(_fetch_layer(self.h, cache.ref, layer, sp, ep, d, n, l0))
+
+    def wait(self):
+        _check(_fetcher_wait(self.h))
+
+    def close(self):
+        if self.h:
+            _fetcher_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def dv_fetcher_create(slot0, slot1, copy_stream=None, unpack_stream=None) -> Fetcher:
+    return Fetcher(slot0, slot1, copy_stream, unpack_stream)
+
+
+def dv_fetch_layer(fetcher: Fetcher, cache: Cache, layer, seq_start, seq_end, host_src,
+                   l0=0) -> None:
+    fetcher.fetch_layer(cache, layer, seq_start, seq_end, host_src, l0)
+
+
+def dv_fetcher_wait(fetcher: Fetcher) -> None:
+    fetcher.wait()
+
+
+def dv_fetcher_destroy(fetcher: Fetcher) -> None:
+    fetcher.close()
 
 
 class Replica:

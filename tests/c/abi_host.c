@@ -47,6 +47,19 @@ int main(void) {
   CHECK(dv_kv_pack(&c, 0, 48, s, e, (void*)0x3000, 16, NULL) == DV_ERR_BUFFER_TOO_SMALL);
   CHECK(dv_kv_pack(NULL, 0, 48, s, e, (void*)0x3000, 16, NULL) == DV_ERR_INVALID_ARG);
   CHECK(strcmp(dv_status_string(DV_ERR_MISALIGNED), "DV_ERR_MISALIGNED") == 0);
+  /* NULL handles are refused before anything reaches the GPU */
+  CHECK(dv_stream_layer(NULL, &c, 0, s, e, (void*)0x3000, 16, 0) == DV_ERR_INVALID_ARG);
+  CHECK(dv_fetch_layer(NULL, &c, 0, s, e, (const void*)0x3000, 16, 0) == DV_ERR_INVALID_ARG);
+  CHECK(dv_streamer_wait(NULL) == DV_ERR_INVALID_ARG);
+  CHECK(dv_fetcher_wait(NULL) == DV_ERR_INVALID_ARG);
+  CHECK(dv_streamer_create(NULL, NULL, NULL, 0, NULL, NULL) == DV_ERR_INVALID_ARG);
+  CHECK(dv_fetcher_create(NULL, NULL, NULL, 0, NULL, NULL) == DV_ERR_INVALID_ARG);
+  CHECK(dv_replica_restore(NULL, &c, -1, NULL, 0, NULL) == DV_ERR_INVALID_ARG);
+  CHECK(dv_replica_restore_batched(NULL, &c, -1, NULL, 0, NULL) == DV_ERR_INVALID_ARG);
+  CHECK(dv_replica_truncate(NULL, 0) == DV_ERR_INVALID_ARG);
+  dv_streamer_destroy(NULL);
+  dv_fetcher_destroy(NULL);
+  dv_replica_destroy(NULL);
   if (failures == 0) printf("abi_host: all checks passed\n");
   return failures == 0 ? 0 : 1;
 }

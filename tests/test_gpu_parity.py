@@ -182,6 +182,83 @@ def test_stream_layers_matches_oracle_and_swap_out():
     st.close()
 
 
+@pytest.mark.parametrize("one_stream", [False, True])
+def test_fetch_layers_matches_oracle(one_stream):
+    """The receiving side of layer streaming: the slabs of [l0, l1) in host
+    memory (the bytes one pack over that range gives) come into a sentinel
+    cache one layer at a time, in order and out of order; the cache then
+    equals the oracle's unpack, and a streamer-fetcher round trip restores
+    the source slices."""
+    g = Geometry("fetch", 6, 3, 4, 64, 128, 2, "fp16")
+    kh, vh = H.host_cache(g, 16)
+    s = np.array([0, 5, 100], np.int32)
+    e = np.array([100, 128, 101], np.int32)
+    l0, l1 = 1, 6
+    n = ORC.staging_bytes(g, l0, l1, s, e)
+    slab = n // (l1 - l0)
+    data = ORC.pack(g, kh, vh, l0, l1, s, e)
+    host = H.pinned(n + 64, fill=0)
+    host.numpy()[:n] = data
+    slots = (H.device_bytes(slab), H.device_bytes(slab))
+    cs = torch.cuda.Stream()
+    us = cs if one_stream else torch.cuda.Stream()
+    kw = np.full(g.tensor_bytes, 0x5A, np.uint8)
+    vw = np.full(g.tensor_bytes, 0x5A, np.uint8)
+    ORC.unpack(g, kw, vw, l0, l1, s, e, data)
+    for order in (range(l0, l1), [5, 2, 4, 1, 3]):
+        back = H.device_cache(g, fill=0x5A)
+        f = dv.Fetcher(slots[0], slots[1], cs, us)
+        torch.cuda.synchronize()
+        for layer in order:
+            f.fetch_layer(back, layer, s, e, host, l0=l0)
+        f.wait()
+        assert np.array_equal(H.to_np(back.k), kw) and np.array_equal(H.to_np(back.v), vw)
+        f.close()
+    # round trip: stream out of one cache, fetch into another, layer by layer
+    cache = H.device_cache(g, fill=(kh, vh))
+    back = H.device_cache(g, fill=0x5A)
+    out = H.pinned(n)
+    ps, pc = torch.cuda.Stream(), torch.cuda.Stream()
+    st = dv.Streamer(H.device_bytes(slab), H.device_bytes(slab), ps, pc)
+    f = dv.Fetcher(slots[0], slots[1], cs, us)
+    torch.cuda.synchronize()
+    for layer in range(l0, l1):
+        st.stream_layer(cache, layer, s, e, out, l0=l0)
+        cs.wait_stream(pc)  # the layer's bytes are in host memory before they are fetched
+        f.fetch_layer(back, layer, s, e, out, l0=l0)
+    f.wait()
+    st.wait()
+    assert np.array_equal(H.to_np(back.k), kw) and np.array_equal(H.to_np(back.v), vw)
+    st.close()
+    f.close()
+
+
+def test_fetcher_errors_enqueue_nothing():
+    g = Geometry("fetcherr", 3, 2, 2, 64, 64, 2, "fp16")
+    s, e = np.zeros(2, np.int32), np.full(2, 64, np.int32)
+    n = ORC.staging_bytes(g, 0, 3, s, e)
+    slab = n // 3
+    back = H.device_cache(g, fill=0x11)
+    host = H.pinned(n, fill=0x22)
+    big = (H.device_bytes(slab), H.device_bytes(slab))
+    small = (H.device_bytes(slab // 2), H.device_bytes(slab // 2))
+    assert _status(lambda: dv.Fetcher(big[0], big[0])) == dv.DV_ERR_INVALID_ARG
+    f = dv.Fetcher(small[0], small[1])
+    assert _status(lambda: f.fetch_layer(back, 0, s, e, host)) == dv.DV_ERR_BUFFER_TOO_SMALL
+    f.close()
+    f = dv.Fetcher(big[0], big[1])
+    assert _status(lambda: f.fetch_layer(back, 2, s, e, (host.data_ptr(), 2 * slab))) == \
+        dv.DV_ERR_BUFFER_TOO_SMALL                        # layer 2 lies past the buffer
+    assert _status(lambda: f.fetch_layer(back, 0, s, e, host, l0=1)) == dv.DV_ERR_RANGE
+    pageable = np.zeros(n, np.uint8)
+    assert _status(lambda: f.fetch_layer(back, 0, s, e, (pageable.ctypes.data, n))) == \
+        dv.DV_ERR_INVALID_ARG
+    f.wait()
+    f.close()
+    torch.cuda.synchronize()
+    assert (H.to_np(back.k) == 0x11).all() and (H.to_np(back.v) == 0x11).all()
+
+
 @pytest.mark.parametrize("staged", [False, True])
 def test_replica_snapshot_deltas_restore_truncate(staged):
     g = Geometry("rep", 3, 4, 2, 128, 64, 2, "bf16")
