@@ -719,6 +719,8 @@ class MicrobatchSwapping:
         self.per_token = dv.dv_staging_bytes(self.slots[0], 0, L, self.zs,
                                              np.ones(g.batch, np.int32)) // g.batch
         self.staging = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+        self.fslots = (torch.empty(256 << 20, dtype=torch.uint8, device="cuda"),
+                       torch.empty(256 << 20, dtype=torch.uint8, device="cuda"))
         self.refs = []
         self.replicas, self.arenas, self.lens, self.seeds = [], [], [], []
         for m, (p, o) in enumerate(self.mbs):
@@ -763,31 +765,38 @@ class MicrobatchSwapping:
                 dv.dv_kv_unpack(self.refs[m], 0, g.num_layers, ln, ln + act, tok, stream=s)
         return act
 
-    def run(self, mode, s, s2=None):
-        """`rounds` rounds over the N microbatches; returns the seconds taken."""
+    def run(self, mode, s, s2=None, s3=None):
+        """`rounds` rounds over the N microbatches; returns the seconds taken.
+        Swap-ins are replica restores pipelined through a fetcher: its copies
+        on one stream, its unpacks on another (serial: the compute stream)."""
         torch, dv, g = self.torch, self.dv, self.g
         L = g.num_layers
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         if mode == "serial":
             slot = self.slots[0]
+            fc = torch.cuda.Stream()
+            fetcher = dv.Fetcher(self.fslots[0], self.fslots[1], fc, s)
             for _ in range(self.rounds):
                 for m in range(self.N):
-                    self.replicas[m].restore_batched(slot, staging=self.staging, stream=s)
+                    fc.wait_stream(s)  # after the previous append and compute
+                    self.replicas[m].restore_fetched(slot, fetcher)
                     act = self._compute_and_write(m, slot, s)
                     ln = self.lens[m]
                     self.replicas[m].append(slot, 0, L, ln, ln + act, step=self.step_no[m],
                                             stream=s)
                     self.lens[m] = ln + act
                     self.step_no[m] += 1
+            self.last = (0, self.N - 1)
         else:
             ready = [torch.cuda.Event() for _ in range(2)]
             done = [torch.cuda.Event() for _ in range(2)]
             order = [m for _ in range(self.rounds) for m in range(self.N)]
+            # copies on s2 (after the swap-outs queued there), unpacks on s3
+            fetcher = dv.Fetcher(self.fslots[0], self.fslots[1], s2, s3)
             # prefetch the first microbatch into slot 0
-            self.replicas[order[0]].restore_batched(self.slots[0], staging=self.staging,
-                                                    stream=s2)
-            ready[0].record(s2)
+            self.replicas[order[0]].restore_fetched(self.slots[0], fetcher)
+            ready[0].record(s3)
             for i, m in enumerate(order):
                 sl = i % 2
                 slot = self.slots[sl]
@@ -796,9 +805,8 @@ class MicrobatchSwapping:
                 done[sl].record(s)
                 if i + 1 < len(order):  # the next microbatch comes in on the other slot
                     nxt = order[i + 1]
-                    self.replicas[nxt].restore_batched(self.slots[1 - sl], staging=self.staging,
-                                                       stream=s2)
-                    ready[1 - sl].record(s2)
+                    self.replicas[nxt].restore_fetched(self.slots[1 - sl], fetcher)
+                    ready[1 - sl].record(s3)
                 # swap-out of this microbatch's step: its token, into its replica
                 s2.wait_event(done[sl])
                 ln = self.lens[m]
@@ -808,26 +816,37 @@ class MicrobatchSwapping:
                 self.step_no[m] += 1
                 # the slot is refilled two microbatches later, after this append
             s.wait_stream(s2)
+            s.wait_stream(s3)
+            self.last = ((len(order) - 1) % 2, order[-1])
         torch.cuda.synchronize()
+        fetcher.close()
         return time.perf_counter() - t0
 
     def check(self):
-        """Each replica restored into a zeroed slot equals the reference cache on
-        the used prefix (needs keep_refs)."""
+        """The slot the last microbatch step ran in (swapped in during the run,
+        then written) and each replica restored into a zeroed slot equal the
+        reference cache on the used prefix (needs keep_refs)."""
         torch, dv, g = self.torch, self.dv, self.g
         L = g.num_layers
-        for m in range(self.N):
-            slot = self.slots[0]
-            slot.k.zero_()
-            slot.v.zero_()
-            self.replicas[m].restore(slot, staging=self.staging)
+
+        def same(slot, m):
             n = dv.dv_staging_bytes(slot, 0, L, self.zs, self.lens[m])
             a = torch.empty(n, dtype=torch.uint8, device="cuda")
             b = torch.empty(n, dtype=torch.uint8, device="cuda")
             dv.dv_kv_pack(slot, 0, L, self.zs, self.lens[m], a)
             dv.dv_kv_pack(self.refs[m], 0, L, self.zs, self.lens[m], b)
             torch.cuda.synchronize()
-            if not torch.equal(a, b):
+            return bool(torch.equal(a, b))
+
+        sl, m_last = self.last
+        if not same(self.slots[sl], m_last):
+            return False
+        for m in range(self.N):
+            slot = self.slots[0]
+            slot.k.zero_()
+            slot.v.zero_()
+            self.replicas[m].restore(slot, staging=self.staging)
+            if not same(slot, m):
                 return False
         return True
 
@@ -842,19 +861,24 @@ class MicrobatchSwapping:
         torch = self.torch
         # the swap stream runs at high priority: its short unpack kernels then
         # get SMs ahead of the compute, so its copy-engine pipeline never stalls
-        s, s2 = torch.cuda.Stream(), torch.cuda.Stream(priority=-1)
+        s = torch.cuda.Stream()
+        s2, s3 = torch.cuda.Stream(priority=-1), torch.cuda.Stream(priority=-1)
         t_serial = self.run("serial", s)
         self.reset()
-        t_double = self.run("double", s, s2)
+        t_double = self.run("double", s, s2, s3)
         steps = self.rounds * self.N
         # the parts on their own: a swap-in (restore) and a compute + write
         slot = self.slots[0]
         torch.cuda.synchronize()
         t0 = time.perf_counter()
+        fc = torch.cuda.Stream()
+        fetcher = self.dv.Fetcher(self.fslots[0], self.fslots[1], fc, s)
         for m in range(self.N):
-            self.replicas[m].restore_batched(slot, staging=self.staging, stream=s)
+            fc.wait_stream(s)
+            self.replicas[m].restore_fetched(slot, fetcher)
         s.synchronize()
         t_in = (time.perf_counter() - t0) / self.N
+        fetcher.close()
         in_bytes = sum(r.info()[1] for r in self.replicas) / self.N
         t0 = time.perf_counter()
         for m in range(self.N):

@@ -340,6 +340,22 @@ dv_status dv_replica_restore_batched(const dv_replica* replica, const dv_cache* 
                                      int64_t upto_step, void* staging, size_t staging_bytes,
                                      dv_stream stream);
 
+/* The restore of dv_replica_restore_batched with the host-to-device copies
+ * pipelined through a fetcher (see dv_fetcher_create): the log is cut into
+ * pieces of at most the fetcher's slot size (a record long enough for the
+ * tile kernel, or larger than a slot, into groups of whole layers; the other
+ * records into runs that one record-batched launch takes), and each piece is
+ * copied into the fetcher's next free slot on its copy stream and unpacked on
+ * its unpack stream, so the copy of piece i+1 overlaps the unpack of piece
+ * i.  Same result as dv_replica_restore (append order).  The caller orders
+ * the fetcher's streams after earlier work on the cache; an event recorded on
+ * the unpack stream after the call marks the end of the restore.
+ * DV_ERR_BUFFER_TOO_SMALL (before anything is enqueued) when a record that
+ * goes by itself has a layer slab larger than a slot; otherwise the errors of
+ * dv_replica_restore. */
+dv_status dv_replica_restore_fetched(const dv_replica* replica, const dv_cache* cache,
+                                     int64_t upto_step, dv_fetcher* fetcher);
+
 /* Drops every record with step >= step (the acknowledged prefix is kept). */
 dv_status dv_replica_truncate(dv_replica* replica, int64_t step);
 

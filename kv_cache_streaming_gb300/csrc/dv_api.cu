@@ -362,6 +362,100 @@ struct dv_replica {
   std::vector<int32_t> ranges;
 };
 
+namespace {
+
+// The records of a restore, validated against the cache: the non-empty ones
+// in append order, their ranges for the record kernel, and which of them go
+// by themselves (long ranges, for the tile kernel, or larger than a piece).
+struct RestorePlan {
+  std::vector<const Record*> todo;
+  std::vector<dv::RecordRanges> recs;
+  std::vector<char> alone;
+  dv::Plan base;  // the cache: geometry, resolved K / V, layers [0, the last record's l1)
+  size_t total = 0;
+
+  // How many records from i on one record-batched launch takes: consecutive
+  // records not alone, whose writes are disjoint, that fit the parameters
+  // and (piece > 0) piece bytes together.
+  int run_at(int i, size_t piece) const {
+    int run = 0;
+    while (i + run < (int)todo.size() && !alone[i + run]) ++run;
+    int k = dv::records_per_launch(base, recs.data() + i, run);
+    size_t bytes = 0;
+    for (int j = 0; j < k; ++j) {
+      if (piece && bytes + todo[i + j]->bytes > piece) return j;
+      bytes += todo[i + j]->bytes;
+    }
+    return k;
+  }
+};
+
+// Validates every record of `r` with step < upto (all when upto < 0) against
+// `cache` before anything is enqueued.  piece > 0: the bytes one copy can
+// carry; a record larger than that goes by itself in groups of layers, so
+// one of its layer slabs must fit.
+dv_status plan_restore(const dv_replica* r, const dv_cache* cache, int64_t upto, size_t piece,
+                       RestorePlan* rp) {
+  if (!r) return fail(DV_ERR_INVALID_ARG, "replica is NULL");
+  if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
+  if (cache->batch != r->batch)
+    return fail(DV_ERR_INVALID_ARG, "cache batch %d differs from the replica's %d", cache->batch,
+                r->batch);
+  int32_t l_end = 0;
+  try {
+    dv::Plan q;
+    for (const Record& rec : r->records) {
+      if (upto >= 0 && rec.step >= upto) break;
+      const int32_t* s = r->ranges.data() + rec.ranges;
+      const dv_status st = plan_ranges(cache, rec.l0, rec.l1, s, s + r->batch, &q);
+      if (st != DV_OK) return st;
+      if ((size_t)q.bytes != rec.bytes)
+        return fail(DV_ERR_INVALID_ARG, "record of step %lld does not match this cache geometry",
+                    (long long)rec.step);
+      if (rec.bytes == 0) continue;
+      const bool by_itself = dv::auto_kind(q) == dv::kTile || (piece && rec.bytes > piece);
+      if (by_itself && piece && piece < (size_t)dv::layer_slab_bytes(q))
+        return fail(DV_ERR_BUFFER_TOO_SMALL, "a staging piece of %zu bytes holds less than one "
+                    "layer slab (%lld bytes) of the record of step %lld", piece,
+                    (long long)dv::layer_slab_bytes(q), (long long)rec.step);
+      rp->todo.push_back(&rec);
+      rp->recs.push_back(dv::RecordRanges{rec.l0, rec.l1, s, s + r->batch});
+      rp->alone.push_back(by_itself);
+      if (rec.l1 > l_end) l_end = rec.l1;
+      rp->total += rec.bytes;
+    }
+  } catch (...) {
+    return fail(DV_ERR_INVALID_ARG, "out of host memory for the restore plan");
+  }
+  if (rp->todo.empty()) return DV_OK;
+  std::vector<int32_t> zero((size_t)r->batch, 0);
+  dv_status st = plan_ranges(cache, 0, l_end, zero.data(), zero.data(), &rp->base);
+  if (st != DV_OK) return st;
+  return resolve_cache(cache, &rp->base);
+}
+
+// Copies `bytes` from `src` (host memory) into the fetcher's next slot on its
+// copy stream, after that slot's previous unpack, then runs unpack(slot) on
+// its unpack stream after the copy.
+template <typename Unpack>
+cudaError_t fetch_piece(dv_fetcher* h, const void* src, size_t bytes, Unpack&& unpack) {
+  const int i = h->next;
+  cudaError_t err;
+  if (h->used[i] && (err = cudaStreamWaitEvent(h->copy, h->freed[i], 0)) != cudaSuccess)
+    return err;
+  if ((err = cudaMemcpyAsync(h->slot[i], src, bytes, cudaMemcpyDefault, h->copy)) != cudaSuccess)
+    return err;
+  if ((err = cudaEventRecord(h->copied[i], h->copy)) != cudaSuccess) return err;
+  if ((err = cudaStreamWaitEvent(h->unpack, h->copied[i], 0)) != cudaSuccess) return err;
+  if ((err = unpack(h->slot[i])) != cudaSuccess) return err;
+  if ((err = cudaEventRecord(h->freed[i], h->unpack)) != cudaSuccess) return err;
+  h->used[i] = true;
+  h->next = i ^ 1;
+  return cudaSuccess;
+}
+
+}  // namespace
+
 extern "C" {
 
 int32_t dv_abi_version(void) { return DV_ABI_VERSION; }
@@ -667,23 +761,10 @@ dv_status dv_fetch_layer(dv_fetcher* h, const dv_cache* cache, int32_t layer,
       return fail(DV_ERR_INVALID_ARG, "host_src must be pinned host or device memory");
     }
   }
-  const int i = h->next;
-  cudaError_t err;
-  if (h->used[i] && (err = cudaStreamWaitEvent(h->copy, h->freed[i], 0)) != cudaSuccess)
-    return cuda_fail(err, "cudaStreamWaitEvent(slot free)");
-  if ((err = cudaMemcpyAsync(h->slot[i], static_cast<const uint8_t*>(host_src) + off,
-                             (size_t)p.bytes, cudaMemcpyDefault, h->copy)) != cudaSuccess)
-    return cuda_fail(err, "fetch_layer copy");
-  if ((err = cudaEventRecord(h->copied[i], h->copy)) != cudaSuccess)
-    return cuda_fail(err, "cudaEventRecord(copied)");
-  if ((err = cudaStreamWaitEvent(h->unpack, h->copied[i], 0)) != cudaSuccess)
-    return cuda_fail(err, "cudaStreamWaitEvent(copied)");
-  if ((err = dv::launch_unpack(p, h->slot[i], h->unpack, dv::kAuto)) != cudaSuccess)
-    return cuda_fail(err, "fetch_layer unpack launch");
-  if ((err = cudaEventRecord(h->freed[i], h->unpack)) != cudaSuccess)
-    return cuda_fail(err, "cudaEventRecord(freed)");
-  h->used[i] = true;
-  h->next = i ^ 1;
+  const cudaError_t err =
+      fetch_piece(h, static_cast<const uint8_t*>(host_src) + off, (size_t)p.bytes,
+                  [&](void* slot) { return dv::launch_unpack(p, slot, h->unpack, dv::kAuto); });
+  if (err != cudaSuccess) return cuda_fail(err, "fetch_layer");
   return DV_OK;
 }
 
@@ -793,100 +874,92 @@ dv_status dv_replica_restore(const dv_replica* r, const dv_cache* cache, int64_t
 dv_status dv_replica_restore_batched(const dv_replica* r, const dv_cache* cache,
                                     int64_t upto_step, void* staging, size_t staging_bytes,
                                     dv_stream stream) {
-  if (!r) return fail(DV_ERR_INVALID_ARG, "replica is NULL");
-  if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
-  if (cache->batch != r->batch)
-    return fail(DV_ERR_INVALID_ARG, "cache batch %d differs from the replica's %d", cache->batch,
-                r->batch);
-  // Validate every record against this cache before enqueuing anything, and
-  // sort them into long-range records (unpacked one by one with the tile
-  // kernel, as dv_swap_in would) and the rest (batched).
-  std::vector<const Record*> todo;
-  std::vector<dv::RecordRanges> recs;
-  std::vector<char> alone;
-  int32_t l_end = 0;
-  size_t total = 0;
-  try {
-    dv::Plan q;
-    for (const Record& rec : r->records) {
-      if (upto_step >= 0 && rec.step >= upto_step) break;
-      const int32_t* s = r->ranges.data() + rec.ranges;
-      dv_status st = plan_ranges(cache, rec.l0, rec.l1, s, s + r->batch, &q);
-      if (st != DV_OK) return st;
-      if ((size_t)q.bytes != rec.bytes)
-        return fail(DV_ERR_INVALID_ARG, "record of step %lld does not match this cache geometry",
-                    (long long)rec.step);
-      if (rec.bytes == 0) continue;
-      const bool by_itself =
-          dv::auto_kind(q) == dv::kTile || (staging && rec.bytes > staging_bytes);
-      if (by_itself && staging && staging_bytes < (size_t)dv::layer_slab_bytes(q))
-        return fail(DV_ERR_BUFFER_TOO_SMALL, "staging of %zu bytes holds less than one layer "
-                    "slab (%lld bytes) of the record of step %lld", staging_bytes,
-                    (long long)dv::layer_slab_bytes(q), (long long)rec.step);
-      todo.push_back(&rec);
-      recs.push_back(dv::RecordRanges{rec.l0, rec.l1, s, s + r->batch});
-      alone.push_back(by_itself);
-      if (rec.l1 > l_end) l_end = rec.l1;
-      total += rec.bytes;
-    }
-  } catch (...) {
-    return fail(DV_ERR_INVALID_ARG, "out of host memory for the restore plan");
-  }
-  const int n = (int)todo.size();
+  RestorePlan rp;
+  dv_status st = plan_restore(r, cache, upto_step, staging ? staging_bytes : 0, &rp);
+  if (st != DV_OK) return st;
+  const int n = (int)rp.todo.size();
   if (n == 0) return DV_OK;
-  dv::Plan base;
-  {
-    std::vector<int32_t> zero((size_t)r->batch, 0);
-    dv_status st = plan_ranges(cache, 0, l_end, zero.data(), zero.data(), &base);
-    if (st != DV_OK) return st;
-    if ((st = resolve_cache(cache, &base)) != DV_OK) return st;
-  }
   void* arena_dev = nullptr;
   void* stg = nullptr;
   if (!staging) {
-    dv_status st = check_host(r->arena, "replica arena", &arena_dev);
-    if (st != DV_OK) return st;
-    base.host_side = true;
+    if ((st = check_host(r->arena, "replica arena", &arena_dev)) != DV_OK) return st;
+    rp.base.host_side = true;
   } else {
-    const dv_status st =
-        resolve(staging, total < staging_bytes ? total : staging_bytes, false, "staging", &stg);
-    if (st != DV_OK) return st;
+    const size_t need = rp.total < staging_bytes ? rp.total : staging_bytes;
+    if ((st = resolve(staging, need, false, "staging", &stg)) != DV_OK) return st;
   }
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   int i = 0;
   while (i < n) {
-    const Record& first = *todo[i];
-    if (alone[i]) {
+    const Record& first = *rp.todo[i];
+    if (rp.alone[i]) {
       const int32_t* s = r->ranges.data() + first.ranges;
-      const dv_status st = dv_swap_in(cache, first.l0, first.l1, s, s + r->batch,
-                                      r->arena + first.offset, first.bytes, staging,
-                                      staging_bytes, stream);
+      st = dv_swap_in(cache, first.l0, first.l1, s, s + r->batch, r->arena + first.offset,
+                      first.bytes, staging, staging_bytes, stream);
       if (st != DV_OK) return st;
       ++i;
       continue;
     }
-    int run = 0;
-    while (i + run < n && !alone[i + run]) ++run;
-    int k = dv::records_per_launch(base, recs.data() + i, run);
+    const int k = rp.run_at(i, staging ? staging_bytes : 0);
     size_t bytes = 0;
-    for (int j = 0; j < k; ++j) {
-      if (staging && bytes + todo[i + j]->bytes > staging_bytes) {
-        k = j;
-        break;
-      }
-      bytes += todo[i + j]->bytes;
-    }
+    for (int j = 0; j < k; ++j) bytes += rp.todo[i + j]->bytes;
     cudaError_t err;
     if (staging) {
       if ((err = cudaMemcpyAsync(stg, r->arena + first.offset, bytes, cudaMemcpyHostToDevice,
                                  cs)) != cudaSuccess)
         return cuda_fail(err, "restore copy");
-      err = dv::launch_unpack_records(base, recs.data() + i, k, stg, cs);
+      err = dv::launch_unpack_records(rp.base, rp.recs.data() + i, k, stg, cs);
     } else {
-      err = dv::launch_unpack_records(base, recs.data() + i, k,
+      err = dv::launch_unpack_records(rp.base, rp.recs.data() + i, k,
                                       static_cast<uint8_t*>(arena_dev) + first.offset, cs);
     }
     if (err != cudaSuccess) return cuda_fail(err, "batched restore launch");
+    i += k;
+  }
+  return DV_OK;
+}
+
+dv_status dv_replica_restore_fetched(const dv_replica* r, const dv_cache* cache,
+                                    int64_t upto_step, dv_fetcher* h) {
+  if (!h) return fail(DV_ERR_INVALID_ARG, "fetcher is NULL");
+  RestorePlan rp;
+  dv_status st = plan_restore(r, cache, upto_step, h->slot_bytes, &rp);
+  if (st != DV_OK) return st;
+  const int n = (int)rp.todo.size();
+  cudaError_t err = cudaSuccess;
+  int i = 0;
+  while (i < n) {
+    const Record& first = *rp.todo[i];
+    if (rp.alone[i]) {
+      // Whole layers at a time, as many as a slot holds.
+      const int32_t* s = r->ranges.data() + first.ranges;
+      dv::Plan q;
+      if ((st = plan_ranges(cache, first.l0, first.l1, s, s + r->batch, &q)) != DV_OK) return st;
+      q.k = rp.base.k;
+      q.v = rp.base.v;
+      const int64_t slab = dv::layer_slab_bytes(q);
+      const int64_t fit = (int64_t)(h->slot_bytes / (size_t)slab);
+      const int32_t group = (int32_t)(fit < (int64_t)(q.l1 - q.l0) ? fit : (int64_t)(q.l1 - q.l0));
+      for (int32_t la = first.l0; la < first.l1; la += group) {
+        const int32_t lb = la + group < first.l1 ? la + group : first.l1;
+        dv::Plan g = q;
+        dv::restrict_layers(g, la, lb);
+        const uint8_t* src = r->arena + first.offset + (size_t)(la - first.l0) * (size_t)slab;
+        err = fetch_piece(h, src, (size_t)g.bytes, [&](void* slot) {
+          return dv::launch_unpack(g, slot, h->unpack, dv::kAuto);
+        });
+        if (err != cudaSuccess) return cuda_fail(err, "fetched restore (layers)");
+      }
+      ++i;
+      continue;
+    }
+    const int k = rp.run_at(i, h->slot_bytes);
+    size_t bytes = 0;
+    for (int j = 0; j < k; ++j) bytes += rp.todo[i + j]->bytes;
+    err = fetch_piece(h, r->arena + first.offset, bytes, [&](void* slot) {
+      return dv::launch_unpack_records(rp.base, rp.recs.data() + i, k, slot, h->unpack);
+    });
+    if (err != cudaSuccess) return cuda_fail(err, "fetched restore (records)");
     i += k;
   }
   return DV_OK;

@@ -80,6 +80,7 @@ _replica_create = _sig("dv_replica_create", [ctypes.POINTER(_P), _P, _SZ, _I32])
 _replica_append = _sig("dv_replica_append", [_P] + _RANGE + [_I64, _P, _SZ, _P])
 _replica_restore = _sig("dv_replica_restore", [_P, _CP, _I64, _P, _SZ, _P])
 _replica_restore_batched = _sig("dv_replica_restore_batched", [_P, _CP, _I64, _P, _SZ, _P])
+_replica_restore_fetched = _sig("dv_replica_restore_fetched", [_P, _CP, _I64, _P])
 _replica_truncate = _sig("dv_replica_truncate", [_P, _I64])
 _replica_info = _sig("dv_replica_info", [_P, ctypes.POINTER(_I64), ctypes.POINTER(_SZ)])
 _replica_destroy = _sig("dv_replica_destroy", [_P], None)
@@ -377,6 +378,9 @@ class Replica:
         st, sn = _buf(staging)
         _check(_replica_restore_batched(self.h, cache.ref, upto_step, st, sn, _stream(stream)))
 
+    def restore_fetched(self, cache: Cache, fetcher: "Fetcher", upto_step=-1):
+        _check(_replica_restore_fetched(self.h, cache.ref, upto_step, fetcher.h))
+
     def truncate(self, step):
         _check(_replica_truncate(self.h, step))
 
@@ -415,6 +419,11 @@ def dv_replica_restore(replica: Replica, cache: Cache, upto_step=-1, staging=Non
 def dv_replica_restore_batched(replica: Replica, cache: Cache, upto_step=-1, staging=None,
                                stream=None) -> None:
     replica.restore_batched(cache, upto_step, staging, stream)
+
+
+def dv_replica_restore_fetched(replica: Replica, cache: Cache, fetcher: Fetcher,
+                               upto_step=-1) -> None:
+    replica.restore_fetched(cache, fetcher, upto_step)
 
 
 def dv_replica_truncate(replica: Replica, step) -> None:

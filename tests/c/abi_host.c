@@ -56,6 +56,7 @@ int main(void) {
   CHECK(dv_fetcher_create(NULL, NULL, NULL, 0, NULL, NULL) == DV_ERR_INVALID_ARG);
   CHECK(dv_replica_restore(NULL, &c, -1, NULL, 0, NULL) == DV_ERR_INVALID_ARG);
   CHECK(dv_replica_restore_batched(NULL, &c, -1, NULL, 0, NULL) == DV_ERR_INVALID_ARG);
+  CHECK(dv_replica_restore_fetched(NULL, &c, -1, NULL) == DV_ERR_INVALID_ARG);
   CHECK(dv_replica_truncate(NULL, 0) == DV_ERR_INVALID_ARG);
   dv_streamer_destroy(NULL);
   dv_fetcher_destroy(NULL);

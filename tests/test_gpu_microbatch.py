@@ -20,8 +20,8 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("mode", ["serial", "double"])
 def test_microbatch_swapping_restores_the_reference(mode):
     mb = bench.MicrobatchSwapping(torch, dv, rounds=2, keep_refs=True)
-    s, s2 = torch.cuda.Stream(), torch.cuda.Stream()
-    mb.run(mode, s, s2)
+    s, s2, s3 = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    mb.run(mode, s, s2, s3)
     assert all(rep.info()[0] == 1 + 2 for rep in mb.replicas)  # snapshot + 2 deltas
     assert mb.check()
     del mb

@@ -2,7 +2,8 @@
 oracle's in-order restore of the same log: a snapshot and many decode deltas
 in few launches, records with their own layer ranges, records that rewrite
 what earlier records wrote (later wins), empty records, more records than one
-launch takes, batch 1024, fused and staged, upto_step, and the errors."""
+launch takes, batch 1024, fused, staged and pipelined through a fetcher,
+upto_step, and the errors."""
 import numpy as np
 import pytest
 import torch
@@ -56,12 +57,23 @@ class Log:
         self.records.append((l0, l1, s.copy(), e.copy(),
                              ORC.pack(self.g, self.kh, self.vh, l0, l1, s, e)))
 
-    def check(self, staging_bytes=None, upto=-1, batched=True):
+    def check(self, staging_bytes=None, upto=-1, batched=True, slot_bytes=None,
+              one_stream=False):
+        """Restores into a zeroed cache and compares with the oracle: record by
+        record, record-batched (fused, or staged through staging_bytes), or
+        pipelined through a fetcher with slots of slot_bytes."""
         torch.cuda.synchronize()
         g = self.g
         z = H.device_cache(g, fill="zero")
         staging = H.device_bytes(staging_bytes) if staging_bytes else None
-        if batched:
+        if slot_bytes:
+            cs = torch.cuda.Stream()
+            f = dv.Fetcher(H.device_bytes(slot_bytes), H.device_bytes(slot_bytes), cs,
+                           cs if one_stream else torch.cuda.Stream())
+            self.rep.restore_fetched(z, f, upto_step=upto)
+            f.wait()
+            f.close()
+        elif batched:
             self.rep.restore_batched(z, upto_step=upto, staging=staging)
         else:
             self.rep.restore(z, upto_step=upto, staging=staging)
@@ -122,6 +134,8 @@ def test_batched_restore_matches_oracle(g):
     log.check(staging_bytes=log.rep.info()[1])    # staged, everything fits
     log.check(upto=7)                             # snapshot + first deltas only
     log.check(batched=False)                      # the per-record restore agrees
+    log.check(slot_bytes=log.rep.info()[1])       # pipelined through a fetcher
+    log.check(slot_bytes=min_staging(log), upto=9)
 
 
 def test_staging_smaller_than_the_log():
@@ -135,6 +149,8 @@ def test_staging_smaller_than_the_log():
     assert slab < snap
     for stg in (slab, slab + 16, 3 * slab // 2 // 16 * 16, max(snap, slab), 2 * snap):
         log.check(staging_bytes=stg)
+        log.check(slot_bytes=stg)
+    log.check(slot_bytes=slab, one_stream=True)
 
 
 def test_many_records_several_launches():
@@ -153,6 +169,7 @@ def test_many_records_several_launches():
     log.check()
     log.check(staging_bytes=50 * one)
     log.check(staging_bytes=log.rep.info()[1])
+    log.check(slot_bytes=50 * one)
 
 
 def test_batch_1024_two_records_per_launch():
@@ -183,6 +200,7 @@ def test_overlapping_deltas_later_wins():
         log.append(0, 2, pos, pos + 1)
     log.check()
     log.check(staging_bytes=ORC.staging_bytes(g, 0, 2, pos, pos + 1))
+    log.check(slot_bytes=ORC.staging_bytes(g, 0, 2, pos, pos + 1))
 
 
 def test_errors_enqueue_nothing():
@@ -193,6 +211,12 @@ def test_errors_enqueue_nothing():
     with pytest.raises(dv.DvError) as ei:       # a record larger than staging needs a slab
         log.rep.restore_batched(z, staging=H.device_bytes(min_staging(log) - 16))
     assert ei.value.status == dv.DV_ERR_BUFFER_TOO_SMALL
+    small = min_staging(log) - 16                # ... and so does a fetcher's slot
+    f = dv.Fetcher(H.device_bytes(small), H.device_bytes(small))
+    with pytest.raises(dv.DvError) as ei:
+        log.rep.restore_fetched(z, f)
+    assert ei.value.status == dv.DV_ERR_BUFFER_TOO_SMALL
+    f.close()
     other = Geometry("other", 3, 5, 2, 128, 300, 2, "fp16")  # records do not fit this cache
     zo = H.device_cache(other, fill="zero")
     with pytest.raises(dv.DvError) as ei:
