@@ -53,11 +53,12 @@ def parse_args():
     ap.add_argument("--no-swap", action="store_true", help="skip the swap / link section")
     ap.add_argument("--kernel-case", default=None,
                     choices=["tile-pack", "tile-unpack", "delta-pack", "delta-unpack",
-                             "record-restore"],
+                             "flat-pack", "flat-unpack", "record-restore"],
                     help="run one kernel of the step on an 8-layer cache of the workload's "
                          "shape, 5 launches, and exit (a small case for profilers); "
-                         "record-restore: 5 staged batched restores of 96 decode deltas of "
-                         "the whole cache, one record-kernel launch each")
+                         "flat-*: ragged 16..64-token ranges of the OPT-13B-shaped cache, "
+                         "flat kernel; record-restore: 5 staged batched restores of 96 "
+                         "decode deltas of the whole cache, one record-kernel launch each")
     return ap.parse_args()
 
 
@@ -1243,6 +1244,9 @@ def run_kernel_case(case):
     if case == "record-restore":
         run_record_case(torch, dv, synth_gpu)
         return
+    if case.startswith("flat"):
+        run_flat_case(case, torch, dv, synth_gpu)
+        return
     g = replace(GPT2, num_layers=8)
     k = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
     v = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
@@ -1260,6 +1264,32 @@ def run_kernel_case(case):
             dv.dv_kv_unpack(cache, 0, g.num_layers, s, e, stg)
     torch.cuda.synchronize()
     print(f"{case}: 5 launches of {2 * n} algorithmic bytes each")
+
+
+def run_flat_case(case, torch, dv, synth_gpu):
+    """Ragged short ranges, the flat kernel's domain: 16..64 tokens at seeded
+    positions of each of the 8 sequences of the OPT-13B-shaped cache, all 40
+    layers (about 260 MB of staging, more than L2), 5 launches."""
+    from synth.configs import OPT13B
+    g = OPT13B
+    k = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+    v = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+    synth_gpu.fill_cache(g, k, v, seed_of(3))
+    cache = dv.Cache.from_geometry(g, k, v)
+    rng = np.random.default_rng(seed_of(3))
+    s = rng.integers(0, g.max_seq - 64, size=g.batch).astype(np.int32)
+    e = (s + rng.integers(16, 65, size=g.batch)).astype(np.int32)
+    n = dv.dv_staging_bytes(cache, 0, g.num_layers, s, e)
+    stg = torch.empty(n, dtype=torch.uint8, device="cuda")
+    dv.dv_kv_pack(cache, 0, g.num_layers, s, e, stg, variant=dv.DV_VARIANT_FLAT)
+    for _ in range(5):
+        if case.endswith("-pack"):
+            dv.dv_kv_pack(cache, 0, g.num_layers, s, e, stg, variant=dv.DV_VARIANT_FLAT)
+        else:
+            dv.dv_kv_unpack(cache, 0, g.num_layers, s, e, stg, variant=dv.DV_VARIANT_FLAT)
+    torch.cuda.synchronize()
+    print(f"{case}: 5 launches of {2 * n} algorithmic bytes each "
+          f"(ranges of {int((e - s).min())}..{int((e - s).max())} tokens)")
 
 
 def run_record_case(torch, dv, synth_gpu):

@@ -17,6 +17,11 @@ def test_readme_example_runs():
     exec(compile(code, "README.md", "exec"), ns)
     torch.cuda.synchronize()
     k, v, stg, host = ns["k"], ns["v"], ns["stg"], ns["host"]
-    assert torch.equal(host.cuda(), stg)  # the zero-copy swap-out wrote the pack's bytes
+    assert torch.equal(host.cuda(), stg)  # the swap-out and the streamer wrote the pack's bytes
+    back = torch.empty_like(stg)
+    cache = ns["cache"]
+    ns["dv"].dv_kv_pack(cache, 0, ns["L"], ns["s"], ns["e"], back)
+    torch.cuda.synchronize()
+    assert torch.equal(back, stg)  # the fetches and restores put the same bytes back
     del ns
     torch.cuda.empty_cache()
