@@ -113,9 +113,9 @@ typedef enum {
   DV_VARIANT_AUTO = 0, /* equal-length ranges (e.g. one-token decode deltas): the
                           token kernel below 640 16-byte chunks per head and range
                           (80 tokens at head_dim 64, fp16), the tile kernel above;
-                          ragged ranges: the flat kernel below a mean of 384 chunks,
+                          ragged ranges: the flat kernel below a mean of 768 chunks,
                           the tile kernel above */
-  DV_VARIANT_FLAT = 1, /* one 16-byte chunk per thread, staging order */
+  DV_VARIANT_FLAT = 1, /* staging order, each warp a window of 128 chunks */
   DV_VARIANT_TILE = 2, /* token tiles; K transposed through shared memory */
   DV_VARIANT_TOKEN = 3 /* every non-empty range equally long: one chunk per thread */
 } dv_variant;

@@ -10,7 +10,7 @@
 // one V row.  Bytes are copied as bit patterns and never pass through
 // floating point.
 //
-// Three kernels, each with a pack and an unpack form:
+// Four kernels, each with a pack and an unpack form but the last:
 //  * tile_kernel (long ranges): one CTA of 256 threads moves one tile, up to TB
 //    tokens of one (layer, K|V, sequence, head); TB * C = 1024 chunks (16 KiB)
 //    when C is 8 or 16, four in flight per thread.  A V tile is one contiguous
@@ -27,10 +27,14 @@
 //    token found with multiply-high divisions by host constants; no shared
 //    memory, no barrier.  A one-token K record is C isolated 16-byte chunks
 //    (S * 16 bytes apart) by the layout itself.
-//  * flat_kernel (ragged short ranges): thread per staging chunk, in staging
-//    order; the sequence by binary search over the prefix table passed by
-//    value, head and token by a multiply-high division with the sequence's
-//    host constant; no shared memory, no barrier.
+//  * flat_kernel (ragged short ranges): each warp moves windows of 128
+//    consecutive staging chunks; the window head's slab and sequence are
+//    found once (binary search over the prefix table passed by value), and
+//    each lane splits its own offset into head, token and chunk with the
+//    sequence's multiply-high constant (a window that crosses a sequence
+//    looks each chunk up on its own); no shared memory, no barrier.
+//  * record_unpack_kernel (batched restore of log records): the flat
+//    kernel's unpack with one more level, a record table in the parameters.
 // All launches use programmatic dependent launch: a kernel waits for the grids
 // it depends on (griddepcontrol.wait) before touching memory, then lets the
 // next launch in the stream be scheduled.  Nothing waits on anything else
@@ -72,6 +76,10 @@ struct KParams {
 #endif
 #ifndef DV_TILE_MIN_BLOCKS
 #define DV_TILE_MIN_BLOCKS 5  // resident CTAs per SM the tile kernel is compiled for
+#endif
+#ifndef DV_FLAT_MIN_BLOCKS
+#define DV_FLAT_MIN_BLOCKS 4  // resident CTAs per SM the flat kernel is compiled for
+                              // (5 spills: 20-40% slower on 16..64-token unpacks)
 #endif
 #ifndef DV_LOOKUP_HOST_SCALE
 #define DV_LOOKUP_HOST_SCALE 2  // flat / record kernels on host memory: CTAs per tile-kernel CTA
@@ -165,94 +173,142 @@ __device__ __forceinline__ uint64_t div64_by(uint64_t n, uint64_t d, uint64_t m)
   return q;
 }
 
-// Addresses of the cache chunks of staging chunks base + u * kThreads
-// (u < kFlatUnroll); nullptr where there is none.  Reads only the kernel
+constexpr int kWin = 32 * kFlatUnroll;  // chunks of one warp's window
+
+// Address of the cache chunk of staging chunk g < total: the (layer, K|V)
+// slab, the sequence (the last one whose run starts at or before the chunk's
+// token-head; a non-empty one, as in find_seq), head, token and chunk, each
+// from the kernel parameters alone.
+template <int MAXB, int LOG2C>
+__device__ __forceinline__ uint4* flat_addr(const KParams<MAXB>& p, int64_t g) {
+  const int32_t C = LOG2C >= 0 ? (1 << LOG2C) : p.C;
+  const int64_t lkv = (int64_t)div64_by((uint64_t)g, (uint64_t)p.lkv_chunks, p.m_lkv);
+  const int32_t r = (int32_t)(g - lkv * p.lkv_chunks);
+  const int32_t rec = LOG2C >= 0 ? (r >> LOG2C) : r / C;
+  const int32_t c = r - rec * C;
+  int b = 0;
+#pragma unroll
+  for (int half = MAXB / 2; half > 0; half >>= 1)
+    if (b + half < p.B && p.H * p.tok_pre[b + half] <= rec) b += half;
+  const int32_t rr = rec - p.H * p.tok_pre[b];
+  const int32_t len = p.seq_len[b];
+  const int32_t h = p.m_len[b] ? (int32_t)div_by((uint32_t)rr, (uint32_t)len, p.m_len[b]) : rr;
+  const int64_t t = p.seq_start[b] + (rr - h * len);
+  const int64_t l = p.l0 + (lkv >> 1);
+  const int64_t bh = (int64_t)b * p.H + h;
+  uint4* ptr = (lkv & 1) == 0 ? p.k + l * p.layer_chunks + ((bh * C + c) * p.S + t)
+                              : p.v + l * p.layer_chunks + ((bh * p.S + t) * C + c);
+  return ((lkv & 1) == 0 ? DV_OK_K(ptr, 1) : DV_OK_V(ptr, 2)) ? ptr : nullptr;
+}
+
+// Addresses of the chunks w0 + u * 32 + lane (u < kFlatUnroll) of one warp's
+// window of kWin consecutive staging chunks; nullptr where there is none.
+// The window head's (layer, K|V) slab and sequence are looked up once for
+// the warp; when the whole window lies inside that sequence's block of the
+// slab, each lane only splits its own offset into head, token and chunk.
+// Otherwise each chunk is looked up on its own.  Reads only the kernel
 // parameters, so it may run before griddepcontrol.wait.
 template <int MAXB, int LOG2C>
-__device__ __forceinline__ void flat_lookup(const KParams<MAXB>& p, int64_t base,
+__device__ __forceinline__ void flat_window(const KParams<MAXB>& p, int64_t w0, int lane,
                                             uint4* (&cptr)[kFlatUnroll]) {
   const int32_t C = LOG2C >= 0 ? (1 << LOG2C) : p.C;
 #pragma unroll
-  for (int u = 0; u < kFlatUnroll; ++u) {
-    const int64_t g = base + u * kThreads;
-    cptr[u] = nullptr;
-    if (g >= p.total || !DV_OK_S(p.stg + g, 3)) continue;
-    const int64_t lkv = (int64_t)div64_by((uint64_t)g, (uint64_t)p.lkv_chunks, p.m_lkv);
-    const int32_t r = (int32_t)(g - lkv * p.lkv_chunks);
-    const int32_t rec = LOG2C >= 0 ? (r >> LOG2C) : r / C;
-    const int32_t c = r - rec * C;
-    // The last sequence whose run starts at or before this token-head (a
-    // non-empty one, as in find_seq): a fixed-depth search without branches,
-    // so that the four chunks' lookups overlap.
-    int b = 0;
+  for (int u = 0; u < kFlatUnroll; ++u) cptr[u] = nullptr;
+  if (w0 >= p.total) return;
+  const int64_t lkv = (int64_t)div64_by((uint64_t)w0, (uint64_t)p.lkv_chunks, p.m_lkv);
+  const int32_t r0 = (int32_t)(w0 - lkv * p.lkv_chunks);
+  const int32_t rec0 = LOG2C >= 0 ? (r0 >> LOG2C) : r0 / C;
+  int b = 0;
 #pragma unroll
-    for (int half = MAXB / 2; half > 0; half >>= 1)
-      if (b + half < p.B && p.H * p.tok_pre[b + half] <= rec) b += half;
-    const int32_t rr = rec - p.H * p.tok_pre[b];
+  for (int half = MAXB / 2; half > 0; half >>= 1)
+    if (b + half < p.B && p.H * p.tok_pre[b + half] <= rec0) b += half;
+  const int32_t lo = p.H * p.tok_pre[b] * C;      // sequence b's block in the slab
+  const int32_t hi = p.H * p.tok_pre[b + 1] * C;
+  if (r0 + kWin <= hi) {
     const int32_t len = p.seq_len[b];
-    const int32_t h = p.m_len[b] ? (int32_t)div_by((uint32_t)rr, (uint32_t)len, p.m_len[b])
-                                 : rr;
-    const int64_t t = p.seq_start[b] + (rr - h * len);
-    const int64_t l = p.l0 + (lkv >> 1);
-    const int64_t bh = (int64_t)b * p.H + h;
-    uint4* ptr = (lkv & 1) == 0 ? p.k + l * p.layer_chunks + ((bh * C + c) * p.S + t)
-                                : p.v + l * p.layer_chunks + ((bh * p.S + t) * C + c);
-    if ((lkv & 1) == 0 ? DV_OK_K(ptr, 1) : DV_OK_V(ptr, 2)) cptr[u] = ptr;
+    const uint32_t m = p.m_len[b];
+    const bool is_k = (lkv & 1) == 0;
+    uint4* const slab = (is_k ? p.k : p.v) + (p.l0 + (lkv >> 1)) * p.layer_chunks;
+    const int64_t bh0 = (int64_t)b * p.H;
+    const int64_t s0 = p.seq_start[b];
+#pragma unroll
+    for (int u = 0; u < kFlatUnroll; ++u) {
+      const int64_t g = w0 + u * 32 + lane;
+      if (g >= p.total || !DV_OK_S(p.stg + g, 3)) continue;
+      const int32_t q = r0 - lo + u * 32 + lane;  // chunk in the sequence's block
+      const int32_t tokc = LOG2C >= 0 ? (q >> LOG2C) : q / C;
+      const int32_t c = q - tokc * C;
+      const int32_t h = m ? (int32_t)div_by((uint32_t)tokc, (uint32_t)len, m) : tokc;
+      const int64_t t = s0 + (tokc - h * len);
+      const int64_t bh = bh0 + h;
+      uint4* ptr = is_k ? slab + ((bh * C + c) * p.S + t) : slab + ((bh * p.S + t) * C + c);
+      if (is_k ? DV_OK_K(ptr, 1) : DV_OK_V(ptr, 2)) cptr[u] = ptr;
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < kFlatUnroll; ++u) {
+      const int64_t g = w0 + u * 32 + lane;
+      if (g < p.total && DV_OK_S(p.stg + g, 3)) cptr[u] = flat_addr<MAXB, LOG2C>(p, g);
+    }
   }
 }
 
-// One unpack round whose staging loads are issued before its addresses are
-// known: `cptr` is looked up (when `lookup`) while the loads are in flight.
-template <int MAXB, int LOG2C, typename Params, typename Lookup>
-__device__ __forceinline__ void unpack_round(const Params& p, int64_t base,
+// One unpack round whose staging loads (chunks g0 + u * USTRIDE) are issued
+// before their addresses are known: `cptr` is looked up (when `lookup`, by
+// find(key, cptr)) while the loads are in flight.
+template <int USTRIDE, typename Params, typename Lookup>
+__device__ __forceinline__ void unpack_round(const Params& p, int64_t g0, int64_t key,
                                              uint4* (&cptr)[kFlatUnroll], bool lookup,
                                              Lookup&& find) {
   uint4 val[kFlatUnroll];
 #pragma unroll
   for (int u = 0; u < kFlatUnroll; ++u) {
-    const int64_t g = base + u * kThreads;
+    const int64_t g = g0 + u * USTRIDE;
     if (g < p.total && DV_OK_S(p.stg + g, 3)) val[u] = ld_stream(p.stg + g);
   }
-  if (lookup) find(base, cptr);
+  if (lookup) find(key, cptr);
 #pragma unroll
   for (int u = 0; u < kFlatUnroll; ++u)
     if (cptr[u]) *cptr[u] = val[u];
 }
 
-// Each thread moves kFlatUnroll chunks per round, kThreads apart.  The first
-// round's addresses are looked up before the wait for the preceding grid.
-// Pack: each later round's addresses are looked up while the previous
-// round's loads are in flight.  Unpack reads staging in order: each round's
-// staging loads go first, and its lookups run while they are in flight.
+// Each warp moves a window of kWin consecutive staging chunks per round (its
+// lanes kFlatUnroll chunks each, 32 apart, so every warp instruction covers
+// 512 contiguous staging bytes).  The first round's addresses are looked up
+// before the wait for the preceding grid.  Pack: each later round's
+// addresses are looked up while the previous round's loads are in flight.
+// Unpack reads staging in order: each round's staging loads go first, and
+// its lookups run while they are in flight.
 template <bool PACK, int MAXB, int LOG2C>
-__global__ void __launch_bounds__(kThreads, 5)
+__global__ void __launch_bounds__(kThreads, DV_FLAT_MIN_BLOCKS)
 flat_kernel(const __grid_constant__ KParams<MAXB> p) {
+  const int lane = threadIdx.x & 31;
   const int64_t step = (int64_t)gridDim.x * (kThreads * kFlatUnroll);
-  int64_t base = (int64_t)blockIdx.x * (kThreads * kFlatUnroll) + threadIdx.x;
+  int64_t w0 = ((int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * kWin;
   uint4* cptr[kFlatUnroll];
-  flat_lookup<MAXB, LOG2C>(p, base, cptr);
+  flat_window<MAXB, LOG2C>(p, w0, lane, cptr);
   pdl_enter();
   if (PACK) {
-    for (; base < p.total; base += step) {
+    for (; w0 < p.total; w0 += step) {
       uint4 val[kFlatUnroll];
 #pragma unroll
       for (int u = 0; u < kFlatUnroll; ++u)
         if (cptr[u]) val[u] = ld_stream(cptr[u]);
       uint4* next[kFlatUnroll];
-      flat_lookup<MAXB, LOG2C>(p, base + step, next);
+      flat_window<MAXB, LOG2C>(p, w0 + step, lane, next);
 #pragma unroll
       for (int u = 0; u < kFlatUnroll; ++u) {
-        if (cptr[u]) p.stg[base + u * kThreads] = val[u];
+        if (cptr[u]) p.stg[w0 + u * 32 + lane] = val[u];
         cptr[u] = next[u];
       }
     }
   } else {
-    const auto find = [&p](int64_t b, uint4* (&c)[kFlatUnroll]) {
-      flat_lookup<MAXB, LOG2C>(p, b, c);
+    const auto find = [&p, lane](int64_t w, uint4* (&c)[kFlatUnroll]) {
+      flat_window<MAXB, LOG2C>(p, w, lane, c);
     };
-    if (base < p.total) unpack_round<MAXB, LOG2C>(p, base, cptr, false, find);
-    for (base += step; base < p.total; base += step)
-      unpack_round<MAXB, LOG2C>(p, base, cptr, true, find);
+    if (w0 < p.total) unpack_round<32>(p, w0 + lane, w0, cptr, false, find);
+    for (w0 += step; w0 < p.total; w0 += step)
+      unpack_round<32>(p, w0 + lane, w0, cptr, true, find);
   }
 }
 
@@ -403,9 +459,9 @@ record_unpack_kernel(const __grid_constant__ RecParams p) {
   record_lookup<LOG2C>(p, base, cptr);
   pdl_enter();
   const auto find = [&p](int64_t b, uint4* (&c)[kFlatUnroll]) { record_lookup<LOG2C>(p, b, c); };
-  if (base < p.total) unpack_round<0, LOG2C>(p, base, cptr, false, find);
+  if (base < p.total) unpack_round<kThreads>(p, base, base, cptr, false, find);
   for (base += step; base < p.total; base += step)
-    unpack_round<0, LOG2C>(p, base, cptr, true, find);
+    unpack_round<kThreads>(p, base, base, cptr, true, find);
 }
 
 // Contiguous run of `cnt` chunks between the V cache and staging.
@@ -848,7 +904,7 @@ int auto_kind(const Plan& p) {
   // Equal-length ranges: the token kernel up to about 640 chunks per run
   // (measured on GB300: between 64 and 96 tokens at head_dim 64, between 32
   // and 48 at 128 in fp16), the tile kernel beyond.  Ragged ranges: the flat
-  // kernel below the tile kernel's crossover.
+  // kernel below the tile kernel's crossover (auto_uses_tile).
   if (token_supported(p))
     return tile_supported(p) && (int64_t)p.max_len * p.C >= 640 ? kTile : kToken;
   return auto_uses_tile(p) ? kTile : kFlat;
@@ -856,11 +912,11 @@ int auto_kind(const Plan& p) {
 
 bool auto_uses_tile(const Plan& p) {
   if (!tile_supported(p) || p.active == 0) return false;
-  // Tiles pay once a (layer, K|V, sequence, head) run holds about 384 chunks
-  // (6 KiB) on average: measured on GB300, the flat kernel wins below (e.g.
-  // 40 tokens for head_dim 64, 24 for head_dim 128 in fp16), the tile kernel
-  // above.
-  return p.tokens * p.C >= (int64_t)384 * p.active;
+  // Tiles pay once a (layer, K|V, sequence, head) run holds about 768 chunks
+  // (12 KiB) on average: measured on GB300 with ragged ranges, the flat
+  // kernel wins at 636 chunks per run for head_dim 64 and at 458 for 128 in
+  // fp16, the tile kernel at 1155 and at 1024.
+  return p.tokens * p.C >= (int64_t)768 * p.active;
 }
 
 bool checked_build() { return DV_CHECKED != 0; }
