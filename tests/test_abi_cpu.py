@@ -120,3 +120,39 @@ def test_binding_refuses_ranges_of_the_wrong_length():
     ro = np.zeros(4, np.int32)
     ro.setflags(write=False)  # read-only arrays are accepted (copied)
     assert dv.dv_staging_bytes(c, 0, 2, ro, ro + 3) == 2 * 2 * 2 * 64 * 2 * 12
+
+
+def test_last_error_is_per_thread():
+    """Threads that fail validation at the same time each read their own
+    message (the library's only mutable global state is that thread-local
+    string)."""
+    import threading
+    g = Geometry("thr", 2, 2, 2, 64, 32, 2, "fp16")
+    c = _cache(g)
+    ok = np.zeros(2, np.int32), np.full(2, 32, np.int32)
+    barrier = threading.Barrier(8)
+    seen = {}
+
+    def worker(i):
+        barrier.wait()
+        for _ in range(200):
+            if i % 2:  # a layer range past the cache
+                with pytest.raises(dv.DvError) as ei:
+                    dv.dv_staging_bytes(c, 0, 3 + i, *ok)
+                want = f"layer range [0,{3 + i})"
+            else:       # a token range past max_seq
+                e = np.array([32, 40 + i], np.int32)
+                with pytest.raises(dv.DvError) as ei:
+                    dv.dv_staging_bytes(c, 0, 2, ok[0], e)
+                want = f"[0,{40 + i})"
+            if want not in str(ei.value):
+                seen[i] = str(ei.value)
+                return
+        seen[i] = None
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(8)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert all(v is None for v in seen.values()) and len(seen) == 8, seen

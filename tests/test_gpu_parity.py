@@ -417,3 +417,48 @@ def test_replica_compaction():
     vw = np.where(np.repeat(mv, 2), vh, 0).astype(np.uint8)
     assert np.array_equal(H.to_np(after.k), kw) and np.array_equal(H.to_np(after.v), vw)
     rep.close()
+
+
+def test_concurrent_calls_from_threads():
+    """Eight host threads, each on its own stream, pack different ranges of
+    one cache and unpack them into caches of their own at the same time (the
+    library holds no per-call global state): every result equals the
+    oracle's."""
+    import threading
+    g = Geometry("thr", 3, 4, 4, 128, 256, 2, "fp16")
+    kh, vh = H.host_cache(g, 77)
+    cache = H.device_cache(g, fill=(kh, vh))
+    rng = np.random.default_rng(77)
+    jobs = [P.random_ranges(g, rng) for _ in range(8)]
+    outs = [H.device_bytes(ORC.staging_bytes(g, 0, g.num_layers, s, e)) for s, e in jobs]
+    backs = [H.device_cache(g, fill=0x5A) for _ in jobs]
+    torch.cuda.synchronize()
+    barrier = threading.Barrier(len(jobs))
+    errors = []
+
+    def worker(i):
+        try:
+            s, e = jobs[i]
+            st = torch.cuda.Stream()
+            barrier.wait()
+            for _ in range(20):
+                dv.dv_kv_pack(cache, 0, g.num_layers, s, e, outs[i], stream=st)
+                dv.dv_kv_unpack(backs[i], 0, g.num_layers, s, e, outs[i], stream=st)
+            st.synchronize()
+        except Exception as ex:  # reported below, from the main thread
+            errors.append(repr(ex))
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(jobs))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for (s, e), out, back in zip(jobs, outs, backs):
+        n = ORC.staging_bytes(g, 0, g.num_layers, s, e)
+        want = ORC.pack(g, kh, vh, 0, g.num_layers, s, e)
+        assert np.array_equal(H.to_np(out)[:n], want)
+        kw = np.full(g.tensor_bytes, 0x5A, np.uint8)
+        vw = np.full(g.tensor_bytes, 0x5A, np.uint8)
+        ORC.unpack(g, kw, vw, 0, g.num_layers, s, e, want)
+        assert np.array_equal(H.to_np(back.k), kw) and np.array_equal(H.to_np(back.v), vw)
