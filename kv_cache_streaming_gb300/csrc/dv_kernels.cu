@@ -399,46 +399,96 @@ struct RecParams {
 };
 static_assert(sizeof(RecParams) <= 32764, "kernel parameters are limited to 32764 bytes");
 
-// Cache addresses of launch chunks base + u * kThreads (nullptr where there is
-// none); parameters only, so it may run before griddepcontrol.wait.
+// Address of the cache chunk of launch chunk g < total: the record (the last
+// one starting at or before g), its (layer, K|V) slab, the sequence (the last
+// one of the record whose run starts at or before the chunk's token-head; a
+// non-empty one, as in find_seq), head, token and chunk, from the kernel
+// parameters alone.  The searches are fixed-depth and free of branches.
 template <int LOG2C>
-__device__ __forceinline__ void record_lookup(const RecParams& p, int64_t base,
+__device__ __forceinline__ uint4* record_addr(const RecParams& p, int64_t g) {
+  const int32_t C = LOG2C >= 0 ? (1 << LOG2C) : p.C;
+  int r = 0;
+#pragma unroll
+  for (int half = kRecMax / 2; half > 0; half >>= 1)
+    if (r + half < p.nrec && p.rec_pre[r + half] <= g) r += half;
+  const int64_t q = g - p.rec_pre[r];
+  const int64_t lkv = (int64_t)div64_by((uint64_t)q, (uint64_t)p.rec_lkv[r], p.rec_m[r]);
+  const int32_t w = (int32_t)(q - lkv * p.rec_lkv[r]);
+  const int32_t rec = LOG2C >= 0 ? (w >> LOG2C) : w / C;
+  const int32_t c = w - rec * C;
+  const int32_t tab = p.rec_tab[r];
+  const int32_t pre = tab + p.B;  // tok_pre of the record
+  int b = 0;
+#pragma unroll
+  for (int half = kMaxBatch / 2; half > 0; half >>= 1)
+    if (b + half < p.B && p.H * p.words[pre + b + half] <= rec) b += half;
+  const int32_t rr = rec - p.H * p.words[pre + b];
+  const int32_t len = p.words[pre + b + 1] - p.words[pre + b];
+  const uint32_t m = (uint32_t)p.words[pre + p.B + 1 + b];
+  const int32_t h = m ? (int32_t)div_by((uint32_t)rr, (uint32_t)len, m) : rr;
+  const int64_t t = p.words[tab + b] + (rr - h * len);
+  const int64_t l = p.rec_l0[r] + (lkv >> 1);
+  const int64_t bh = (int64_t)b * p.H + h;
+  uint4* ptr = (lkv & 1) == 0 ? p.k + l * p.layer_chunks + ((bh * C + c) * p.S + t)
+                              : p.v + l * p.layer_chunks + ((bh * p.S + t) * C + c);
+  return ((lkv & 1) == 0 ? DV_OK_K(ptr, 31) : DV_OK_V(ptr, 32)) ? ptr : nullptr;
+}
+
+// Addresses of the chunks w0 + u * 32 + lane (u < kFlatUnroll) of one warp's
+// window of the launch, as flat_window finds them, with the record looked up
+// first: once for the window head, and when the whole window lies inside
+// one sequence's block of one slab of that record, each lane only splits its
+// own offset; otherwise each chunk is looked up on its own.  Parameters
+// only, so it may run before griddepcontrol.wait.
+template <int LOG2C>
+__device__ __forceinline__ void record_window(const RecParams& p, int64_t w0, int lane,
                                               uint4* (&cptr)[kFlatUnroll]) {
   const int32_t C = LOG2C >= 0 ? (1 << LOG2C) : p.C;
 #pragma unroll
-  for (int u = 0; u < kFlatUnroll; ++u) {
-    const int64_t g = base + u * kThreads;
-    cptr[u] = nullptr;
-    if (g >= p.total || !DV_OK_S(p.stg + g, 33)) continue;
-    // Fixed-depth searches without branches, so that the four chunks'
-    // lookups overlap: the last record starting at or before g ...
-    int r = 0;
+  for (int u = 0; u < kFlatUnroll; ++u) cptr[u] = nullptr;
+  if (w0 >= p.total) return;
+  int r = 0;
 #pragma unroll
-    for (int half = kRecMax / 2; half > 0; half >>= 1)
-      if (r + half < p.nrec && p.rec_pre[r + half] <= g) r += half;
-    const int64_t q = g - p.rec_pre[r];
-    const int64_t lkv = (int64_t)div64_by((uint64_t)q, (uint64_t)p.rec_lkv[r], p.rec_m[r]);
-    const int32_t w = (int32_t)(q - lkv * p.rec_lkv[r]);
-    const int32_t rec = LOG2C >= 0 ? (w >> LOG2C) : w / C;
-    const int32_t c = w - rec * C;
-    const int32_t tab = p.rec_tab[r];
-    const int32_t pre = tab + p.B;           // tok_pre of the record
-    // ... and the last sequence of that record whose run starts at or
-    // before the chunk's token-head (a non-empty one, as in find_seq).
-    int b = 0;
+  for (int half = kRecMax / 2; half > 0; half >>= 1)
+    if (r + half < p.nrec && p.rec_pre[r + half] <= w0) r += half;
+  const int64_t q0 = w0 - p.rec_pre[r];
+  const int64_t lkv = (int64_t)div64_by((uint64_t)q0, (uint64_t)p.rec_lkv[r], p.rec_m[r]);
+  const int32_t r0 = (int32_t)(q0 - lkv * p.rec_lkv[r]);
+  const int32_t rec0 = LOG2C >= 0 ? (r0 >> LOG2C) : r0 / C;
+  const int32_t tab = p.rec_tab[r];
+  const int32_t pre = tab + p.B;
+  int b = 0;
 #pragma unroll
-    for (int half = kMaxBatch / 2; half > 0; half >>= 1)
-      if (b + half < p.B && p.H * p.words[pre + b + half] <= rec) b += half;
-    const int32_t rr = rec - p.H * p.words[pre + b];
+  for (int half = kMaxBatch / 2; half > 0; half >>= 1)
+    if (b + half < p.B && p.H * p.words[pre + b + half] <= rec0) b += half;
+  const int32_t lo = p.H * p.words[pre + b] * C;  // sequence b's block in the slab
+  const int32_t hi = p.H * p.words[pre + b + 1] * C;
+  if (r0 + kWin <= hi) {
     const int32_t len = p.words[pre + b + 1] - p.words[pre + b];
     const uint32_t m = (uint32_t)p.words[pre + p.B + 1 + b];
-    const int32_t h = m ? (int32_t)div_by((uint32_t)rr, (uint32_t)len, m) : rr;
-    const int64_t t = p.words[tab + b] + (rr - h * len);
-    const int64_t l = p.rec_l0[r] + (lkv >> 1);
-    const int64_t bh = (int64_t)b * p.H + h;
-    uint4* ptr = (lkv & 1) == 0 ? p.k + l * p.layer_chunks + ((bh * C + c) * p.S + t)
-                                : p.v + l * p.layer_chunks + ((bh * p.S + t) * C + c);
-    if ((lkv & 1) == 0 ? DV_OK_K(ptr, 31) : DV_OK_V(ptr, 32)) cptr[u] = ptr;
+    const bool is_k = (lkv & 1) == 0;
+    uint4* const slab = (is_k ? p.k : p.v) + (p.rec_l0[r] + (lkv >> 1)) * p.layer_chunks;
+    const int64_t bh0 = (int64_t)b * p.H;
+    const int64_t s0 = p.words[tab + b];
+#pragma unroll
+    for (int u = 0; u < kFlatUnroll; ++u) {
+      const int64_t g = w0 + u * 32 + lane;
+      if (g >= p.total || !DV_OK_S(p.stg + g, 33)) continue;
+      const int32_t q = r0 - lo + u * 32 + lane;  // chunk in the sequence's block
+      const int32_t tokc = LOG2C >= 0 ? (q >> LOG2C) : q / C;
+      const int32_t c = q - tokc * C;
+      const int32_t h = m ? (int32_t)div_by((uint32_t)tokc, (uint32_t)len, m) : tokc;
+      const int64_t t = s0 + (tokc - h * len);
+      const int64_t bh = bh0 + h;
+      uint4* ptr = is_k ? slab + ((bh * C + c) * p.S + t) : slab + ((bh * p.S + t) * C + c);
+      if (is_k ? DV_OK_K(ptr, 31) : DV_OK_V(ptr, 32)) cptr[u] = ptr;
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < kFlatUnroll; ++u) {
+      const int64_t g = w0 + u * 32 + lane;
+      if (g < p.total && DV_OK_S(p.stg + g, 33)) cptr[u] = record_addr<LOG2C>(p, g);
+    }
   }
 }
 
@@ -448,20 +498,24 @@ __device__ __forceinline__ void record_lookup(const RecParams& p, int64_t base,
 // chunk (staging order [layer][K|V][sequence][head][token][chunk]).  Records
 // of one launch write disjoint parts of the cache (the host splits launches
 // where they would not), so their order inside a launch does not matter.
-// The source is read in order (often from host memory, a long round trip):
-// each round's loads go first and its lookups run while they are in flight.
+// Each warp moves windows of kWin consecutive chunks, as the flat kernel
+// does.  The source is read in order (often from host memory, a long round
+// trip): each round's loads go first and its lookups run while they are in
+// flight.
 template <int LOG2C>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, DV_FLAT_MIN_BLOCKS)
 record_unpack_kernel(const __grid_constant__ RecParams p) {
+  const int lane = threadIdx.x & 31;
   const int64_t step = (int64_t)gridDim.x * (kThreads * kFlatUnroll);
-  int64_t base = (int64_t)blockIdx.x * (kThreads * kFlatUnroll) + threadIdx.x;
+  int64_t w0 = ((int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * kWin;
   uint4* cptr[kFlatUnroll];
-  record_lookup<LOG2C>(p, base, cptr);
+  record_window<LOG2C>(p, w0, lane, cptr);
   pdl_enter();
-  const auto find = [&p](int64_t b, uint4* (&c)[kFlatUnroll]) { record_lookup<LOG2C>(p, b, c); };
-  if (base < p.total) unpack_round<kThreads>(p, base, base, cptr, false, find);
-  for (base += step; base < p.total; base += step)
-    unpack_round<kThreads>(p, base, base, cptr, true, find);
+  const auto find = [&p, lane](int64_t w, uint4* (&c)[kFlatUnroll]) {
+    record_window<LOG2C>(p, w, lane, c);
+  };
+  if (w0 < p.total) unpack_round<32>(p, w0 + lane, w0, cptr, false, find);
+  for (w0 += step; w0 < p.total; w0 += step) unpack_round<32>(p, w0 + lane, w0, cptr, true, find);
 }
 
 // Contiguous run of `cnt` chunks between the V cache and staging.
