@@ -4,7 +4,10 @@
  * and checks (1) both packs agree, (2) every byte of the selected slices came
  * back and every other byte stayed zero, (3) the first staging record is the
  * K row of token s_0 of (layer 0, sequence 0, head 0) read through the layout.
- * Exit status 0 when every check holds. */
+ * Then the same bytes go out layer by layer through a streamer and come back
+ * through a fetcher, and a replica (snapshot + one decode token) is restored
+ * record-batched and pipelined through the fetcher.  Exit status 0 when every
+ * check holds. */
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -83,6 +86,91 @@ int main(void) {
             const int sel = t >= s[b] && t < e[b];
             if (bk[ki] != (sel ? hk[ki] : 0) || bv[vi] != (sel ? hv[vi] : 0)) ++failures;
           }
+
+  /* Layer by layer from C: the streamer copies each layer's slab out to pinned
+   * host memory, the fetcher copies it back into another zeroed cache; the
+   * bytes out equal one pack, the cache back equals the unpack above. */
+  void *slot[4], *yk, *yv;
+  const size_t slab = bytes / L;
+  for (int i = 0; i < 4; ++i) CHECK(cudaMalloc(&slot[i], slab) == cudaSuccess);
+  CHECK(cudaMalloc(&yk, n * P) == cudaSuccess && cudaMalloc(&yv, n * P) == cudaSuccess);
+  cudaMemset(yk, 0, n * P);
+  cudaMemset(yv, 0, n * P);
+  uint8_t* out = NULL;
+  CHECK(cudaHostAlloc((void**)&out, bytes, cudaHostAllocDefault) == cudaSuccess);
+  cudaStream_t ps, cs, fc, fu;
+  cudaStreamCreate(&ps);
+  cudaStreamCreate(&cs);
+  cudaStreamCreate(&fc);
+  cudaStreamCreate(&fu);
+  cudaEvent_t out_done;
+  cudaEventCreateWithFlags(&out_done, cudaEventDisableTiming);
+  dv_streamer* st = NULL;
+  dv_fetcher* ft = NULL;
+  CHECK(dv_streamer_create(&st, slot[0], slot[1], slab, ps, cs) == DV_OK);
+  CHECK(dv_fetcher_create(&ft, slot[2], slot[3], slab, fc, fu) == DV_OK);
+  dv_cache y = c;
+  y.k_base = yk;
+  y.v_base = yv;
+  CHECK(cudaDeviceSynchronize() == cudaSuccess);
+  for (int l = 0; l < L; ++l) {
+    CHECK(dv_stream_layer(st, &c, l, s, e, out, bytes, 0) == DV_OK);
+    cudaEventRecord(out_done, cs);         /* layer l is in host memory ... */
+    cudaStreamWaitEvent(fc, out_done, 0);  /* ... before it is fetched */
+    CHECK(dv_fetch_layer(ft, &y, l, s, e, out, bytes, 0) == DV_OK);
+  }
+  CHECK(dv_streamer_wait(st) == DV_OK && dv_fetcher_wait(ft) == DV_OK);
+  CHECK(memcmp(out, host, bytes) == 0);
+  uint16_t* yk_h = (uint16_t*)malloc(n * P);
+  uint16_t* yv_h = (uint16_t*)malloc(n * P);
+  cudaMemcpy(yk_h, yk, n * P, cudaMemcpyDeviceToHost);
+  cudaMemcpy(yv_h, yv, n * P, cudaMemcpyDeviceToHost);
+  CHECK(memcmp(yk_h, bk, n * P) == 0 && memcmp(yv_h, bv, n * P) == 0);
+
+  /* A replica of the ranges (snapshot) and one decode token after each range
+   * (where it fits), restored record-batched and pipelined through the
+   * fetcher into zeroed caches: both give the selected slices of [s, e + 1). */
+  int32_t e1[B];
+  for (int b = 0; b < B; ++b) e1[b] = e[b] < S ? e[b] + 1 : e[b];
+  size_t delta = 0;
+  CHECK(dv_staging_bytes(&c, 0, L, e, e1, &delta) == DV_OK);
+  uint8_t* arena = NULL;
+  CHECK(cudaHostAlloc((void**)&arena, bytes + delta, cudaHostAllocMapped) == cudaSuccess);
+  dv_replica* rep = NULL;
+  CHECK(dv_replica_create(&rep, arena, bytes + delta, B) == DV_OK);
+  CHECK(dv_replica_append(rep, &c, 0, L, s, e, 0, NULL, 0, NULL) == DV_OK);
+  CHECK(dv_replica_append(rep, &c, 0, L, e, e1, 1, NULL, 0, NULL) == DV_OK);
+  for (int mode = 0; mode < 2; ++mode) {
+    cudaMemset(yk, 0, n * P);
+    cudaMemset(yv, 0, n * P);
+    CHECK(cudaDeviceSynchronize() == cudaSuccess);
+    if (mode == 0) {
+      CHECK(dv_replica_restore_batched(rep, &y, -1, NULL, 0, NULL) == DV_OK);
+    } else {
+      CHECK(dv_replica_restore_fetched(rep, &y, -1, ft) == DV_OK);
+      CHECK(dv_fetcher_wait(ft) == DV_OK);
+    }
+    CHECK(cudaDeviceSynchronize() == cudaSuccess);
+    cudaMemcpy(yk_h, yk, n * P, cudaMemcpyDeviceToHost);
+    cudaMemcpy(yv_h, yv, n * P, cudaMemcpyDeviceToHost);
+    int bad = 0;
+    for (int l = 0; l < L; ++l)
+      for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h)
+          for (int t = 0; t < S; ++t)
+            for (int d = 0; d < D; ++d) {
+              const size_t ki = (size_t)l * B * H * D * S +
+                                ((((size_t)b * H + h) * (D / X) + d / X) * S + t) * X + d % X;
+              const size_t vi = (size_t)l * B * H * D * S + (((size_t)b * H + h) * S + t) * D + d;
+              const int sel = t >= s[b] && t < e1[b];
+              if (yk_h[ki] != (sel ? hk[ki] : 0) || yv_h[vi] != (sel ? hv[vi] : 0)) ++bad;
+            }
+    CHECK(bad == 0);
+  }
+  dv_replica_destroy(rep);
+  dv_fetcher_destroy(ft);
+  dv_streamer_destroy(st);
+  cudaEventDestroy(out_done);
   if (failures == 0) printf("gpu_roundtrip: all checks passed\n");
   return failures == 0 ? 0 : 1;
 }
