@@ -224,7 +224,7 @@ __device__ __forceinline__ void flat_window(const KParams<MAXB>& p, int64_t w0, 
     if (b + half < p.B && p.H * p.tok_pre[b + half] <= rec0) b += half;
   const int32_t lo = p.H * p.tok_pre[b] * C;      // sequence b's block in the slab
   const int32_t hi = p.H * p.tok_pre[b + 1] * C;
-  if (r0 + kWin <= hi) {
+  if (r0 <= hi - kWin) {  // (r0 + kWin could pass INT32_MAX in a slab near 2^31 chunks)
     const int32_t len = p.seq_len[b];
     const uint32_t m = p.m_len[b];
     const bool is_k = (lkv & 1) == 0;
@@ -463,7 +463,7 @@ __device__ __forceinline__ void record_window(const RecParams& p, int64_t w0, in
     if (b + half < p.B && p.H * p.words[pre + b + half] <= rec0) b += half;
   const int32_t lo = p.H * p.words[pre + b] * C;  // sequence b's block in the slab
   const int32_t hi = p.H * p.words[pre + b + 1] * C;
-  if (r0 + kWin <= hi) {
+  if (r0 <= hi - kWin) {  // (r0 + kWin could pass INT32_MAX in a slab near 2^31 chunks)
     const int32_t len = p.words[pre + b + 1] - p.words[pre + b];
     const uint32_t m = (uint32_t)p.words[pre + p.B + 1 + b];
     const bool is_k = (lkv & 1) == 0;
