@@ -59,12 +59,16 @@
  *    nothing when it fails.  On success the work is enqueued on the given
  *    stream(s) and the call returns; buffers must stay alive and unmodified
  *    until the stream reaches that point.  A launch failure returns
- *    DV_ERR_CUDA.  No call blocks except dv_streamer_wait and the
- *    synchronous helpers marked as such.
+ *    DV_ERR_CUDA.  No call blocks except dv_streamer_wait, dv_fetcher_wait
+ *    and the synchronous helpers marked as such.
+ *  - Tracing: every call that enqueues work pushes an NVTX range named
+ *    after the call for its duration (nested when one call makes another),
+ *    so NVTX-aware profilers show each call with the launches and copies it
+ *    enqueued; without such a profiler the ranges cost nothing.
  *  - Errors: every call returns a dv_status; dv_last_error() gives a
  *    message for the calling thread's most recent failure.
- *  - Threads: calls on distinct handles may run concurrently; a streamer or
- *    replica handle must not be used by two threads at once.
+ *  - Threads: calls on distinct handles may run concurrently; a streamer,
+ *    fetcher or replica handle must not be used by two threads at once.
  */
 #ifndef DV_H_
 #define DV_H_

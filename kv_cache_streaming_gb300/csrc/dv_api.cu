@@ -14,7 +14,35 @@
 #include "../../include/dv.h"
 #include "dv_plan.h"
 
+#ifndef DV_NVTX
+#define DV_NVTX 1  // NVTX ranges around every ABI call that enqueues work
+#endif
+#if DV_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
+
 namespace {
+
+// A named range on the calling thread's NVTX stack for the duration of one
+// ABI call, so that a timeline taken with an NVTX-aware profiler shows each
+// call and the launches and copies it enqueued; without a profiler attached
+// the push and pop do nothing.
+struct Trace {
+  explicit Trace(const char* name) {
+#if DV_NVTX
+    nvtxRangePushA(name);
+#else
+    (void)name;
+#endif
+  }
+  ~Trace() {
+#if DV_NVTX
+    nvtxRangePop();
+#endif
+  }
+  Trace(const Trace&) = delete;
+  Trace& operator=(const Trace&) = delete;
+};
 
 thread_local std::string g_last_error;
 
@@ -509,18 +537,21 @@ dv_status dv_staging_bytes(const dv_cache* cache, int32_t l0, int32_t l1,
 
 dv_status dv_kv_pack(const dv_cache* cache, int32_t l0, int32_t l1, const int32_t* seq_start,
                      const int32_t* seq_end, void* dst, size_t dst_bytes, dv_stream stream) {
+  const Trace trace("dv_kv_pack");
   return do_pack(cache, l0, l1, seq_start, seq_end, dst, dst_bytes, stream, dv::kAuto);
 }
 
 dv_status dv_kv_unpack(const dv_cache* cache, int32_t l0, int32_t l1, const int32_t* seq_start,
                        const int32_t* seq_end, const void* src, size_t src_bytes,
                        dv_stream stream) {
+  const Trace trace("dv_kv_unpack");
   return do_unpack(cache, l0, l1, seq_start, seq_end, src, src_bytes, stream, dv::kAuto);
 }
 
 dv_status dv_kv_pack_variant(const dv_cache* cache, int32_t l0, int32_t l1,
                              const int32_t* seq_start, const int32_t* seq_end, void* dst,
                              size_t dst_bytes, dv_stream stream, int32_t variant) {
+  const Trace trace("dv_kv_pack_variant");
   return do_pack(cache, l0, l1, seq_start, seq_end, dst, dst_bytes, stream, variant);
 }
 
@@ -528,12 +559,14 @@ dv_status dv_kv_unpack_variant(const dv_cache* cache, int32_t l0, int32_t l1,
                                const int32_t* seq_start, const int32_t* seq_end,
                                const void* src, size_t src_bytes, dv_stream stream,
                                int32_t variant) {
+  const Trace trace("dv_kv_unpack_variant");
   return do_unpack(cache, l0, l1, seq_start, seq_end, src, src_bytes, stream, variant);
 }
 
 dv_status dv_naive_gather(const dv_cache* cache, int32_t l0, int32_t l1,
                           const int32_t* seq_start, const int32_t* seq_end, void* dst,
                           size_t dst_bytes, dv_stream stream, int64_t* num_copies) {
+  const Trace trace("dv_naive_gather");
   if (num_copies) *num_copies = 0;
   dv::Plan p;
   dv_status st = plan_ranges(cache, l0, l1, seq_start, seq_end, &p);
@@ -589,6 +622,7 @@ dv_status dv_naive_gather(const dv_cache* cache, int32_t l0, int32_t l1,
 dv_status dv_swap_out(const dv_cache* cache, int32_t l0, int32_t l1, const int32_t* seq_start,
                       const int32_t* seq_end, void* host_dst, size_t host_bytes, void* staging,
                       size_t staging_bytes, dv_stream stream) {
+  const Trace trace("dv_swap_out");
   return do_swap(Dir::kOut, cache, l0, l1, seq_start, seq_end, host_dst, host_bytes, staging,
                  staging_bytes, stream);
 }
@@ -596,6 +630,7 @@ dv_status dv_swap_out(const dv_cache* cache, int32_t l0, int32_t l1, const int32
 dv_status dv_swap_in(const dv_cache* cache, int32_t l0, int32_t l1, const int32_t* seq_start,
                      const int32_t* seq_end, const void* host_src, size_t host_bytes,
                      void* staging, size_t staging_bytes, dv_stream stream) {
+  const Trace trace("dv_swap_in");
   return do_swap(Dir::kIn, cache, l0, l1, seq_start, seq_end, const_cast<void*>(host_src),
                  host_bytes, staging, staging_bytes, stream);
 }
@@ -636,6 +671,7 @@ dv_status dv_streamer_create(dv_streamer** out, void* slot0, void* slot1, size_t
 dv_status dv_stream_layer(dv_streamer* h, const dv_cache* cache, int32_t layer,
                           const int32_t* seq_start, const int32_t* seq_end, void* host_dst,
                           size_t host_dst_bytes, int32_t l0) {
+  const Trace trace("dv_stream_layer");
   if (!h) return fail(DV_ERR_INVALID_ARG, "streamer is NULL");
   if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
   if (l0 < 0 || layer < l0)
@@ -736,6 +772,7 @@ dv_status dv_fetcher_create(dv_fetcher** out, void* slot0, void* slot1, size_t s
 dv_status dv_fetch_layer(dv_fetcher* h, const dv_cache* cache, int32_t layer,
                          const int32_t* seq_start, const int32_t* seq_end, const void* host_src,
                          size_t host_src_bytes, int32_t l0) {
+  const Trace trace("dv_fetch_layer");
   if (!h) return fail(DV_ERR_INVALID_ARG, "fetcher is NULL");
   if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
   if (l0 < 0 || layer < l0)
@@ -809,6 +846,7 @@ dv_status dv_replica_create(dv_replica** out, void* host_arena, size_t arena_byt
 dv_status dv_replica_append(dv_replica* r, const dv_cache* cache, int32_t l0, int32_t l1,
                             const int32_t* seq_start, const int32_t* seq_end, int64_t step,
                             void* staging, size_t staging_bytes, dv_stream stream) {
+  const Trace trace("dv_replica_append");
   if (!r) return fail(DV_ERR_INVALID_ARG, "replica is NULL");
   if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
   if (cache->batch != r->batch)
@@ -844,6 +882,7 @@ dv_status dv_replica_append(dv_replica* r, const dv_cache* cache, int32_t l0, in
 
 dv_status dv_replica_restore(const dv_replica* r, const dv_cache* cache, int64_t upto_step,
                              void* staging, size_t staging_bytes, dv_stream stream) {
+  const Trace trace("dv_replica_restore");
   if (!r) return fail(DV_ERR_INVALID_ARG, "replica is NULL");
   if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
   if (cache->batch != r->batch)
@@ -874,6 +913,7 @@ dv_status dv_replica_restore(const dv_replica* r, const dv_cache* cache, int64_t
 dv_status dv_replica_restore_batched(const dv_replica* r, const dv_cache* cache,
                                     int64_t upto_step, void* staging, size_t staging_bytes,
                                     dv_stream stream) {
+  const Trace trace("dv_replica_restore_batched");
   RestorePlan rp;
   dv_status st = plan_restore(r, cache, upto_step, staging ? staging_bytes : 0, &rp);
   if (st != DV_OK) return st;
@@ -921,6 +961,7 @@ dv_status dv_replica_restore_batched(const dv_replica* r, const dv_cache* cache,
 
 dv_status dv_replica_restore_fetched(const dv_replica* r, const dv_cache* cache,
                                     int64_t upto_step, dv_fetcher* h) {
+  const Trace trace("dv_replica_restore_fetched");
   if (!h) return fail(DV_ERR_INVALID_ARG, "fetcher is NULL");
   RestorePlan rp;
   dv_status st = plan_restore(r, cache, upto_step, h->slot_bytes, &rp);
