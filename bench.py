@@ -1175,7 +1175,7 @@ def run_mine(args):
     b.torch.cuda.empty_cache()
     workloads = workload_section(b.torch, b.dv) if extra else None
     cpu = None
-    if rank == 0:
+    if rank == 0 and world == 1:  # the CPU baseline is an N = 1 figure
         cores = host_cores()
         smp = OracleSample(min(GPT2.num_layers, 2 * cores), threads=cores)
         moved, dt = smp.step()
