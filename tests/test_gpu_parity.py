@@ -1,5 +1,7 @@
 """Parity of the CUDA path with the oracle, byte for byte, on seeded inputs
 small enough for the oracle (several tiles, ragged tails, empty ranges)."""
+import zlib
+
 import numpy as np
 import pytest
 import torch
@@ -28,6 +30,8 @@ GEOMS = [
     Geometry("c5", 2, 3, 2, 40, 90, 2, "fp16"),         # odd C
     Geometry("c64", 2, 2, 2, 512, 40, 2, "fp16"),       # the largest C the tile kernel takes
     Geometry("c128", 1, 2, 2, 1024, 20, 2, "fp16"),     # beyond it: flat kernel only
+    Geometry("s1", 2, 3, 2, 64, 1, 2, "fp16"),          # max_seq 1: a K token is contiguous
+    Geometry("b1", 2, 1, 3, 128, 64, 2, "bf16"),        # batch 1
 ]
 
 
@@ -107,7 +111,7 @@ def test_tiny_workload(variant):
 
 @pytest.mark.parametrize("g", GEOMS, ids=lambda g: g.name)
 def test_pack_unpack_geometries(g):
-    rng = np.random.default_rng(abs(hash(g.name)) % 2**32)
+    rng = np.random.default_rng(zlib.crc32(g.name.encode()))  # stable across processes
     kh, vh = H.host_cache(g, 1234)
     cache = H.device_cache(g, fill=(kh, vh))
     for name, s, e in range_sets(g, rng):
