@@ -137,3 +137,25 @@ def test_planted_mistake_is_caught(name, tmp_path):
     r = subprocess.run([sys.executable, str(Path(P.__file__)), str(lib)],
                        cwd=str(Path(P.__file__).parent.parent), capture_output=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin"
+
+
+def test_restore_overlapping_records_later_wins():
+    """Records unpacked in append order: where a later record covers slices an
+    earlier one wrote, the later bytes stay (the replica log of Fig 10 is
+    replayed in order).  Expected cache built from the independent layout
+    masks alone: B's bytes where B selects, else A's where A selects, else 0."""
+    g = Geometry("o", 3, 3, 2, 32, 16, 2, "raw")
+    rng = np.random.default_rng(24)
+    ka, va = P.random_cache(g, rng)
+    kb, vb = P.random_cache(g, rng)
+    sa, ea = np.array([0, 2, 5], np.int32), np.array([9, 7, 16], np.int32)
+    sb, eb = np.array([4, 0, 15], np.int32), np.array([12, 3, 16], np.int32)
+    recs = [(0, 3, sa, ea, ORC.pack(g, ka, va, 0, 3, sa, ea)),
+            (1, 3, sb, eb, ORC.pack(g, kb, vb, 1, 3, sb, eb))]
+    k2, v2 = ORC.restore(g, recs)
+    mka, mva = (np.repeat(m, 2) for m in P.selected_mask(g, 0, 3, sa, ea))
+    mkb, mvb = (np.repeat(m, 2) for m in P.selected_mask(g, 1, 3, sb, eb))
+    assert (mka & mkb).any()  # the records do overlap
+    want_k = np.where(mkb, kb, np.where(mka, ka, 0)).astype(np.uint8)
+    want_v = np.where(mvb, vb, np.where(mva, va, 0)).astype(np.uint8)
+    assert np.array_equal(k2, want_k) and np.array_equal(v2, want_v)
