@@ -542,6 +542,29 @@ class Bench:
                                                staging=stg, stream=s))
             res[f"out_{name}_gbs"] = n / t_out / 1e9
             res[f"in_{name}_gbs"] = n / t_in / 1e9
+        # the layer-pipelined forms: dv_stream_layer out, dv_fetch_layer in, one
+        # layer slab per slot, copies on their own stream
+        slab = n // g.num_layers
+        slots = [torch.empty(slab, dtype=torch.uint8, device="cuda") for _ in range(4)]
+        cp = torch.cuda.Stream()
+        st = dv.Streamer(slots[0], slots[1], s, cp)
+        ft = dv.Fetcher(slots[2], slots[3], cp, s)
+
+        def stream_out():
+            for l in range(g.num_layers):
+                st.stream_layer(self.cache, l, zs, full, host)
+            s.wait_stream(cp)
+
+        def fetch_in():
+            cp.wait_stream(s)
+            for l in range(g.num_layers):
+                ft.fetch_layer(self.cache_b, l, zs, full, host)
+
+        res["stream_out_gbs"] = n / timed(stream_out) / 1e9
+        res["fetch_in_gbs"] = n / timed(fetch_in) / 1e9
+        st.close()
+        ft.close()
+        del slots
         best_out = max(res["out_fused_gbs"], res["out_staged_gbs"])
         best_in = max(res["in_fused_gbs"], res["in_staged_gbs"])
         res["out_frac_of_link"] = best_out / res["link_d2h_gbs"]
