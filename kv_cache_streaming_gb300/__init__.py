@@ -10,7 +10,8 @@ replica of decode deltas that a cache can be restored from.
 All work runs in the hand-written sm_103a kernels of ``libdv.so`` behind the C
 ABI of ``include/dv.h``; this package only marshals arguments (see
 ``kv_cache_streaming_gb300.dv``).  Importing it fails if ``libdv.so`` has not
-been built (``python -m kv_cache_streaming_gb300.build``).
+been built (``python kv_cache_streaming_gb300/build.py``; the build script
+runs by path, since importing this package needs the library).
 """
 from .dv import (  # noqa: F401
     DV_MAX_BATCH, DV_OK, DV_ERR_INVALID_ARG, DV_ERR_RANGE, DV_ERR_BUFFER_TOO_SMALL,

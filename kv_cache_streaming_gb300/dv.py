@@ -27,7 +27,7 @@ DV_VARIANT_AUTO, DV_VARIANT_FLAT, DV_VARIANT_TILE, DV_VARIANT_TOKEN = 0, 1, 2, 3
 
 if not library_path.exists():
     raise ImportError(f"{library_path} is missing: build it with "
-                      "`python -m kv_cache_streaming_gb300.build` (needs nvcc)")
+                      "`python kv_cache_streaming_gb300/build.py` (needs nvcc)")
 lib = ctypes.CDLL(str(library_path))
 
 
