@@ -156,3 +156,23 @@ def test_last_error_is_per_thread():
     for t in threads:
         t.join()
     assert all(v is None for v in seen.values()) and len(seen) == 8, seen
+
+
+def test_package_without_the_library_refuses_to_import(tmp_path):
+    """No CPU fallback: a copy of the package without libdv.so fails at import
+    with a message that names the missing library and the build step."""
+    import shutil
+    import subprocess
+    import sys
+    pkg = Path(dv.__file__).resolve().parent
+    dst = tmp_path / pkg.name
+    dst.mkdir()
+    for name in ("__init__.py", "dv.py"):
+        shutil.copy(pkg / name, dst / name)
+    r = subprocess.run([sys.executable, "-c", f"import {pkg.name}"], cwd=str(tmp_path),
+                       capture_output=True, text=True, timeout=120,
+                       env={k: v for k, v in __import__("os").environ.items()
+                            if k not in ("PYTHONPATH", "DV_LIBRARY")})
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "libdv.so is missing" in r.stderr
+    assert "build.py" in r.stderr
