@@ -1151,6 +1151,113 @@ def workload_section(torch, dv):
     return out
 
 
+def hbm_section(torch, dv, peak):
+    """Device-resident pack and unpack of each larger workload's own ranges
+    (staging buffer in device memory, inputs larger than L2, L2 flushed before
+    every timed launch or graph replay), as GB/s read + written and as a
+    fraction of the HBM copy peak.  Per workload: every resident layer in one
+    launch, the same layers one launch per layer (a CUDA graph of the layer
+    launches, as layer streaming issues them), and one-token decode deltas
+    (a CUDA graph of 8 deltas at positions 8 tokens apart, so that no two
+    share a cache line).  Prefix ranges go to the tile kernel and deltas to
+    the token kernel, which is also what the automatic choice takes for
+    them; each is forced here so that the label names the kernel timed.
+    After the timed unpacks, the second cache is packed again and must give
+    the staging bytes back."""
+    from synth.configs import OPT13B, OPT66B_STAGE, BLOOM_STAGE, opt13b_lengths, \
+        opt66b_microbatches, bloom_lengths
+    from synth import gpu as synth_gpu
+    s = torch.cuda.Stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    tile, token = dv.DV_VARIANT_TILE, dv.DV_VARIANT_TOKEN
+
+    def timed(fn, per=1, reps=5):
+        ms = []
+        with torch.cuda.stream(s):
+            for r in range(reps + 1):
+                flush.fill_(r)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(s)
+                fn()
+                b.record(s)
+                torch.cuda.synchronize()
+                if r:
+                    ms.append(a.elapsed_time(b))
+        return statistics.median(ms) / 1e3 / per
+
+    def graphed(calls):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s, capture_error_mode="relaxed"):
+            for fn in calls:
+                fn()
+        return graph
+
+    def figure(payload, secs, kernel, launches):
+        gbs = 2 * payload / secs / 1e9
+        return {"kernel": kernel, "launches": launches, "payload_bytes_per_launch": payload,
+                "us_per_launch": round(secs * 1e6, 2), "gbs": round(gbs, 1),
+                "frac_of_peak": round(gbs / peak, 4)}
+
+    cases = [
+        ("opt-13b: used prefixes [0, len), lognormal(400)", OPT13B, 3,
+         np.zeros(OPT13B.batch, np.int32), opt13b_lengths()),
+        ("opt-66b-stage: microbatch 0 at the end of generation [0, p + o)", OPT66B_STAGE, 4,
+         np.zeros(OPT66B_STAGE.batch, np.int32),
+         (lambda p, o: (p + o).astype(np.int32))(*opt66b_microbatches()[0])),
+        ("bloom-176b-stage: replica snapshot [0, len0), uniform [64, 1536]", BLOOM_STAGE, 5,
+         np.zeros(BLOOM_STAGE.batch, np.int32), bloom_lengths()),
+    ]
+    out = {}
+    for name, g, idx, st, en in cases:
+        L = g.num_layers
+        ka = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+        va = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+        synth_gpu.fill_cache(g, ka, va, seed_of(idx))
+        ca = dv.Cache.from_geometry(g, ka, va)
+        kb = torch.zeros(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+        vb = torch.zeros(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+        cb = dv.Cache.from_geometry(g, kb, vb)
+        n = dv.dv_staging_bytes(ca, 0, L, st, en)
+        slab = n // L
+        stg = torch.empty(n, dtype=torch.uint8, device="cuda")
+        sp = stg.data_ptr()
+        res = {"layers": L, "payload_bytes": n}
+        res["pack_all_layers"] = figure(n, timed(
+            lambda: dv.dv_kv_pack(ca, 0, L, st, en, stg, s, variant=tile)), "tile", 1)
+        res["unpack_all_layers"] = figure(n, timed(
+            lambda: dv.dv_kv_unpack(cb, 0, L, st, en, stg, s, variant=tile)), "tile", 1)
+        gp = graphed([lambda l=l: dv.dv_kv_pack(ca, l, l + 1, st, en, (sp + l * slab, slab), s,
+                                                 variant=tile) for l in range(L)])
+        res["pack_per_layer"] = figure(slab, timed(gp.replay, per=L), "tile", L)
+        gu = graphed([lambda l=l: dv.dv_kv_unpack(cb, l, l + 1, st, en, (sp + l * slab, slab),
+                                                   s, variant=tile) for l in range(L)])
+        res["unpack_per_layer"] = figure(slab, timed(gu.replay, per=L), "tile", L)
+        del gp, gu
+        back = torch.empty_like(stg)
+        dv.dv_kv_pack(cb, 0, L, st, en, back, s)
+        torch.cuda.synchronize()
+        res["verified"] = bool(torch.equal(back, stg))
+        del back
+        # one-token deltas at 8 positions 8 tokens apart, inside the cache
+        pos = [((en - 1 + 8 * k) % g.max_seq).astype(np.int32) for k in range(8)]
+        dsz = dv.dv_staging_bytes(ca, 0, L, pos[0], pos[0] + 1)
+        gp = graphed([lambda k=k: dv.dv_kv_pack(ca, 0, L, pos[k], pos[k] + 1,
+                                                 (sp + k * dsz, dsz), s, variant=token)
+                      for k in range(8)])
+        res["delta_pack"] = figure(dsz, timed(gp.replay, per=8), "token", 8)
+        gu = graphed([lambda k=k: dv.dv_kv_unpack(cb, 0, L, pos[k], pos[k] + 1,
+                                                   (sp + k * dsz, dsz), s, variant=token)
+                      for k in range(8)])
+        res["delta_unpack"] = figure(dsz, timed(gu.replay, per=8), "token", 8)
+        del gp, gu
+        out[name] = res
+        del ca, cb, ka, va, kb, vb, stg
+        torch.cuda.empty_cache()
+    del flush
+    return out
+
+
 def run_mine(args):
     import torch
     rank, world, local = dist_init()
@@ -1197,6 +1304,8 @@ def run_mine(args):
     mb_swap = MicrobatchSwapping(b.torch, b.dv).measure() if extra else None
     b.torch.cuda.empty_cache()
     workloads = workload_section(b.torch, b.dv) if extra else None
+    b.torch.cuda.empty_cache()
+    hbm = hbm_section(b.torch, b.dv, peaks()[0]) if extra else None
     cpu = None
     if rank == 0 and world == 1:  # the CPU baseline is an N = 1 figure
         cores = host_cores()
@@ -1248,6 +1357,7 @@ def run_mine(args):
         "decode_streaming": streaming,
         "microbatch_swapping": mb_swap,
         "workloads": workloads,
+        "hbm_by_workload": hbm,
         "gpu_launches": b.launches_per_step * args.steps,
         "clocks": clk,
     }
