@@ -53,12 +53,15 @@ def parse_args():
     ap.add_argument("--no-swap", action="store_true", help="skip the swap / link section")
     ap.add_argument("--kernel-case", default=None,
                     choices=["tile-pack", "tile-unpack", "delta-pack", "delta-unpack",
-                             "flat-pack", "flat-unpack", "record-restore"],
+                             "flat-pack", "flat-unpack", "record-restore", "swap-out",
+                             "swap-in"],
                     help="run one kernel of the step on an 8-layer cache of the workload's "
                          "shape, 5 launches, and exit (a small case for profilers); "
                          "flat-*: ragged 16..64-token ranges of the OPT-13B-shaped cache, "
                          "flat kernel; record-restore: 5 staged batched restores of 96 "
-                         "decode deltas of the whole cache, one record-kernel launch each")
+                         "decode deltas of the whole cache, one record-kernel launch each; "
+                         "swap-*: fused swap of the 8-layer prompt to / from pinned host "
+                         "memory (the tile kernel on the host link)")
     return ap.parse_args()
 
 
@@ -1386,8 +1389,19 @@ def run_kernel_case(case):
     synth_gpu.fill_cache(g, k, v, seed_of(2))
     cache = dv.Cache.from_geometry(g, k, v)
     (ps, pe), deltas = gpt2_ranges()
-    s, e = (ps, pe) if case.startswith("tile") else deltas[0]
+    s, e = deltas[0] if case.startswith("delta") else (ps, pe)
     n = dv.dv_staging_bytes(cache, 0, g.num_layers, s, e)
+    if case.startswith("swap"):
+        host = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+        dv.dv_swap_out(cache, 0, g.num_layers, s, e, host)
+        for _ in range(5):
+            if case == "swap-out":
+                dv.dv_swap_out(cache, 0, g.num_layers, s, e, host)
+            else:
+                dv.dv_swap_in(cache, 0, g.num_layers, s, e, host)
+        torch.cuda.synchronize()
+        print(f"{case}: 5 fused launches of {n} payload bytes each over the host link")
+        return
     stg = torch.empty(n, dtype=torch.uint8, device="cuda")
     dv.dv_kv_pack(cache, 0, g.num_layers, s, e, stg)
     for _ in range(5):
