@@ -62,10 +62,12 @@ class Log:
         """Restores into a zeroed cache and compares with the oracle: record by
         record, record-batched (fused, or staged through staging_bytes), or
         pipelined through a fetcher with slots of slot_bytes."""
-        torch.cuda.synchronize()
         g = self.g
         z = H.device_cache(g, fill="zero")
         staging = H.device_bytes(staging_bytes) if staging_bytes else None
+        # the zero fill (on torch's stream) ends before the fetcher's streams
+        # touch the cache
+        torch.cuda.synchronize()
         if slot_bytes:
             cs = torch.cuda.Stream()
             f = dv.Fetcher(H.device_bytes(slot_bytes), H.device_bytes(slot_bytes), cs,
