@@ -110,6 +110,8 @@ def _buf(x, nbytes=None):
     if isinstance(x, tuple):
         return int(x[0]), int(x[1] if nbytes is None else nbytes)
     if hasattr(x, "data_ptr"):
+        if hasattr(x, "is_contiguous") and not x.is_contiguous():
+            raise TypeError("a tensor buffer must be contiguous (its bytes are one range)")
         n = x.numel() * x.element_size()
         return x.data_ptr(), int(n if nbytes is None else nbytes)
     raise TypeError(f"cannot use {type(x).__name__} as a buffer")

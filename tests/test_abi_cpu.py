@@ -122,6 +122,18 @@ def test_binding_refuses_ranges_of_the_wrong_length():
     assert dv.dv_staging_bytes(c, 0, 2, ro, ro + 3) == 2 * 2 * 2 * 64 * 2 * 12
 
 
+def test_binding_refuses_a_non_contiguous_tensor_buffer():
+    """A buffer is one byte range: a strided view is refused before the
+    library sees its address."""
+    import torch
+    g = Geometry("v", 2, 4, 2, 64, 16, 2, "raw")
+    c = _cache(g)
+    s = np.zeros(4, np.int32)
+    strided = torch.zeros(64, 64, dtype=torch.uint8).t()
+    with pytest.raises(TypeError):
+        dv.dv_kv_pack(c, 0, 2, s, s + 1, strided, stream=0)
+
+
 def test_last_error_is_per_thread():
     """Threads that fail validation at the same time each read their own
     message (the library's only mutable global state is that thread-local
