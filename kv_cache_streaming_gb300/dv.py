@@ -157,6 +157,9 @@ class Cache:
 
     def __init__(self, num_layers, batch, num_heads, head_dim, max_seq, elem_bytes, k, v,
                  layer_stride_elems=0):
+        for t in (k, v):
+            if hasattr(t, "is_contiguous") and not t.is_contiguous():
+                raise TypeError("K and V tensors must be contiguous (the layout is by address)")
         self.k, self.v = k, v  # keep the tensors alive
         kp = k.data_ptr() if hasattr(k, "data_ptr") else int(k)
         vp = v.data_ptr() if hasattr(v, "data_ptr") else int(v)

@@ -132,6 +132,8 @@ def test_binding_refuses_a_non_contiguous_tensor_buffer():
     strided = torch.zeros(64, 64, dtype=torch.uint8).t()
     with pytest.raises(TypeError):
         dv.dv_kv_pack(c, 0, 2, s, s + 1, strided, stream=0)
+    with pytest.raises(TypeError):
+        dv.Cache.from_geometry(g, strided, torch.zeros(16))
 
 
 def test_last_error_is_per_thread():
