@@ -55,14 +55,15 @@ def parse_args():
     ap.add_argument("--kernel-case", default=None,
                     choices=["tile-pack", "tile-unpack", "delta-pack", "delta-unpack",
                              "flat-pack", "flat-unpack", "record-restore", "swap-out",
-                             "swap-in"],
+                             "swap-in", "ragged-pack", "ragged-unpack"],
                     help="run one kernel of the step on an 8-layer cache of the workload's "
                          "shape, 5 launches, and exit (a small case for profilers); "
                          "flat-*: ragged 16..64-token ranges of the OPT-13B-shaped cache, "
                          "flat kernel; record-restore: 5 staged batched restores of 96 "
                          "decode deltas of the whole cache, one record-kernel launch each; "
                          "swap-*: fused swap of the 8-layer prompt to / from pinned host "
-                         "memory (the tile kernel on the host link)")
+                         "memory (the tile kernel on the host link); ragged-*: the OPT-13B "
+                         "workload's lognormal used prefixes, 4 layers, tile kernel")
     return ap.parse_args()
 
 
@@ -1397,6 +1398,9 @@ def run_kernel_case(case):
     if case.startswith("flat"):
         run_flat_case(case, torch, dv, synth_gpu)
         return
+    if case.startswith("ragged"):
+        run_ragged_case(case, torch, dv, synth_gpu)
+        return
     g = replace(GPT2, num_layers=8)
     k = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
     v = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
@@ -1451,6 +1455,33 @@ def run_flat_case(case, torch, dv, synth_gpu):
     torch.cuda.synchronize()
     print(f"{case}: 5 launches of {2 * n} algorithmic bytes each "
           f"(ranges of {int((e - s).min())}..{int((e - s).max())} tokens)")
+
+
+def run_ragged_case(case, torch, dv, synth_gpu):
+    """Ragged long ranges, the tile kernel on the OPT-13B workload's used
+    prefixes (lognormal, median 400): 4 of the 40 layers (about 590 MB of
+    staging, more than L2; under 2 GB on the device), 5 launches."""
+    from dataclasses import replace
+    from synth.configs import OPT13B, opt13b_lengths
+    g = replace(OPT13B, num_layers=4)
+    k = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+    v = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+    synth_gpu.fill_cache(g, k, v, seed_of(3))
+    cache = dv.Cache.from_geometry(g, k, v)
+    s = np.zeros(g.batch, np.int32)
+    e = opt13b_lengths()
+    n = dv.dv_staging_bytes(cache, 0, g.num_layers, s, e)
+    stg = torch.empty(n, dtype=torch.uint8, device="cuda")
+    tile = dv.DV_VARIANT_TILE
+    dv.dv_kv_pack(cache, 0, g.num_layers, s, e, stg, variant=tile)
+    for _ in range(5):
+        if case.endswith("-pack"):
+            dv.dv_kv_pack(cache, 0, g.num_layers, s, e, stg, variant=tile)
+        else:
+            dv.dv_kv_unpack(cache, 0, g.num_layers, s, e, stg, variant=tile)
+    torch.cuda.synchronize()
+    print(f"{case}: 5 launches of {2 * n} algorithmic bytes each "
+          f"(prefixes of {int(e.min())}..{int(e.max())} tokens)")
 
 
 def run_record_case(torch, dv, synth_gpu):
