@@ -119,6 +119,21 @@ MUTANTS = {
                          "for (int64_t t = seq_start[b] + (seq_start[b] < seq_end[b] && seq_end[b] < S); t < seq_end[b] + (seq_start[b] < seq_end[b] && seq_end[b] < S); ++t)"),
     "d_reversed": ("const int64_t x = 16 / P;\n  int64_t off = 0;",
                    "const int64_t x = 16 / P;\n  int64_t off = 0;\n  const int64_t dflip = D - 1;"),
+    # unpack alone writes V slices into K (pack untouched)
+    "unpack_v_into_k": ("uint8_t* dst =\n                  kv == 0 ?",
+                        "uint8_t* dst =\n                  kv >= 0 ?"),
+    # layer and K/V loops exchanged in pack and unpack alike (round trips still hold)
+    "layer_inside_kv": ("for (int64_t l = l0; l < l1; ++l)\n    for (int kv = 0; kv < 2; ++kv)",
+                        "for (int kv = 0; kv < 2; ++kv)\n    for (int64_t l = l0; l < l1; ++l)"),
+    # sequence and head loops exchanged in pack and unpack alike
+    "head_outside_sequence": ("      for (int64_t b = 0; b < B; ++b)\n        for (int64_t h = 0; h < H; ++h)\n          for (int64_t t",
+                              "      for (int64_t h = 0; h < H; ++h)\n        for (int64_t b = 0; b < B; ++b)\n          for (int64_t t"),
+    # the size formula without its factor 2 (K and V)
+    "size_without_kv": ("return 2 * (int64_t)(l1 - l0) * H * D * tokens;",
+                        "return (int64_t)(l1 - l0) * H * D * tokens;"),
+    # the sampled lookup one element off inside a token
+    "source_of_d_shifted": ("t = seq_start[b] + r / D, d = r % D;",
+                            "t = seq_start[b] + r / D, d = (r + 1) % D;"),
 }
 
 
