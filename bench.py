@@ -56,7 +56,8 @@ def parse_args():
     ap.add_argument("--kernel-case", default=None,
                     choices=["tile-pack", "tile-unpack", "delta-pack", "delta-unpack",
                              "flat-pack", "flat-unpack", "record-restore", "swap-out",
-                             "swap-in", "ragged-pack", "ragged-unpack"],
+                             "swap-in", "ragged-pack", "ragged-unpack", "delta-graph-pack",
+                             "delta-graph-unpack"],
                     help="run one kernel of the step on an 8-layer cache of the workload's "
                          "shape, 5 launches, and exit (a small case for profilers); "
                          "flat-*: ragged 16..64-token ranges of the OPT-13B-shaped cache, "
@@ -64,7 +65,10 @@ def parse_args():
                          "decode deltas of the whole cache, one record-kernel launch each; "
                          "swap-*: fused swap of the 8-layer prompt to / from pinned host "
                          "memory (the tile kernel on the host link); ragged-*: the OPT-13B "
-                         "workload's lognormal used prefixes, 4 layers, tile kernel")
+                         "workload's lognormal used prefixes, 4 layers, tile kernel; "
+                         "delta-graph-*: a CUDA graph of 32 one-token deltas 8 tokens apart "
+                         "on a BLOOM-stage-shaped cache cut to 4 layers and max_seq 512, "
+                         "5 replays (for graph-level counters)")
     return ap.parse_args()
 
 
@@ -1407,6 +1411,9 @@ def run_kernel_case(case):
     if case.startswith("ragged"):
         run_ragged_case(case, torch, dv, synth_gpu)
         return
+    if case.startswith("delta-graph"):
+        run_delta_graph_case(case, torch, dv, synth_gpu)
+        return
     g = replace(GPT2, num_layers=8)
     k = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
     v = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
@@ -1488,6 +1495,39 @@ def run_ragged_case(case, torch, dv, synth_gpu):
     torch.cuda.synchronize()
     print(f"{case}: 5 launches of {2 * n} algorithmic bytes each "
           f"(prefixes of {int(e.min())}..{int(e.max())} tokens)")
+
+
+def run_delta_graph_case(case, torch, dv, synth_gpu):
+    """One-token deltas of every sequence at all layers of a BLOOM-stage-shaped
+    cache (batch 32, 112 heads, head_dim 128, bf16) cut to 4 layers and
+    max_seq 512 (3.8 GB): 32 deltas at positions 8 tokens apart (no two share
+    a K line), captured in one CUDA graph and replayed 5 times.  The graph
+    writes 235 MB of deltas, more than L2, so graph-level DRAM counters include
+    the write-back of the partly written K lines."""
+    from dataclasses import replace
+    from synth.configs import BLOOM_STAGE
+    g = replace(BLOOM_STAGE, num_layers=4, max_seq=512)
+    k = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+    v = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+    synth_gpu.fill_cache(g, k, v, seed_of(5))
+    cache = dv.Cache.from_geometry(g, k, v)
+    nd = 32
+    pos = [np.full(g.batch, 8 * i + 3, np.int32) for i in range(nd)]
+    one = dv.dv_staging_bytes(cache, 0, g.num_layers, pos[0], pos[0] + 1)
+    stg = torch.empty(nd * one, dtype=torch.uint8, device="cuda")
+    sp = stg.data_ptr()
+    s = torch.cuda.Stream()
+    fn = dv.dv_kv_pack if case.endswith("-pack") else dv.dv_kv_unpack
+    for i in range(nd):  # eager first calls (occupancy queries) and the staging contents
+        dv.dv_kv_pack(cache, 0, g.num_layers, pos[i], pos[i] + 1, (sp + i * one, one), s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s, capture_error_mode="relaxed"):
+        for i in range(nd):
+            fn(cache, 0, g.num_layers, pos[i], pos[i] + 1, (sp + i * one, one), s)
+    for _ in range(5):
+        graph.replay()
+    torch.cuda.synchronize()
+    print(f"{case}: 5 replays of a graph of {nd} deltas of {one} bytes each")
 
 
 def run_record_case(torch, dv, synth_gpu):
