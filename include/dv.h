@@ -95,7 +95,7 @@ typedef enum {
   DV_ERR_MISALIGNED = 4,       /* a pointer or stride not 16-byte aligned */
   DV_ERR_CUDA = 5,             /* a CUDA runtime call or launch failed */
   DV_ERR_TIMEOUT = 6,          /* reserved for bounded waits */
-  DV_ERR_UNSUPPORTED = 7       /* a geometry this build does not handle */
+  DV_ERR_UNSUPPORTED = 7       /* a geometry the library does not handle */
 } dv_status;
 
 /* Cache geometry and base pointers; owned by the caller. */
