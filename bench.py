@@ -1,21 +1,30 @@
 #!/usr/bin/env python
 """Benchmark of the KV-cache buffered copy on GB300.
 
-Workload (one step): a GPT2-1.5B-shaped cache (48 layers, batch 8, 25 heads,
-head_dim 64, max_seq 1024, fp16 bit patterns from the seeded generator).
-  1. The prompt range [0,1000) of all 8 sequences is packed layer by layer
-     (48 packs of 51.2 MB), as layer-by-layer prompt streaming does.
-  2. 24 decode steps each pack one token per layer, sequence and head
-     (2.46 MB) into its own slot of a reused delta buffer.
-  3. Everything is unpacked again, into a second cache: the 48 layer slabs
-     and the 24 deltas (what a swap-in / restore does on the receiving side).
+Headline workload (one step): the BLOOM-176B pipeline-stage-shaped cache
+(14 resident layers, batch 32, 112 heads, head_dim 128, max_seq 2048, bf16
+bit patterns from the seeded generator; used lengths len0 uniform in
+[64, 1536]), as the replica of §3 "Fault detection and recovery" (Fig 10)
+builds and uses it:
+  1. the snapshot: the used prefixes [0, len0) of all 14 layers packed into a
+     device log buffer (19.1 GB, one launch);
+  2. 256 decode steps' one-token deltas (one token of every sequence at all
+     layers, 25.7 MB each) packed into the log after it, in an order where no
+     two consecutive packs share a K line (as between real decode steps,
+     whose compute evicts L2);
+  3. the restore: the whole log (snapshot + 256 deltas) unpacked into a second
+     cache with one dv_kv_unpack_records call.
 `value` is the pack/unpack throughput of that step with every buffer in HBM:
-bytes read plus bytes written by all 144 launches, divided by the step time
-(the step runs as one CUDA graph replay).  `e2e` is the same byte count
-through the public API with pinned host buffers: the layer streamer copies
-each slab to the host, the deltas go to a host replica, and swap-in / restore
-bring everything back (host link inside the timed region).  `swap` reports
-swap-out / swap-in of the used cache against the measured host-link peak.
+bytes read plus bytes written by all its launches, divided by the step time
+(the step runs as one CUDA graph replay on one stream; every buffer is read at
+least 19 GB of traffic after it was written, so L2 serves none of it).  `e2e`
+is the same byte count through the public API with pinned host buffers: the
+snapshot and the deltas appended to a host replica (dv_replica_append, the
+pack writing straight over the host link), then restored into the second
+cache through a fetcher (dv_replica_restore_fetched).  Side sections: the
+GPT2-1.5B step (layer-by-layer prompt packs + 24 deltas), swap against the
+measured host-link peak, the other workloads, microbatch swapping and decode
+streaming.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -35,21 +44,39 @@ sys.path.insert(0, str(ROOT))
 
 import numpy as np  # noqa: E402
 
-from synth.configs import GPT2, GPT2_PROMPT, GPT2_DECODE_STEPS, seed_of, gpt2_ranges  # noqa: E402
+from synth.configs import (GPT2, GPT2_PROMPT, GPT2_DECODE_STEPS, BLOOM_STAGE,  # noqa: E402
+                           BLOOM_DECODE_STEPS, Geometry, seed_of, gpt2_ranges, bloom_lengths)
 
 METRIC = "KV pack/unpack GB/s (bytes read + written, HBM-resident step)"
 UNIT = "GB/s"
-WORKLOAD = ("gpt2-1.5b-shaped KV cache L48 B8 H25 D64 S1024 fp16: prompt [0,1000) packed "
-            "layer by layer + 24 one-token decode deltas, all unpacked into a second cache")
+WORKLOAD = ("bloom-176b-stage-shaped KV cache L14 B32 H112 D128 S2048 bf16: replica snapshot "
+            "[0, len0) (len0 uniform [64, 1536]) + 256 one-token decode deltas packed, then the "
+            "whole log restored into a second cache")
 HBM_NOMINAL_GBS = 7900.0  # GB300 HBM3e, nominal (the measured copy peak is the roofline)
 CPU_SAMPLE_SECONDS = 12.0  # CPU work of each oracle baseline sample (all its threads)
-L2_NOTE = "inputs larger than L2: 10.07 GB read + written per step"
+L2_NOTE = ("inputs larger than L2: 102.9 GB read + written per step; every buffer read at "
+           "least 19 GB of traffic after it was written; consecutive delta packs share no K line")
+
+
+def workload_config(world):
+    """The `config` of both arms' JSON lines (the same workload either way)."""
+    g = BLOOM_STAGE
+    return {"workload": WORKLOAD, "layers": g.num_layers, "batch": g.batch,
+            "heads": g.num_heads, "head_dim": g.head_dim, "max_seq": g.max_seq,
+            "elem": "bf16", "decode_steps": BLOOM_DECODE_STEPS, "l2": L2_NOTE,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def delta_order(n, stride=8):
+    """0, 8, 16, ..., 1, 9, ...: no two consecutive entries are within 8 of
+    each other, so consecutive one-token packs never read the same K line."""
+    return [k for r in range(stride) for k in range(r, n, stride)]
 
 
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-swap", action="store_true", help="skip the swap / link section")
@@ -73,13 +100,15 @@ def parse_args():
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
-# tile kernels, from one ncu capture of an 8-layer launch of this workload's
-# shape (`--kernel-case tile-pack` / `tile-unpack`), scaled by 1/8 to one
-# layer (traffic grows with the tiles processed).  Set an entry to None when
-# the kernel changes, until it is captured again.
+# headline step's kernels, from one ncu capture of a smaller case of the same
+# kernel (`--kernel-case ...`), scaled to one launch of the step by the units
+# it moves (traffic grows in proportion).  None until captured, and set back to
+# None whenever the kernel changes.
 TRAFFIC_PER_LAUNCH = {
-    "pack prompt layer (tile kernel)": (409.637632e6 + 351.859200e6) / 8,
-    "unpack prompt layer (tile kernel)": (409.633280e6 + 351.618816e6) / 8,
+    "pack snapshot (tile kernel)": None,
+    "pack one-token delta (token kernel)": None,
+    "unpack snapshot (tile kernel)": None,
+    "unpack 256 one-token deltas (run kernel)": None,
 }
 
 
@@ -195,54 +224,64 @@ def host_cores() -> int:
 
 
 class OracleSample:
-    """The oracle on layers [0, nl) of the workload: per-layer prompt packs,
-    the 24 deltas of those layers, and the unpacks into a zeroed cache (the
-    same operations as the GPU step, on a bounded number of layers).  With
-    `threads` > 1 the layers are dealt out to that many threads; the oracle's
-    C functions run without the interpreter lock, so each thread has a core."""
+    """The oracle on a bounded sample of the headline workload.  A unit is one
+    layer and two sequences of the BLOOM-stage cache (a cache of that shape:
+    1 layer, batch 2, 112 heads, head_dim 128, max_seq 2048): the snapshot pack
+    of the two sequences' [0, len0), their 256 one-token deltas, and the unpack
+    of the snapshot and every delta into a zeroed cache, in log order.  The 224
+    units of the workload are dealt round-robin to `threads` threads, each with
+    its own seeded cache; the oracle's C functions run without the interpreter
+    lock, so each thread has a core.  A step runs `units` units."""
 
-    def __init__(self, nl, threads=1):
+    UNIT_G = Geometry("bloom-unit", 1, 2, 112, 128, 2048, 2, "bf16")
+
+    def __init__(self, units, threads=1):
         from concurrent.futures import ThreadPoolExecutor
-        from dataclasses import replace
         import oracle
         import synth
-        self.nl = nl
-        self.threads = max(1, min(threads, nl))
-        self.g = replace(GPT2, num_layers=nl)
-        seed = seed_of(2)
-        self.kh = synth.fill_bytes(seed, 0, self.g.tensor_bytes, self.g.kind)
-        self.vh = synth.fill_bytes(seed, 1, self.g.tensor_bytes, self.g.kind)
+        g = self.UNIT_G
+        self.threads = max(1, min(threads, units))
+        len0 = bloom_lengths()
+        pairs = [len0[2 * j:2 * j + 2].astype(np.int32) for j in range(BLOOM_STAGE.batch // 2)]
+        every = [(l, pairs[j]) for l in range(BLOOM_STAGE.num_layers) for j in range(len(pairs))]
+        self.units = every[:units]
         self.orc = oracle.default()
-        (self.ps, self.pe), self.deltas = gpt2_ranges()
+        seed = seed_of(5)
+        self.caches = []
+        for t in range(self.threads):
+            kh = synth.fill_bytes(seed * 100 + t, 0, g.tensor_bytes, g.kind)
+            vh = synth.fill_bytes(seed * 100 + t, 1, g.tensor_bytes, g.kind)
+            self.caches.append((kh, vh, np.zeros_like(kh), np.zeros_like(vh)))
         self.pool = ThreadPoolExecutor(self.threads) if self.threads > 1 else None
         how = ("single-thread C loop nest" if self.threads == 1 else
-               f"C loop nest, layers dealt to {self.threads} threads")
-        self.desc = f"layers 0..{nl - 1} of the 48 (prompt packs, 24 deltas, unpacks), {how}"
+               f"C loop nest, units dealt to {self.threads} threads")
+        self.desc = (f"{len(self.units)} of the workload's 224 units (one layer x two sequences: "
+                     f"snapshot pack, 256 one-token delta packs, all unpacked), {how}")
 
-    def _layers(self, layers, kz, vz):
-        g, orc = self.g, self.orc
+    def _units(self, t, units):
+        g, orc = self.UNIT_G, self.orc
+        kh, vh, kz, vz = self.caches[t]
+        zs = np.zeros(2, np.int32)
         moved = 0
-        for l in layers:
-            slab = orc.pack(g, self.kh, self.vh, l, l + 1, self.ps, self.pe)
-            dels = [orc.pack(g, self.kh, self.vh, l, l + 1, s, e) for s, e in self.deltas]
-            orc.unpack(g, kz, vz, l, l + 1, self.ps, self.pe, slab)
-            for (s, e), d in zip(self.deltas, dels):
-                orc.unpack(g, kz, vz, l, l + 1, s, e, d)
-            moved += 2 * 2 * (slab.size + sum(d.size for d in dels))
+        for _, l0 in units:
+            snap = orc.pack(g, kh, vh, 0, 1, zs, l0)
+            dels = [orc.pack(g, kh, vh, 0, 1, l0 + k, l0 + k + 1)
+                    for k in range(BLOOM_DECODE_STEPS)]
+            orc.unpack(g, kz, vz, 0, 1, zs, l0, snap)
+            for k, d in enumerate(dels):
+                orc.unpack(g, kz, vz, 0, 1, l0 + k, l0 + k + 1, d)
+            moved += 2 * 2 * (snap.size + sum(d.size for d in dels))
         return moved
 
     def step(self):
         """Returns (bytes read + written, seconds)."""
-        kz = np.zeros_like(self.kh)
-        vz = np.zeros_like(self.vh)
-        parts = [list(range(i, self.nl, self.threads)) for i in range(self.threads)]
+        parts = [self.units[t::self.threads] for t in range(self.threads)]
         t0 = time.perf_counter()
         if self.pool is None:
-            moved = self._layers(parts[0], kz, vz)
+            moved = self._units(0, parts[0])
         else:
-            moved = sum(self.pool.map(lambda p: self._layers(p, kz, vz), parts))
-        dt = time.perf_counter() - t0
-        return moved, dt
+            moved = sum(self.pool.map(lambda t: self._units(t, parts[t]), range(self.threads)))
+        return moved, time.perf_counter() - t0
 
     def run(self, cpu_seconds):
         """Repeats step() until the threads together have worked about
@@ -262,14 +301,17 @@ class OracleSample:
 
 
 def run_reference(args):
+    """The reference arm: the oracle, as it stands, on the machine's host cores.
+    Each step is a bounded sample of the headline workload (one unit per
+    core), sized so that the whole run stays near two minutes."""
     rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return
-    # About 0.2 s of oracle work per layer and core: each step gives every host
-    # core the same number of layers, sized to keep the whole run near two minutes.
     cores = host_cores()
-    per_core = int(max(1, min(4, 120.0 / (0.2 * (args.steps + args.warmup)))))
-    smp = OracleSample(min(GPT2.num_layers, cores * per_core), threads=cores)
+    # about 0.5 s of oracle work per unit and core
+    per_core = int(max(1, min(4, 100.0 / (0.5 * (args.steps + args.warmup)))))
+    smp = OracleSample(cores * per_core, threads=cores)
     for _ in range(args.warmup):
         smp.step()
     moved = secs = 0.0
@@ -282,9 +324,9 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * secs / max(args.steps, 1), 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "u16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "l2": "n/a (CPU)", "parallelism": "replicas"},
+            "config": workload_config(world),
             "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": smp.threads,
-                             "kind": "oracle", "sample": smp.desc},
+                             "kind": "oracle", "sample": smp.desc + " per step"},
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     smp.close()
@@ -292,6 +334,254 @@ def run_reference(args):
 
 
 # ---- the GPU arm ---------------------------------------------------------------
+
+class Bloom:
+    """The headline step on the BLOOM-176B-stage-shaped cache (see the module
+    docstring): snapshot + 256 one-token deltas packed into a device log, the
+    whole log restored into a second cache."""
+
+    def __init__(self):
+        import torch
+        import kv_cache_streaming_gb300 as dv
+        from synth import gpu as synth_gpu
+        self.torch, self.dv = torch, dv
+        g = self.g = BLOOM_STAGE
+        L = g.num_layers
+        self.k = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+        self.v = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+        synth_gpu.fill_cache(g, self.k, self.v, seed_of(5))
+        self.kb = torch.zeros_like(self.k)
+        self.vb = torch.zeros_like(self.v)
+        self.cache = dv.Cache.from_geometry(g, self.k, self.v)
+        self.cache_b = dv.Cache.from_geometry(g, self.kb, self.vb)
+        self.zs = np.zeros(g.batch, np.int32)
+        self.len0 = bloom_lengths()
+        self.nd = BLOOM_DECODE_STEPS
+        self.deltas = [(self.len0 + k, self.len0 + k + 1) for k in range(self.nd)]
+        self.order = delta_order(self.nd)
+        self.snap = dv.dv_staging_bytes(self.cache, 0, L, self.zs, self.len0)
+        self.dsz = dv.dv_staging_bytes(self.cache, 0, L, *self.deltas[0])
+        self.total = self.snap + self.nd * self.dsz
+        self.log = torch.empty(self.total, dtype=torch.uint8, device="cuda")
+        self.records = [(0, L, self.zs, self.len0)] + [(0, L, s, e) for s, e in self.deltas]
+        self.bytes_per_step = 2 * 2 * self.total
+        self.stream = torch.cuda.Stream()
+
+    def delta_at(self, k):
+        """(address, bytes) of delta k's record in the device log."""
+        return (self.log.data_ptr() + self.snap + k * self.dsz, self.dsz)
+
+    def device_step(self, s):
+        """Snapshot pack, the 256 delta packs (in `order`), the restore."""
+        dv, L = self.dv, self.g.num_layers
+        dv.dv_kv_pack(self.cache, 0, L, self.zs, self.len0, (self.log.data_ptr(), self.snap), s)
+        for k in self.order:
+            a, b = self.deltas[k]
+            dv.dv_kv_pack(self.cache, 0, L, a, b, self.delta_at(k), s)
+        dv.dv_kv_unpack_records(self.cache_b, self.records, self.log, s)
+
+    def launches_per_step(self):
+        # snapshot pack, one pack per delta, the restore: the snapshot by the
+        # tile kernel, the 256-record run by one run-kernel launch
+        return 1 + self.nd + 2
+
+    def capture(self):
+        torch = self.torch
+        with torch.cuda.stream(self.stream):
+            self.device_step(self.stream)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream, capture_error_mode="relaxed"):
+            self.device_step(self.stream)
+        torch.cuda.synchronize()
+
+    def timed_value(self, steps, warmup, world):
+        torch = self.torch
+        for _ in range(warmup):
+            self.graph.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            for _ in range(steps):
+                self.graph.replay()
+            e1.record(self.stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return e0.elapsed_time(e1) / 1e3
+
+    def clear_b(self):
+        self.kb.zero_()
+        self.vb.zero_()
+        self.torch.cuda.synchronize()
+
+    def verify(self):
+        """The second cache equals the first on [0, len0 + 256) of every
+        sequence and is zero beyond (it started zeroed)."""
+        torch, g = self.torch, self.g
+        torch.cuda.synchronize()
+        L, B, H, D, S = g.num_layers, g.batch, g.num_heads, g.head_dim, g.max_seq
+        x = 16 // g.elem_bytes
+        views = []
+        for t in (self.k, self.v, self.kb, self.vb):
+            views.append(t.view(torch.int16))
+        ka, va, kb, vb = views
+        ka, kb = (t.view(L, B, H, D // x, S, x) for t in (ka, kb))
+        va, vb = (t.view(L, B, H, S, D) for t in (va, vb))
+        for b_ in range(B):
+            n = int(self.len0[b_]) + self.nd
+            if not (torch.equal(kb[:, b_, :, :, :n], ka[:, b_, :, :, :n]) and
+                    torch.equal(vb[:, b_, :, :n], va[:, b_, :, :n])):
+                return False
+            if kb[:, b_, :, :, n:].any() or vb[:, b_, :, n:].any():
+                return False
+        return True
+
+    def kernel_times(self, reps=5):
+        """Average launch time of each launch kind as it runs in the step: the
+        step's launches of one kind captured in their own CUDA graph, replayed
+        `reps` times (L2 flushed before each replay), CUDA events on the
+        launching stream around each replay.  Returns (kind, seconds per
+        launch, algorithmic bytes per launch, launches per step)."""
+        torch, dv, g = self.torch, self.dv, self.g
+        L = g.num_layers
+        s = self.stream
+        lp = self.log.data_ptr()
+        kinds = {
+            "pack snapshot (tile kernel)": (
+                [lambda: dv.dv_kv_pack(self.cache, 0, L, self.zs, self.len0, (lp, self.snap), s)],
+                2 * self.snap),
+            "pack one-token delta (token kernel)": (
+                [lambda k=k: dv.dv_kv_pack(self.cache, 0, L, *self.deltas[k], self.delta_at(k), s)
+                 for k in self.order], 2 * self.dsz),
+            "unpack snapshot (tile kernel)": (
+                [lambda: dv.dv_kv_unpack(self.cache_b, 0, L, self.zs, self.len0,
+                                         (lp, self.snap), s)], 2 * self.snap),
+            "unpack 256 one-token deltas (run kernel)": (
+                [lambda: dv.dv_kv_unpack_records(self.cache_b, self.records[1:],
+                                                 (lp + self.snap, self.nd * self.dsz), s)],
+                2 * self.nd * self.dsz),
+        }
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        out = []
+        for name, (calls, nbytes) in kinds.items():
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=s, capture_error_mode="relaxed"):
+                for fn in calls:
+                    fn()
+            ms = []
+            with torch.cuda.stream(s):
+                for r in range(reps + 1):
+                    flush.fill_(r)
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(s)
+                    graph.replay()
+                    b.record(s)
+                    torch.cuda.synchronize()
+                    if r:
+                        ms.append(a.elapsed_time(b))
+            n = len(calls)
+            out.append((name, statistics.median(ms) / 1e3 / n, nbytes, n))
+            del graph
+        del flush
+        return out
+
+    # one step through the public API with pinned host buffers
+    def setup_e2e(self):
+        torch, dv, g = self.torch, self.dv, self.g
+        self.arena = torch.empty(self.total, dtype=torch.uint8, pin_memory=True)
+        self.replica = dv.Replica(self.arena, g.batch)
+        slot = dv.dv_staging_bytes(self.cache, 0, 1, self.zs, self.len0)  # one snapshot layer
+        self.slots = (torch.empty(slot, dtype=torch.uint8, device="cuda"),
+                      torch.empty(slot, dtype=torch.uint8, device="cuda"))
+        self.in_copy = torch.cuda.Stream()
+        self.in_unpack = torch.cuda.Stream()
+        self.fetcher = dv.Fetcher(self.slots[0], self.slots[1], self.in_copy, self.in_unpack)
+
+    def e2e_step(self):
+        """The snapshot and the 256 deltas appended to the host replica (each
+        a pack storing straight into pinned memory over the host link, in
+        decode order), then the restore of the whole log into the second cache
+        through the fetcher: the copy of piece i+1 (copy engine) overlaps the
+        unpack of piece i."""
+        g, s = self.g, self.stream
+        L = g.num_layers
+        rep = self.replica
+        rep.truncate(0)
+        rep.append(self.cache, 0, L, self.zs, self.len0, step=0, stream=s)
+        for k, (a, b) in enumerate(self.deltas):
+            rep.append(self.cache, 0, L, a, b, step=k + 1, stream=s)
+        self.in_copy.wait_stream(s)      # the log is in host memory
+        self.in_unpack.wait_stream(s)    # and the second cache is free
+        rep.restore_fetched(self.cache_b, self.fetcher)
+        s.wait_stream(self.in_unpack)
+
+    def timed_e2e(self, steps, warmup, world):
+        """Seconds of each of `steps` end-to-end steps, each timed from an idle
+        GPU to its last unpack (the host link is shared with other tenants of
+        the machine: the median step is the robust figure)."""
+        torch = self.torch
+        for _ in range(warmup):
+            self.e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        ts = []
+        for _ in range(steps):
+            t0 = time.perf_counter()
+            self.e2e_step()
+            torch.cuda.synchronize()
+            ts.append(time.perf_counter() - t0)
+        barrier(world)
+        return ts
+
+    def close_e2e(self):
+        self.fetcher.close()
+        self.replica.close()
+        del self.arena, self.slots
+
+
+def link_peaks(torch, nbytes=2 << 30, reps=3):
+    """The host link measured in this run: large pinned cudaMemcpyAsync each
+    way alone and both ways at once (GB/s, median of `reps`)."""
+    s = torch.cuda.Stream()
+    host = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    host2 = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    dev2 = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    s2 = torch.cuda.Stream()
+
+    def timed(fn):
+        ts = []
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s):
+                a.record(s)
+                fn()
+                b.record(s)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) / 1e3)
+        return statistics.median(ts)
+
+    def both():
+        s2.wait_stream(s)
+        host.copy_(dev, non_blocking=True)
+        with torch.cuda.stream(s2):
+            dev2.copy_(host2, non_blocking=True)
+        s.wait_stream(s2)
+
+    out = {"d2h_gbs": nbytes / timed(lambda: host.copy_(dev, non_blocking=True)) / 1e9,
+           "h2d_gbs": nbytes / timed(lambda: dev.copy_(host, non_blocking=True)) / 1e9,
+           "bidir_gbs": 2 * nbytes / timed(both) / 1e9}
+    del host, dev, host2, dev2
+    torch.cuda.empty_cache()
+    return {k: round(v, 2) for k, v in out.items()}
+
 
 class Bench:
     def __init__(self):
@@ -1281,6 +1571,55 @@ def hbm_section(torch, dv, peak):
     return out
 
 
+def gpt2_section(torch, steps=100):
+    """The GPT2-1.5B step (48 per-layer prompt packs, 24 one-token deltas, all
+    unpacked into a second cache) as a side section: its value with every
+    launch on one stream (packs, then unpacks: each slab read ~5 GB of traffic
+    after it was written), the same step with each unpack on a second stream
+    right after its pack (sender and receiver overlapped; part of each slab
+    can still be in L2 then), per-kernel times, the swap / link figures and
+    the end-to-end step through the API (layer streamer out, fetcher in,
+    deltas to a replica and back)."""
+    b = Bench()
+    b.capture()
+    serial = b.timed_serial(steps)
+    two = b.timed_value(steps, 3, 1) / steps
+    b.clear_b()
+    b.graph_serial.replay()
+    ok = b.verify()
+    kt = b.kernel_times()
+    swap = b.swap_section()
+    b.setup_e2e()
+    b.clear_b()
+    ts = b.timed_e2e(10, 2, 1)
+    e2e_ok = b.verify()
+    hbm_peak = peaks()[0]
+    out = {"workload": ("gpt2-1.5b-shaped KV cache L48 B8 H25 D64 S1024 fp16: prompt [0,1000) "
+                        "packed layer by layer + 24 one-token decode deltas, all unpacked into a "
+                        "second cache"),
+           "bytes_per_step": b.bytes_per_step,
+           "value": round(b.bytes_per_step / serial / 1e9, 2),
+           "frac_of_measured_peak": round(b.bytes_per_step / serial / 1e9 / hbm_peak, 4),
+           "timing": "one stream: every pack, then every unpack; CUDA graph; mean over "
+                     f"{steps} replays",
+           "two_stream_value": round(b.bytes_per_step / two / 1e9, 2),
+           "two_stream_note": "each unpack right after its pack on a second stream: part of "
+                              "the slab may still be in L2",
+           "verified": ok,
+           "kernels": [{"kernel": n_, "avg_launch_us": round(t * 1e6, 2),
+                        "gbs": round(nb / t / 1e9, 1),
+                        "frac_of_peak": round(nb / t / 1e9 / hbm_peak, 4),
+                        "launches_per_step": c} for n_, t, nb, c in kt],
+           "e2e_gbs": round(b.bytes_per_step / statistics.median(ts) / 1e9, 2),
+           "e2e_verified": e2e_ok,
+           "e2e_path": "per layer: dv_stream_layer (pack + D2H copy) then dv_fetch_layer (H2D "
+                       "copy + unpack on the fetcher's two streams); dv_replica_append x24 "
+                       "(fused) + dv_replica_restore_batched (staged)"}
+    del b
+    torch.cuda.empty_cache()
+    return out, swap
+
+
 def run_mine(args):
     import torch
     rank, world, local = dist_init()
@@ -1291,7 +1630,7 @@ def run_mine(args):
         __graft_entry__.build()
     barrier(world)
     __graft_entry__.build()  # no-op when up to date; every rank imports the package
-    b = Bench()
+    b = Bloom()
     b.capture()
     clocks = ClockSampler(local)
     clocks.start()
@@ -1299,43 +1638,52 @@ def run_mine(args):
     clk = clocks.stop()
     secs = max_over_ranks(secs, world)
     value = whole_job_rate(b.bytes_per_step, args.steps, secs, world)
+    b.clear_b()
+    b.graph.replay()
     step_ok = b.verify()
-    serial = b.timed_serial()
-    # kernel roofline, live
+    # kernel roofline, live: the launch kind with the most time per step
     kt = b.kernel_times()
     hbm_peak, peak_kind = peaks()
-    top = max(kt, key=lambda r: r[1] * r[3])
-    name, t_launch, nbytes, _ = top
+    name, t_launch, nbytes, _ = max(kt, key=lambda r: r[1] * r[3])
     achieved = nbytes / t_launch / 1e9
     # e2e through the public API with host buffers
+    link = link_peaks(torch)
     b.setup_e2e()
-    e2e_steps = max(3, min(args.steps, 20))
+    e2e_steps = max(3, min(args.steps, 10))
     b.clear_b()
-    e2e_ts = b.timed_e2e(e2e_steps, 2, world)
+    e2e_ts = b.timed_e2e(e2e_steps, 1, world)
     e2e_ok = b.verify()
     e2e_med = max_over_ranks(statistics.median(e2e_ts), world)
     e2e_value = whole_job_rate(b.bytes_per_step, 1, e2e_med, world)
     e2e_all = whole_job_rate(b.bytes_per_step, e2e_steps, max_over_ranks(sum(e2e_ts), world),
                              world)
-    h2d = d2h = b.g.num_layers * b.slab + GPT2_DECODE_STEPS * b.dsz
+    link_bytes = 2 * b.total  # every log byte crosses once each way
+    serial_link_s = b.total / (link["d2h_gbs"] * 1e9) + b.total / (link["h2d_gbs"] * 1e9)
+    b.close_e2e()
+    per_step = {"bytes_per_step": b.bytes_per_step, "log_bytes": b.total,
+                "snapshot_bytes": b.snap, "delta_bytes": b.dsz,
+                "launches_per_step": b.launches_per_step()}
+    del b
+    torch.cuda.empty_cache()
     # The sections below describe one GPU and only rank 0 prints them: the other
     # ranks skip them (they would pin about 20 GB of host memory each).
     extra = rank == 0 and not args.no_swap
-    swap = b.swap_section() if extra else None
-    naive = naive_vs_buffered(b.torch, b.dv) if extra else None
-    streaming = DecodeStreaming(b.torch, b.dv).measure() if extra else None
-    mb_swap = MicrobatchSwapping(b.torch, b.dv).measure() if extra else None
-    b.torch.cuda.empty_cache()
-    workloads = workload_section(b.torch, b.dv) if extra else None
-    b.torch.cuda.empty_cache()
-    hbm = hbm_section(b.torch, b.dv, peaks()[0]) if extra else None
+    gpt2, swap = gpt2_section(torch) if extra else (None, None)
+    naive = naive_vs_buffered(torch, __import__("kv_cache_streaming_gb300")) if extra else None
+    import kv_cache_streaming_gb300 as dv
+    streaming = DecodeStreaming(torch, dv).measure() if extra else None
+    mb_swap = MicrobatchSwapping(torch, dv).measure() if extra else None
+    torch.cuda.empty_cache()
+    workloads = workload_section(torch, dv) if extra else None
+    torch.cuda.empty_cache()
+    hbm = hbm_section(torch, dv, hbm_peak) if extra else None
     cpu = None
     if rank == 0 and world == 1:  # the CPU baseline is an N = 1 figure
         cores = host_cores()
-        smp = OracleSample(min(GPT2.num_layers, 2 * cores), threads=cores)
+        smp = OracleSample(2 * cores, threads=cores)
         moved, dt, passes = smp.run(cpu_seconds=CPU_SAMPLE_SECONDS)
         smp.close()
-        one = OracleSample(4)
+        one = OracleSample(2)
         moved1, dt1, passes1 = one.run(cpu_seconds=CPU_SAMPLE_SECONDS)
         cpu = {"value": round(moved / dt / 1e9, 3), "unit": UNIT, "cores": smp.threads,
                "kind": "oracle",
@@ -1350,16 +1698,14 @@ def run_mine(args):
         "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": round(1e3 * secs / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "l2": L2_NOTE,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "timing": "CUDA-graph replay of the step (packs on one stream, each unpack "
-                             "after its pack on a second stream), CUDA events on the launching stream",
-                   "step_verified": step_ok,
-                   "frac_of_measured_peak": round(value / hbm_peak, 4),
-                   "frac_of_nominal_peak": round(value / HBM_NOMINAL_GBS, 4),
-                   "serial_step_ms": round(serial * 1e3, 4),
-                   "serial_value": round(b.bytes_per_step / serial / 1e9, 2),
-                   "kernel_timing": "per launch kind: its launches of one step in a CUDA graph, L2 flushed before each replay, median of 5"},
+        "config": workload_config(world),
+        "timing": "CUDA-graph replay of the step on one stream, CUDA events on that stream; "
+                  "per-kernel figures: each launch kind of one step in its own CUDA graph, L2 "
+                  "flushed before each replay, median of 5",
+        "step_verified": step_ok,
+        "frac_of_measured_peak": round(value / hbm_peak, 4),
+        "frac_of_nominal_peak": round(value / HBM_NOMINAL_GBS, 4),
+        "step": per_step,
         "roofline": {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1),
                      "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                      "peak_kind": peak_kind, "nominal_peak": HBM_NOMINAL_GBS,
@@ -1368,25 +1714,32 @@ def run_mine(args):
                      "algorithmic_bytes_per_launch": nbytes,
                      "avg_launch_us": round(t_launch * 1e6, 2)},
         "kernels": [{"kernel": n_, "avg_launch_us": round(t * 1e6, 2),
-                     "gbs": round(nb / t / 1e9, 1), "launches_per_step": c}
+                     "gbs": round(nb / t / 1e9, 1), "frac_of_peak": round(nb / t / 1e9 / hbm_peak, 4),
+                     "launches_per_step": c, "ms_per_step": round(t * c * 1e3, 3),
+                     "traffic": TRAFFIC_PER_LAUNCH.get(n_)}
                     for n_, t, nb, c in kt],
         "cpu_baseline": cpu,
-        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "verified": e2e_ok,
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": per_step["log_bytes"],
+                "d2h_bytes_per_step": per_step["log_bytes"], "steps": e2e_steps, "verified": e2e_ok,
+                "link_gbs": round(world * link_bytes / e2e_med / 1e9, 2),
+                "link_peaks_gbs": link,
+                "link_frac_of_serial_peak": round(serial_link_s / e2e_med, 4),
+                "link_frac_of_bidir_peak": round(link_bytes / e2e_med / 1e9 / link["bidir_gbs"], 4),
                 "timing": "median step (each step synchronised); over all steps: "
-                          f"{e2e_all:.1f} GB/s, slowest step {max(e2e_ts) * 1e3:.2f} ms, "
-                          f"fastest {min(e2e_ts) * 1e3:.2f} ms",
-                "path": "per layer: dv_stream_layer (pack + D2H copy) then dv_fetch_layer "
-                        "(H2D copy + unpack on the fetcher's two streams), overlapping the "
-                        "next layer's D2H; dv_replica_append x24 (fused) + "
-                        "dv_replica_restore_batched (staged)"},
+                          f"{e2e_all:.1f} GB/s, slowest step {max(e2e_ts) * 1e3:.1f} ms, "
+                          f"fastest {min(e2e_ts) * 1e3:.1f} ms",
+                "path": "dv_replica_append of the snapshot and of the 256 deltas (fused: the "
+                        "pack stores into pinned host memory), then dv_replica_restore_fetched "
+                        "into the second cache (one-layer slots; the snapshot by layers, the "
+                        "deltas as runs of records)"},
+        "gpt2_step": gpt2,
         "swap": swap,
         "naive_vs_buffered": naive,
         "decode_streaming": streaming,
         "microbatch_swapping": mb_swap,
         "workloads": workloads,
         "hbm_by_workload": hbm,
-        "gpu_launches": b.launches_per_step * args.steps,
+        "gpu_launches": per_step["launches_per_step"] * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

@@ -171,6 +171,25 @@ dv_status dv_kv_unpack_variant(const dv_cache* cache, int32_t l0, int32_t l1,
                                const void* src, size_t src_bytes, dv_stream stream,
                                int32_t variant);
 
+/* Scatter of a log (Table 1 scatter, applied to many records at once; the
+ * restore side of §3 "Microbatch swapping", Fig 9, and of the replication log
+ * of "Fault detection and recovery", Fig 10): `src` holds num_records
+ * staging buffers back to back, record i being the staging bytes of layers
+ * [layers[2i], layers[2i+1]) and of the ranges at ranges + 2*batch*i
+ * (batch starts, then batch ends, host memory, read during the call).  The
+ * result is that of dv_kv_unpack of each record in order (a later record wins
+ * where two write the same slice).  src: device memory or pinned, mapped host
+ * memory of src_bytes (at least the records' total).  Records long enough for
+ * the tile kernel are unpacked by themselves; runs of one-token records (the
+ * decode deltas of consecutive steps over the same sequences: record k one
+ * token further on than the one before) are unpacked together, each K row's
+ * consecutive tokens written as one span; the other records go in as few
+ * record-batched launches as the kernel parameters allow.  Validates every
+ * record before enqueuing anything. */
+dv_status dv_kv_unpack_records(const dv_cache* cache, int32_t num_records,
+                               const int32_t* layers, const int32_t* ranges, const void* src,
+                               size_t src_bytes, dv_stream stream);
+
 /* The naive transfer the pages measure buffered copies against (§5.1, Fig 11:
  * "many cudaMemcpy calls" for the small non-contiguous regions): the same bytes
  * as dv_kv_pack written to `dst` (device or pinned host memory) with one

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -392,50 +393,74 @@ struct dv_replica {
 
 namespace {
 
-// The records of a restore, validated against the cache: the non-empty ones
-// in append order, their ranges for the record kernel, and which of them go
-// by themselves (long ranges, for the tile kernel, or larger than a piece).
-struct RestorePlan {
-  std::vector<const Record*> todo;
+// One record of a log: its layers, its ranges (batch starts, then batch ends)
+// and where its staging bytes lie relative to the log's first byte.
+struct LogRec {
+  int32_t l0, l1;
+  const int32_t* ranges;
+  size_t offset, bytes;
+  int64_t step;
+};
+
+// Shortest run of one-token records that goes to the run kernel; shorter
+// stretches go to the record kernel.
+constexpr int kMinRun = 2;
+
+// The non-empty records of a log, validated against a cache, and how they go:
+//  - alone: long ranges (the tile kernel's, normally a snapshot), or larger
+//    than a piece, unpacked by themselves;
+//  - run[i] >= kMinRun: records i .. i + run[i] - 1 are a run of one-token
+//    records (run_length), unpacked by the run kernel;
+//  - the others, consecutive and disjoint, by the record kernel.
+struct LogPlan {
+  std::vector<LogRec> todo;
   std::vector<dv::RecordRanges> recs;
   std::vector<char> alone;
+  std::vector<int> run;
   dv::Plan base;  // the cache: geometry, resolved K / V, layers [0, the last record's l1)
   size_t total = 0;
 
-  // How many records from i on one record-batched launch takes: consecutive
-  // records not alone, whose writes are disjoint, that fit the parameters
-  // and (piece > 0) piece bytes together.
-  int run_at(int i, size_t piece) const {
-    int run = 0;
-    while (i + run < (int)todo.size() && !alone[i + run]) ++run;
-    int k = dv::records_per_launch(base, recs.data() + i, run);
+  // How many records from i on one record-kernel launch takes: consecutive
+  // records neither alone nor the start of a run, whose writes are disjoint,
+  // that fit the parameters and (piece > 0) piece bytes together.
+  int batch_at(int i, size_t piece) const {
+    int n = 0;
+    while (i + n < (int)todo.size() && !alone[i + n] && (n == 0 || run[i + n] < kMinRun)) ++n;
+    const int k = dv::records_per_launch(base, recs.data() + i, n);
     size_t bytes = 0;
     for (int j = 0; j < k; ++j) {
-      if (piece && bytes + todo[i + j]->bytes > piece) return j;
-      bytes += todo[i + j]->bytes;
+      if (piece && bytes + todo[i + j].bytes > piece) return j;
+      bytes += todo[i + j].bytes;
     }
     return k;
   }
+
+  // Records per run-kernel launch from a run starting at i (piece > 0: as many
+  // as piece bytes hold).
+  int run_piece(int i, size_t piece) const {
+    int64_t k = dv::run_max_records(base, recs[i]);
+    if (piece) {
+      const int64_t fit = (int64_t)(piece / todo[i].bytes);
+      if (fit < k) k = fit;
+    }
+    return k < 1 ? 1 : (int)k;
+  }
 };
 
-// Validates every record of `r` with step < upto (all when upto < 0) against
-// `cache` before anything is enqueued.  piece > 0: the bytes one copy can
-// carry; a record larger than that goes by itself in groups of layers, so
-// one of its layer slabs must fit.
-dv_status plan_restore(const dv_replica* r, const dv_cache* cache, int64_t upto, size_t piece,
-                       RestorePlan* rp) {
-  if (!r) return fail(DV_ERR_INVALID_ARG, "replica is NULL");
+// Validates every record of `all` against `cache` before anything is
+// enqueued and plans the log.  piece > 0: the bytes one copy can carry; a
+// record larger than that goes by itself in groups of layers, so one of its
+// layer slabs must fit.
+dv_status plan_log(const dv_cache* cache, const std::vector<LogRec>& all, size_t piece,
+                   LogPlan* lp) {
   if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
-  if (cache->batch != r->batch)
-    return fail(DV_ERR_INVALID_ARG, "cache batch %d differs from the replica's %d", cache->batch,
-                r->batch);
+  const int32_t B = cache->batch;
   int32_t l_end = 0;
   try {
     dv::Plan q;
-    for (const Record& rec : r->records) {
-      if (upto >= 0 && rec.step >= upto) break;
-      const int32_t* s = r->ranges.data() + rec.ranges;
-      const dv_status st = plan_ranges(cache, rec.l0, rec.l1, s, s + r->batch, &q);
+    for (const LogRec& rec : all) {
+      const int32_t* s = rec.ranges;
+      const dv_status st = plan_ranges(cache, rec.l0, rec.l1, s, s + B, &q);
       if (st != DV_OK) return st;
       if ((size_t)q.bytes != rec.bytes)
         return fail(DV_ERR_INVALID_ARG, "record of step %lld does not match this cache geometry",
@@ -446,20 +471,105 @@ dv_status plan_restore(const dv_replica* r, const dv_cache* cache, int64_t upto,
         return fail(DV_ERR_BUFFER_TOO_SMALL, "a staging piece of %zu bytes holds less than one "
                     "layer slab (%lld bytes) of the record of step %lld", piece,
                     (long long)dv::layer_slab_bytes(q), (long long)rec.step);
-      rp->todo.push_back(&rec);
-      rp->recs.push_back(dv::RecordRanges{rec.l0, rec.l1, s, s + r->batch});
-      rp->alone.push_back(by_itself);
+      lp->todo.push_back(rec);
+      lp->recs.push_back(dv::RecordRanges{rec.l0, rec.l1, s, s + B});
+      lp->alone.push_back(by_itself);
       if (rec.l1 > l_end) l_end = rec.l1;
-      rp->total += rec.bytes;
+      lp->total += rec.bytes;
     }
   } catch (...) {
     return fail(DV_ERR_INVALID_ARG, "out of host memory for the restore plan");
   }
-  if (rp->todo.empty()) return DV_OK;
-  std::vector<int32_t> zero((size_t)r->batch, 0);
-  dv_status st = plan_ranges(cache, 0, l_end, zero.data(), zero.data(), &rp->base);
+  if (lp->todo.empty()) return DV_OK;
+  std::vector<int32_t> zero((size_t)B, 0);
+  dv_status st = plan_ranges(cache, 0, l_end, zero.data(), zero.data(), &lp->base);
   if (st != DV_OK) return st;
-  return resolve_cache(cache, &rp->base);
+  if ((st = resolve_cache(cache, &lp->base)) != DV_OK) return st;
+  // Runs of one-token records, greedily from the front, among the records
+  // that do not go alone and lie back to back.
+  const int n = (int)lp->todo.size();
+  lp->run.assign((size_t)n, 1);
+  for (int i = 0; i < n;) {
+    if (lp->alone[i]) {
+      ++i;
+      continue;
+    }
+    int m = i + 1;
+    while (m < n && !lp->alone[m] &&
+           lp->todo[m].offset == lp->todo[m - 1].offset + lp->todo[m - 1].bytes)
+      ++m;
+    const int len = dv::run_length(lp->base, lp->recs.data() + i, m - i);
+    if (len >= kMinRun) {
+      lp->run[i] = len;
+      i += len;
+    } else {
+      ++i;
+    }
+  }
+  return DV_OK;
+}
+
+// The records of `r` with step < upto (all when upto < 0), planned for `cache`.
+dv_status plan_restore(const dv_replica* r, const dv_cache* cache, int64_t upto, size_t piece,
+                       LogPlan* lp) {
+  if (!r) return fail(DV_ERR_INVALID_ARG, "replica is NULL");
+  if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
+  if (cache->batch != r->batch)
+    return fail(DV_ERR_INVALID_ARG, "cache batch %d differs from the replica's %d", cache->batch,
+                r->batch);
+  std::vector<LogRec> all;
+  try {
+    for (const Record& rec : r->records) {
+      if (upto >= 0 && rec.step >= upto) break;
+      all.push_back(LogRec{rec.l0, rec.l1, r->ranges.data() + rec.ranges, rec.offset, rec.bytes,
+                           rec.step});
+    }
+  } catch (...) {
+    return fail(DV_ERR_INVALID_ARG, "out of host memory for the restore plan");
+  }
+  return plan_log(cache, all, piece, lp);
+}
+
+// Enqueues the unpack of every planned record straight from `src` (the
+// device-visible address of the log's first byte; host memory when
+// `host_side`), on `stream`.
+dv_status unpack_log_direct(const dv_cache* cache, LogPlan& lp, const uint8_t* src,
+                            bool host_side, cudaStream_t stream) {
+  lp.base.host_side = host_side;
+  const int n = (int)lp.todo.size();
+  cudaError_t err = cudaSuccess;
+  for (int i = 0; i < n;) {
+    const LogRec& first = lp.todo[i];
+    if (lp.alone[i]) {
+      dv::Plan q;
+      const dv_status st = plan_ranges(cache, first.l0, first.l1, first.ranges,
+                                       first.ranges + cache->batch, &q);
+      if (st != DV_OK) return st;
+      q.k = lp.base.k;
+      q.v = lp.base.v;
+      q.host_side = host_side;
+      if ((err = dv::launch_unpack(q, src + first.offset, stream, dv::kAuto)) != cudaSuccess)
+        return cuda_fail(err, "log unpack launch");
+      ++i;
+    } else if (lp.run[i] >= kMinRun) {
+      const int len = lp.run[i];
+      for (int j = 0; j < len;) {
+        const int k = std::min(lp.run_piece(i + j, 0), len - j);
+        if ((err = dv::launch_unpack_run(lp.base, lp.recs[i + j], k,
+                                         src + lp.todo[i + j].offset, stream)) != cudaSuccess)
+          return cuda_fail(err, "run unpack launch");
+        j += k;
+      }
+      i += len;
+    } else {
+      const int k = lp.batch_at(i, 0);
+      if ((err = dv::launch_unpack_records(lp.base, lp.recs.data() + i, k, src + first.offset,
+                                           stream)) != cudaSuccess)
+        return cuda_fail(err, "record unpack launch");
+      i += k;
+    }
+  }
+  return DV_OK;
 }
 
 // Copies `bytes` from `src` (host memory) into the fetcher's next slot on its
@@ -914,46 +1024,55 @@ dv_status dv_replica_restore_batched(const dv_replica* r, const dv_cache* cache,
                                     int64_t upto_step, void* staging, size_t staging_bytes,
                                     dv_stream stream) {
   const Trace trace("dv_replica_restore_batched");
-  RestorePlan rp;
-  dv_status st = plan_restore(r, cache, upto_step, staging ? staging_bytes : 0, &rp);
+  LogPlan lp;
+  dv_status st = plan_restore(r, cache, upto_step, staging ? staging_bytes : 0, &lp);
   if (st != DV_OK) return st;
-  const int n = (int)rp.todo.size();
+  const int n = (int)lp.todo.size();
   if (n == 0) return DV_OK;
-  void* arena_dev = nullptr;
-  void* stg = nullptr;
-  if (!staging) {
-    if ((st = check_host(r->arena, "replica arena", &arena_dev)) != DV_OK) return st;
-    rp.base.host_side = true;
-  } else {
-    const size_t need = rp.total < staging_bytes ? rp.total : staging_bytes;
-    if ((st = resolve(staging, need, false, "staging", &stg)) != DV_OK) return st;
-  }
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  int i = 0;
-  while (i < n) {
-    const Record& first = *rp.todo[i];
-    if (rp.alone[i]) {
-      const int32_t* s = r->ranges.data() + first.ranges;
+  if (!staging) {  // fused: every kernel reads the arena over the host link
+    void* arena_dev = nullptr;
+    if ((st = check_host(r->arena, "replica arena", &arena_dev)) != DV_OK) return st;
+    return unpack_log_direct(cache, lp, static_cast<const uint8_t*>(arena_dev), true, cs);
+  }
+  void* stg = nullptr;
+  const size_t need = lp.total < staging_bytes ? lp.total : staging_bytes;
+  if ((st = resolve(staging, need, false, "staging", &stg)) != DV_OK) return st;
+  uint8_t* sp = static_cast<uint8_t*>(stg);
+  cudaError_t err;
+  for (int i = 0; i < n;) {
+    const LogRec& first = lp.todo[i];
+    if (lp.alone[i]) {
+      const int32_t* s = first.ranges;
       st = dv_swap_in(cache, first.l0, first.l1, s, s + r->batch, r->arena + first.offset,
                       first.bytes, staging, staging_bytes, stream);
       if (st != DV_OK) return st;
       ++i;
       continue;
     }
-    const int k = rp.run_at(i, staging ? staging_bytes : 0);
-    size_t bytes = 0;
-    for (int j = 0; j < k; ++j) bytes += rp.todo[i + j]->bytes;
-    cudaError_t err;
-    if (staging) {
-      if ((err = cudaMemcpyAsync(stg, r->arena + first.offset, bytes, cudaMemcpyHostToDevice,
-                                 cs)) != cudaSuccess)
-        return cuda_fail(err, "restore copy");
-      err = dv::launch_unpack_records(rp.base, rp.recs.data() + i, k, stg, cs);
-    } else {
-      err = dv::launch_unpack_records(rp.base, rp.recs.data() + i, k,
-                                      static_cast<uint8_t*>(arena_dev) + first.offset, cs);
+    if (lp.run[i] >= kMinRun) {  // a run, in pieces of as many records as staging holds
+      const int len = lp.run[i];
+      for (int j = 0; j < len;) {
+        const int k = std::min(lp.run_piece(i + j, staging_bytes), len - j);
+        const LogRec& f = lp.todo[i + j];
+        if ((err = cudaMemcpyAsync(sp, r->arena + f.offset, (size_t)k * f.bytes,
+                                   cudaMemcpyHostToDevice, cs)) != cudaSuccess)
+          return cuda_fail(err, "restore copy");
+        if ((err = dv::launch_unpack_run(lp.base, lp.recs[i + j], k, sp, cs)) != cudaSuccess)
+          return cuda_fail(err, "run restore launch");
+        j += k;
+      }
+      i += len;
+      continue;
     }
-    if (err != cudaSuccess) return cuda_fail(err, "batched restore launch");
+    const int k = lp.batch_at(i, staging_bytes);
+    size_t bytes = 0;
+    for (int j = 0; j < k; ++j) bytes += lp.todo[i + j].bytes;
+    if ((err = cudaMemcpyAsync(sp, r->arena + first.offset, bytes, cudaMemcpyHostToDevice, cs)) !=
+        cudaSuccess)
+      return cuda_fail(err, "restore copy");
+    if ((err = dv::launch_unpack_records(lp.base, lp.recs.data() + i, k, sp, cs)) != cudaSuccess)
+      return cuda_fail(err, "batched restore launch");
     i += k;
   }
   return DV_OK;
@@ -963,21 +1082,20 @@ dv_status dv_replica_restore_fetched(const dv_replica* r, const dv_cache* cache,
                                     int64_t upto_step, dv_fetcher* h) {
   const Trace trace("dv_replica_restore_fetched");
   if (!h) return fail(DV_ERR_INVALID_ARG, "fetcher is NULL");
-  RestorePlan rp;
-  dv_status st = plan_restore(r, cache, upto_step, h->slot_bytes, &rp);
+  LogPlan lp;
+  dv_status st = plan_restore(r, cache, upto_step, h->slot_bytes, &lp);
   if (st != DV_OK) return st;
-  const int n = (int)rp.todo.size();
+  const int n = (int)lp.todo.size();
   cudaError_t err = cudaSuccess;
-  int i = 0;
-  while (i < n) {
-    const Record& first = *rp.todo[i];
-    if (rp.alone[i]) {
+  for (int i = 0; i < n;) {
+    const LogRec& first = lp.todo[i];
+    if (lp.alone[i]) {
       // Whole layers at a time, as many as a slot holds.
-      const int32_t* s = r->ranges.data() + first.ranges;
+      const int32_t* s = first.ranges;
       dv::Plan q;
       if ((st = plan_ranges(cache, first.l0, first.l1, s, s + r->batch, &q)) != DV_OK) return st;
-      q.k = rp.base.k;
-      q.v = rp.base.v;
+      q.k = lp.base.k;
+      q.v = lp.base.v;
       const int64_t slab = dv::layer_slab_bytes(q);
       const int64_t fit = (int64_t)(h->slot_bytes / (size_t)slab);
       const int32_t group = (int32_t)(fit < (int64_t)(q.l1 - q.l0) ? fit : (int64_t)(q.l1 - q.l0));
@@ -994,16 +1112,72 @@ dv_status dv_replica_restore_fetched(const dv_replica* r, const dv_cache* cache,
       ++i;
       continue;
     }
-    const int k = rp.run_at(i, h->slot_bytes);
+    if (lp.run[i] >= kMinRun) {  // a run, in pieces of as many records as a slot holds
+      const int len = lp.run[i];
+      for (int j = 0; j < len;) {
+        const int k = std::min(lp.run_piece(i + j, h->slot_bytes), len - j);
+        const LogRec& f = lp.todo[i + j];
+        const dv::RecordRanges& fr = lp.recs[i + j];
+        err = fetch_piece(h, r->arena + f.offset, (size_t)k * f.bytes, [&](void* slot) {
+          return dv::launch_unpack_run(lp.base, fr, k, slot, h->unpack);
+        });
+        if (err != cudaSuccess) return cuda_fail(err, "fetched restore (run)");
+        j += k;
+      }
+      i += len;
+      continue;
+    }
+    const int k = lp.batch_at(i, h->slot_bytes);
     size_t bytes = 0;
-    for (int j = 0; j < k; ++j) bytes += rp.todo[i + j]->bytes;
+    for (int j = 0; j < k; ++j) bytes += lp.todo[i + j].bytes;
     err = fetch_piece(h, r->arena + first.offset, bytes, [&](void* slot) {
-      return dv::launch_unpack_records(rp.base, rp.recs.data() + i, k, slot, h->unpack);
+      return dv::launch_unpack_records(lp.base, lp.recs.data() + i, k, slot, h->unpack);
     });
     if (err != cudaSuccess) return cuda_fail(err, "fetched restore (records)");
     i += k;
   }
   return DV_OK;
+}
+
+dv_status dv_kv_unpack_records(const dv_cache* cache, int32_t num_records,
+                               const int32_t* layers, const int32_t* ranges, const void* src,
+                               size_t src_bytes, dv_stream stream) {
+  const Trace trace("dv_kv_unpack_records");
+  if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
+  if (num_records < 0) return fail(DV_ERR_INVALID_ARG, "num_records %d < 0", num_records);
+  if (num_records > 0 && (!layers || !ranges))
+    return fail(DV_ERR_INVALID_ARG, "layers / ranges is NULL");
+  if (cache->batch <= 0 || cache->batch > dv::kMaxBatch)
+    return fail(DV_ERR_INVALID_ARG, "cache batch %d outside [1, %d]", cache->batch,
+                dv::kMaxBatch);
+  std::vector<LogRec> all;
+  size_t off = 0;
+  try {
+    all.reserve((size_t)num_records);
+    for (int32_t i = 0; i < num_records; ++i) {
+      const int32_t* rg = ranges + (size_t)i * 2 * cache->batch;
+      size_t bytes = 0;
+      const dv_status st = dv_staging_bytes(cache, layers[2 * i], layers[2 * i + 1], rg,
+                                            rg + cache->batch, &bytes);
+      if (st != DV_OK) return st;
+      all.push_back(LogRec{layers[2 * i], layers[2 * i + 1], rg, off, bytes, (int64_t)i});
+      off += bytes;
+    }
+  } catch (...) {
+    return fail(DV_ERR_INVALID_ARG, "out of host memory for the record plan");
+  }
+  if (off == 0) return DV_OK;
+  if (src_bytes < off)
+    return fail(DV_ERR_BUFFER_TOO_SMALL, "the records need %zu bytes, src has %zu", off,
+                src_bytes);
+  LogPlan lp;
+  dv_status st = plan_log(cache, all, 0, &lp);
+  if (st != DV_OK) return st;
+  void* d = nullptr;
+  bool host_side = false;
+  if ((st = resolve(src, off, true, "src", &d, &host_side)) != DV_OK) return st;
+  return unpack_log_direct(cache, lp, static_cast<const uint8_t*>(d), host_side,
+                           static_cast<cudaStream_t>(stream));
 }
 
 dv_status dv_replica_truncate(dv_replica* r, int64_t step) {

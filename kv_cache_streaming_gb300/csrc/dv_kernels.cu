@@ -116,6 +116,17 @@ __device__ __forceinline__ void pdl_enter() {
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
 
+// A 16-byte load cached in L2 only, whose miss fetches a 64-byte segment from
+// DRAM rather than the default whole 128-byte line (the PTX prefetch-size
+// qualifier).  Volatile so that it stays after griddepcontrol.wait.
+__device__ __forceinline__ uint4 ld_seg64(const uint4* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.L2::64B.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
 #ifndef DV_CHECKED
 #define DV_CHECKED 0  // 1: every global access is checked against the host-validated extents
 #endif
@@ -363,13 +374,13 @@ __device__ __forceinline__ uint4* token_lookup(const TokParams<MAXB>& p, uint32_
 // shortest chain from launch to the copy.  The first address is computed
 // before the wait for the preceding grid, so only the copy is left after it.
 //
-// Pack reads K chunks at normal L2 priority, everything else as a stream: a
-// K chunk shares its 128-byte line with the next 7 tokens of its K row (the
-// x-interleaved layout), and DRAM delivers the whole line, so the deltas of
-// the following decode steps find it in L2 unless other traffic evicted it.
-// An evict-first load gives the line up at once and each step fetches it
-// again (one-token pack 3.4 against 2.9 us per 2.46 MB delta, GPT2-1.5B shape,
-// 24 consecutive steps).
+// A K chunk of a one-token range is alone in its 128-byte line (the rest of
+// the line holds the next tokens of its K row).  By default a miss brings the
+// whole line in from DRAM; the pack asks for a 64-byte segment instead
+// (measured on the full BLOOM-stage delta, 25.7 MB: 28.0 -> 24.4 us, DRAM
+// reads 144 -> 80 bytes per K chunk), and reads it at normal L2 priority, so
+// that the decode deltas of the next steps still find the segment in L2 when
+// nothing evicted it in between.  V rows are read as a stream.
 template <bool PACK, int MAXB, int LOG2C>
 __global__ void __launch_bounds__(kThreads)
 token_kernel(const __grid_constant__ TokParams<MAXB> p) {
@@ -380,7 +391,7 @@ token_kernel(const __grid_constant__ TokParams<MAXB> p) {
   pdl_enter();
   for (; g < p.total; g += stride) {
     if (ptr) {
-      if (PACK) p.stg[g] = is_k ? __ldcg(ptr) : ld_stream(ptr);
+      if (PACK) p.stg[g] = is_k ? ld_seg64(ptr) : ld_stream(ptr);
       else *ptr = ld_stream(p.stg + g);
     }
     ptr = token_lookup<MAXB, LOG2C>(p, g + stride, is_k);
@@ -531,23 +542,36 @@ record_unpack_kernel(const __grid_constant__ RecParams p) {
   for (w0 += step; w0 < p.total; w0 += step) unpack_round<32>(p, w0 + lane, w0, cptr, true, find);
 }
 
-// Contiguous run of `cnt` chunks between the V cache and staging.
-template <bool PACK, typename Params>
-__device__ __forceinline__ void copy_run(const Params& p, uint4* cache, uint4* stg, int cnt) {
+// Staging index of chunk q of a tile, q = t * C + c (token t, chunk c).  The
+// tile kernel's staging tokens are contiguous (index q); a run of log records
+// holds one token per record, so consecutive tokens are `rs` chunks apart.
+template <bool STRIDED, int LOG2C>
+__device__ __forceinline__ int64_t stg_index(int q, int32_t C, int64_t rs) {
+  if (!STRIDED) return q;
+  const int t = LOG2C >= 0 ? q >> LOG2C : q / C;
+  return (int64_t)t * rs + (q - t * C);
+}
+
+// Run of `cnt` chunks between a contiguous span of the V cache and staging
+// (contiguous too, or tokens of C chunks `rs` apart when STRIDED).
+template <bool PACK, bool STRIDED, int LOG2C, typename Params>
+__device__ __forceinline__ void copy_run(const Params& p, uint4* cache, uint4* stg, int cnt,
+                                         int32_t C, int64_t rs) {
   for (int q0 = threadIdx.x; q0 < cnt; q0 += kThreads * kTileUnroll) {
     uint4 val[kTileUnroll];
     bool ok[kTileUnroll];
 #pragma unroll
     for (int u = 0; u < kTileUnroll; ++u) {
       const int q = q0 + u * kThreads;
-      ok[u] = q < cnt && DV_OK_V(cache + q, 21) && DV_OK_S(stg + q, 22);
-      if (ok[u]) val[u] = PACK ? ld_stream(cache + q) : ld_stream(stg + q);
+      const int64_t sq = stg_index<STRIDED, LOG2C>(q, C, rs);
+      ok[u] = q < cnt && DV_OK_V(cache + q, 21) && DV_OK_S(stg + sq, 22);
+      if (ok[u]) val[u] = PACK ? ld_stream(cache + q) : ld_stream(stg + sq);
     }
 #pragma unroll
     for (int u = 0; u < kTileUnroll; ++u) {
       const int q = q0 + u * kThreads;
       if (ok[u]) {
-        if (PACK) stg[q] = val[u];
+        if (PACK) stg[stg_index<STRIDED, LOG2C>(q, C, rs)] = val[u];
         else cache[q] = val[u];
       }
     }
@@ -556,10 +580,12 @@ __device__ __forceinline__ void copy_run(const Params& p, uint4* cache, uint4* s
 
 // One tile, uniform across the CTA: its staging chunks, the cache chunk its
 // first token starts at (V: the start of the contiguous run; K: row 0, row c
-// at + c * S), its token count, and whether it is a V tile.
+// at + c * S), its token count, whether it is a V tile, and (strided tiles)
+// the staging chunks from one token to the next.
 struct TileJob {
   uint4* stg;
   uint4* cache;
+  int64_t rs;
   int32_t n;
   bool is_v;
 };
@@ -579,6 +605,7 @@ __device__ __forceinline__ TileJob decode_tile(const KParams<MAXB>& p, int64_t t
   const int64_t bh = (int64_t)b * p.H + h;
   TileJob j;
   j.n = min(TB, len - t0);
+  j.rs = C;
   j.stg = p.stg + lkv * p.lkv_chunks + ((int64_t)p.H * p.tok_pre[b] + (int64_t)h * len + t0) * C;
   j.is_v = (lkv & 1) != 0;
   j.cache = j.is_v ? p.v + l * p.layer_chunks + (bh * p.S + p.seq_start[b] + t0) * C
@@ -586,20 +613,21 @@ __device__ __forceinline__ TileJob decode_tile(const KParams<MAXB>& p, int64_t t
   return j;
 }
 
-// Moves one tile (see tile_kernel).
-template <bool PACK, int MAXB, int LOG2C>
-__device__ __forceinline__ void copy_tile(const KParams<MAXB>& p, const TileJob& job,
-                                          uint4* smem) {
+// Moves one tile (see tile_kernel).  STRIDED: the tile's tokens lie job.rs
+// chunks apart in staging (a run of log records) instead of back to back.
+template <bool PACK, bool STRIDED, int LOG2C, typename Params>
+__device__ __forceinline__ void copy_tile(const Params& p, const TileJob& job, uint4* smem) {
   constexpr int TB = TileShape<LOG2C>::TB;
   constexpr int LOG2TB = TileShape<LOG2C>::LOG2TB;
   const int32_t C = LOG2C >= 0 ? (1 << LOG2C) : p.C;
   const int32_t SROW = C | 1;
   const int32_t TC = TB * C;  // chunk slots of a full tile
   uint4* const stg = job.stg;
+  const int64_t rs = job.rs;
   const int32_t n = job.n;
   const int32_t cnt = n * C;            // chunks in this tile
   if (job.is_v) {
-    copy_run<PACK>(p, job.cache, stg, cnt);
+    copy_run<PACK, STRIDED, LOG2C>(p, job.cache, stg, cnt, C, rs);
   } else if (PACK) {
     // K: row c of this tile starts at ck + c * S.
     uint4* ck = job.cache;
@@ -623,7 +651,8 @@ __device__ __forceinline__ void copy_tile(const KParams<MAXB>& p, const TileJob&
     for (int q = threadIdx.x; q < cnt; q += kThreads) {
       const int t = LOG2C >= 0 ? q >> LOG2C : q / C;
       const int c = q - t * C;
-      if (DV_OK_S(stg + q, 32)) stg[q] = smem[t * SROW + c];
+      const int64_t sq = stg_index<STRIDED, LOG2C>(q, C, rs);
+      if (DV_OK_S(stg + sq, 32)) stg[sq] = smem[t * SROW + c];
     }
     __syncthreads();
   } else {
@@ -633,7 +662,8 @@ __device__ __forceinline__ void copy_tile(const KParams<MAXB>& p, const TileJob&
 #pragma unroll
       for (int u = 0; u < kTileUnroll; ++u) {
         const int q = q0 + u * kThreads;
-        if (q < cnt && DV_OK_S(stg + q, 33)) val[u] = ld_stream(stg + q);
+        const int64_t sq = stg_index<STRIDED, LOG2C>(q, C, rs);
+        if (q < cnt && DV_OK_S(stg + sq, 33)) val[u] = ld_stream(stg + sq);
       }
 #pragma unroll
       for (int u = 0; u < kTileUnroll; ++u) {
@@ -667,9 +697,87 @@ tile_kernel(const __grid_constant__ KParams<MAXB> p) {
   // reads only the kernel parameters), so its loads start right after it.
   const TileJob first = decode_tile<LOG2TB>(p, tile, C);
   pdl_enter();
-  copy_tile<PACK, MAXB, LOG2C>(p, first, smem);
+  copy_tile<PACK, false, LOG2C>(p, first, smem);
   for (tile += gridDim.x; tile < p.total; tile += gridDim.x)
-    copy_tile<PACK, MAXB, LOG2C>(p, decode_tile<LOG2TB>(p, tile, C), smem);
+    copy_tile<PACK, false, LOG2C>(p, decode_tile<LOG2TB>(p, tile, C), smem);
+}
+
+// ---- runs of one-token log records (replica restore) -------------------------
+
+// n consecutive log records over the same layers [l0, l0 + nl) and the same
+// A non-empty sequences, each record one token per sequence, one token further
+// on than the record before: record j holds token act_p[a] + j of sequence
+// act_b[a].  The records lie back to back in `stg`, rec_chunks apart, each in
+// staging order [layer][K|V][a][head][chunk].
+template <int MAXB>
+struct RunParams {
+  uint4* k;
+  uint4* v;
+  uint4* stg;
+  int64_t layer_chunks;
+  int64_t rec_chunks;      // chunks of one record: staging stride from token j to j + 1
+  int64_t total;           // tiles
+  int64_t k_lim, v_lim, stg_lim;  // checked builds: extents (chunks) the host validated
+  int32_t l0, H, C, S;
+  int32_t n;               // records of the run
+  int32_t ah;              // A * H: tiles of one token block of one (layer, K|V)
+  int64_t tiles_per_lkv;   // A * H * ceil(n / TB)  (< 2^31)
+  uint64_t m_tpl;          // ceil(2^64 / tiles_per_lkv) (0 when it is 1)
+  uint64_t m_ah;           // ceil(2^32 / ah)
+  uint64_t m_H;            // ceil(2^32 / H)
+  int32_t act_b[MAXB];
+  int32_t act_p[MAXB];
+};
+
+// Tile `tile` of a run: (layer, K|V) slab, token block, then (sequence, head),
+// so that the CTAs working side by side read neighbouring C-chunk segments of
+// the same TB records.  Its tokens are j0 .. j0 + n - 1 of the run, that is
+// cache tokens act_p[a] + j0 ..; token j of the tile is at staging chunk
+// j * rec_chunks of the tile's base.
+template <int LOG2TB, int MAXB>
+__device__ __forceinline__ TileJob decode_run_tile(const RunParams<MAXB>& p, int64_t tile,
+                                                   int32_t C) {
+  constexpr int TB = 1 << LOG2TB;
+  const int64_t lkv = (int64_t)div64_by((uint64_t)tile, (uint64_t)p.tiles_per_lkv, p.m_tpl);
+  const uint32_t r = (uint32_t)(tile - lkv * p.tiles_per_lkv);
+  const uint32_t jb = div_by(r, (uint32_t)p.ah, p.m_ah);
+  const uint32_t ah = r - jb * (uint32_t)p.ah;
+  const uint32_t a = div_by(ah, (uint32_t)p.H, p.m_H);
+  const uint32_t h = ah - a * (uint32_t)p.H;
+  const int32_t j0 = (int32_t)(jb << LOG2TB);
+  const int64_t l = p.l0 + (lkv >> 1);
+  const int64_t bh = (int64_t)p.act_b[a] * p.H + h;
+  const int64_t t0 = (int64_t)p.act_p[a] + j0;
+  TileJob j;
+  j.n = min(TB, p.n - j0);
+  j.rs = p.rec_chunks;
+  j.stg = p.stg + (int64_t)j0 * p.rec_chunks + (lkv * p.ah + ah) * C;
+  j.is_v = (lkv & 1) != 0;
+  j.cache = j.is_v ? p.v + l * p.layer_chunks + (bh * p.S + t0) * C
+                   : p.k + l * p.layer_chunks + bh * C * p.S + t0;
+  return j;
+}
+
+// Unpacks a run of one-token records as the tile kernel unpacks long ranges:
+// per (layer, K|V, sequence, head) and block of TB consecutive records, the
+// TB tokens' C-chunk rows are read from the TB records (full 32-byte sectors),
+// and K goes out as C rows of TB consecutive chunks through the shared-memory
+// transpose.  A restore of one record at a time, or of records in staging
+// order, writes each K chunk alone into a half-filled sector; here the tokens
+// that share a K sector or line are written together.
+template <int MAXB, int LOG2C>
+__global__ void __launch_bounds__(kThreads, DV_TILE_MIN_BLOCKS)
+run_unpack_kernel(const __grid_constant__ RunParams<MAXB> p) {
+  extern __shared__ uint4 smem[];  // TB rows of (C | 1) chunks
+  constexpr int LOG2TB = TileShape<LOG2C>::LOG2TB;
+  const int32_t C = LOG2C >= 0 ? (1 << LOG2C) : p.C;
+  int64_t tile = blockIdx.x;
+  if (tile >= p.total) return;
+  const TileJob first = decode_run_tile<LOG2TB>(p, tile, C);
+  pdl_enter();
+  copy_tile<false, true, LOG2C>(p, first, smem);
+  for (tile += gridDim.x; tile < p.total; tile += gridDim.x)
+    copy_tile<false, true, LOG2C>(p, decode_run_tile<LOG2TB>(p, tile, C), smem);
 }
 
 // ---- host side -------------------------------------------------------------
@@ -940,6 +1048,54 @@ cudaError_t run_records(const Plan& cache, const RecordRanges* recs, int n, cons
   return launch_kernel(kernel, grid, 0, stream, kp);
 }
 
+template <int MAXB, int LOG2C>
+cudaError_t run_run(const Plan& cache, const RecordRanges& first, int n, const void* src,
+                    cudaStream_t stream) {
+  static std::atomic<int64_t> occ_cache{0};
+  constexpr int TB = TileShape<LOG2C>::TB;
+  RunParams<MAXB> kp;
+  kp.k = static_cast<uint4*>(cache.k);
+  kp.v = static_cast<uint4*>(cache.v);
+  kp.stg = static_cast<uint4*>(const_cast<void*>(src));
+  kp.layer_chunks = cache.layer_chunks;
+  kp.k_lim = kp.v_lim = cache_limit(cache);
+  int32_t a = 0;
+  for (int32_t b = 0; b < cache.B; ++b) {
+    if (first.end[b] <= first.start[b]) continue;
+    kp.act_b[a] = b;
+    kp.act_p[a] = first.start[b];
+    ++a;
+  }
+  const int64_t ah = (int64_t)a * cache.H;
+  const int64_t nblk = ((int64_t)n + TB - 1) / TB;
+  const int32_t nl = first.l1 - first.l0;
+  if (a == 0 || n <= 0 || nl <= 0) return cudaSuccess;
+  if (ah * nblk >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
+  kp.l0 = first.l0;
+  kp.H = cache.H;
+  kp.C = cache.C;
+  kp.S = cache.S;
+  kp.n = n;
+  kp.ah = (int32_t)ah;
+  kp.rec_chunks = 2 * (int64_t)nl * ah * cache.C;
+  kp.tiles_per_lkv = ah * nblk;
+  kp.total = 2 * (int64_t)nl * kp.tiles_per_lkv;
+  kp.m_tpl = div64_magic((uint64_t)kp.tiles_per_lkv);
+  kp.m_ah = div_magic((uint32_t)ah);
+  kp.m_H = div_magic((uint32_t)cache.H);
+  kp.stg_lim = (int64_t)n * kp.rec_chunks;
+  const size_t smem = (size_t)TB * (cache.C | 1) * sizeof(uint4);
+  const auto kernel = run_unpack_kernel<MAXB, LOG2C>;
+  // From host memory, a run shorter than the token block leaves each tile
+  // (and so each CTA's bytes in flight over the link) that much emptier than
+  // a full one: scale the CTA cap up to match, at most 8x.
+  const int64_t fill = n < TB ? (TB + n - 1) / n : 1;
+  const int64_t cap = host_cap(cache, (int64_t)sm_count() * blocks_per_sm(kernel, smem, occ_cache),
+                               fill < 8 ? fill : 8);
+  const unsigned grid = (unsigned)(kp.total < cap ? kp.total : cap);
+  return launch_kernel(kernel, grid, smem, stream, kp);
+}
+
 // Whether record k writes a part of the cache that one of recs[0, k) writes:
 // their layer ranges meet and, for some sequence, so do their token ranges.
 // `lo` / `hi` hold the hull of the token ranges of recs[0, k) per sequence.
@@ -1028,6 +1184,58 @@ int records_per_launch(const Plan& cache, const RecordRanges* recs, int n) {
     }
   }
   return k;
+}
+
+int run_length(const Plan& cache, const RecordRanges* recs, int n) {
+  if (n <= 0 || !tile_supported(cache)) return n > 0 ? 1 : 0;
+  const RecordRanges& f = recs[0];
+  const int32_t B = cache.B;
+  bool any = false;
+  for (int32_t b = 0; b < B; ++b) {
+    const int32_t len = f.end[b] - f.start[b];
+    if (len > 1) return 1;
+    any = any || len == 1;
+  }
+  if (!any) return 1;
+  int k = 1;
+  for (; k < n; ++k) {
+    const RecordRanges& x = recs[k];
+    if (x.l0 != f.l0 || x.l1 != f.l1) break;
+    bool same = true;
+    for (int32_t b = 0; b < B && same; ++b) {
+      const bool act = f.end[b] > f.start[b];
+      if (act) same = x.start[b] == f.start[b] + k && x.end[b] == x.start[b] + 1;
+      else same = x.end[b] <= x.start[b];
+    }
+    if (!same) break;
+  }
+  return k;
+}
+
+int run_max_records(const Plan& cache, const RecordRanges& first) {
+  int64_t a = 0;
+  for (int32_t b = 0; b < cache.B; ++b) a += first.end[b] > first.start[b];
+  const int64_t ah = a * cache.H;
+  if (ah == 0) return INT32_MAX;
+  const int64_t tb = cache.C == 8 ? TileShape<3>::TB : cache.C == 16 ? TileShape<4>::TB
+                                                                      : TileShape<-1>::TB;
+  const int64_t blocks = (((int64_t)1 << 31) - 1) / ah;  // tiles of one slab stay below 2^31
+  const int64_t m = blocks * tb;
+  return m < INT32_MAX ? (int)m : INT32_MAX;
+}
+
+cudaError_t launch_unpack_run(const Plan& cache, const RecordRanges& first, int n,
+                              const void* src, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  if (!tile_supported(cache)) return cudaErrorInvalidValue;
+  if (cache.B <= kSmallBatch) {
+    if (cache.C == 8) return run_run<kSmallBatch, 3>(cache, first, n, src, stream);
+    if (cache.C == 16) return run_run<kSmallBatch, 4>(cache, first, n, src, stream);
+    return run_run<kSmallBatch, -1>(cache, first, n, src, stream);
+  }
+  if (cache.C == 8) return run_run<kMaxBatch, 3>(cache, first, n, src, stream);
+  if (cache.C == 16) return run_run<kMaxBatch, 4>(cache, first, n, src, stream);
+  return run_run<kMaxBatch, -1>(cache, first, n, src, stream);
 }
 
 cudaError_t launch_unpack_records(const Plan& cache, const RecordRanges* recs, int n,

@@ -82,6 +82,22 @@ int records_per_launch(const Plan& cache, const RecordRanges* recs, int n);
 cudaError_t launch_unpack_records(const Plan& cache, const RecordRanges* recs, int n,
                                   const void* src, cudaStream_t stream);
 
+// How many of recs[0, n), from the first, form a run that one
+// launch_unpack_run call can take: records over the same layers and the same
+// non-empty sequences, each one token per sequence, the token of record k
+// being k after the first record's (1 when recs[0] is not such a record, or
+// the geometry is beyond the tile kernel).  The records must lie back to back
+// in the source.
+int run_length(const Plan& cache, const RecordRanges* recs, int n);
+// The most records of a run one launch_unpack_run call takes (its tile count
+// stays below 2^31).
+int run_max_records(const Plan& cache, const RecordRanges& first);
+// Unpacks n records of a run that starts with `first` (n at most run_length
+// and run_max_records) from `src` in one launch: the tile kernel's unpack,
+// each tile TB consecutive records of one (layer, K|V, sequence, head).
+cudaError_t launch_unpack_run(const Plan& cache, const RecordRanges& first, int n,
+                              const void* src, cudaStream_t stream);
+
 // Whether this library was built with device-side bounds checks, and the
 // first out-of-bounds access they recorded since the last call (0 if none;
 // the record is cleared).  Synchronous.

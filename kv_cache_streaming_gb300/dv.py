@@ -67,6 +67,7 @@ _swap_out = _sig("dv_swap_out", _RANGE + [_P, _SZ, _P, _SZ, _P])
 _swap_in = _sig("dv_swap_in", _RANGE + [_P, _SZ, _P, _SZ, _P])
 _swap_out_noalloc = _sig("dv_swap_out_noalloc", _RANGE + [_P, _SZ, _P])
 _naive_gather = _sig("dv_naive_gather", _RANGE + [_P, _SZ, _P, ctypes.POINTER(_I64)])
+_unpack_records = _sig("dv_kv_unpack_records", [_CP, _I32, _I32P, _I32P, _P, _SZ, _P])
 DV_NOALLOC_STAGING_BYTES = 64 << 20
 _streamer_create = _sig("dv_streamer_create", [ctypes.POINTER(_P), _P, _P, _SZ, _P, _P])
 _stream_layer = _sig("dv_stream_layer", [_P, _CP, _I32, _I32P, _I32P, _P, _SZ, _I32])
@@ -225,6 +226,37 @@ def dv_kv_unpack(cache: Cache, l0, l1, seq_start, seq_end, src, stream=None,
     s, e, sp, ep = _ranges(seq_start, seq_end, cache.c.batch)
     d, n = _buf(src, src_bytes)
     _check(_unpack(cache.ref, l0, l1, sp, ep, d, n, _stream(stream), variant))
+
+
+def _record_tables(records, batch):
+    """int32 arrays of a record list [(l0, l1, seq_start, seq_end), ...]: the
+    layer pairs, and per record the starts then the ends."""
+    n = len(records)
+    layers = np.empty(2 * n, np.int32)
+    ranges = np.empty(2 * batch * n, np.int32)
+    for i, (l0, l1, s, e) in enumerate(records):
+        s = np.asarray(s, dtype=np.int32).reshape(-1)
+        e = np.asarray(e, dtype=np.int32).reshape(-1)
+        if s.size != batch or e.size != batch:
+            raise ValueError(f"record {i}: seq_start / seq_end need {batch} entries")
+        layers[2 * i:2 * i + 2] = (l0, l1)
+        ranges[2 * batch * i:2 * batch * i + batch] = s
+        ranges[2 * batch * i + batch:2 * batch * (i + 1)] = e
+    return layers, ranges
+
+
+def dv_kv_unpack_records(cache: Cache, records, src, stream=None, src_bytes=None) -> None:
+    """Unpacks log records [(l0, l1, seq_start, seq_end), ...] lying back to
+    back in ``src`` (device or pinned host memory), as dv_kv_unpack of each in
+    order."""
+    d, n = _buf(src, src_bytes)
+    if not records:
+        _check(_unpack_records(cache.ref, 0, None, None, d, n, _stream(stream)))
+        return
+    layers, ranges = _record_tables(records, cache.c.batch)
+    lp, layers = _addr(layers)
+    rp, ranges = _addr(ranges)
+    _check(_unpack_records(cache.ref, len(records), lp, rp, d, n, _stream(stream)))
 
 
 def dv_naive_gather(cache: Cache, l0, l1, seq_start, seq_end, dst, stream=None,

@@ -82,25 +82,39 @@ def _make_finite(elems: np.ndarray, kind: str) -> np.ndarray:
 _UINT = {1: np.uint8, 2: np.uint16, 4: np.uint32, 8: np.uint64}
 
 
-def fill_bytes(seed: int, kv: int, nbytes: int, kind: str = "fp16") -> np.ndarray:
-    """The whole fill of one cache tensor of ``nbytes`` bytes, as uint8."""
-    if nbytes % 8:
+def fill_bytes(seed: int, kv: int, nbytes: int, kind: str = "fp16", offset: int = 0,
+               threads: int = 1) -> np.ndarray:
+    """Bytes [offset, offset + nbytes) of the fill of one cache tensor, as
+    uint8 (offset and nbytes whole 64-bit words).  threads > 1 splits the
+    blocks over that many threads (numpy releases the interpreter lock)."""
+    if nbytes % 8 or offset % 8:
         raise ValueError("cache tensors are a whole number of 64-bit words")
     base = stream_base(seed, kv)
     out = np.empty(nbytes, dtype=np.uint8)
-    step = 1 << 24  # words per block, bounds the temporaries
+    step = 1 << 22  # words per block, bounds the temporaries
     nwords = nbytes // 8
-    for w0 in range(0, nwords, step):
+    w_off = offset // 8
+
+    def block(w0):
         w1 = min(nwords, w0 + step)
-        words = _words(base, np.arange(w0, w1, dtype=np.uint64))
+        words = _words(base, np.arange(w_off + w0, w_off + w1, dtype=np.uint64))
         out[8 * w0: 8 * w1] = words.view(np.uint8) if words.dtype.byteorder in "=<" else \
             words.astype("<u8").view(np.uint8)
-    if kind in FINITE_MASKS:
-        emask, ebit, esize = FINITE_MASKS[kind]
-        view = out.view(_UINT[esize])
-        t = view.dtype.type
-        bad = (view & t(emask)) == t(emask)
-        view[bad] &= t(~ebit & ((1 << (8 * esize)) - 1))
+        if kind in FINITE_MASKS:
+            emask, ebit, esize = FINITE_MASKS[kind]
+            view = out[8 * w0: 8 * w1].view(_UINT[esize])
+            t = view.dtype.type
+            bad = (view & t(emask)) == t(emask)
+            view[bad] &= t(~ebit & ((1 << (8 * esize)) - 1))
+
+    starts = range(0, nwords, step)
+    if threads > 1 and nwords > step:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(block, starts))
+    else:
+        for w0 in starts:
+            block(w0)
     return out
 
 

@@ -103,3 +103,55 @@ def assert_prefix_equal_rest_zero(g, got, want, lengths):
         assert torch.equal(gv[:, b, :, :n, :], wv[:, b, :, :n, :]), f"V of sequence {b}"
         assert not gk[:, b, :, :, n:, :].any(), f"K of sequence {b} written past {n}"
         assert not gv[:, b, :, n:, :].any(), f"V of sequence {b} written past {n}"
+
+
+def layer_geometry(g):
+    """The one-layer geometry of g's layers (the oracle's unit of work for
+    full-size comparisons, layer by layer)."""
+    from dataclasses import replace
+    return replace(g, name=g.name + "-layer", num_layers=1)
+
+
+def host_layer(g, seed, l, threads=4):
+    """Bytes of layer l of the seeded cache of geometry g (K, V), computed on
+    the host: the generator's fill of the tensor from layer l's first byte."""
+    lb = g.layer_elems * g.elem_bytes
+    g1 = layer_geometry(g)
+    return (synth.fill_bytes(seed, 0, g1.tensor_bytes, g.kind, offset=l * lb, threads=threads),
+            synth.fill_bytes(seed, 1, g1.tensor_bytes, g.kind, offset=l * lb, threads=threads))
+
+
+def layer_workers(per_worker_bytes, most=4):
+    """How many layers to compare at once: up to `most`, as host memory
+    allows (MemAvailable, with a quarter kept free)."""
+    avail = 0
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    avail = int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return max(1, min(most, int(0.75 * avail) // max(per_worker_bytes, 1)))
+
+
+def for_each_layer(fn, layers, per_worker_bytes):
+    """Runs fn(l) for every layer in `layers`, several at once on threads (the
+    oracle's C calls and numpy release the interpreter lock); re-raises the
+    first failure."""
+    from concurrent.futures import ThreadPoolExecutor
+    workers = layer_workers(per_worker_bytes)
+    if workers == 1:
+        for l in layers:
+            fn(l)
+        return
+    with ThreadPoolExecutor(workers) as ex:
+        for r in [ex.submit(fn, l) for l in layers]:
+            r.result()
+
+
+def device_layer(g, cache, l):
+    """Layer l of a device cache (K, V bytes) copied to host numpy arrays."""
+    lb = g.layer_elems * g.elem_bytes
+    return (cache.k[l * lb:(l + 1) * lb].cpu().numpy(),
+            cache.v[l * lb:(l + 1) * lb].cpu().numpy())

@@ -226,3 +226,108 @@ def test_errors_enqueue_nothing():
     assert ei.value.status == dv.DV_ERR_INVALID_ARG
     assert not H.to_np(z.k).any() and not H.to_np(z.v).any()
     assert not H.to_np(zo.k).any() and not H.to_np(zo.v).any()
+
+
+def decode_run_log(g, seed, steps, finish_at=None, rng=None):
+    """Snapshot, then `steps` one-token deltas of every live sequence (a run of
+    one-token records for the run kernel); at step `finish_at` every third
+    sequence finishes (the run breaks and a new one starts with fewer
+    sequences)."""
+    rng = rng or np.random.default_rng(seed)
+    B, S, L = g.batch, g.max_seq, g.num_layers
+    zero = np.zeros(B, np.int32)
+    pos = rng.integers(0, S - steps, size=B).astype(np.int32)
+    full = ORC.staging_bytes(g, 0, L, zero, np.full(B, S, np.int32))
+    log = Log(g, seed, 2 * full)
+    log.append(0, L, zero, pos)
+    live = np.ones(B, bool)
+    for k in range(steps):
+        if finish_at is not None and k == finish_at:
+            live[::3] = False
+            if not live.any():
+                live[-1] = True
+        act = live.astype(np.int32)
+        log.append(0, L, pos, pos + act)
+        pos = pos + act
+    return log
+
+
+RUN_GEOMS = GEOMS + [
+    Geometry("c16-long", 2, 3, 2, 128, 400, 2, "bf16"),   # TB = 64: runs over several blocks
+    Geometry("c8-long", 2, 2, 3, 64, 400, 2, "fp16"),     # TB = 128
+]
+
+
+@pytest.mark.parametrize("g", RUN_GEOMS, ids=lambda g: g.name)
+def test_runs_of_one_token_records(g):
+    """Runs of one-token decode deltas (the run kernel): long runs crossing
+    token blocks, a run broken where sequences finish, fused, staged with a
+    buffer that cuts the runs into pieces of 37 records, and through a
+    fetcher whose slots hold 37 or 1 records."""
+    steps = min(g.max_seq - 2, 150)
+    log = decode_run_log(g, 707, steps, finish_at=steps // 3)
+    one = log.records[1][4].size
+    log.check()
+    log.check(staging_bytes=log.rep.info()[1])
+    log.check(staging_bytes=max(min_staging(log), 37 * one))
+    log.check(slot_bytes=max(min_staging(log), 37 * one))
+    log.check(slot_bytes=max(min_staging(log), one), upto=20)
+    log.check(upto=steps // 3 + 5)
+
+
+def test_run_lengths_around_the_token_block():
+    """Runs of every length near the tile's token block (64 tokens at head_dim
+    128, 2-byte elements), each followed by a record that breaks the run."""
+    g = Geometry("runlen", 2, 4, 2, 128, 700, 2, "fp16")
+    B = g.batch
+    zero = np.zeros(B, np.int32)
+    log = Log(g, 808, 2 * ORC.staging_bytes(g, 0, 2, zero, np.full(B, 700, np.int32)))
+    pos = np.array([0, 5, 63, 64], np.int32)
+    for n in (1, 2, 3, 63, 64, 65, 127, 129):
+        for k in range(n):
+            log.append(0, 2, pos, pos + 1)
+            pos = pos + 1
+        log.append(0, 2, pos, pos + np.array([1, 0, 1, 0], np.int32))   # breaks the run
+        pos = pos + np.array([1, 0, 1, 0], np.int32)
+    assert pos.max() <= 700
+    log.check()
+    log.check(staging_bytes=log.rep.info()[1])
+
+
+@pytest.mark.parametrize("where", ["device", "host"])
+def test_unpack_records_matches_oracle(where):
+    """dv_kv_unpack_records of a log held in device memory or pinned host
+    memory: the standard log (snapshot, deltas, ragged, empty and overlapping
+    records) and a decode run, against the oracle's in-order unpack."""
+    for g, log in ((GEOMS[0], standard_log(GEOMS[0], 909)),
+                   (GEOMS[1], decode_run_log(GEOMS[1], 910, 90, finish_at=40))):
+        records = [(l0, l1, s, e) for l0, l1, s, e, _ in log.records]
+        data = np.concatenate([d for *_, d in log.records])
+        src = torch.from_numpy(data)
+        src = src.cuda() if where == "device" else src.pin_memory()
+        z = H.device_cache(g, fill="zero")
+        torch.cuda.synchronize()
+        dv.dv_kv_unpack_records(z, records, src)
+        kw, vw = ORC.restore(g, log.records)
+        assert np.array_equal(H.to_np(z.k), kw), g.name
+        assert np.array_equal(H.to_np(z.v), vw), g.name
+
+
+def test_unpack_records_errors_enqueue_nothing():
+    g = GEOMS[0]
+    log = decode_run_log(g, 911, 20)
+    records = [(l0, l1, s, e) for l0, l1, s, e, _ in log.records]
+    data = torch.from_numpy(np.concatenate([d for *_, d in log.records])).cuda()
+    z = H.device_cache(g, fill="zero")
+    torch.cuda.synchronize()
+    with pytest.raises(dv.DvError) as ei:          # one byte short
+        dv.dv_kv_unpack_records(z, records, data, src_bytes=data.numel() - 16)
+    assert ei.value.status == dv.DV_ERR_BUFFER_TOO_SMALL
+    bad = list(records)
+    l0, l1, s, e = bad[5]
+    bad[5] = (l0, l1, s, e + g.max_seq)            # a range past the cache
+    with pytest.raises(dv.DvError) as ei:
+        dv.dv_kv_unpack_records(z, bad, data)
+    assert ei.value.status == dv.DV_ERR_RANGE
+    assert not H.to_np(z.k).any() and not H.to_np(z.v).any()
+    dv.dv_kv_unpack_records(z, [], None)           # nothing to do

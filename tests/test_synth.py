@@ -54,3 +54,14 @@ def test_workload_draws_are_seeded_and_in_range():
     l5 = configs.bloom_lengths()
     assert l5.min() >= 64 and l5.max() <= 1536
     assert (l5 + configs.BLOOM_DECODE_STEPS).max() <= configs.BLOOM_STAGE.max_seq
+
+
+def test_fill_bytes_offset_and_threads_give_the_same_bytes():
+    """A window [offset, offset + n) of the fill equals that slice of the whole
+    fill, and the threaded fill equals the serial one."""
+    for kind in ("fp16", "bf16", "raw"):
+        whole = synth.fill_bytes(11, 0, 1 << 22, kind)
+        for off, n in ((0, 4096), (8, 800), (1 << 20, 1 << 20), ((1 << 22) - 64, 64)):
+            assert np.array_equal(synth.fill_bytes(11, 0, n, kind, offset=off), whole[off:off + n])
+        big = synth.fill_bytes(12, 1, 3 << 25, kind, offset=1 << 21)
+        assert np.array_equal(synth.fill_bytes(12, 1, 3 << 25, kind, offset=1 << 21, threads=4), big)
