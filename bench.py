@@ -84,7 +84,8 @@ def parse_args():
                     choices=["tile-pack", "tile-unpack", "delta-pack", "delta-unpack",
                              "flat-pack", "flat-unpack", "record-restore", "swap-out",
                              "swap-in", "ragged-pack", "ragged-unpack", "delta-graph-pack",
-                             "delta-graph-unpack"],
+                             "delta-graph-unpack", "bloom-snapshot-pack",
+                             "bloom-snapshot-unpack", "bloom-delta-pack", "bloom-run-restore"],
                     help="run one kernel of the step on an 8-layer cache of the workload's "
                          "shape, 5 launches, and exit (a small case for profilers); "
                          "flat-*: ragged 16..64-token ranges of the OPT-13B-shaped cache, "
@@ -95,7 +96,10 @@ def parse_args():
                          "workload's lognormal used prefixes, 4 layers, tile kernel; "
                          "delta-graph-*: a CUDA graph of 32 one-token deltas 8 tokens apart "
                          "on a BLOOM-stage-shaped cache cut to 4 layers and max_seq 512, "
-                         "5 replays (for graph-level counters)")
+                         "5 replays (for graph-level counters); bloom-*: the headline "
+                         "step's kernels on its workload cut to 2 layers and batch 16 "
+                         "(snapshot pack / unpack: 3 launches; delta pack: 8 launches, 8 "
+                         "tokens apart; run restore: 3 launches of 256 one-token records)")
     return ap.parse_args()
 
 
@@ -939,14 +943,16 @@ def naive_vs_buffered(torch, dv, reps=3):
 
 
 class DecodeStreaming:
-    """Decode steps with the step's delta streamed to a host replica (§3 "Token
-    computation and streaming parallelization", Fig 7c).  A decode step is a
-    stand-in compute (a full read of the cache's K and V, as attention reads
-    them, reduced on the device) followed by the decode write of the new token
-    (an unpack of a seeded one-token buffer).  The delta of step i is packed
-    straight into pinned host memory, either on the compute stream after the
-    step ("inline") or on a side stream that waits only for step i's write
-    ("overlapped"), so that it runs while step i+1 computes.  Each mode's
+    """Decode steps with each step's delta streamed to a host replica (§3
+    "Token computation and streaming parallelization", Fig 7c), on the
+    GPT2-1.5B-shaped cache.  A decode step is a stand-in compute (a full read
+    of the cache's K and V, as attention reads them, reduced on the device)
+    followed by the decode write of the new token (an unpack of a seeded
+    one-token buffer).  Modes: "compute_only"; "inline", each delta appended
+    (dv_replica_append, the pack storing straight into pinned memory) on the
+    compute stream after its step; "overlapped", each delta streamed by the
+    library's dv_delta_streamer on a side stream that waits only for its own
+    step's write, so that it runs while the next step computes.  Each mode's
     `steps` decode steps are one CUDA graph."""
 
     def __init__(self, torch, dv, steps=GPT2_DECODE_STEPS):
@@ -961,11 +967,11 @@ class DecodeStreaming:
         self.dsz = dv.dv_staging_bytes(self.cache, 0, g.num_layers, *self.deltas[0])
         self.tokens = torch.empty(steps * self.dsz, dtype=torch.uint8, device="cuda")
         synth_gpu.fill_tensor(self.tokens, 777, 0, g.kind)
-        self.host = torch.empty(steps * self.dsz, dtype=torch.uint8, pin_memory=True)
+        self.arena = torch.empty(steps * self.dsz, dtype=torch.uint8, pin_memory=True)
+        self.replica = dv.Replica(self.arena, g.batch)
         self.acc = torch.zeros(1, dtype=torch.int64, device="cuda")
         self.kv32 = (self.k.view(torch.int32), self.v.view(torch.int32))
         self.s_side = torch.cuda.Stream()
-        self.events = [torch.cuda.Event() for _ in range(steps)]
 
     def _compute_and_write(self, i, s):
         torch, dv, g = self.torch, self.dv, self.g
@@ -974,34 +980,34 @@ class DecodeStreaming:
         tok = self.tokens[i * self.dsz:(i + 1) * self.dsz]
         dv.dv_kv_unpack(self.cache, 0, g.num_layers, a, b, tok, stream=s)
 
-    def run(self, mode, s):
-        """Enqueues `steps` decode steps on stream `s` (inside a capture or not)."""
-        dv, g = self.dv, self.g
-        hp = self.host.data_ptr()
+    def run(self, mode, s, ds=None):
+        """Enqueues `steps` decode steps on stream `s` (inside a capture or
+        not); `ds` is the delta streamer of the overlapped mode."""
+        g = self.g
         for i in range(self.steps):
             self._compute_and_write(i, s)
             a, b = self.deltas[i]
-            dst = (hp + i * self.dsz, self.dsz)
             if mode == "inline":
-                dv.dv_kv_pack(self.cache, 0, g.num_layers, a, b, dst, stream=s)
+                self.replica.append(self.cache, 0, g.num_layers, a, b, step=i, stream=s)
             elif mode == "overlapped":
-                self.events[i].record(s)
-                self.s_side.wait_event(self.events[i])
-                dv.dv_kv_pack(self.cache, 0, g.num_layers, a, b, dst, stream=self.s_side)
+                ds.stream(self.cache, 0, g.num_layers, a, b, step=i)
         if mode == "overlapped":
-            s.wait_stream(self.s_side)
+            ds.join()
 
     def measure(self, reps=5):
         torch = self.torch
         s = torch.cuda.Stream()
+        ds = self.dv.DeltaStreamer(self.replica, s, self.s_side)
         out = {}
         for mode in ("compute_only", "inline", "overlapped"):
+            self.replica.truncate(0)
             with torch.cuda.stream(s):
-                self.run(mode, s)
+                self.run(mode, s, ds)
             torch.cuda.synchronize()
+            self.replica.truncate(0)
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=s, capture_error_mode="relaxed"):
-                self.run(mode, s)
+                self.run(mode, s, ds)
             ts = []
             with torch.cuda.stream(s):
                 for r in range(reps + 1):
@@ -1015,13 +1021,16 @@ class DecodeStreaming:
                         ts.append(a.elapsed_time(b))
             out[mode] = statistics.median(ts) / self.steps
             del graph
-        same = bool(torch.equal(self.host.cuda(), self.tokens))
+        same = bool(torch.equal(self.arena.cuda(), self.tokens))
+        ds.close()
         base = out["compute_only"]
         return {"steps": self.steps, "delta_bytes": self.dsz,
                 "step_ms": {k: round(v, 4) for k, v in out.items()},
                 "overhead_inline": round(out["inline"] / base - 1, 4),
                 "overhead_overlapped": round(out["overlapped"] / base - 1, 4),
-                "replica_equals_written_tokens": same}
+                "replica_equals_written_tokens": same,
+                "path": "dv_delta_streamer (side stream) against dv_replica_append on the "
+                        "compute stream"}
 
 
 class MicrobatchSwapping:
@@ -1030,16 +1039,18 @@ class MicrobatchSwapping:
     cache lives in a host replica (a snapshot of its prompt cache plus one
     record per decode step: the swap-out is delta-only).  A round processes
     the microbatches in turn: swap-in (restore snapshot + deltas into a device
-    slot, copy engine + unpack), a stand-in compute (a read of the used bytes
-    of the slot, as attention reads them) and the decode write of one token
+    cache, copy engine + unpack), a stand-in compute (a read of the used bytes
+    of the cache, as attention reads them) and the decode write of one token
     per active sequence, then the swap-out of that token (a one-token pack
     straight into the replica).
-      serial: one device slot, everything in order on one stream.
-      double: two slots (the pages' 2*M); while microbatch x computes in one
-              slot, the other slot takes x-1's swap-out and then x+1's
-              swap-in on a second, high-priority stream, ordered by events."""
+      serial: one device cache, everything in order on one stream (swap-ins
+              through a fetcher whose unpacks run on that stream).
+      double: the library's dv_swapper over two caches (the pages' 2*M):
+              while microbatch x computes in one cache, x+1 is swapped in to
+              the other on high-priority streams, and x's update is swapped
+              out after its compute."""
 
-    def __init__(self, torch, dv, rounds=8, keep_refs=False):
+    def __init__(self, torch, dv, rounds=8):
         from synth import gpu as synth_gpu
         from synth.configs import OPT66B_STAGE, opt66b_microbatches
         self.torch, self.dv, self.rounds = torch, dv, rounds
@@ -1054,11 +1065,9 @@ class MicrobatchSwapping:
             torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")) for _ in range(2)]
         self.per_token = dv.dv_staging_bytes(self.slots[0], 0, L, self.zs,
                                              np.ones(g.batch, np.int32)) // g.batch
-        self.staging = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
         self.fslots = (torch.empty(256 << 20, dtype=torch.uint8, device="cuda"),
                        torch.empty(256 << 20, dtype=torch.uint8, device="cuda"))
-        self.refs = []
-        self.replicas, self.arenas, self.lens, self.seeds = [], [], [], []
+        self.replicas, self.arenas, self.lens = [], [], []
         for m, (p, o) in enumerate(self.mbs):
             seed = seed_of(4) * 10 + m
             cap = int((p.sum() + g.batch * (rounds + 1)) * self.per_token)  # + per_op's
@@ -1067,22 +1076,17 @@ class MicrobatchSwapping:
             slot = self.slots[0]
             synth_gpu.fill_cache(g, slot.k, slot.v, seed)
             rep.append(slot, 0, L, self.zs, p, step=0)  # the prompt cache arrives
-            if keep_refs:
-                k2 = slot.k.clone()
-                v2 = slot.v.clone()
-                self.refs.append(dv.Cache.from_geometry(g, k2, v2))
             torch.cuda.synchronize()
             self.arenas.append(arena)
             self.replicas.append(rep)
             self.lens.append(p.copy())
-            self.seeds.append(seed)
         self.step_no = [1] * self.N
         self.tok = torch.empty(g.batch * self.per_token, dtype=torch.uint8, device="cuda")
         self.acc = torch.zeros(1, dtype=torch.int64, device="cuda")
 
     def _compute_and_write(self, m, slot, s):
         """Stand-in compute on stream s, then the decode write of microbatch m's
-        next token into `slot` and the delta appended to its replica."""
+        next token into `slot`; returns the active sequences."""
         torch, dv, g = self.torch, self.dv, self.g
         p, o = self.mbs[m]
         ln = self.lens[m]
@@ -1097,14 +1101,10 @@ class MicrobatchSwapping:
             with torch.cuda.stream(s):
                 self.synth_gpu.fill_tensor(tok, 1000 * m + self.step_no[m], 0, g.kind, s)
             dv.dv_kv_unpack(slot, 0, g.num_layers, ln, ln + act, tok, stream=s)
-            if self.refs:
-                dv.dv_kv_unpack(self.refs[m], 0, g.num_layers, ln, ln + act, tok, stream=s)
         return act
 
     def run(self, mode, s, s2=None, s3=None):
-        """`rounds` rounds over the N microbatches; returns the seconds taken.
-        Swap-ins are replica restores pipelined through a fetcher: its copies
-        on one stream, its unpacks on another (serial: the compute stream)."""
+        """`rounds` rounds over the N microbatches; returns the seconds taken."""
         torch, dv, g = self.torch, self.dv, self.g
         L = g.num_layers
         torch.cuda.synchronize()
@@ -1123,68 +1123,26 @@ class MicrobatchSwapping:
                                             stream=s)
                     self.lens[m] = ln + act
                     self.step_no[m] += 1
-            self.last = (0, self.N - 1)
+            torch.cuda.synchronize()
+            fetcher.close()
         else:
-            ready = [torch.cuda.Event() for _ in range(2)]
-            done = [torch.cuda.Event() for _ in range(2)]
-            order = [m for _ in range(self.rounds) for m in range(self.N)]
-            # copies on s2 (after the swap-outs queued there), unpacks on s3
             fetcher = dv.Fetcher(self.fslots[0], self.fslots[1], s2, s3)
-            # prefetch the first microbatch into slot 0
-            self.replicas[order[0]].restore_fetched(self.slots[0], fetcher)
-            ready[0].record(s3)
+            sw = dv.Swapper(self.slots[0], self.slots[1], fetcher, s, s2)
+            order = [m for _ in range(self.rounds) for m in range(self.N)]
             for i, m in enumerate(order):
-                sl = i % 2
-                slot = self.slots[sl]
-                s.wait_event(ready[sl])
-                act = self._compute_and_write(m, slot, s)
-                done[sl].record(s)
-                if i + 1 < len(order):  # the next microbatch comes in on the other slot
-                    nxt = order[i + 1]
-                    self.replicas[nxt].restore_fetched(self.slots[1 - sl], fetcher)
-                    ready[1 - sl].record(s3)
-                # swap-out of this microbatch's step: its token, into its replica
-                s2.wait_event(done[sl])
+                sl = sw.acquire(self.replicas[m])
+                if i + 1 < len(order):  # the next microbatch comes in to the other cache
+                    sw.prefetch(self.replicas[order[i + 1]])
+                act = self._compute_and_write(m, self.slots[sl], s)
                 ln = self.lens[m]
-                self.replicas[m].append(slot, 0, L, ln, ln + act, step=self.step_no[m],
-                                        stream=s2)
+                sw.release(self.replicas[m], 0, L, ln, ln + act, step=self.step_no[m])
                 self.lens[m] = ln + act
                 self.step_no[m] += 1
-                # the slot is refilled two microbatches later, after this append
-            s.wait_stream(s2)
-            s.wait_stream(s3)
-            self.last = ((len(order) - 1) % 2, order[-1])
-        torch.cuda.synchronize()
-        fetcher.close()
-        return time.perf_counter() - t0
-
-    def check(self):
-        """The slot the last microbatch step ran in (swapped in during the run,
-        then written) and each replica restored into a zeroed slot equal the
-        reference cache on the used prefix (needs keep_refs)."""
-        torch, dv, g = self.torch, self.dv, self.g
-        L = g.num_layers
-
-        def same(slot, m):
-            n = dv.dv_staging_bytes(slot, 0, L, self.zs, self.lens[m])
-            a = torch.empty(n, dtype=torch.uint8, device="cuda")
-            b = torch.empty(n, dtype=torch.uint8, device="cuda")
-            dv.dv_kv_pack(slot, 0, L, self.zs, self.lens[m], a)
-            dv.dv_kv_pack(self.refs[m], 0, L, self.zs, self.lens[m], b)
+            sw.wait()
             torch.cuda.synchronize()
-            return bool(torch.equal(a, b))
-
-        sl, m_last = self.last
-        if not same(self.slots[sl], m_last):
-            return False
-        for m in range(self.N):
-            slot = self.slots[0]
-            slot.k.zero_()
-            slot.v.zero_()
-            self.replicas[m].restore(slot, staging=self.staging)
-            if not same(slot, m):
-                return False
-        return True
+            sw.close()
+            fetcher.close()
+        return time.perf_counter() - t0
 
     def reset(self):
         """Back to the prompt caches: every replica keeps its snapshot only."""
@@ -1767,6 +1725,9 @@ def run_kernel_case(case):
     if case.startswith("delta-graph"):
         run_delta_graph_case(case, torch, dv, synth_gpu)
         return
+    if case.startswith("bloom"):
+        run_bloom_case(case, torch, dv, synth_gpu)
+        return
     g = replace(GPT2, num_layers=8)
     k = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
     v = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
@@ -1881,6 +1842,53 @@ def run_delta_graph_case(case, torch, dv, synth_gpu):
         graph.replay()
     torch.cuda.synchronize()
     print(f"{case}: 5 replays of a graph of {nd} deltas of {one} bytes each")
+
+
+def run_bloom_case(case, torch, dv, synth_gpu):
+    """The headline step's kernels on its workload (BLOOM-176B stage, bf16,
+    112 heads, head_dim 128, max_seq 2048, len0 uniform in [64, 1536]) cut to
+    2 of the 14 layers and the first 16 of the 32 sequences: 3.8 GB of cache,
+    1.4 GB of snapshot staging (inputs larger than L2, a few GB on the device).
+    Traffic per launch scales to the full step's launch by the bytes moved."""
+    from dataclasses import replace
+    g = replace(BLOOM_STAGE, num_layers=2, batch=16)
+    L = g.num_layers
+    k = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+    v = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+    synth_gpu.fill_cache(g, k, v, seed_of(5))
+    cache = dv.Cache.from_geometry(g, k, v)
+    len0 = bloom_lengths()[:g.batch]
+    zs = np.zeros(g.batch, np.int32)
+    if case in ("bloom-snapshot-pack", "bloom-snapshot-unpack"):
+        n = dv.dv_staging_bytes(cache, 0, L, zs, len0)
+        stg = torch.empty(n, dtype=torch.uint8, device="cuda")
+        dv.dv_kv_pack(cache, 0, L, zs, len0, stg)
+        for _ in range(3):
+            if case.endswith("-pack"):
+                dv.dv_kv_pack(cache, 0, L, zs, len0, stg)
+            else:
+                dv.dv_kv_unpack(cache, 0, L, zs, len0, stg)
+        torch.cuda.synchronize()
+        print(f"{case}: 3 launches of {2 * n} algorithmic bytes each")
+        return
+    nd = BLOOM_DECODE_STEPS
+    one = dv.dv_staging_bytes(cache, 0, L, len0, len0 + 1)
+    log = torch.empty(nd * one, dtype=torch.uint8, device="cuda")
+    lp = log.data_ptr()
+    for j in range(nd):
+        dv.dv_kv_pack(cache, 0, L, len0 + j, len0 + j + 1, (lp + j * one, one))
+    if case == "bloom-delta-pack":
+        for j in range(0, 64, 8):
+            dv.dv_kv_pack(cache, 0, L, len0 + j, len0 + j + 1, (lp + j * one, one))
+        torch.cuda.synchronize()
+        print(f"{case}: 8 launches of {2 * one} algorithmic bytes each")
+        return
+    back = dv.Cache.from_geometry(g, torch.zeros_like(k), torch.zeros_like(v))
+    records = [(0, L, len0 + j, len0 + j + 1) for j in range(nd)]
+    for _ in range(3):
+        dv.dv_kv_unpack_records(back, records, log)
+    torch.cuda.synchronize()
+    print(f"{case}: 3 launches of {2 * nd * one} algorithmic bytes each ({nd} records)")
 
 
 def run_record_case(torch, dv, synth_gpu):

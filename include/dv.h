@@ -21,6 +21,13 @@
  *                    per-step decode deltas (§3 "Token computation and
  *                    streaming parallelization", Fig 7c) appended to a
  *                    host-side replica, and the restore of a cache from it.
+ *   dv_kv_unpack_records  the scatter of a whole log of records at once.
+ *   dv_swapper_*     §3 "Microbatch swapping" (Fig 9): N microbatches
+ *                    through two device caches, the next swapped in while
+ *                    one computes, each step's update swapped out after it.
+ *   dv_delta_*       §3 "Token computation and streaming parallelization"
+ *                    (Fig 7c): each step's delta streamed on a side stream
+ *                    while the next step computes.
  *
  * Cache layout (the FasterTransformer-style layout the pages build on).  Per
  * layer, with x = 16 / elem_bytes elements per 16-byte chunk:
@@ -209,14 +216,25 @@ dv_status dv_naive_gather(const dv_cache* cache, int32_t l0, int32_t l1,
  *    host_dst over the host link (one launch, no device buffer).
  *  - staging != NULL: staged path, groups of whole layers are packed into
  *    `staging` (device, staging_bytes >= one layer's slab) and copied to
- *    the host with cudaMemcpyAsync, all in order on `stream`. */
+ *    the host with cudaMemcpyAsync.  When staging holds two layer slabs or
+ *    more, it is used in two halves: the pack of one group (on `stream`)
+ *    overlaps the copy of the other, which runs on a copy stream the library
+ *    owns (one per CUDA context, made on the first such call there: make it
+ *    outside a stream capture), ordered by events; the work is complete in
+ *    `stream`'s order when it returns.  With room for one slab only,
+ *    everything runs in order on `stream`.
+ *  Should a launch or copy fail partway (DV_ERR_CUDA), the groups before it
+ *  stay enqueued; validation failures enqueue nothing. */
 dv_status dv_swap_out(const dv_cache* cache, int32_t l0, int32_t l1, const int32_t* seq_start,
                       const int32_t* seq_end, void* host_dst, size_t host_bytes, void* staging,
                       size_t staging_bytes, dv_stream stream);
 
 /* Swap-in (§3 microbatch swapping; Table 1 fetch + scatter).  The inverse of
  * dv_swap_out: host_src holds staging bytes; staging == NULL unpacks straight
- * from host memory, otherwise layer groups go host -> staging -> cache. */
+ * from host memory, otherwise layer groups go host -> staging -> cache, in
+ * two halves as for dv_swap_out (the copy of one group, on the library's copy
+ * stream after the work enqueued on `stream` so far, overlaps the unpack of
+ * the other on `stream`). */
 dv_status dv_swap_in(const dv_cache* cache, int32_t l0, int32_t l1, const int32_t* seq_start,
                      const int32_t* seq_end, const void* host_src, size_t host_bytes,
                      void* staging, size_t staging_bytes, dv_stream stream);
@@ -240,12 +258,15 @@ dv_status dv_swap_in(const dv_cache* cache, int32_t l0, int32_t l1, const int32_
  *  - The buffer is DV_NOALLOC_STAGING_BYTES (64 MiB) of device memory that
  *    every GPU loading libdv holds until the process exits.  Layers are
  *    packed into it in groups and copied to host_dst, as on dv_swap_out's
- *    staged path, so the whole swap may be larger; one layer of the ranges
+ *    staged path (in two halves when each holds a layer), so the whole swap
+ *    may be larger; one layer of the ranges
  *    larger than 64 MiB is refused with DV_ERR_BUFFER_TOO_SMALL before
  *    anything is enqueued.
- *  - The first call on a device looks up the buffer's device address on the
- *    current device (cudaGetSymbolAddress); make that first call on each
- *    device before any stream capture.
+ *  - The first call in a CUDA context looks up the buffer's device address
+ *    there (cudaGetSymbolAddress, with the context current) and keeps it for
+ *    that context; a device reset or another context gets a lookup of its
+ *    own.  Make the first call in each context before any stream capture
+ *    (the staged path may also create its copy stream then).
  *  - All calls share the one buffer, which keeps the last call's bytes
  *    (nothing in it needs to start at zero: each group is packed in full
  *    before it is copied).  Calls whose work overlaps on the GPU (on
@@ -385,6 +406,93 @@ dv_status dv_replica_truncate(dv_replica* replica, int64_t step);
 dv_status dv_replica_info(const dv_replica* replica, int64_t* num_records, size_t* bytes_used);
 
 void dv_replica_destroy(dv_replica* replica);
+
+/* ---- microbatch swapping through two device caches (§3 "Microbatch
+ * swapping", Fig 9) -------------------------------------------------------- */
+
+/* N microbatches share two device caches of one geometry (the pages' 2*M of
+ * GPU memory for a stage).  Each microbatch lives in host memory as a replica
+ * (dv_replica: a snapshot of its prompt cache, then one record per decode
+ * step).  While microbatch x computes in one cache, the next one, (x+1) % N,
+ * is swapped in to the other cache, and the update of x's step is swapped
+ * out after its compute: swap-in = the replica restored through a fetcher
+ * (dv_replica_restore_fetched, on the fetcher's copy and unpack streams),
+ * swap-out = the step's delta appended to the replica (dv_replica_append,
+ * fused, on the swap stream).  A swap-in writes the microbatch's recorded
+ * slices only; the rest of the cache keeps what an earlier microbatch left.
+ *
+ * Use, per step of microbatch x:  dv_swapper_acquire(x) -> the cache to
+ * compute in;  dv_swapper_prefetch(next);  the step's kernels on the compute
+ * stream;  dv_swapper_release(x, the slices the step wrote, step).  No call
+ * blocks the host.  The caller orders earlier work on the two caches before
+ * the first call.  Borrows the caches, the fetcher and the streams; owns six
+ * events.  Not for two threads at once. */
+typedef struct dv_swapper dv_swapper;
+
+dv_status dv_swapper_create(dv_swapper** out, const dv_cache* slot0, const dv_cache* slot1,
+                            dv_fetcher* fetcher, dv_stream compute_stream, dv_stream swap_stream);
+
+/* Makes microbatch `mb` resident for its next step.  If it was prefetched (or
+ * is still in a cache from its last step), the compute stream waits for that
+ * swap-in; otherwise it is swapped in now to the cache the previous step did
+ * not use, and the compute stream waits for that.  *slot receives the cache
+ * (0 or 1) that holds it.  DV_ERR_INVALID_ARG while another microbatch is
+ * acquired and not released. */
+dv_status dv_swapper_acquire(dv_swapper* sw, const dv_replica* mb, int32_t* slot);
+
+/* Swaps microbatch `mb` in to the cache the current step does not use, on
+ * the fetcher's streams, as soon as that cache's last step and swap-out are
+ * done (no host wait).  A no-op when `mb` is already in a cache. */
+dv_status dv_swapper_prefetch(dv_swapper* sw, const dv_replica* mb);
+
+/* Ends the acquired microbatch's step: after everything enqueued so far on
+ * the compute stream, the slices of (l0, l1, ranges) of its cache (the
+ * token the step wrote) are appended to its replica as the record of `step`,
+ * on the swap stream; the cache is free for a prefetch once that append has
+ * read it.  Errors of dv_replica_append, checked before anything is
+ * enqueued. */
+dv_status dv_swapper_release(dv_swapper* sw, dv_replica* mb, int32_t l0, int32_t l1,
+                             const int32_t* seq_start, const int32_t* seq_end, int64_t step);
+
+/* Blocks the calling thread until every swap issued so far has finished. */
+dv_status dv_swapper_wait(dv_swapper* sw);
+
+void dv_swapper_destroy(dv_swapper* sw);
+
+/* ---- decode deltas streamed beside the compute (§3 "Token computation and
+ * streaming parallelization", Fig 7c) -------------------------------------- */
+
+/* Streams each decode step's delta to a host replica on a side stream while
+ * the compute stream goes on with the next step: the pages stream step i's
+ * cache while step i+1 computes, with the GPU side on its own CUDA stream.
+ * staging: NULL (the pack stores straight into the replica's pinned arena) or
+ * a device buffer of at least one layer slab of a delta.  Borrows the replica,
+ * the streams and the staging buffer; owns two events.  The calls can be
+ * captured in a CUDA graph on the compute stream (the side stream joins and
+ * leaves the capture through the events; call dv_delta_streamer_join before
+ * the capture ends). */
+typedef struct dv_delta_streamer dv_delta_streamer;
+
+dv_status dv_delta_streamer_create(dv_delta_streamer** out, dv_replica* replica,
+                                   dv_stream compute_stream, dv_stream side_stream,
+                                   void* staging, size_t staging_bytes);
+
+/* After everything enqueued so far on the compute stream (the step's writes),
+ * the slices of (l0, l1, ranges) of `cache` are appended to the replica as the
+ * record of `step`, on the side stream; the compute stream does not wait.
+ * Errors of dv_replica_append, checked before anything is enqueued. */
+dv_status dv_delta_stream(dv_delta_streamer* ds, const dv_cache* cache, int32_t l0, int32_t l1,
+                          const int32_t* seq_start, const int32_t* seq_end, int64_t step);
+
+/* Makes the compute stream wait for every delta streamed so far (before it
+ * overwrites or frees streamed slices, or ends a graph capture). */
+dv_status dv_delta_streamer_join(dv_delta_streamer* ds);
+
+/* Blocks the calling thread until every delta streamed so far is in the
+ * replica. */
+dv_status dv_delta_streamer_wait(dv_delta_streamer* ds);
+
+void dv_delta_streamer_destroy(dv_delta_streamer* ds);
 
 #ifdef __cplusplus
 } /* extern "C" */

@@ -26,4 +26,8 @@ from .dv import (  # noqa: F401
     dv_replica_restore_fetched,
     dv_replica_truncate,
     dv_replica_info, dv_replica_destroy,
+    Swapper, dv_swapper_create, dv_swapper_acquire, dv_swapper_prefetch, dv_swapper_release,
+    dv_swapper_wait, dv_swapper_destroy,
+    DeltaStreamer, dv_delta_streamer_create, dv_delta_stream, dv_delta_streamer_join,
+    dv_delta_streamer_wait, dv_delta_streamer_destroy,
 )

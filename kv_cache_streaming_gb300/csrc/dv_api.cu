@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 #include <vector>
@@ -82,6 +83,69 @@ GetRangeFn get_range_fn() {
   }();
   return fn;
 }
+
+// A driver entry point fetched through the runtime (nullptr if unavailable).
+void* driver_fn(const char* name) {
+  void* f = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess) {
+    cudaGetLastError();
+    f = nullptr;
+  }
+  return f;
+}
+
+// A library-owned stream for the copies of a pipelined staged swap, one per
+// CUDA context (created on first use there, with the context current; kept
+// until the process exits).  nullptr when none can be had, or when none
+// exists yet and `caller` is being captured into a graph (no stream is made
+// during a capture): the swap then runs in order on the caller's stream.
+cudaStream_t copy_stream(cudaStream_t caller) {
+  static std::mutex mu;
+  static std::vector<std::pair<unsigned long long, cudaStream_t>> streams;
+  unsigned long long id = 0;
+  if (!dv::context_id(&id)) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& e : streams)
+    if (e.first == id) return e.second;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(caller, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (cap != cudaStreamCaptureStatusNone) return nullptr;
+  cudaStream_t cs = nullptr;
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  try {
+    streams.emplace_back(id, cs);
+  } catch (...) {
+    cudaStreamDestroy(cs);
+    return nullptr;
+  }
+  return cs;
+}
+
+// Events a pipelined swap orders its two streams with, created per call and
+// released when the call returns (a recorded event is freed once it
+// completes).
+struct Events {
+  cudaEvent_t e[5] = {};
+  int n = 0;
+  cudaError_t make() {
+    for (; n < 5; ++n) {
+      const cudaError_t err = cudaEventCreateWithFlags(&e[n], cudaEventDisableTiming);
+      if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
+  }
+  ~Events() {
+    for (int i = 0; i < n; ++i) cudaEventDestroy(e[i]);
+  }
+};
 
 // Validates geometry and ranges (no pointer is touched) and fills `p`.
 dv_status plan_ranges(const dv_cache* c, int32_t l0, int32_t l1, const int32_t* s,
@@ -307,10 +371,75 @@ dv_status do_swap(Dir dir, const dv_cache* c, int32_t l0, int32_t l1, const int3
     return fail(DV_ERR_BUFFER_TOO_SMALL, "staging of %zu bytes holds less than one layer slab "
                 "(%lld bytes)", staging_bytes, (long long)slab);
   const int64_t fit = (int64_t)(staging_bytes / (size_t)slab);
-  const int32_t group = (int32_t)(fit < (int64_t)(l1 - l0) ? fit : (int64_t)(l1 - l0));
+  const int32_t nl = l1 - l0;
+  uint8_t* hp = static_cast<uint8_t*>(host);
+  // Pipelined: the staging buffer in two halves, the copies on the library's
+  // copy stream, so that the pack (unpack) of one group of layers overlaps
+  // the copy of the other.  Needs room for a layer in each half.
+  cudaStream_t cs = fit >= 2 && nl >= 2 ? copy_stream(stream) : nullptr;
+  Events ev;
+  if (cs && ev.make() != cudaSuccess) {
+    cudaGetLastError();
+    cs = nullptr;
+  }
+  if (cs) {
+    const int32_t group = (int32_t)(fit / 2 < (int64_t)nl ? fit / 2 : (int64_t)nl);
+    const size_t half = (size_t)group * (size_t)slab;
+    void* stg = nullptr;
+    if ((st = resolve(staging, 2 * half, false, "staging", &stg)) != DV_OK) return st;
+    uint8_t* sp = static_cast<uint8_t*>(stg);
+    cudaEvent_t start = ev.e[0], a[2] = {ev.e[1], ev.e[2]}, b[2] = {ev.e[3], ev.e[4]};
+    if (dir == Dir::kIn) {  // copies into staging wait for the caller's earlier work
+      if ((err = cudaEventRecord(start, stream)) != cudaSuccess ||
+          (err = cudaStreamWaitEvent(cs, start, 0)) != cudaSuccess)
+        return cuda_fail(err, "swap-in: order the copy stream");
+    }
+    int g = 0;
+    for (int32_t la = l0; la < l1; la += group, ++g) {
+      const int32_t lb = la + group < l1 ? la + group : l1;
+      const int h = g & 1;
+      dv::Plan q = p;
+      dv::restrict_layers(q, la, lb);
+      uint8_t* hchunk = hp + (int64_t)(la - l0) * slab;
+      uint8_t* half_h = sp + h * half;
+      if (dir == Dir::kOut) {  // a[h]: packed into half h;  b[h]: half h copied out
+        if (g >= 2 && (err = cudaStreamWaitEvent(stream, b[h], 0)) != cudaSuccess)
+          return cuda_fail(err, "swap-out: wait for a free half");
+        if ((err = dv::launch_pack(q, half_h, stream, dv::kAuto)) != cudaSuccess)
+          return cuda_fail(err, "swap-out pack launch");
+        if ((err = cudaEventRecord(a[h], stream)) != cudaSuccess ||
+            (err = cudaStreamWaitEvent(cs, a[h], 0)) != cudaSuccess)
+          return cuda_fail(err, "swap-out: order the copy");
+        if ((err = cudaMemcpyAsync(hchunk, half_h, (size_t)q.bytes, cudaMemcpyDeviceToHost,
+                                   cs)) != cudaSuccess)
+          return cuda_fail(err, "swap-out copy");
+        if ((err = cudaEventRecord(b[h], cs)) != cudaSuccess)
+          return cuda_fail(err, "swap-out: record the copy");
+      } else {  // a[h]: half h copied in;  b[h]: half h unpacked
+        if (g >= 2 && (err = cudaStreamWaitEvent(cs, b[h], 0)) != cudaSuccess)
+          return cuda_fail(err, "swap-in: wait for a free half");
+        if ((err = cudaMemcpyAsync(half_h, hchunk, (size_t)q.bytes, cudaMemcpyHostToDevice,
+                                   cs)) != cudaSuccess)
+          return cuda_fail(err, "swap-in copy");
+        if ((err = cudaEventRecord(a[h], cs)) != cudaSuccess ||
+            (err = cudaStreamWaitEvent(stream, a[h], 0)) != cudaSuccess)
+          return cuda_fail(err, "swap-in: order the unpack");
+        if ((err = dv::launch_unpack(q, half_h, stream, dv::kAuto)) != cudaSuccess)
+          return cuda_fail(err, "swap-in unpack launch");
+        if ((err = cudaEventRecord(b[h], stream)) != cudaSuccess)
+          return cuda_fail(err, "swap-in: record the unpack");
+      }
+    }
+    if (dir == Dir::kOut) {  // the swap is done, in the caller's stream, when both copies are
+      for (int h = 0; h < 2 && h < g; ++h)
+        if ((err = cudaStreamWaitEvent(stream, b[h], 0)) != cudaSuccess)
+          return cuda_fail(err, "swap-out: join the copy stream");
+    }
+    return DV_OK;
+  }
+  const int32_t group = (int32_t)(fit < (int64_t)nl ? fit : (int64_t)nl);
   void* stg = nullptr;
   if ((st = resolve(staging, (size_t)(group * slab), false, "staging", &stg)) != DV_OK) return st;
-  uint8_t* hp = static_cast<uint8_t*>(host);
   for (int32_t la = l0; la < l1; la += group) {
     const int32_t lb = la + group < l1 ? la + group : l1;
     dv::Plan q = p;
@@ -336,6 +465,25 @@ dv_status do_swap(Dir dir, const dv_cache* c, int32_t l0, int32_t l1, const int3
 }  // namespace
 
 namespace dv {
+bool context_id(unsigned long long* id) {
+  using GetCurrentFn = CUresult (*)(CUcontext*);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static const GetCurrentFn get_current =
+      reinterpret_cast<GetCurrentFn>(driver_fn("cuCtxGetCurrent"));
+  static const GetIdFn get_id = reinterpret_cast<GetIdFn>(driver_fn("cuCtxGetId"));
+  if (!get_current || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return false;
+  if (!ctx) {  // the runtime makes the device's primary context current on first use
+    if (cudaFree(nullptr) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  }
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
 dv_status set_error(dv_status st, const char* fmt, ...) {
   char buf[512];
   va_list ap;
@@ -1200,5 +1348,285 @@ dv_status dv_replica_info(const dv_replica* r, int64_t* num_records, size_t* byt
 }
 
 void dv_replica_destroy(dv_replica* r) { delete r; }
+
+// ---- microbatch swapping through two device caches (Fig 9) -------------------
+
+struct dv_swapper {
+  dv_cache slot[2];
+  dv_fetcher* fetcher;
+  cudaStream_t compute;
+  cudaStream_t swap;
+  const dv_replica* holds[2];  // microbatch swapped in to each cache (or on its way)
+  const dv_replica* cur;       // the acquired microbatch, NULL between steps
+  int current;                 // its cache
+  int last;                    // the cache of the last acquire, -1 before the first
+  cudaEvent_t ready[2];        // after a cache's swap-in (fetcher's unpack stream)
+  cudaEvent_t computed[2];     // after a step's compute (compute stream)
+  cudaEvent_t freed[2];        // after a cache's last swap-out (swap stream)
+  bool ready_set[2], freed_set[2];
+};
+
+namespace {
+
+// Swaps `mb` in to cache i on the fetcher's streams, after that cache's
+// previous step and swap-out.
+dv_status swap_in_slot(dv_swapper* sw, int i, const dv_replica* mb) {
+  dv_fetcher* f = sw->fetcher;
+  cudaError_t err;
+  if (sw->freed_set[i]) {
+    if ((err = cudaStreamWaitEvent(f->copy, sw->freed[i], 0)) != cudaSuccess ||
+        (err = cudaStreamWaitEvent(f->unpack, sw->freed[i], 0)) != cudaSuccess)
+      return cuda_fail(err, "swapper: wait for the cache's swap-out");
+  }
+  const dv_status st = dv_replica_restore_fetched(mb, &sw->slot[i], -1, f);
+  if (st != DV_OK) return st;
+  if ((err = cudaEventRecord(sw->ready[i], f->unpack)) != cudaSuccess)
+    return cuda_fail(err, "swapper: record the swap-in");
+  sw->ready_set[i] = true;
+  sw->holds[i] = mb;
+  return DV_OK;
+}
+
+bool same_geometry(const dv_cache& a, const dv_cache& b) {
+  return a.num_layers == b.num_layers && a.batch == b.batch && a.num_heads == b.num_heads &&
+         a.head_dim == b.head_dim && a.max_seq == b.max_seq && a.elem_bytes == b.elem_bytes &&
+         a.layer_stride_elems == b.layer_stride_elems;
+}
+
+}  // namespace
+
+dv_status dv_swapper_create(dv_swapper** out, const dv_cache* slot0, const dv_cache* slot1,
+                            dv_fetcher* fetcher, dv_stream compute_stream, dv_stream swap_stream) {
+  if (!out) return fail(DV_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!slot0 || !slot1 || !fetcher)
+    return fail(DV_ERR_INVALID_ARG, "slot0 / slot1 / fetcher is NULL");
+  if (!same_geometry(*slot0, *slot1))
+    return fail(DV_ERR_INVALID_ARG, "the two caches must have the same geometry");
+  if (slot0->k_base == slot1->k_base || slot0->v_base == slot1->v_base)
+    return fail(DV_ERR_INVALID_ARG, "the two caches must not share memory");
+  std::vector<int32_t> zero((size_t)(slot0->batch > 0 ? slot0->batch : 1), 0);
+  for (const dv_cache* c : {slot0, slot1}) {
+    dv::Plan p;
+    dv_status st = plan_ranges(c, 0, c->num_layers, zero.data(), zero.data(), &p);
+    if (st != DV_OK) return st;
+    if ((st = resolve_cache(c, &p)) != DV_OK) return st;
+  }
+  dv_swapper* sw = new (std::nothrow) dv_swapper();
+  if (!sw) return fail(DV_ERR_INVALID_ARG, "out of host memory for the swapper handle");
+  sw->slot[0] = *slot0;
+  sw->slot[1] = *slot1;
+  sw->fetcher = fetcher;
+  sw->compute = compute_stream;
+  sw->swap = swap_stream;
+  sw->holds[0] = sw->holds[1] = nullptr;
+  sw->cur = nullptr;
+  sw->current = -1;
+  sw->last = -1;
+  sw->ready_set[0] = sw->ready_set[1] = sw->freed_set[0] = sw->freed_set[1] = false;
+  cudaEvent_t* evs[6] = {&sw->ready[0], &sw->ready[1], &sw->computed[0], &sw->computed[1],
+                         &sw->freed[0], &sw->freed[1]};
+  int made = 0;
+  cudaError_t err = cudaSuccess;
+  for (; made < 6; ++made)
+    if ((err = cudaEventCreateWithFlags(evs[made], cudaEventDisableTiming)) != cudaSuccess) break;
+  if (made < 6) {
+    for (int i = 0; i < made; ++i) cudaEventDestroy(*evs[i]);
+    delete sw;
+    return cuda_fail(err, "cudaEventCreateWithFlags");
+  }
+  *out = sw;
+  return DV_OK;
+}
+
+dv_status dv_swapper_acquire(dv_swapper* sw, const dv_replica* mb, int32_t* slot) {
+  const Trace trace("dv_swapper_acquire");
+  if (!sw || !mb || !slot) return fail(DV_ERR_INVALID_ARG, "swapper / microbatch / slot is NULL");
+  if (sw->cur) return fail(DV_ERR_INVALID_ARG, "the current microbatch has not been released");
+  if (mb->batch != sw->slot[0].batch)
+    return fail(DV_ERR_INVALID_ARG, "microbatch batch %d differs from the caches' %d", mb->batch,
+                sw->slot[0].batch);
+  int i = sw->holds[0] == mb ? 0 : sw->holds[1] == mb ? 1 : -1;
+  if (i < 0) {  // not swapped in: now, into the cache the last step did not use
+    i = sw->last < 0 ? 0 : 1 - sw->last;
+    const dv_status st = swap_in_slot(sw, i, mb);
+    if (st != DV_OK) return st;
+  }
+  if (sw->ready_set[i]) {
+    const cudaError_t err = cudaStreamWaitEvent(sw->compute, sw->ready[i], 0);
+    if (err != cudaSuccess) return cuda_fail(err, "swapper: wait for the swap-in");
+  }
+  sw->cur = mb;
+  sw->current = i;
+  sw->last = i;
+  *slot = i;
+  return DV_OK;
+}
+
+dv_status dv_swapper_prefetch(dv_swapper* sw, const dv_replica* mb) {
+  const Trace trace("dv_swapper_prefetch");
+  if (!sw || !mb) return fail(DV_ERR_INVALID_ARG, "swapper / microbatch is NULL");
+  if (mb->batch != sw->slot[0].batch)
+    return fail(DV_ERR_INVALID_ARG, "microbatch batch %d differs from the caches' %d", mb->batch,
+                sw->slot[0].batch);
+  if (sw->holds[0] == mb || sw->holds[1] == mb) return DV_OK;  // already there
+  const int j = sw->last < 0 ? 0 : 1 - sw->last;
+  return swap_in_slot(sw, j, mb);
+}
+
+dv_status dv_swapper_release(dv_swapper* sw, dv_replica* mb, int32_t l0, int32_t l1,
+                             const int32_t* seq_start, const int32_t* seq_end, int64_t step) {
+  const Trace trace("dv_swapper_release");
+  if (!sw || !mb) return fail(DV_ERR_INVALID_ARG, "swapper / microbatch is NULL");
+  if (sw->cur != mb) return fail(DV_ERR_INVALID_ARG, "this microbatch is not the acquired one");
+  const int i = sw->current;
+  size_t bytes = 0;
+  dv_status st = dv_staging_bytes(&sw->slot[i], l0, l1, seq_start, seq_end, &bytes);
+  if (st != DV_OK) return st;
+  if (!mb->records.empty() && step < mb->records.back().step)
+    return fail(DV_ERR_INVALID_ARG, "step %lld is before the last record's %lld",
+                (long long)step, (long long)mb->records.back().step);
+  if (mb->used + bytes > mb->arena_bytes)
+    return fail(DV_ERR_BUFFER_TOO_SMALL, "replica arena full: %zu + %zu > %zu bytes", mb->used,
+                bytes, mb->arena_bytes);
+  cudaError_t err;
+  if ((err = cudaEventRecord(sw->computed[i], sw->compute)) != cudaSuccess ||
+      (err = cudaStreamWaitEvent(sw->swap, sw->computed[i], 0)) != cudaSuccess)
+    return cuda_fail(err, "swapper: order the swap-out after the step");
+  if ((st = dv_replica_append(mb, &sw->slot[i], l0, l1, seq_start, seq_end, step, nullptr, 0,
+                              sw->swap)) != DV_OK)
+    return st;
+  if ((err = cudaEventRecord(sw->freed[i], sw->swap)) != cudaSuccess)
+    return cuda_fail(err, "swapper: record the swap-out");
+  sw->freed_set[i] = true;
+  sw->cur = nullptr;
+  return DV_OK;
+}
+
+dv_status dv_swapper_wait(dv_swapper* sw) {
+  if (!sw) return fail(DV_ERR_INVALID_ARG, "swapper is NULL");
+  for (int i = 0; i < 2; ++i) {
+    cudaError_t err = cudaSuccess;
+    if (sw->ready_set[i] && (err = cudaEventSynchronize(sw->ready[i])) != cudaSuccess)
+      return cuda_fail(err, "cudaEventSynchronize");
+    if (sw->freed_set[i] && (err = cudaEventSynchronize(sw->freed[i])) != cudaSuccess)
+      return cuda_fail(err, "cudaEventSynchronize");
+  }
+  return DV_OK;
+}
+
+void dv_swapper_destroy(dv_swapper* sw) {
+  if (!sw) return;
+  for (cudaEvent_t e : {sw->ready[0], sw->ready[1], sw->computed[0], sw->computed[1],
+                        sw->freed[0], sw->freed[1]})
+    cudaEventDestroy(e);
+  delete sw;
+}
+
+// ---- decode deltas streamed beside the compute (Fig 7c) ------------------------
+
+struct dv_delta_streamer {
+  dv_replica* replica;
+  cudaStream_t compute;
+  cudaStream_t side;
+  void* staging;
+  size_t staging_bytes;
+  cudaEvent_t written;   // after a step's writes (compute stream)
+  cudaEvent_t streamed;  // after the last append (side stream)
+  bool any;
+};
+
+dv_status dv_delta_streamer_create(dv_delta_streamer** out, dv_replica* replica,
+                                   dv_stream compute_stream, dv_stream side_stream,
+                                   void* staging, size_t staging_bytes) {
+  if (!out) return fail(DV_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!replica) return fail(DV_ERR_INVALID_ARG, "replica is NULL");
+  if (compute_stream == side_stream)
+    return fail(DV_ERR_INVALID_ARG, "the side stream must differ from the compute stream");
+  if (staging) {
+    void* d = nullptr;
+    const dv_status st = resolve(staging, staging_bytes, false, "staging", &d);
+    if (st != DV_OK) return st;
+  }
+  dv_delta_streamer* ds = new (std::nothrow) dv_delta_streamer();
+  if (!ds) return fail(DV_ERR_INVALID_ARG, "out of host memory for the delta streamer handle");
+  ds->replica = replica;
+  ds->compute = compute_stream;
+  ds->side = side_stream;
+  ds->staging = staging;
+  ds->staging_bytes = staging ? staging_bytes : 0;
+  ds->any = false;
+  cudaError_t err = cudaEventCreateWithFlags(&ds->written, cudaEventDisableTiming);
+  if (err == cudaSuccess) {
+    err = cudaEventCreateWithFlags(&ds->streamed, cudaEventDisableTiming);
+    if (err != cudaSuccess) cudaEventDestroy(ds->written);
+  }
+  if (err != cudaSuccess) {
+    delete ds;
+    return cuda_fail(err, "cudaEventCreateWithFlags");
+  }
+  *out = ds;
+  return DV_OK;
+}
+
+dv_status dv_delta_stream(dv_delta_streamer* ds, const dv_cache* cache, int32_t l0, int32_t l1,
+                          const int32_t* seq_start, const int32_t* seq_end, int64_t step) {
+  const Trace trace("dv_delta_stream");
+  if (!ds) return fail(DV_ERR_INVALID_ARG, "delta streamer is NULL");
+  dv_replica* r = ds->replica;
+  if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
+  if (cache->batch != r->batch)
+    return fail(DV_ERR_INVALID_ARG, "cache batch %d differs from the replica's %d", cache->batch,
+                r->batch);
+  size_t bytes = 0;
+  dv_status st = dv_staging_bytes(cache, l0, l1, seq_start, seq_end, &bytes);
+  if (st != DV_OK) return st;
+  if (!r->records.empty() && step < r->records.back().step)
+    return fail(DV_ERR_INVALID_ARG, "step %lld is before the last record's %lld",
+                (long long)step, (long long)r->records.back().step);
+  if (r->used + bytes > r->arena_bytes)
+    return fail(DV_ERR_BUFFER_TOO_SMALL, "replica arena full: %zu + %zu > %zu bytes", r->used,
+                bytes, r->arena_bytes);
+  if (ds->staging && bytes > 0) {
+    dv::Plan p;
+    if ((st = plan_ranges(cache, l0, l1, seq_start, seq_end, &p)) != DV_OK) return st;
+    if ((size_t)dv::layer_slab_bytes(p) > ds->staging_bytes)
+      return fail(DV_ERR_BUFFER_TOO_SMALL, "staging of %zu bytes holds less than one layer slab "
+                  "(%lld bytes)", ds->staging_bytes, (long long)dv::layer_slab_bytes(p));
+  }
+  cudaError_t err;
+  if ((err = cudaEventRecord(ds->written, ds->compute)) != cudaSuccess ||
+      (err = cudaStreamWaitEvent(ds->side, ds->written, 0)) != cudaSuccess)
+    return cuda_fail(err, "delta stream: order the append after the step");
+  if ((st = dv_replica_append(r, cache, l0, l1, seq_start, seq_end, step, ds->staging,
+                              ds->staging_bytes, ds->side)) != DV_OK)
+    return st;
+  if ((err = cudaEventRecord(ds->streamed, ds->side)) != cudaSuccess)
+    return cuda_fail(err, "delta stream: record the append");
+  ds->any = true;
+  return DV_OK;
+}
+
+dv_status dv_delta_streamer_join(dv_delta_streamer* ds) {
+  if (!ds) return fail(DV_ERR_INVALID_ARG, "delta streamer is NULL");
+  if (!ds->any) return DV_OK;
+  const cudaError_t err = cudaStreamWaitEvent(ds->compute, ds->streamed, 0);
+  return err == cudaSuccess ? DV_OK : cuda_fail(err, "delta stream: join");
+}
+
+dv_status dv_delta_streamer_wait(dv_delta_streamer* ds) {
+  if (!ds) return fail(DV_ERR_INVALID_ARG, "delta streamer is NULL");
+  if (!ds->any) return DV_OK;
+  const cudaError_t err = cudaEventSynchronize(ds->streamed);
+  return err == cudaSuccess ? DV_OK : cuda_fail(err, "cudaEventSynchronize");
+}
+
+void dv_delta_streamer_destroy(dv_delta_streamer* ds) {
+  if (!ds) return;
+  cudaEventDestroy(ds->written);
+  cudaEventDestroy(ds->streamed);
+  delete ds;
+}
 
 }  // extern "C"

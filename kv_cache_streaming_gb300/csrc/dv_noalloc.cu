@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "../../include/dv.h"
 #include "dv_plan.h"
@@ -16,35 +18,39 @@ namespace {
 // The built-in staging buffer.  Every GPU that loads libdv holds these bytes
 // until the process exits.  Host code must not pass the name itself to a
 // kernel (on the host it names a stand-in, not device memory): the device
-// address comes from cudaGetSymbolAddress, once per device.
+// address comes from cudaGetSymbolAddress, once per CUDA context.
 static __device__ __align__(256) unsigned char g_noalloc_staging[DV_NOALLOC_STAGING_BYTES];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_addr[kMaxDevices] = {};
+std::vector<std::pair<unsigned long long, void*>> g_addr;  // (context id, address)
 
-// Device address of the built-in buffer on the current device; resolved with
-// that device current on the first call there.
+// Device address of the built-in buffer in the current CUDA context, looked
+// up (cudaGetSymbolAddress, with the context current) on the first call in
+// that context and kept per context: a device reset or a new context gets an
+// id of its own and a fresh lookup, never a stale address.
 dv_status staging_address(void** out) {
-  int dev = -1;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess)
-    return dv::set_error(DV_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorName(err));
-  if (dev < 0 || dev >= kMaxDevices)
-    return dv::set_error(DV_ERR_UNSUPPORTED, "device %d is beyond the %d devices supported", dev,
-                         kMaxDevices);
+  unsigned long long id = 0;
+  if (!dv::context_id(&id))
+    return dv::set_error(DV_ERR_CUDA, "dv_swap_out_noalloc: no current CUDA context");
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_addr[dev]) {
-    void* p = nullptr;
-    err = cudaGetSymbolAddress(&p, g_noalloc_staging);
-    if (err != cudaSuccess || !p) {
-      cudaGetLastError();
-      return dv::set_error(DV_ERR_CUDA, "cudaGetSymbolAddress of the built-in staging buffer: %s",
-                           cudaGetErrorName(err));
+  for (const auto& e : g_addr)
+    if (e.first == id) {
+      *out = e.second;
+      return DV_OK;
     }
-    g_addr[dev] = p;
+  void* p = nullptr;
+  const cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_staging);
+  if (err != cudaSuccess || !p) {
+    cudaGetLastError();
+    return dv::set_error(DV_ERR_CUDA, "cudaGetSymbolAddress of the built-in staging buffer: %s",
+                         cudaGetErrorName(err));
   }
-  *out = g_addr[dev];
+  try {
+    g_addr.emplace_back(id, p);
+  } catch (...) {
+    return dv::set_error(DV_ERR_INVALID_ARG, "out of host memory for the buffer address");
+  }
+  *out = p;
   return DV_OK;
 }
 

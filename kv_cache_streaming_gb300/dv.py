@@ -85,6 +85,18 @@ _replica_restore_fetched = _sig("dv_replica_restore_fetched", [_P, _CP, _I64, _P
 _replica_truncate = _sig("dv_replica_truncate", [_P, _I64])
 _replica_info = _sig("dv_replica_info", [_P, ctypes.POINTER(_I64), ctypes.POINTER(_SZ)])
 _replica_destroy = _sig("dv_replica_destroy", [_P], None)
+_swapper_create = _sig("dv_swapper_create", [ctypes.POINTER(_P), _CP, _CP, _P, _P, _P])
+_swapper_acquire = _sig("dv_swapper_acquire", [_P, _P, ctypes.POINTER(_I32)])
+_swapper_prefetch = _sig("dv_swapper_prefetch", [_P, _P])
+_swapper_release = _sig("dv_swapper_release", [_P, _P, _I32, _I32, _I32P, _I32P, _I64])
+_swapper_wait = _sig("dv_swapper_wait", [_P])
+_swapper_destroy = _sig("dv_swapper_destroy", [_P], None)
+_delta_streamer_create = _sig("dv_delta_streamer_create",
+                              [ctypes.POINTER(_P), _P, _P, _P, _P, _SZ])
+_delta_stream = _sig("dv_delta_stream", [_P, _CP, _I32, _I32, _I32P, _I32P, _I64])
+_delta_streamer_join = _sig("dv_delta_streamer_join", [_P])
+_delta_streamer_wait = _sig("dv_delta_streamer_wait", [_P])
+_delta_streamer_destroy = _sig("dv_delta_streamer_destroy", [_P], None)
 
 
 class DvError(RuntimeError):
@@ -473,3 +485,122 @@ def dv_replica_info(replica: Replica):
 
 def dv_replica_destroy(replica: Replica) -> None:
     replica.close()
+
+
+class Swapper:
+    """Handle of ``dv_swapper``: microbatches through two device caches."""
+
+    def __init__(self, slot0: Cache, slot1: Cache, fetcher: Fetcher, compute_stream=None,
+                 swap_stream=None):
+        self._keep = (slot0, slot1, fetcher, compute_stream, swap_stream)
+        self.slots = (slot0, slot1)
+        h = _P()
+        _check(_swapper_create(ctypes.byref(h), slot0.ref, slot1.ref, fetcher.h,
+                               _stream(compute_stream), _stream(swap_stream)))
+        self.h = h
+
+    def acquire(self, mb: Replica) -> int:
+        """The cache (0 or 1) that holds microbatch ``mb`` for its next step."""
+        slot = _I32(-1)
+        _check(_swapper_acquire(self.h, mb.h, ctypes.byref(slot)))
+        return slot.value
+
+    def prefetch(self, mb: Replica) -> None:
+        _check(_swapper_prefetch(self.h, mb.h))
+
+    def release(self, mb: Replica, l0, l1, seq_start, seq_end, step) -> None:
+        s, e, sp, ep = _ranges(seq_start, seq_end, self.slots[0].c.batch)
+        _check(_swapper_release(self.h, mb.h, l0, l1, sp, ep, step))
+
+    def wait(self):
+        _check(_swapper_wait(self.h))
+
+    def close(self):
+        if self.h:
+            _swapper_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def dv_swapper_create(slot0, slot1, fetcher, compute_stream=None, swap_stream=None) -> Swapper:
+    return Swapper(slot0, slot1, fetcher, compute_stream, swap_stream)
+
+
+def dv_swapper_acquire(sw: Swapper, mb: Replica) -> int:
+    return sw.acquire(mb)
+
+
+def dv_swapper_prefetch(sw: Swapper, mb: Replica) -> None:
+    sw.prefetch(mb)
+
+
+def dv_swapper_release(sw: Swapper, mb: Replica, l0, l1, seq_start, seq_end, step) -> None:
+    sw.release(mb, l0, l1, seq_start, seq_end, step)
+
+
+def dv_swapper_wait(sw: Swapper) -> None:
+    sw.wait()
+
+
+def dv_swapper_destroy(sw: Swapper) -> None:
+    sw.close()
+
+
+class DeltaStreamer:
+    """Handle of ``dv_delta_streamer``: decode deltas streamed to a replica on
+    a side stream."""
+
+    def __init__(self, replica: Replica, compute_stream=None, side_stream=None, staging=None):
+        st, sn = _buf(staging)
+        self._keep = (replica, compute_stream, side_stream, staging)
+        h = _P()
+        _check(_delta_streamer_create(ctypes.byref(h), replica.h, _stream(compute_stream),
+                                      _stream(side_stream), st, sn))
+        self.h = h
+
+    def stream(self, cache: Cache, l0, l1, seq_start, seq_end, step) -> None:
+        s, e, sp, ep = _ranges(seq_start, seq_end, cache.c.batch)
+        _check(_delta_stream(self.h, cache.ref, l0, l1, sp, ep, step))
+
+    def join(self):
+        _check(_delta_streamer_join(self.h))
+
+    def wait(self):
+        _check(_delta_streamer_wait(self.h))
+
+    def close(self):
+        if self.h:
+            _delta_streamer_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def dv_delta_streamer_create(replica, compute_stream=None, side_stream=None,
+                             staging=None) -> DeltaStreamer:
+    return DeltaStreamer(replica, compute_stream, side_stream, staging)
+
+
+def dv_delta_stream(ds: DeltaStreamer, cache: Cache, l0, l1, seq_start, seq_end, step) -> None:
+    ds.stream(cache, l0, l1, seq_start, seq_end, step)
+
+
+def dv_delta_streamer_join(ds: DeltaStreamer) -> None:
+    ds.join()
+
+
+def dv_delta_streamer_wait(ds: DeltaStreamer) -> None:
+    ds.wait()
+
+
+def dv_delta_streamer_destroy(ds: DeltaStreamer) -> None:
+    ds.close()
