@@ -85,7 +85,8 @@ def parse_args():
                              "flat-pack", "flat-unpack", "record-restore", "swap-out",
                              "swap-in", "ragged-pack", "ragged-unpack", "delta-graph-pack",
                              "delta-graph-unpack", "bloom-snapshot-pack",
-                             "bloom-snapshot-unpack", "bloom-delta-pack", "bloom-run-restore"],
+                             "bloom-snapshot-unpack", "bloom-delta-pack", "bloom-run-restore",
+                             "short-ragged-pack", "short-ragged-unpack"],
                     help="run one kernel of the step on an 8-layer cache of the workload's "
                          "shape, 5 launches, and exit (a small case for profilers); "
                          "flat-*: ragged 16..64-token ranges of the OPT-13B-shaped cache, "
@@ -99,7 +100,8 @@ def parse_args():
                          "5 replays (for graph-level counters); bloom-*: the headline "
                          "step's kernels on its workload cut to 2 layers and batch 16 "
                          "(snapshot pack / unpack: 3 launches; delta pack: 8 launches, 8 "
-                         "tokens apart; run restore: 3 launches of 256 one-token records)")
+                         "tokens apart; run restore: 3 launches of 256 one-token records); "
+                         "short-ragged-*: the flat-* ranges under the automatic kernel choice")
     return ap.parse_args()
 
 
@@ -109,10 +111,15 @@ def parse_args():
 # it moves (traffic grows in proportion).  None until captured, and set back to
 # None whenever the kernel changes.
 TRAFFIC_PER_LAUNCH = {
-    "pack snapshot (tile kernel)": None,
-    "pack one-token delta (token kernel)": None,
-    "unpack snapshot (tile kernel)": None,
-    "unpack 256 one-token deltas (run kernel)": None,
+    # bloom-snapshot-pack: 2.868 GB per launch of the cut x 19.137 / 1.463 GB
+    "pack snapshot (tile kernel)": 2.8685e9 * 19136724992 / 1463074816,
+    # bloom-delta-pack: 4.594 MB of reads per launch of the cut (its 1.8 MB of
+    # staging writes are still in L2 when it ends) x 14
+    "pack one-token delta (token kernel)": 4.594e6 * 14,
+    # bloom-snapshot-unpack: 2.866 GB per launch of the cut
+    "unpack snapshot (tile kernel)": 2.8657e9 * 19136724992 / 1463074816,
+    # bloom-run-restore: 0.884 GB per launch of the cut (256 records) x 14
+    "unpack 256 one-token deltas (run kernel)": 0.8838e9 * 14,
 }
 
 
@@ -507,21 +514,26 @@ class Bloom:
         self.fetcher = dv.Fetcher(self.slots[0], self.slots[1], self.in_copy, self.in_unpack)
 
     def e2e_step(self):
-        """The snapshot and the 256 deltas appended to the host replica (each
-        a pack storing straight into pinned memory over the host link, in
-        decode order), then the restore of the whole log into the second cache
-        through the fetcher: the copy of piece i+1 (copy engine) overlaps the
-        unpack of piece i."""
+        """The log through the host replica and back: the snapshot appended
+        layer by layer (each a pack storing straight into pinned memory over
+        the host link), each layer restored into the second cache through the
+        fetcher as soon as it is in host memory (the host-to-device copy of
+        layer l overlaps the device-to-host pack of layer l+1), then the 256
+        deltas appended in decode order and restored (runs of records, the
+        copy of one piece overlapping the unpack of the previous)."""
         g, s = self.g, self.stream
         L = g.num_layers
         rep = self.replica
         rep.truncate(0)
-        rep.append(self.cache, 0, L, self.zs, self.len0, step=0, stream=s)
+        self.in_unpack.wait_stream(s)    # the second cache is free
+        for l in range(L):
+            rep.append(self.cache, l, l + 1, self.zs, self.len0, step=l, stream=s)
+            self.in_copy.wait_stream(s)  # layer l is in host memory
+            rep.restore_fetched(self.cache_b, self.fetcher, upto_step=l + 1, from_step=l)
         for k, (a, b) in enumerate(self.deltas):
-            rep.append(self.cache, 0, L, a, b, step=k + 1, stream=s)
-        self.in_copy.wait_stream(s)      # the log is in host memory
-        self.in_unpack.wait_stream(s)    # and the second cache is free
-        rep.restore_fetched(self.cache_b, self.fetcher)
+            rep.append(self.cache, 0, L, a, b, step=L + k, stream=s)
+        self.in_copy.wait_stream(s)      # the deltas are in host memory
+        rep.restore_fetched(self.cache_b, self.fetcher, from_step=L)
         s.wait_stream(self.in_unpack)
 
     def timed_e2e(self, steps, warmup, world):
@@ -1686,10 +1698,11 @@ def run_mine(args):
                 "timing": "median step (each step synchronised); over all steps: "
                           f"{e2e_all:.1f} GB/s, slowest step {max(e2e_ts) * 1e3:.1f} ms, "
                           f"fastest {min(e2e_ts) * 1e3:.1f} ms",
-                "path": "dv_replica_append of the snapshot and of the 256 deltas (fused: the "
-                        "pack stores into pinned host memory), then dv_replica_restore_fetched "
-                        "into the second cache (one-layer slots; the snapshot by layers, the "
-                        "deltas as runs of records)"},
+                "path": "dv_replica_append of the snapshot one layer at a time (fused: the "
+                        "pack stores into pinned host memory), each layer restored through a "
+                        "fetcher (dv_replica_restore_fetched_steps) while the next goes out; "
+                        "then the 256 deltas appended and restored as runs of records "
+                        "(one-layer slots)"},
         "gpt2_step": gpt2,
         "swap": swap,
         "naive_vs_buffered": naive,
@@ -1716,7 +1729,7 @@ def run_kernel_case(case):
     if case == "record-restore":
         run_record_case(torch, dv, synth_gpu)
         return
-    if case.startswith("flat"):
+    if case.startswith("flat") or case.startswith("short-ragged"):
         run_flat_case(case, torch, dv, synth_gpu)
         return
     if case.startswith("ragged"):
@@ -1759,9 +1772,10 @@ def run_kernel_case(case):
 
 
 def run_flat_case(case, torch, dv, synth_gpu):
-    """Ragged short ranges, the flat kernel's domain: 16..64 tokens at seeded
-    positions of each of the 8 sequences of the OPT-13B-shaped cache, all 40
-    layers (about 260 MB of staging, more than L2), 5 launches."""
+    """Ragged short ranges: 16..64 tokens at seeded positions of each of the 8
+    sequences of the OPT-13B-shaped cache, all 40 layers (about 260 MB of
+    staging, more than L2), 5 launches; flat-*: the flat kernel forced,
+    short-ragged-*: the automatic choice (the tile kernel for these ranges)."""
     from synth.configs import OPT13B
     g = OPT13B
     k = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
@@ -1773,12 +1787,13 @@ def run_flat_case(case, torch, dv, synth_gpu):
     e = (s + rng.integers(16, 65, size=g.batch)).astype(np.int32)
     n = dv.dv_staging_bytes(cache, 0, g.num_layers, s, e)
     stg = torch.empty(n, dtype=torch.uint8, device="cuda")
-    dv.dv_kv_pack(cache, 0, g.num_layers, s, e, stg, variant=dv.DV_VARIANT_FLAT)
+    var = dv.DV_VARIANT_FLAT if case.startswith("flat") else dv.DV_VARIANT_AUTO
+    dv.dv_kv_pack(cache, 0, g.num_layers, s, e, stg, variant=var)
     for _ in range(5):
         if case.endswith("-pack"):
-            dv.dv_kv_pack(cache, 0, g.num_layers, s, e, stg, variant=dv.DV_VARIANT_FLAT)
+            dv.dv_kv_pack(cache, 0, g.num_layers, s, e, stg, variant=var)
         else:
-            dv.dv_kv_unpack(cache, 0, g.num_layers, s, e, stg, variant=dv.DV_VARIANT_FLAT)
+            dv.dv_kv_unpack(cache, 0, g.num_layers, s, e, stg, variant=var)
     torch.cuda.synchronize()
     print(f"{case}: 5 launches of {2 * n} algorithmic bytes each "
           f"(ranges of {int((e - s).min())}..{int((e - s).max())} tokens)")

@@ -124,7 +124,7 @@ typedef enum {
   DV_VARIANT_AUTO = 0, /* equal-length ranges (e.g. one-token decode deltas): the
                           token kernel below 640 16-byte chunks per head and range
                           (80 tokens at head_dim 64, fp16), the tile kernel above;
-                          ragged ranges: the flat kernel below a mean of 768 chunks,
+                          ragged ranges: the flat kernel below a mean of 512 chunks,
                           the tile kernel above */
   DV_VARIANT_FLAT = 1, /* staging order, each warp a window of 128 chunks */
   DV_VARIANT_TILE = 2, /* token tiles; K transposed through shared memory */
@@ -399,6 +399,17 @@ dv_status dv_replica_restore_batched(const dv_replica* replica, const dv_cache* 
  * dv_replica_restore. */
 dv_status dv_replica_restore_fetched(const dv_replica* replica, const dv_cache* cache,
                                      int64_t upto_step, dv_fetcher* fetcher);
+
+/* The restore of dv_replica_restore_fetched limited to the records with
+ * from_step <= step < upto_step (no upper limit when upto_step < 0), in append
+ * order: a cache that already holds the earlier records catches up with the
+ * later ones.  This keeps a standby cache current while the log grows, or lets
+ * a restore start before the last record is appended (the caller orders the
+ * fetcher's copy stream after the appends it restores).  No counterpart on
+ * the pages beyond the recovery of Fig 10, which it performs in parts. */
+dv_status dv_replica_restore_fetched_steps(const dv_replica* replica, const dv_cache* cache,
+                                          int64_t from_step, int64_t upto_step,
+                                          dv_fetcher* fetcher);
 
 /* Drops every record with step >= step (the acknowledged prefix is kept). */
 dv_status dv_replica_truncate(dv_replica* replica, int64_t step);

@@ -23,7 +23,7 @@ from .dv import (  # noqa: F401
     dv_streamer_create, dv_stream_layer, dv_streamer_wait, dv_streamer_destroy,
     dv_fetcher_create, dv_fetch_layer, dv_fetcher_wait, dv_fetcher_destroy,
     dv_replica_create, dv_replica_append, dv_replica_restore, dv_replica_restore_batched,
-    dv_replica_restore_fetched,
+    dv_replica_restore_fetched, dv_replica_restore_fetched_steps,
     dv_replica_truncate,
     dv_replica_info, dv_replica_destroy,
     Swapper, dv_swapper_create, dv_swapper_acquire, dv_swapper_prefetch, dv_swapper_release,

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -657,9 +658,10 @@ dv_status plan_log(const dv_cache* cache, const std::vector<LogRec>& all, size_t
   return DV_OK;
 }
 
-// The records of `r` with step < upto (all when upto < 0), planned for `cache`.
-dv_status plan_restore(const dv_replica* r, const dv_cache* cache, int64_t upto, size_t piece,
-                       LogPlan* lp) {
+// The records of `r` with from <= step < upto (no upper limit when upto < 0),
+// planned for `cache`.
+dv_status plan_restore(const dv_replica* r, const dv_cache* cache, int64_t from, int64_t upto,
+                       size_t piece, LogPlan* lp) {
   if (!r) return fail(DV_ERR_INVALID_ARG, "replica is NULL");
   if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
   if (cache->batch != r->batch)
@@ -669,6 +671,7 @@ dv_status plan_restore(const dv_replica* r, const dv_cache* cache, int64_t upto,
   try {
     for (const Record& rec : r->records) {
       if (upto >= 0 && rec.step >= upto) break;
+      if (rec.step < from) continue;
       all.push_back(LogRec{rec.l0, rec.l1, r->ranges.data() + rec.ranges, rec.offset, rec.bytes,
                            rec.step});
     }
@@ -1173,7 +1176,7 @@ dv_status dv_replica_restore_batched(const dv_replica* r, const dv_cache* cache,
                                     dv_stream stream) {
   const Trace trace("dv_replica_restore_batched");
   LogPlan lp;
-  dv_status st = plan_restore(r, cache, upto_step, staging ? staging_bytes : 0, &lp);
+  dv_status st = plan_restore(r, cache, INT64_MIN, upto_step, staging ? staging_bytes : 0, &lp);
   if (st != DV_OK) return st;
   const int n = (int)lp.todo.size();
   if (n == 0) return DV_OK;
@@ -1229,9 +1232,15 @@ dv_status dv_replica_restore_batched(const dv_replica* r, const dv_cache* cache,
 dv_status dv_replica_restore_fetched(const dv_replica* r, const dv_cache* cache,
                                     int64_t upto_step, dv_fetcher* h) {
   const Trace trace("dv_replica_restore_fetched");
+  return dv_replica_restore_fetched_steps(r, cache, INT64_MIN, upto_step, h);
+}
+
+dv_status dv_replica_restore_fetched_steps(const dv_replica* r, const dv_cache* cache,
+                                          int64_t from_step, int64_t upto_step, dv_fetcher* h) {
+  const Trace trace("dv_replica_restore_fetched_steps");
   if (!h) return fail(DV_ERR_INVALID_ARG, "fetcher is NULL");
   LogPlan lp;
-  dv_status st = plan_restore(r, cache, upto_step, h->slot_bytes, &lp);
+  dv_status st = plan_restore(r, cache, from_step, upto_step, h->slot_bytes, &lp);
   if (st != DV_OK) return st;
   const int n = (int)lp.todo.size();
   cudaError_t err = cudaSuccess;

@@ -1135,11 +1135,13 @@ int auto_kind(const Plan& p) {
 
 bool auto_uses_tile(const Plan& p) {
   if (!tile_supported(p) || p.active == 0) return false;
-  // Tiles pay once a (layer, K|V, sequence, head) run holds about 768 chunks
-  // (12 KiB) on average: measured on GB300 with ragged ranges, the flat
-  // kernel wins at 636 chunks per run for head_dim 64 and at 458 for 128 in
-  // fp16, the tile kernel at 1155 and at 1024.
-  return p.tokens * p.C >= (int64_t)768 * p.active;
+  // Tiles pay once a (layer, K|V, sequence, head) run holds about 512 chunks
+  // (8 KiB) on average, for pack and unpack alike: measured on GB300 with
+  // ragged ranges over all layers, the flat kernel wins at 292 chunks per
+  // run for head_dim 128 and at 477 for 64 in fp16, the tile kernel at 648
+  // and 712 for 128 (unpack 0.77-0.79 of the copy peak against 0.66) and at
+  // 770 for 64.
+  return p.tokens * p.C >= (int64_t)512 * p.active;
 }
 
 bool checked_build() { return DV_CHECKED != 0; }

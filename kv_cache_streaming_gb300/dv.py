@@ -82,6 +82,8 @@ _replica_append = _sig("dv_replica_append", [_P] + _RANGE + [_I64, _P, _SZ, _P])
 _replica_restore = _sig("dv_replica_restore", [_P, _CP, _I64, _P, _SZ, _P])
 _replica_restore_batched = _sig("dv_replica_restore_batched", [_P, _CP, _I64, _P, _SZ, _P])
 _replica_restore_fetched = _sig("dv_replica_restore_fetched", [_P, _CP, _I64, _P])
+_replica_restore_fetched_steps = _sig("dv_replica_restore_fetched_steps",
+                                      [_P, _CP, _I64, _I64, _P])
 _replica_truncate = _sig("dv_replica_truncate", [_P, _I64])
 _replica_info = _sig("dv_replica_info", [_P, ctypes.POINTER(_I64), ctypes.POINTER(_SZ)])
 _replica_destroy = _sig("dv_replica_destroy", [_P], None)
@@ -427,8 +429,12 @@ class Replica:
         st, sn = _buf(staging)
         _check(_replica_restore_batched(self.h, cache.ref, upto_step, st, sn, _stream(stream)))
 
-    def restore_fetched(self, cache: Cache, fetcher: "Fetcher", upto_step=-1):
-        _check(_replica_restore_fetched(self.h, cache.ref, upto_step, fetcher.h))
+    def restore_fetched(self, cache: Cache, fetcher: "Fetcher", upto_step=-1, from_step=None):
+        if from_step is None:
+            _check(_replica_restore_fetched(self.h, cache.ref, upto_step, fetcher.h))
+        else:
+            _check(_replica_restore_fetched_steps(self.h, cache.ref, from_step, upto_step,
+                                                  fetcher.h))
 
     def truncate(self, step):
         _check(_replica_truncate(self.h, step))
@@ -473,6 +479,11 @@ def dv_replica_restore_batched(replica: Replica, cache: Cache, upto_step=-1, sta
 def dv_replica_restore_fetched(replica: Replica, cache: Cache, fetcher: Fetcher,
                                upto_step=-1) -> None:
     replica.restore_fetched(cache, fetcher, upto_step)
+
+
+def dv_replica_restore_fetched_steps(replica: Replica, cache: Cache, from_step, upto_step,
+                                     fetcher: Fetcher) -> None:
+    replica.restore_fetched(cache, fetcher, upto_step, from_step)
 
 
 def dv_replica_truncate(replica: Replica, step) -> None:

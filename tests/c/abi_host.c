@@ -58,6 +58,36 @@ int main(void) {
   CHECK(dv_replica_restore_batched(NULL, &c, -1, NULL, 0, NULL) == DV_ERR_INVALID_ARG);
   CHECK(dv_replica_restore_fetched(NULL, &c, -1, NULL) == DV_ERR_INVALID_ARG);
   CHECK(dv_replica_truncate(NULL, 0) == DV_ERR_INVALID_ARG);
+  CHECK(dv_replica_restore_fetched_steps(NULL, &c, 0, -1, NULL) == DV_ERR_INVALID_ARG);
+  /* the log scatter: tables, counts and ranges are checked on the host */
+  int32_t layers[2] = {0, 48}, ranges[16];
+  memcpy(ranges, s, sizeof s);
+  memcpy(ranges + 8, e, sizeof e);
+  CHECK(dv_kv_unpack_records(NULL, 1, layers, ranges, (void*)0x3000, 16, NULL) ==
+        DV_ERR_INVALID_ARG);
+  CHECK(dv_kv_unpack_records(&c, -1, layers, ranges, (void*)0x3000, 16, NULL) ==
+        DV_ERR_INVALID_ARG);
+  CHECK(dv_kv_unpack_records(&c, 1, NULL, ranges, (void*)0x3000, 16, NULL) ==
+        DV_ERR_INVALID_ARG);
+  CHECK(dv_kv_unpack_records(&c, 1, layers, ranges, (void*)0x3000, 16, NULL) ==
+        DV_ERR_BUFFER_TOO_SMALL);
+  ranges[8] = 1025; /* a range past max_seq */
+  CHECK(dv_kv_unpack_records(&c, 1, layers, ranges, (void*)0x3000, 1u << 30, NULL) ==
+        DV_ERR_RANGE);
+  CHECK(dv_kv_unpack_records(&c, 0, NULL, NULL, NULL, 0, NULL) == DV_OK);
+  /* the swapper and the delta streamer refuse NULL handles and arguments */
+  int32_t slot = 0;
+  CHECK(dv_swapper_create(NULL, &c, &c, NULL, NULL, NULL) == DV_ERR_INVALID_ARG);
+  CHECK(dv_swapper_acquire(NULL, NULL, &slot) == DV_ERR_INVALID_ARG);
+  CHECK(dv_swapper_prefetch(NULL, NULL) == DV_ERR_INVALID_ARG);
+  CHECK(dv_swapper_release(NULL, NULL, 0, 48, s, e, 0) == DV_ERR_INVALID_ARG);
+  CHECK(dv_swapper_wait(NULL) == DV_ERR_INVALID_ARG);
+  CHECK(dv_delta_streamer_create(NULL, NULL, NULL, NULL, NULL, 0) == DV_ERR_INVALID_ARG);
+  CHECK(dv_delta_stream(NULL, &c, 0, 48, s, e, 0) == DV_ERR_INVALID_ARG);
+  CHECK(dv_delta_streamer_join(NULL) == DV_ERR_INVALID_ARG);
+  CHECK(dv_delta_streamer_wait(NULL) == DV_ERR_INVALID_ARG);
+  dv_swapper_destroy(NULL);
+  dv_delta_streamer_destroy(NULL);
   dv_streamer_destroy(NULL);
   dv_fetcher_destroy(NULL);
   dv_replica_destroy(NULL);

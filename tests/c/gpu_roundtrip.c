@@ -6,8 +6,10 @@
  * K row of token s_0 of (layer 0, sequence 0, head 0) read through the layout.
  * Then the same bytes go out layer by layer through a streamer and come back
  * through a fetcher, and a replica (snapshot + one decode token) is restored
- * record-batched and pipelined through the fetcher.  Exit status 0 when every
- * check holds. */
+ * record-batched and pipelined through the fetcher, and unpacked from the
+ * mapped arena by dv_kv_unpack_records.  Decode deltas are streamed on a side
+ * stream (dv_delta_streamer), and the two replicas go through two caches
+ * (dv_swapper).  Exit status 0 when every check holds. */
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -32,6 +34,31 @@ static int failures = 0;
       ++failures;                                                     \
     }                                                                 \
   } while (0)
+
+/* Number of bytes of the device cache (yk, yv) that differ from hk / hv on
+ * tokens [lo_b, hi_b) of every sequence and from zero elsewhere. */
+static int check_cache(const void* yk, const void* yv, const uint16_t* hk, const uint16_t* hv,
+                       const int32_t* lo, const int32_t* hi, size_t n) {
+  uint16_t* gk = (uint16_t*)malloc(n * P);
+  uint16_t* gv = (uint16_t*)malloc(n * P);
+  cudaMemcpy(gk, yk, n * P, cudaMemcpyDeviceToHost);
+  cudaMemcpy(gv, yv, n * P, cudaMemcpyDeviceToHost);
+  int bad = 0;
+  for (int l = 0; l < L; ++l)
+    for (int b = 0; b < B; ++b)
+      for (int h = 0; h < H; ++h)
+        for (int t = 0; t < S; ++t)
+          for (int d = 0; d < D; ++d) {
+            const size_t ki = (size_t)l * B * H * D * S +
+                              ((((size_t)b * H + h) * (D / X) + d / X) * S + t) * X + d % X;
+            const size_t vi = (size_t)l * B * H * D * S + (((size_t)b * H + h) * S + t) * D + d;
+            const int sel = t >= lo[b] && t < hi[b];
+            if (gk[ki] != (sel ? hk[ki] : 0) || gv[vi] != (sel ? hv[vi] : 0)) ++bad;
+          }
+  free(gk);
+  free(gv);
+  return bad;
+}
 
 int main(void) {
   const size_t n = (size_t)L * B * H * D * S; /* elements per tensor */
@@ -167,6 +194,87 @@ int main(void) {
             }
     CHECK(bad == 0);
   }
+
+  /* The same log unpacked by dv_kv_unpack_records straight from the mapped
+   * arena (its device-visible address), records back to back. */
+  {
+    int32_t layers[4] = {0, L, 0, L};
+    int32_t ranges[4 * B];
+    memcpy(ranges, s, sizeof s);
+    memcpy(ranges + B, e, sizeof e);
+    memcpy(ranges + 2 * B, e, sizeof e);
+    memcpy(ranges + 3 * B, e1, sizeof e1);
+    void* arena_dev = NULL;
+    CHECK(cudaHostGetDevicePointer(&arena_dev, arena, 0) == cudaSuccess);
+    cudaMemset(yk, 0, n * P);
+    cudaMemset(yv, 0, n * P);
+    CHECK(dv_kv_unpack_records(&y, 2, layers, ranges, arena_dev, bytes + delta, NULL) == DV_OK);
+    CHECK(cudaDeviceSynchronize() == cudaSuccess);
+    CHECK(check_cache(yk, yv, hk, hv, s, e1, n) == 0);
+  }
+
+  /* Decode deltas streamed on a side stream (dv_delta_streamer) after a
+   * snapshot of [s, e): two more tokens; the replica then restores to
+   * [s, e + 2) (where the tokens fit). */
+  {
+    int32_t lo[B], hi[B];
+    for (int b = 0; b < B; ++b) hi[b] = e[b];
+    const size_t cap = bytes + 2 * delta;
+    uint8_t* ar2 = NULL;
+    CHECK(cudaHostAlloc((void**)&ar2, cap, cudaHostAllocMapped) == cudaSuccess);
+    dv_replica* r2 = NULL;
+    CHECK(dv_replica_create(&r2, ar2, cap, B) == DV_OK);
+    CHECK(dv_replica_append(r2, &c, 0, L, s, e, 0, NULL, 0, ps) == DV_OK);
+    dv_delta_streamer* ds = NULL;
+    CHECK(dv_delta_streamer_create(&ds, r2, ps, cs, NULL, 0) == DV_OK);
+    for (int k = 0; k < 2; ++k) {
+      for (int b = 0; b < B; ++b) {
+        lo[b] = hi[b];
+        hi[b] = hi[b] < S ? hi[b] + 1 : hi[b];
+      }
+      CHECK(dv_delta_stream(ds, &c, 0, L, lo, hi, 1 + k) == DV_OK);
+    }
+    CHECK(dv_delta_streamer_join(ds) == DV_OK && dv_delta_streamer_wait(ds) == DV_OK);
+    cudaMemset(yk, 0, n * P);
+    cudaMemset(yv, 0, n * P);
+    CHECK(cudaDeviceSynchronize() == cudaSuccess);
+    CHECK(dv_replica_restore_batched(r2, &y, -1, NULL, 0, NULL) == DV_OK);
+    CHECK(cudaDeviceSynchronize() == cudaSuccess);
+    CHECK(check_cache(yk, yv, hk, hv, s, hi, n) == 0);
+
+    /* Two microbatches (rep: [s, e + 1), r2: [s, e + 2)) through two caches
+     * (dv_swapper): each acquire hands out a cache holding its replica. */
+    void *wk, *wv;
+    CHECK(cudaMalloc(&wk, n * P) == cudaSuccess && cudaMalloc(&wv, n * P) == cudaSuccess);
+    cudaMemset(wk, 0, n * P);
+    cudaMemset(wv, 0, n * P);
+    cudaMemset(yk, 0, n * P);
+    cudaMemset(yv, 0, n * P);
+    dv_cache w = c;
+    w.k_base = wk;
+    w.v_base = wv;
+    CHECK(cudaDeviceSynchronize() == cudaSuccess);
+    dv_swapper* sw = NULL;
+    CHECK(dv_swapper_create(&sw, &y, &w, ft, ps, cs) == DV_OK);
+    int32_t none[B];
+    memcpy(none, e, sizeof e);
+    dv_replica* mb[2] = {rep, r2};
+    const int32_t* want_hi[2] = {e1, hi};
+    for (int i = 0; i < 4; ++i) {
+      int32_t slot = -1;
+      CHECK(dv_swapper_acquire(sw, mb[i % 2], &slot) == DV_OK);
+      CHECK(dv_swapper_prefetch(sw, mb[(i + 1) % 2]) == DV_OK);
+      CHECK(cudaStreamSynchronize(ps) == cudaSuccess);
+      CHECK(check_cache(slot == 0 ? yk : wk, slot == 0 ? yv : wv, hk, hv, s, want_hi[i % 2], n) ==
+            0);
+      CHECK(dv_swapper_release(sw, mb[i % 2], 0, L, none, none, 10 + i) == DV_OK);
+    }
+    CHECK(dv_swapper_wait(sw) == DV_OK);
+    dv_swapper_destroy(sw);
+    dv_delta_streamer_destroy(ds);
+    dv_replica_destroy(r2);
+  }
+
   dv_replica_destroy(rep);
   dv_fetcher_destroy(ft);
   dv_streamer_destroy(st);

@@ -98,3 +98,37 @@ def test_batched_restore_in_a_globally_captured_graph():
         for c in (fused, staged):
             assert np.array_equal(H.to_np(c.k), kw) and np.array_equal(H.to_np(c.v), vw)
     rep.close()
+
+
+def test_unpack_records_in_a_globally_captured_graph():
+    """dv_kv_unpack_records of a device-resident log (a snapshot, a run of
+    one-token deltas, a ragged record) captured in global mode: each replay
+    gives the oracle's in-order restore."""
+    g = Geometry("caplog", 2, 4, 3, 128, 200, 2, "fp16")
+    kh, vh = H.host_cache(g, 95)
+    zero = np.zeros(g.batch, np.int32)
+    pos = np.array([50, 7, 120, 90], np.int32)
+    records = [(0, g.num_layers, zero, pos.copy())]
+    for k in range(40):
+        records.append((0, g.num_layers, pos.copy(), (pos + 1).astype(np.int32)))
+        pos = pos + 1
+    records.append((0, g.num_layers, pos.copy(), (pos + np.array([2, 0, 3, 1])).astype(np.int32)))
+    data = [ORC.pack(g, kh, vh, a, b, s_, e_) for a, b, s_, e_ in records]
+    kw, vw = ORC.restore(g, [(a, b, s_, e_, d) for (a, b, s_, e_), d in zip(records, data)])
+    log = torch.from_numpy(np.concatenate(data)).cuda()
+    z = H.device_cache(g, fill="zero")
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):  # eager once
+        dv.dv_kv_unpack_records(z, records, log, stream=s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        dv.dv_kv_unpack_records(z, records, log, stream=s)
+    for _ in range(2):
+        z.k.zero_()
+        z.v.zero_()
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(H.to_np(z.k), kw) and np.array_equal(H.to_np(z.v), vw)

@@ -23,7 +23,8 @@ def test_parity_suites_under_the_checked_build():
     env = dict(os.environ, DV_LIBRARY="checked")
     cmd = [sys.executable, "-m", "pytest", "-x", "-q", "-m", "gpu", "-p", "no:cacheprovider",
            "tests/test_gpu_parity.py", "tests/test_gpu_streaming.py",
-           "tests/test_gpu_restore_batched.py", "tests/test_gpu_fuzz.py"]
+           "tests/test_gpu_restore_batched.py", "tests/test_gpu_fuzz.py",
+           "tests/test_gpu_microbatch.py"]
     r = subprocess.run(cmd, cwd=str(ROOT), env=env, capture_output=True, text=True, timeout=1200)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
 

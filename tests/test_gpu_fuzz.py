@@ -177,3 +177,69 @@ def test_random_replica_logs_restore_like_the_oracle(block):
         assert np.array_equal(H.to_np(z.v), vw), where
         rep.close()
         del z, cache, arena, logs
+
+
+@pytest.mark.parametrize("block", range(2))
+def test_random_decode_logs_restore_like_the_oracle(block):
+    """Random decode logs, the run kernel's domain: a snapshot, then stretches
+    of one-token records (each one token further on for the live sequences),
+    broken at random by a change of the live set, a change of layer range, a
+    ragged or multi-token record, a repeated position (a record over the
+    previous one's slices, with new bytes) or new live content.  Restored
+    fused, staged or through a fetcher, and by dv_kv_unpack_records from
+    device memory, each against the oracle's in-order restore."""
+    import torch
+    rng = np.random.default_rng(0xD0C + block)
+    for i in range(16):
+        g = _geometry(rng, 2000 + 100 * block + i, max_bytes=2 << 20)
+        if g.max_seq < 4:
+            continue
+        seed = 9000 + 100 * block + i
+        kh, vh = H.host_cache(g, seed)
+        cache = H.device_cache(g, fill=(kh, vh))
+        B, S, L = g.batch, g.max_seq, g.num_layers
+        zs = np.zeros(B, np.int32)
+        pos = rng.integers(0, max(1, S // 3), size=B).astype(np.int32)
+        logs = [(0, L, zs, pos.copy(), ORC.pack(g, kh, vh, 0, L, zs, pos), cache)]
+        live = rng.random(B) < 0.8
+        l0, l1 = 0, L
+        for r in range(int(rng.integers(2, 90))):
+            u = rng.random()
+            if u < 0.05:
+                live = rng.random(B) < 0.7
+            elif u < 0.08:
+                l0 = int(rng.integers(0, L))
+                l1 = int(rng.integers(l0 + 1, L + 1))
+            elif u < 0.1:
+                kh, vh = H.host_cache(g, seed * 31 + r)
+                cache = H.device_cache(g, fill=(kh, vh))
+            elif u < 0.12:
+                pos = np.maximum(pos - 1, 0).astype(np.int32)   # the last token again
+            act = (live & (pos < S)).astype(np.int32)
+            if rng.random() < 0.05:                              # a multi-token record
+                act = np.minimum(rng.integers(0, 3, size=B), S - pos).astype(np.int32)
+            s, e = pos.copy(), (pos + act).astype(np.int32)
+            logs.append((l0, l1, s, e, ORC.pack(g, kh, vh, l0, l1, s, e), cache))
+            pos = e
+        total = sum(d.size for *_, d, _ in logs)
+        arena = H.pinned(total + 64)
+        rep = dv.Replica(arena, g.batch)
+        for step, (a0, a1, s, e, _, c) in enumerate(logs):
+            rep.append(c, a0, a1, s, e, step=step)
+        slabs = [d.size // (a1 - a0) for a0, a1, _, _, d, _ in logs if d.size]
+        slab = max(slabs) if slabs else 16
+        kw, vw = ORC.restore(g, [(a0, a1, s, e, d) for a0, a1, s, e, d, _ in logs])
+        for how in ("fused", "staged", "fetched"):
+            z = _restore_into_zero(g, rep, how, slab, total, rng)
+            where = (g, len(logs), how)
+            assert np.array_equal(H.to_np(z.k), kw), where
+            assert np.array_equal(H.to_np(z.v), vw), where
+        z = H.device_cache(g, fill="zero")
+        src = torch.from_numpy(np.concatenate([d for *_, d, _ in logs]) if total
+                               else np.zeros(16, np.uint8)).cuda()
+        torch.cuda.synchronize()
+        dv.dv_kv_unpack_records(z, [(a0, a1, s, e) for a0, a1, s, e, _, _ in logs], src)
+        assert np.array_equal(H.to_np(z.k), kw), (g, "unpack_records")
+        assert np.array_equal(H.to_np(z.v), vw), (g, "unpack_records")
+        rep.close()
+        del z, cache, arena, logs

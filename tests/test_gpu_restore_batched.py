@@ -331,3 +331,34 @@ def test_unpack_records_errors_enqueue_nothing():
     assert ei.value.status == dv.DV_ERR_RANGE
     assert not H.to_np(z.k).any() and not H.to_np(z.v).any()
     dv.dv_kv_unpack_records(z, [], None)           # nothing to do
+
+
+def test_fetched_restore_in_parts_matches_the_whole():
+    """dv_replica_restore_fetched_steps: the log restored in consecutive step
+    ranges into the same cache (the snapshot, the first deltas, the rest)
+    equals the oracle's in-order restore of the whole log, and a range that
+    stops short leaves the later records out."""
+    for g, log in ((GEOMS[0], standard_log(GEOMS[0], 111)),
+                   (RUN_GEOMS[-2], decode_run_log(RUN_GEOMS[-2], 112, 120, finish_at=50))):
+        n = len(log.records)
+        slot = max(min_staging(log), 64 << 10)
+        cs = torch.cuda.Stream()
+        f = dv.Fetcher(H.device_bytes(slot), H.device_bytes(slot), cs, torch.cuda.Stream())
+        for cuts in ((1, n // 2), (3, 4, n - 1), (n,)):
+            z = H.device_cache(g, fill="zero")
+            torch.cuda.synchronize()
+            lo = 0
+            for hi in cuts + (n,):
+                log.rep.restore_fetched(z, f, upto_step=hi, from_step=lo)
+                lo = hi
+            f.wait()
+            kw, vw = ORC.restore(g, log.records)
+            assert np.array_equal(H.to_np(z.k), kw), (g.name, cuts)
+            assert np.array_equal(H.to_np(z.v), vw), (g.name, cuts)
+        z = H.device_cache(g, fill="zero")
+        torch.cuda.synchronize()
+        log.rep.restore_fetched(z, f, upto_step=n // 2, from_step=2)
+        f.wait()
+        kw, vw = ORC.restore(g, log.records[2:n // 2])
+        assert np.array_equal(H.to_np(z.k), kw) and np.array_equal(H.to_np(z.v), vw)
+        f.close()
