@@ -519,8 +519,8 @@ class Bloom:
         the host link), each layer restored into the second cache through the
         fetcher as soon as it is in host memory (the host-to-device copy of
         layer l overlaps the device-to-host pack of layer l+1), then the 256
-        deltas appended in decode order and restored (runs of records, the
-        copy of one piece overlapping the unpack of the previous)."""
+        deltas appended in decode order, each 64 restored (one run of records)
+        while the next 64 go out."""
         g, s = self.g, self.stream
         L = g.num_layers
         rep = self.replica
@@ -530,10 +530,14 @@ class Bloom:
             rep.append(self.cache, l, l + 1, self.zs, self.len0, step=l, stream=s)
             self.in_copy.wait_stream(s)  # layer l is in host memory
             rep.restore_fetched(self.cache_b, self.fetcher, upto_step=l + 1, from_step=l)
-        for k, (a, b) in enumerate(self.deltas):
-            rep.append(self.cache, 0, L, a, b, step=L + k, stream=s)
-        self.in_copy.wait_stream(s)      # the deltas are in host memory
-        rep.restore_fetched(self.cache_b, self.fetcher, from_step=L)
+        chunk = 64                       # deltas restored as they accumulate
+        for k0 in range(0, self.nd, chunk):
+            for k in range(k0, min(self.nd, k0 + chunk)):
+                a, b = self.deltas[k]
+                rep.append(self.cache, 0, L, a, b, step=L + k, stream=s)
+            self.in_copy.wait_stream(s)  # these deltas are in host memory
+            rep.restore_fetched(self.cache_b, self.fetcher, upto_step=L + k0 + chunk,
+                                from_step=L + k0)
         s.wait_stream(self.in_unpack)
 
     def timed_e2e(self, steps, warmup, world):
@@ -1701,8 +1705,8 @@ def run_mine(args):
                 "path": "dv_replica_append of the snapshot one layer at a time (fused: the "
                         "pack stores into pinned host memory), each layer restored through a "
                         "fetcher (dv_replica_restore_fetched_steps) while the next goes out; "
-                        "then the 256 deltas appended and restored as runs of records "
-                        "(one-layer slots)"},
+                        "then the 256 deltas appended, each 64 restored as a run of records "
+                        "while the next 64 go out (one-layer slots)"},
         "gpt2_step": gpt2,
         "swap": swap,
         "naive_vs_buffered": naive,

@@ -436,7 +436,10 @@ void dv_replica_destroy(dv_replica* replica);
  * compute in;  dv_swapper_prefetch(next);  the step's kernels on the compute
  * stream;  dv_swapper_release(x, the slices the step wrote, step).  No call
  * blocks the host.  The caller orders earlier work on the two caches before
- * the first call.  Borrows the caches, the fetcher and the streams; owns six
+ * the first call.  A microbatch is known by its replica handle: destroy the
+ * swapper before a replica it has seen, and do not truncate or append to a
+ * replica outside the swapper while it sits in a cache (the cache would no
+ * longer match it).  Borrows the caches, the fetcher and the streams; owns six
  * events.  Not for two threads at once. */
 typedef struct dv_swapper dv_swapper;
 
