@@ -475,8 +475,9 @@ bool context_id(unsigned long long* id) {
   if (!get_current || !get_id) return false;
   CUcontext ctx = nullptr;
   if (get_current(&ctx) != CUDA_SUCCESS) return false;
-  if (!ctx) {  // the runtime makes the device's primary context current on first use
-    if (cudaFree(nullptr) != cudaSuccess) {
+  if (!ctx) {  // setting the current device again makes its primary context current
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) {
       cudaGetLastError();
       return false;
     }
