@@ -512,29 +512,33 @@ class Bloom:
         self.in_copy = torch.cuda.Stream()
         self.in_unpack = torch.cuda.Stream()
         self.fetcher = dv.Fetcher(self.slots[0], self.slots[1], self.in_copy, self.in_unpack)
+        # the appends' staging: packs land here and copy engines take them to
+        # the host, so both directions of the link run on copy engines
+        self.out_staging = torch.empty(slot, dtype=torch.uint8, device="cuda")
 
     def e2e_step(self):
         """The log through the host replica and back: the snapshot appended
-        layer by layer (each a pack storing straight into pinned memory over
-        the host link), each layer restored into the second cache through the
-        fetcher as soon as it is in host memory (the host-to-device copy of
-        layer l overlaps the device-to-host pack of layer l+1), then the 256
-        deltas appended in decode order, each 64 restored (one run of records)
-        while the next 64 go out."""
+        layer by layer (each packed into a device buffer and copied to pinned
+        memory by a copy engine), each layer restored into the second cache
+        through the fetcher as soon as it is in host memory (the host-to-device
+        copy of layer l overlaps the device-to-host copy of layer l+1: copy
+        engines both ways), then the 256 deltas appended in decode order, each
+        64 restored (one run of records) while the next 64 go out."""
         g, s = self.g, self.stream
         L = g.num_layers
         rep = self.replica
         rep.truncate(0)
         self.in_unpack.wait_stream(s)    # the second cache is free
+        stg = self.out_staging
         for l in range(L):
-            rep.append(self.cache, l, l + 1, self.zs, self.len0, step=l, stream=s)
+            rep.append(self.cache, l, l + 1, self.zs, self.len0, step=l, staging=stg, stream=s)
             self.in_copy.wait_stream(s)  # layer l is in host memory
             rep.restore_fetched(self.cache_b, self.fetcher, upto_step=l + 1, from_step=l)
         chunk = 64                       # deltas restored as they accumulate
         for k0 in range(0, self.nd, chunk):
             for k in range(k0, min(self.nd, k0 + chunk)):
                 a, b = self.deltas[k]
-                rep.append(self.cache, 0, L, a, b, step=L + k, stream=s)
+                rep.append(self.cache, 0, L, a, b, step=L + k, staging=stg, stream=s)
             self.in_copy.wait_stream(s)  # these deltas are in host memory
             rep.restore_fetched(self.cache_b, self.fetcher, upto_step=L + k0 + chunk,
                                 from_step=L + k0)
@@ -561,7 +565,7 @@ class Bloom:
     def close_e2e(self):
         self.fetcher.close()
         self.replica.close()
-        del self.arena, self.slots
+        del self.arena, self.slots, self.out_staging
 
 
 def link_peaks(torch, nbytes=2 << 30, reps=3):
@@ -1702,11 +1706,12 @@ def run_mine(args):
                 "timing": "median step (each step synchronised); over all steps: "
                           f"{e2e_all:.1f} GB/s, slowest step {max(e2e_ts) * 1e3:.1f} ms, "
                           f"fastest {min(e2e_ts) * 1e3:.1f} ms",
-                "path": "dv_replica_append of the snapshot one layer at a time (fused: the "
-                        "pack stores into pinned host memory), each layer restored through a "
-                        "fetcher (dv_replica_restore_fetched_steps) while the next goes out; "
-                        "then the 256 deltas appended, each 64 restored as a run of records "
-                        "while the next 64 go out (one-layer slots)"},
+                "path": "dv_replica_append of the snapshot one layer at a time (staged: the "
+                        "pack into a device buffer, a copy engine to the host), each layer "
+                        "restored through a fetcher (dv_replica_restore_fetched_steps) while "
+                        "the next goes out; then the 256 deltas appended the same way, each "
+                        "64 restored as a run of records while the next 64 go out "
+                        "(one-layer slots)"},
         "gpt2_step": gpt2,
         "swap": swap,
         "naive_vs_buffered": naive,
