@@ -64,7 +64,7 @@ def make_microbatches(n, rounds, seed=500):
     return out
 
 
-def run_rounds(mbs, rounds, check_each_step, compute, swap, fetch_streams):
+def run_rounds(mbs, rounds, check_each_step, compute, swap, fetch_streams, prefetch=True):
     """rounds x N steps through a swapper; returns the swapper's two caches."""
     g, L = G, G.num_layers
     caches = [H.device_cache(g, fill="zero") for _ in range(2)]
@@ -78,7 +78,7 @@ def run_rounds(mbs, rounds, check_each_step, compute, swap, fetch_streams):
     for i, m in enumerate(order):
         mb = mbs[m]
         slot = sw.acquire(mb.rep)
-        if i + 1 < len(order):
+        if prefetch and i + 1 < len(order):
             sw.prefetch(mbs[order[i + 1]].rep)
         cache = caches[slot]
         if check_each_step:
@@ -108,14 +108,18 @@ def run_rounds(mbs, rounds, check_each_step, compute, swap, fetch_streams):
     return caches, sw, last
 
 
-@pytest.mark.parametrize("check_each_step", [True, False], ids=["checked", "pipelined"])
-def test_swapper_matches_the_oracle(check_each_step):
+@pytest.mark.parametrize("check_each_step, prefetch",
+                         [(True, True), (False, True), (True, False)],
+                         ids=["checked", "pipelined", "no-prefetch"])
+def test_swapper_matches_the_oracle(check_each_step, prefetch):
+    """no-prefetch: every acquire finds its microbatch out of the caches and
+    swaps it in itself, into the cache the previous step did not use."""
     rounds = 3
     mbs = make_microbatches(4, rounds)
     compute = torch.cuda.Stream()
     swap = torch.cuda.Stream(priority=-1)
     fetch = (torch.cuda.Stream(priority=-1), torch.cuda.Stream(priority=-1))
-    caches, _, last = run_rounds(mbs, rounds, check_each_step, compute, swap, fetch)
+    caches, _, last = run_rounds(mbs, rounds, check_each_step, compute, swap, fetch, prefetch)
     for m, mb in enumerate(mbs):
         assert mb.rep.info()[0] == 1 + rounds
         z = H.device_cache(G, fill="zero")
@@ -146,7 +150,7 @@ def test_swapper_errors():
     mbs = make_microbatches(2, 1, seed=700)
     c0 = H.device_cache(G, fill="zero")
     c1 = H.device_cache(G, fill="zero")
-    f = dv.Fetcher(H.device_bytes(1 << 20), H.device_bytes(1 << 20))
+    f = dv.Fetcher(H.device_bytes(4 << 20), H.device_bytes(4 << 20))
     other = Geometry("other", 3, 6, 4, 128, 150, 2, "fp16")
     with pytest.raises(dv.DvError) as ei:
         dv.Swapper(c0, H.device_cache(other, fill="zero"), f)
