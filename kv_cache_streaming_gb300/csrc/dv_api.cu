@@ -552,15 +552,12 @@ struct LogRec {
   int64_t step;
 };
 
-// Shortest run of one-token records that goes to the run kernel; shorter
-// stretches go to the record kernel.
-constexpr int kMinRun = 2;
-
 // The non-empty records of a log, validated against a cache, and how they go:
 //  - alone: long ranges (the tile kernel's, normally a snapshot), or larger
 //    than a piece, unpacked by themselves;
-//  - run[i] >= kMinRun: records i .. i + run[i] - 1 are a run of one-token
-//    records (run_length), unpacked by the run kernel;
+//  - run[i] > 1: records i .. i + run[i] - 1 are a run of one-token records
+//    (run_length) at least dv::run_min_records long, unpacked by the run
+//    kernel;
 //  - the others, consecutive and disjoint, by the record kernel.
 struct LogPlan {
   std::vector<LogRec> todo;
@@ -575,7 +572,7 @@ struct LogPlan {
   // that fit the parameters and (piece > 0) piece bytes together.
   int batch_at(int i, size_t piece) const {
     int n = 0;
-    while (i + n < (int)todo.size() && !alone[i + n] && (n == 0 || run[i + n] < kMinRun)) ++n;
+    while (i + n < (int)todo.size() && !alone[i + n] && (n == 0 || run[i + n] <= 1)) ++n;
     const int k = dv::records_per_launch(base, recs.data() + i, n);
     size_t bytes = 0;
     for (int j = 0; j < k; ++j) {
@@ -638,6 +635,7 @@ dv_status plan_log(const dv_cache* cache, const std::vector<LogRec>& all, size_t
   // Runs of one-token records, greedily from the front, among the records
   // that do not go alone and lie back to back.
   const int n = (int)lp->todo.size();
+  const int min_run = dv::run_min_records(lp->base);
   lp->run.assign((size_t)n, 1);
   for (int i = 0; i < n;) {
     if (lp->alone[i]) {
@@ -649,7 +647,7 @@ dv_status plan_log(const dv_cache* cache, const std::vector<LogRec>& all, size_t
            lp->todo[m].offset == lp->todo[m - 1].offset + lp->todo[m - 1].bytes)
       ++m;
     const int len = dv::run_length(lp->base, lp->recs.data() + i, m - i);
-    if (len >= kMinRun) {
+    if (len >= min_run) {
       lp->run[i] = len;
       i += len;
     } else {
@@ -703,7 +701,7 @@ dv_status unpack_log_direct(const dv_cache* cache, LogPlan& lp, const uint8_t* s
       if ((err = dv::launch_unpack(q, src + first.offset, stream, dv::kAuto)) != cudaSuccess)
         return cuda_fail(err, "log unpack launch");
       ++i;
-    } else if (lp.run[i] >= kMinRun) {
+    } else if (lp.run[i] > 1) {
       const int len = lp.run[i];
       for (int j = 0; j < len;) {
         const int k = std::min(lp.run_piece(i + j, 0), len - j);
@@ -1202,7 +1200,7 @@ dv_status dv_replica_restore_batched(const dv_replica* r, const dv_cache* cache,
       ++i;
       continue;
     }
-    if (lp.run[i] >= kMinRun) {  // a run, in pieces of as many records as staging holds
+    if (lp.run[i] > 1) {  // a run, in pieces of as many records as staging holds
       const int len = lp.run[i];
       for (int j = 0; j < len;) {
         const int k = std::min(lp.run_piece(i + j, staging_bytes), len - j);
@@ -1270,7 +1268,7 @@ dv_status dv_replica_restore_fetched_steps(const dv_replica* r, const dv_cache* 
       ++i;
       continue;
     }
-    if (lp.run[i] >= kMinRun) {  // a run, in pieces of as many records as a slot holds
+    if (lp.run[i] > 1) {  // a run, in pieces of as many records as a slot holds
       const int len = lp.run[i];
       for (int j = 0; j < len;) {
         const int k = std::min(lp.run_piece(i + j, h->slot_bytes), len - j);

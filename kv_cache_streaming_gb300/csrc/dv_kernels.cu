@@ -1214,6 +1214,17 @@ int run_length(const Plan& cache, const RecordRanges* recs, int n) {
   return k;
 }
 
+int run_min_records(const Plan& cache) {
+  // A run's tiles cost about the same whatever their depth, so a run pays once
+  // it fills a quarter of the token block: measured on GB300 restoring runs of
+  // one-token records from device memory, the record kernel wins at 16 records
+  // and the run kernel at 32 for head_dim 64 (TB = 128), at 8 and at 16 for
+  // head_dim 128 (TB = 64), in 2-byte elements.
+  const int tb = cache.C == 8 ? TileShape<3>::TB : cache.C == 16 ? TileShape<4>::TB
+                                                                 : TileShape<-1>::TB;
+  return tb / 4 > 2 ? tb / 4 : 2;
+}
+
 int run_max_records(const Plan& cache, const RecordRanges& first) {
   int64_t a = 0;
   for (int32_t b = 0; b < cache.B; ++b) a += first.end[b] > first.start[b];

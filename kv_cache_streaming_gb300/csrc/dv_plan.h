@@ -89,6 +89,9 @@ cudaError_t launch_unpack_records(const Plan& cache, const RecordRanges* recs, i
 // the geometry is beyond the tile kernel).  The records must lie back to back
 // in the source.
 int run_length(const Plan& cache, const RecordRanges* recs, int n);
+// The fewest records of a run worth a launch_unpack_run (a quarter of the tile
+// kernel's token block); shorter runs go to the record kernel.
+int run_min_records(const Plan& cache);
 // The most records of a run one launch_unpack_run call takes (its tile count
 // stays below 2^31).
 int run_max_records(const Plan& cache, const RecordRanges& first);
