@@ -189,10 +189,11 @@ dv_status dv_kv_unpack_variant(const dv_cache* cache, int32_t l0, int32_t l1,
  * memory of src_bytes (at least the records' total).  Records long enough for
  * the tile kernel are unpacked by themselves; runs of one-token records (the
  * decode deltas of consecutive steps over the same sequences: record k one
- * token further on than the one before; at least 16 records at head_dim 128,
- * 32 at head_dim 64, in 2-byte elements) are unpacked together, each K row's
- * consecutive tokens written as one span; the other records go in as few
- * record-batched launches as the kernel parameters allow.  Validates every
+ * token further on than the one before; two records or more at head_dim 64
+ * and 128 in 2-byte elements, a quarter of the token block otherwise) are
+ * unpacked together, each K row's consecutive tokens written as one span; the
+ * other records go in as few record-batched launches as the kernel parameters
+ * allow.  Validates every
  * record before enqueuing anything. */
 dv_status dv_kv_unpack_records(const dv_cache* cache, int32_t num_records,
                                const int32_t* layers, const int32_t* ranges, const void* src,

@@ -215,6 +215,15 @@ dv_status plan_ranges(const dv_cache* c, int32_t l0, int32_t l1, const int32_t* 
   return DV_OK;
 }
 
+// Makes the current device's primary context current on a thread that has
+// none yet (one that has made no CUDA runtime call): the pointer attributes of
+// pinned host memory, its device-visible address above all, are answered per
+// context, and a thread without one gets none.
+void ensure_context() {
+  unsigned long long id = 0;
+  dv::context_id(&id);
+}
+
 // Device-visible address of `ptr` after checking its memory kind; when the
 // driver knows the allocation, also that [ptr, ptr + need) lies inside it.
 dv_status resolve(const void* ptr, size_t need, bool allow_host, const char* what, void** dev,
@@ -222,6 +231,7 @@ dv_status resolve(const void* ptr, size_t need, bool allow_host, const char* wha
   if (is_host) *is_host = false;
   if (!ptr) return fail(DV_ERR_INVALID_ARG, "%s is NULL", what);
   if (!aligned16(ptr)) return fail(DV_ERR_MISALIGNED, "%s %p is not 16-byte aligned", what, ptr);
+  ensure_context();
   cudaPointerAttributes a;
   cudaError_t err = cudaPointerGetAttributes(&a, ptr);
   if (err != cudaSuccess) {
@@ -332,6 +342,7 @@ dv_status do_unpack(const dv_cache* c, int32_t l0, int32_t l1, const int32_t* s,
 dv_status check_host(const void* ptr, const char* what, void** dev) {
   if (!ptr) return fail(DV_ERR_INVALID_ARG, "%s is NULL", what);
   if (!aligned16(ptr)) return fail(DV_ERR_MISALIGNED, "%s %p is not 16-byte aligned", what, ptr);
+  ensure_context();
   cudaPointerAttributes a;
   const cudaError_t err = cudaPointerGetAttributes(&a, ptr);
   if (err != cudaSuccess) {

@@ -10,7 +10,7 @@
 // one V row.  Bytes are copied as bit patterns and never pass through
 // floating point.
 //
-// Four kernels, each with a pack and an unpack form but the last:
+// Six kernels, the first three with a pack and an unpack form:
 //  * tile_kernel (long ranges): one CTA of 256 threads moves one tile, up to TB
 //    tokens of one (layer, K|V, sequence, head); TB * C = 1024 chunks (16 KiB)
 //    when C is 8 or 16, four in flight per thread.  A V tile is one contiguous
@@ -33,7 +33,11 @@
 //    each lane splits its own offset into head, token and chunk with the
 //    sequence's multiply-high constant (a window that crosses a sequence
 //    looks each chunk up on its own); no shared memory, no barrier.
-//  * record_unpack_kernel (batched restore of log records): the flat
+//  * run_unpack_kernel / run_group_kernel (batched restore of runs of
+//    one-token log records, the decode deltas of consecutive steps): the
+//    tile kernel's unpack with one token per record, tiles of one head (long
+//    runs) or of several heads side by side (short runs).
+//  * record_unpack_kernel (batched restore of other log records): the flat
 //    kernel's unpack with one more level, a record table in the parameters.
 // All launches use programmatic dependent launch: a kernel waits for the grids
 // it depends on (griddepcontrol.wait) before touching memory, then lets the
@@ -725,6 +729,8 @@ struct RunParams {
   uint64_t m_tpl;          // ceil(2^64 / tiles_per_lkv) (0 when it is 1)
   uint64_t m_ah;           // ceil(2^32 / ah)
   uint64_t m_H;            // ceil(2^32 / H)
+  int32_t log2nt;          // grouped tiles: NT = 2^log2nt >= n token slots per head
+  int32_t groups;          // grouped tiles: G = TB / NT heads per tile
   int32_t act_b[MAXB];
   int32_t act_p[MAXB];
 };
@@ -778,6 +784,96 @@ run_unpack_kernel(const __grid_constant__ RunParams<MAXB> p) {
   copy_tile<false, true, LOG2C>(p, first, smem);
   for (tile += gridDim.x; tile < p.total; tile += gridDim.x)
     copy_tile<false, true, LOG2C>(p, decode_run_tile<LOG2TB>(p, tile, C), smem);
+}
+
+// Cache chunk of chunk c of token t of the g-th (sequence, head) of a grouped
+// tile starting at (sequence, head) index ah0 (K: row c of its block; V: its
+// token row), or nullptr past the last (sequence, head).
+template <int MAXB, int LOG2C>
+__device__ __forceinline__ uint4* group_addr(const RunParams<MAXB>& p, bool is_v, int64_t l,
+                                             uint32_t ah0, int g, int t, int c) {
+  constexpr int32_t C = 1 << LOG2C;
+  const uint32_t ah = ah0 + (uint32_t)g;
+  if (ah >= (uint32_t)p.ah) return nullptr;
+  const uint32_t a = div_by(ah, (uint32_t)p.H, p.m_H);
+  const int64_t bh = (int64_t)p.act_b[a] * p.H + (ah - a * (uint32_t)p.H);
+  const int64_t tt = (int64_t)p.act_p[a] + t;
+  uint4* ptr = is_v ? p.v + l * p.layer_chunks + (bh * p.S + tt) * C + c
+                    : p.k + l * p.layer_chunks + (bh * C + c) * p.S + tt;
+  return (is_v ? DV_OK_V(ptr, 42) : DV_OK_K(ptr, 41)) ? ptr : nullptr;
+}
+
+// Unpacks a run shorter than half the token block (n <= NT = 2^log2nt <=
+// TB / 2) in grouped tiles: a tile is one (layer, K|V) and G = TB / NT
+// consecutive (sequence, head) pairs, each with its n tokens, so that a tile
+// holds as many chunk slots as a full run tile and every thread has work.
+// Token t of the tile reads G * C contiguous chunks of record t (the G heads
+// lie side by side in it).  V goes straight from staging to its token rows; K
+// goes through shared memory ([g][t][c], odd pitch) and out as G * C rows of
+// n consecutive chunks.
+template <int MAXB, int LOG2C>
+__global__ void __launch_bounds__(kThreads, DV_TILE_MIN_BLOCKS)
+run_group_kernel(const __grid_constant__ RunParams<MAXB> p) {
+  extern __shared__ uint4 smem[];  // TB rows of (C | 1) chunks
+  constexpr int C = 1 << LOG2C;
+  constexpr int LOG2TB = TileShape<LOG2C>::LOG2TB;
+  constexpr int TC = (1 << LOG2TB) * C;  // chunk slots of a tile
+  constexpr int SROW = C | 1;
+  const int log2nt = p.log2nt;
+  const int log2gc = LOG2TB - log2nt + LOG2C;  // chunks of one token across the G heads
+  const int n = p.n;
+  int64_t tile = blockIdx.x;
+  if (tile >= p.total) return;
+  pdl_enter();
+  for (; tile < p.total; tile += gridDim.x) {
+    const int64_t lkv = (int64_t)div64_by((uint64_t)tile, (uint64_t)p.tiles_per_lkv, p.m_tpl);
+    const uint32_t ah0 = (uint32_t)(tile - lkv * p.tiles_per_lkv) * (uint32_t)p.groups;
+    const int64_t l = p.l0 + (lkv >> 1);
+    const bool is_v = (lkv & 1) != 0;
+    const uint4* sbase = p.stg + (lkv * p.ah + ah0) * C;
+    // slots in record order: q = (t, g, c), t slowest
+    for (int q0 = threadIdx.x; q0 < TC; q0 += kThreads * kTileUnroll) {
+      uint4 val[kTileUnroll];
+      bool ok[kTileUnroll];
+#pragma unroll
+      for (int u = 0; u < kTileUnroll; ++u) {
+        const int q = q0 + u * kThreads;
+        const int t = q >> log2gc;
+        const int gc = q & ((1 << log2gc) - 1);
+        const uint4* sp = sbase + (int64_t)t * p.rec_chunks + gc;
+        ok[u] = t < n && ah0 + (uint32_t)(gc >> LOG2C) < (uint32_t)p.ah && DV_OK_S(sp, 43);
+        if (ok[u]) val[u] = ld_stream(sp);
+      }
+#pragma unroll
+      for (int u = 0; u < kTileUnroll; ++u) {
+        const int q = q0 + u * kThreads;
+        if (!ok[u]) continue;
+        const int t = q >> log2gc;
+        const int g = (q >> LOG2C) & ((1 << (log2gc - LOG2C)) - 1);
+        const int c = q & (C - 1);
+        if (is_v) {
+          uint4* cp = group_addr<MAXB, LOG2C>(p, true, l, ah0, g, t, c);
+          if (cp) *cp = val[u];
+        } else {
+          smem[((g << log2nt) + t) * SROW + c] = val[u];
+        }
+      }
+    }
+    if (!is_v) {
+      __syncthreads();
+      // slots in cache order: q = (g, c, t), t fastest: each K row's n tokens
+      for (int q = threadIdx.x; q < TC; q += kThreads) {
+        const int t = q & ((1 << log2nt) - 1);
+        const int row = q >> log2nt;
+        const int g = row >> LOG2C;
+        const int c = row & (C - 1);
+        if (t >= n) continue;
+        uint4* cp = group_addr<MAXB, LOG2C>(p, false, l, ah0, g, t, c);
+        if (cp) *cp = smem[((g << log2nt) + t) * SROW + c];
+      }
+      __syncthreads();
+    }
+  }
 }
 
 // ---- host side -------------------------------------------------------------
@@ -1078,13 +1174,33 @@ cudaError_t run_run(const Plan& cache, const RecordRanges& first, int n, const v
   kp.n = n;
   kp.ah = (int32_t)ah;
   kp.rec_chunks = 2 * (int64_t)nl * ah * cache.C;
-  kp.tiles_per_lkv = ah * nblk;
-  kp.total = 2 * (int64_t)nl * kp.tiles_per_lkv;
-  kp.m_tpl = div64_magic((uint64_t)kp.tiles_per_lkv);
   kp.m_ah = div_magic((uint32_t)ah);
   kp.m_H = div_magic((uint32_t)cache.H);
   kp.stg_lim = (int64_t)n * kp.rec_chunks;
+  kp.log2nt = 0;
+  kp.groups = 1;
   const size_t smem = (size_t)TB * (cache.C | 1) * sizeof(uint4);
+  if constexpr (LOG2C >= 0) {
+  if (2 * n <= TB) {  // a short run: grouped tiles
+    int lg = 0;
+    while ((1 << lg) < n) ++lg;
+    kp.log2nt = lg;
+    kp.groups = TB >> lg;
+    kp.tiles_per_lkv = (ah + kp.groups - 1) / kp.groups;
+    kp.total = 2 * (int64_t)nl * kp.tiles_per_lkv;
+    kp.m_tpl = div64_magic((uint64_t)kp.tiles_per_lkv);
+    const auto gkernel = run_group_kernel<MAXB, LOG2C>;
+    static std::atomic<int64_t> occ_group{0};
+    const int64_t fill = ((int64_t(1) << lg) + n - 1) / n;  // <= 2: NT / n
+    const int64_t gcap = host_cap(
+        cache, (int64_t)sm_count() * blocks_per_sm(gkernel, smem, occ_group), fill);
+    const unsigned ggrid = (unsigned)(kp.total < gcap ? kp.total : gcap);
+    return launch_kernel(gkernel, ggrid, smem, stream, kp);
+  }
+  }
+  kp.tiles_per_lkv = ah * nblk;
+  kp.total = 2 * (int64_t)nl * kp.tiles_per_lkv;
+  kp.m_tpl = div64_magic((uint64_t)kp.tiles_per_lkv);
   const auto kernel = run_unpack_kernel<MAXB, LOG2C>;
   // From host memory, a run shorter than the token block leaves each tile
   // (and so each CTA's bytes in flight over the link) that much emptier than
@@ -1215,14 +1331,15 @@ int run_length(const Plan& cache, const RecordRanges* recs, int n) {
 }
 
 int run_min_records(const Plan& cache) {
-  // A run's tiles cost about the same whatever their depth, so a run pays once
-  // it fills a quarter of the token block: measured on GB300 restoring runs of
-  // one-token records from device memory, the record kernel wins at 16 records
-  // and the run kernel at 32 for head_dim 64 (TB = 128), at 8 and at 16 for
-  // head_dim 128 (TB = 64), in 2-byte elements.
-  const int tb = cache.C == 8 ? TileShape<3>::TB : cache.C == 16 ? TileShape<4>::TB
-                                                                 : TileShape<-1>::TB;
-  return tb / 4 > 2 ? tb / 4 : 2;
+  // C = 8 and 16 (head_dim 64 / 128 in 2-byte elements): runs up to half the
+  // token block go in grouped tiles (run_group_kernel), so any run of two
+  // records or more pays.  Other C have no grouped tiles; there a run's tiles
+  // cost about the same whatever their depth, and it pays from a quarter of
+  // the token block (measured with 2-byte elements before grouped tiles: the
+  // record kernel won at 16 records and the run kernel at 32 for TB = 128, at
+  // 8 and at 16 for TB = 64).
+  if (cache.C == 8 || cache.C == 16) return 2;
+  return TileShape<-1>::TB / 4 > 2 ? TileShape<-1>::TB / 4 : 2;
 }
 
 int run_max_records(const Plan& cache, const RecordRanges& first) {

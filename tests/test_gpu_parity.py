@@ -466,3 +466,52 @@ def test_concurrent_calls_from_threads():
         vw = np.full(g.tensor_bytes, 0x5A, np.uint8)
         ORC.unpack(g, kw, vw, 0, g.num_layers, s, e, want)
         assert np.array_equal(H.to_np(back.k), kw) and np.array_equal(H.to_np(back.v), vw)
+
+
+def test_concurrent_staged_swaps_from_threads():
+    """Six host threads, each on its own stream with its own staging buffer,
+    swap different ranges of one cache out to pinned host memory and back in
+    to caches of their own, staged (two halves per buffer: the copies of every
+    thread share the library's copy stream, ordered by each call's events),
+    20 times each: every host buffer and cache equals the oracle's."""
+    import threading
+    g = Geometry("thrswap", 6, 4, 4, 128, 256, 2, "bf16")
+    kh, vh = H.host_cache(g, 78)
+    cache = H.device_cache(g, fill=(kh, vh))
+    rng = np.random.default_rng(78)
+    jobs = [P.random_ranges(g, rng) for _ in range(6)]
+    hosts = [H.pinned(ORC.staging_bytes(g, 0, g.num_layers, s, e), fill=0) for s, e in jobs]
+    stgs = [H.device_bytes(2 * max(16, ORC.staging_bytes(g, 0, 1, s, e))) for s, e in jobs]
+    backs = [H.device_cache(g, fill=0x3C) for _ in jobs]
+    torch.cuda.synchronize()
+    barrier = threading.Barrier(len(jobs))
+    errors = []
+
+    def worker(i):
+        try:
+            s, e = jobs[i]
+            st = torch.cuda.Stream()
+            barrier.wait()
+            for _ in range(20):
+                dv.dv_swap_out(cache, 0, g.num_layers, s, e, hosts[i], staging=stgs[i], stream=st)
+                dv.dv_swap_in(backs[i], 0, g.num_layers, s, e, hosts[i], staging=stgs[i],
+                              stream=st)
+            st.synchronize()
+        except Exception as ex:  # reported below, from the main thread
+            errors.append(repr(ex))
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(jobs))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for (s, e), host, back in zip(jobs, hosts, backs):
+        n = ORC.staging_bytes(g, 0, g.num_layers, s, e)
+        want = ORC.pack(g, kh, vh, 0, g.num_layers, s, e)
+        assert np.array_equal(host[:n].numpy(), want)
+        kw = np.full(g.tensor_bytes, 0x3C, np.uint8)
+        vw = np.full(g.tensor_bytes, 0x3C, np.uint8)
+        ORC.unpack(g, kw, vw, 0, g.num_layers, s, e, want)
+        assert np.array_equal(H.to_np(back.k), kw) and np.array_equal(H.to_np(back.v), vw)

@@ -275,21 +275,24 @@ def test_runs_of_one_token_records(g):
     log.check(upto=steps // 3 + 5)
 
 
-def test_run_lengths_around_the_token_block():
+@pytest.mark.parametrize("g", [Geometry("runlen16", 2, 4, 2, 128, 720, 2, "fp16"),
+                               Geometry("runlen8", 2, 4, 3, 64, 720, 2, "bf16")],
+                         ids=["C16", "C8"])
+def test_run_lengths_around_the_token_block(g):
     """Runs of every length near the tile's token block (64 tokens at head_dim
-    128, 2-byte elements), each followed by a record that breaks the run."""
-    g = Geometry("runlen", 2, 4, 2, 128, 700, 2, "fp16")
+    128, 128 at 64, in 2-byte elements) and near half of it (the longest run
+    in grouped tiles), each followed by a record that breaks the run."""
     B = g.batch
     zero = np.zeros(B, np.int32)
-    log = Log(g, 808, 2 * ORC.staging_bytes(g, 0, 2, zero, np.full(B, 700, np.int32)))
+    log = Log(g, 808, 2 * ORC.staging_bytes(g, 0, 2, zero, np.full(B, g.max_seq, np.int32)))
     pos = np.array([0, 5, 63, 64], np.int32)
-    for n in (1, 2, 3, 63, 64, 65, 127, 129):
+    for n in (1, 2, 3, 5, 17, 32, 33, 63, 64, 65, 127, 129):
         for k in range(n):
             log.append(0, 2, pos, pos + 1)
             pos = pos + 1
         log.append(0, 2, pos, pos + np.array([1, 0, 1, 0], np.int32))   # breaks the run
         pos = pos + np.array([1, 0, 1, 0], np.int32)
-    assert pos.max() <= 700
+    assert pos.max() <= g.max_seq
     log.check()
     log.check(staging_bytes=log.rep.info()[1])
 
