@@ -86,7 +86,7 @@ def parse_args():
                              "swap-in", "ragged-pack", "ragged-unpack", "delta-graph-pack",
                              "delta-graph-unpack", "bloom-snapshot-pack",
                              "bloom-snapshot-unpack", "bloom-delta-pack", "bloom-run-restore",
-                             "short-ragged-pack", "short-ragged-unpack"],
+                             "short-ragged-pack", "short-ragged-unpack", "gpt2-step"],
                     help="run one kernel of the step on an 8-layer cache of the workload's "
                          "shape, 5 launches, and exit (a small case for profilers); "
                          "flat-*: ragged 16..64-token ranges of the OPT-13B-shaped cache, "
@@ -101,7 +101,9 @@ def parse_args():
                          "step's kernels on its workload cut to 2 layers and batch 16 "
                          "(snapshot pack / unpack: 3 launches; delta pack: 8 launches, 8 "
                          "tokens apart; run restore: 3 launches of 256 one-token records); "
-                         "short-ragged-*: the flat-* ranges under the automatic kernel choice")
+                         "short-ragged-*: the flat-* ranges under the automatic kernel choice; "
+                         "gpt2-step: the GPT2-1.5B side-section step (one stream), 3 graph "
+                         "replays after one eager step")
     return ap.parse_args()
 
 
@@ -1749,6 +1751,19 @@ def run_kernel_case(case):
         return
     if case.startswith("bloom"):
         run_bloom_case(case, torch, dv, synth_gpu)
+        return
+    if case == "gpt2-step":
+        b = Bench()
+        with torch.cuda.stream(b.stream):
+            b.device_step(b.stream, two_streams=False)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=b.stream, capture_error_mode="relaxed"):
+            b.device_step(b.stream, two_streams=False)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        print(f"gpt2-step: 3 replays of {b.launches_per_step} launches, verified {b.verify()}")
         return
     g = replace(GPT2, num_layers=8)
     k = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
