@@ -91,7 +91,8 @@ def parse_args():
                          "shape, 5 launches, and exit (a small case for profilers); "
                          "flat-*: ragged 16..64-token ranges of the OPT-13B-shaped cache, "
                          "flat kernel; record-restore: 5 staged batched restores of 96 "
-                         "decode deltas of the whole cache, one record-kernel launch each; "
+                         "one-token deltas (even and odd sequences in turn: no runs) of the "
+                         "whole cache, one record-kernel launch each; "
                          "swap-*: fused swap of the 8-layer prompt to / from pinned host "
                          "memory (the tile kernel on the host link); ragged-*: the OPT-13B "
                          "workload's lognormal used prefixes, 4 layers, tile kernel; "
@@ -1932,9 +1933,11 @@ def run_bloom_case(case, torch, dv, synth_gpu):
 
 def run_record_case(torch, dv, synth_gpu):
     """A replica of 96 one-token decode deltas (positions 928..1023) of the
-    workload's cache, 236 MB (more than L2), restored 5 times through a device
-    staging buffer: each restore is one host-to-device copy and one launch of
-    the record kernel (96 records of batch 8 fit one launch)."""
+    workload's cache, the even and the odd sequences taking turns (so no two
+    consecutive records share their live sequences and no run forms: the record
+    kernel's case), 118 MB, restored 5 times through a device staging buffer:
+    each restore is one host-to-device copy and one launch of the record kernel
+    (96 records of batch 8 fit one launch)."""
     g = GPT2
     k = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
     v = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
@@ -1943,25 +1946,28 @@ def run_record_case(torch, dv, synth_gpu):
     back = dv.Cache.from_geometry(g, torch.zeros_like(k), torch.zeros_like(v))
     p0, nd = 928, 96
     pos = np.full(g.batch, p0, np.int32)
-    one = dv.dv_staging_bytes(cache, 0, g.num_layers, pos, pos + 1)
-    arena = torch.empty(nd * one, dtype=torch.uint8, pin_memory=True)
+    parity = np.arange(g.batch) % 2
+    recs = [(pos + i, pos + i + (parity == i % 2)) for i in range(nd)]
+    total = sum(dv.dv_staging_bytes(cache, 0, g.num_layers, a, b) for a, b in recs)
+    arena = torch.empty(total, dtype=torch.uint8, pin_memory=True)
     rep = dv.Replica(arena, g.batch)
-    for i in range(nd):
-        rep.append(cache, 0, g.num_layers, pos + i, pos + i + 1, step=i)
-    stg = torch.empty(nd * one, dtype=torch.uint8, device="cuda")
+    for i, (a, b) in enumerate(recs):
+        rep.append(cache, 0, g.num_layers, a, b, step=i)
+    stg = torch.empty(total, dtype=torch.uint8, device="cuda")
     for _ in range(5):
         rep.restore_batched(back, staging=stg)
     torch.cuda.synchronize()
-    n = dv.dv_staging_bytes(cache, 0, g.num_layers, pos, pos + nd)
-    a = torch.empty(n, dtype=torch.uint8, device="cuda")
-    b = torch.empty(n, dtype=torch.uint8, device="cuda")
-    dv.dv_kv_pack(cache, 0, g.num_layers, pos, pos + nd, a)
-    dv.dv_kv_pack(back, 0, g.num_layers, pos, pos + nd, b)
-    torch.cuda.synchronize()
-    assert torch.equal(a, b), "restored slices differ from the source cache"
+    for s_, e_ in recs:  # every restored slice equals the source cache's
+        n = dv.dv_staging_bytes(cache, 0, g.num_layers, s_, e_)
+        a = torch.empty(n, dtype=torch.uint8, device="cuda")
+        b = torch.empty(n, dtype=torch.uint8, device="cuda")
+        dv.dv_kv_pack(cache, 0, g.num_layers, s_, e_, a)
+        dv.dv_kv_pack(back, 0, g.num_layers, s_, e_, b)
+        torch.cuda.synchronize()
+        assert torch.equal(a, b), "restored slices differ from the source cache"
     rep.close()
-    print(f"record-restore: 5 launches of {2 * nd * one} algorithmic bytes each "
-          f"({nd} records, {n} bytes of cache slices)")
+    print(f"record-restore: 5 launches of {2 * total} algorithmic bytes each "
+          f"({nd} records, {total} bytes)")
 
 
 def main():
