@@ -8,7 +8,8 @@ the library this file builds).
 Translation units compile in parallel; the result is
 ``kv_cache_streaming_gb300/libdv.so``.  The CUDA runtime is linked
 statically; the driver is reached through the runtime, so the library also
-loads (for symbol checks) on a machine without a GPU driver.
+loads (for symbol checks) on a machine without a GPU driver.  A linker
+version script (``csrc/libdv.map``) exports the C ABI alone.
 """
 from __future__ import annotations
 
@@ -25,7 +26,7 @@ CSRC = PKG / "csrc"
 OBJ = PKG / "_build"
 LIB = PKG / "libdv.so"
 LIB_CHECKED = PKG / "libdv_checked.so"  # device-side bounds checks (debugging)
-SOURCES = ["dv_api.cu", "dv_kernels.cu", "dv_noalloc.cu"]
+SOURCES = ["dv_api.cu", "dv_replica.cu", "dv_sched.cu", "dv_kernels.cu", "dv_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -57,7 +58,8 @@ def _stale(target: Path, deps) -> bool:
 def build(force: bool = False, checked: bool = False) -> Path:
     """Builds libdv.so, or with `checked` the bounds-checked libdv_checked.so."""
     lib = LIB_CHECKED if checked else LIB
-    deps = [CSRC / s for s in SOURCES] + [CSRC / "dv_plan.h", ROOT / "include" / "dv.h",
+    deps = [CSRC / s for s in SOURCES] + [CSRC / "dv_plan.h", CSRC / "dv_host.h",
+                                          CSRC / "libdv.map", ROOT / "include" / "dv.h",
                                           Path(__file__)]
     if not force and not _stale(lib, deps):
         return lib
@@ -65,7 +67,8 @@ def build(force: bool = False, checked: bool = False) -> Path:
     with ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(lambda src: _compile(src, checked), SOURCES))
     tmp = lib.with_suffix(f".{os.getpid()}.tmp")
-    subprocess.run([nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", str(tmp),
+    subprocess.run([nvcc(), *ARCH, "-shared", "-cudart", "static",
+                    "-Xlinker", f"--version-script={CSRC / 'libdv.map'}", "-o", str(tmp),
                     *map(str, objs)], check=True)
     os.replace(tmp, lib)
     return lib

@@ -1,10 +1,10 @@
-// libdv C ABI: argument validation, planning, the swap paths, the layer
-// streamer and the host-side replica log.  The copy work itself is in
-// dv_kernels.cu; this file only validates, plans and enqueues.
+// libdv C ABI, part 1: status and errors, argument validation and pointer
+// resolution (shared with the other parts through dv_host.h), pack and unpack,
+// the swap paths, and the layer streamer and fetcher.  The copy work itself is
+// in dv_kernels.cu; this file only validates, plans and enqueues.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <algorithm>
 #include <climits>
 #include <cstdarg>
 #include <cstdio>
@@ -14,54 +14,11 @@
 #include <string>
 #include <vector>
 
-#include "../../include/dv.h"
-#include "dv_plan.h"
-
-#ifndef DV_NVTX
-#define DV_NVTX 1  // NVTX ranges around every ABI call that enqueues work
-#endif
-#if DV_NVTX
-#include <nvtx3/nvToolsExt.h>
-#endif
+#include "dv_host.h"
 
 namespace {
 
-// A named range on the calling thread's NVTX stack for the duration of one
-// ABI call, so that a timeline taken with an NVTX-aware profiler shows each
-// call and the launches and copies it enqueued; without a profiler attached
-// the push and pop do nothing.
-struct Trace {
-  explicit Trace(const char* name) {
-#if DV_NVTX
-    nvtxRangePushA(name);
-#else
-    (void)name;
-#endif
-  }
-  ~Trace() {
-#if DV_NVTX
-    nvtxRangePop();
-#endif
-  }
-  Trace(const Trace&) = delete;
-  Trace& operator=(const Trace&) = delete;
-};
-
 thread_local std::string g_last_error;
-
-dv_status fail(dv_status st, const char* fmt, ...) {
-  char buf[512];
-  va_list ap;
-  va_start(ap, fmt);
-  vsnprintf(buf, sizeof(buf), fmt, ap);
-  va_end(ap);
-  g_last_error = buf;
-  return st;
-}
-
-dv_status cuda_fail(cudaError_t err, const char* what) {
-  return fail(DV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(err), cudaGetErrorString(err));
-}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -97,56 +54,52 @@ void* driver_fn(const char* name) {
   return f;
 }
 
-// A library-owned stream for the copies of a pipelined staged swap, one per
-// CUDA context (created on first use there, with the context current; kept
-// until the process exits).  nullptr when none can be had, or when none
-// exists yet and `caller` is being captured into a graph (no stream is made
-// during a capture): the swap then runs in order on the caller's stream.
-cudaStream_t copy_stream(cudaStream_t caller) {
-  static std::mutex mu;
-  static std::vector<std::pair<unsigned long long, cudaStream_t>> streams;
-  unsigned long long id = 0;
-  if (!dv::context_id(&id)) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  for (const auto& e : streams)
-    if (e.first == id) return e.second;
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(caller, &cap) != cudaSuccess) {
-    cudaGetLastError();
-    return nullptr;
-  }
-  if (cap != cudaStreamCaptureStatusNone) return nullptr;
-  cudaStream_t cs = nullptr;
-  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
-    cudaGetLastError();
-    return nullptr;
-  }
-  try {
-    streams.emplace_back(id, cs);
-  } catch (...) {
-    cudaStreamDestroy(cs);
-    return nullptr;
-  }
-  return cs;
+}  // namespace
+
+namespace dv {
+
+dv_status fail(dv_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
 }
 
-// Events a pipelined swap orders its two streams with, created per call and
-// released when the call returns (a recorded event is freed once it
-// completes).
-struct Events {
-  cudaEvent_t e[5] = {};
-  int n = 0;
-  cudaError_t make() {
-    for (; n < 5; ++n) {
-      const cudaError_t err = cudaEventCreateWithFlags(&e[n], cudaEventDisableTiming);
-      if (err != cudaSuccess) return err;
+dv_status cuda_fail(cudaError_t err, const char* what) {
+  return fail(DV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(err), cudaGetErrorString(err));
+}
+
+bool context_id(unsigned long long* id) {
+  using GetCurrentFn = CUresult (*)(CUcontext*);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static const GetCurrentFn get_current =
+      reinterpret_cast<GetCurrentFn>(driver_fn("cuCtxGetCurrent"));
+  static const GetIdFn get_id = reinterpret_cast<GetIdFn>(driver_fn("cuCtxGetId"));
+  if (!get_current || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return false;
+  if (!ctx) {  // setting the current device again makes its primary context current
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
     }
-    return cudaSuccess;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
   }
-  ~Events() {
-    for (int i = 0; i < n; ++i) cudaEventDestroy(e[i]);
-  }
-};
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Makes the current device's primary context current on a thread that has
+// none yet (one that has made no CUDA runtime call): the pointer attributes of
+// pinned host memory, its device-visible address above all, are answered per
+// context, and a thread without one gets none.
+void ensure_context() {
+  unsigned long long id = 0;
+  dv::context_id(&id);
+}
 
 // Validates geometry and ranges (no pointer is touched) and fills `p`.
 dv_status plan_ranges(const dv_cache* c, int32_t l0, int32_t l1, const int32_t* s,
@@ -215,19 +168,10 @@ dv_status plan_ranges(const dv_cache* c, int32_t l0, int32_t l1, const int32_t* 
   return DV_OK;
 }
 
-// Makes the current device's primary context current on a thread that has
-// none yet (one that has made no CUDA runtime call): the pointer attributes of
-// pinned host memory, its device-visible address above all, are answered per
-// context, and a thread without one gets none.
-void ensure_context() {
-  unsigned long long id = 0;
-  dv::context_id(&id);
-}
-
 // Device-visible address of `ptr` after checking its memory kind; when the
 // driver knows the allocation, also that [ptr, ptr + need) lies inside it.
 dv_status resolve(const void* ptr, size_t need, bool allow_host, const char* what, void** dev,
-                  bool* is_host = nullptr) {
+                  bool* is_host) {
   if (is_host) *is_host = false;
   if (!ptr) return fail(DV_ERR_INVALID_ARG, "%s is NULL", what);
   if (!aligned16(ptr)) return fail(DV_ERR_MISALIGNED, "%s %p is not 16-byte aligned", what, ptr);
@@ -292,6 +236,87 @@ dv_status resolve_cache(const dv_cache* c, dv::Plan* p) {
   return DV_OK;
 }
 
+// Memory kind check for the host side of a swap (pinned host memory).
+dv_status check_host(const void* ptr, const char* what, void** dev) {
+  if (!ptr) return fail(DV_ERR_INVALID_ARG, "%s is NULL", what);
+  if (!aligned16(ptr)) return fail(DV_ERR_MISALIGNED, "%s %p is not 16-byte aligned", what, ptr);
+  ensure_context();
+  cudaPointerAttributes a;
+  const cudaError_t err = cudaPointerGetAttributes(&a, ptr);
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return fail(DV_ERR_INVALID_ARG, "%s: cudaPointerGetAttributes failed", what);
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer)
+    return fail(DV_ERR_INVALID_ARG, "%s must be pinned, mapped host memory", what);
+  *dev = a.devicePointer;
+  return DV_OK;
+}
+
+}  // namespace dv
+
+using dv::check_host;
+using dv::cuda_fail;
+using dv::fail;
+using dv::fetch_piece;
+using dv::plan_ranges;
+using dv::resolve;
+using dv::resolve_cache;
+using dv::Trace;
+
+namespace {
+
+// A library-owned stream for the copies of a pipelined staged swap, one per
+// CUDA context (created on first use there, with the context current; kept
+// until the process exits).  nullptr when none can be had, or when none
+// exists yet and `caller` is being captured into a graph (no stream is made
+// during a capture): the swap then runs in order on the caller's stream.
+cudaStream_t copy_stream(cudaStream_t caller) {
+  static std::mutex mu;
+  static std::vector<std::pair<unsigned long long, cudaStream_t>> streams;
+  unsigned long long id = 0;
+  if (!dv::context_id(&id)) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& e : streams)
+    if (e.first == id) return e.second;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(caller, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (cap != cudaStreamCaptureStatusNone) return nullptr;
+  cudaStream_t cs = nullptr;
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  try {
+    streams.emplace_back(id, cs);
+  } catch (...) {
+    cudaStreamDestroy(cs);
+    return nullptr;
+  }
+  return cs;
+}
+
+// Events a pipelined swap orders its two streams with, created per call and
+// released when the call returns (a recorded event is freed once it
+// completes).
+struct Events {
+  cudaEvent_t e[5] = {};
+  int n = 0;
+  cudaError_t make() {
+    for (; n < 5; ++n) {
+      const cudaError_t err = cudaEventCreateWithFlags(&e[n], cudaEventDisableTiming);
+      if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
+  }
+  ~Events() {
+    for (int i = 0; i < n; ++i) cudaEventDestroy(e[i]);
+  }
+};
+
 dv_status check_variant(const dv::Plan& p, int32_t variant) {
   if (variant < dv::kAuto || variant > dv::kToken)
     return fail(DV_ERR_INVALID_ARG, "unknown variant %d", variant);
@@ -336,23 +361,6 @@ dv_status do_unpack(const dv_cache* c, int32_t l0, int32_t l1, const int32_t* s,
   if ((st = resolve(src, (size_t)p.bytes, true, "src", &d, &p.host_side)) != DV_OK) return st;
   const cudaError_t err = dv::launch_unpack(p, d, stream, variant);
   return err == cudaSuccess ? DV_OK : cuda_fail(err, "unpack launch");
-}
-
-// Memory kind check for the host side of a swap (pinned host memory).
-dv_status check_host(const void* ptr, const char* what, void** dev) {
-  if (!ptr) return fail(DV_ERR_INVALID_ARG, "%s is NULL", what);
-  if (!aligned16(ptr)) return fail(DV_ERR_MISALIGNED, "%s %p is not 16-byte aligned", what, ptr);
-  ensure_context();
-  cudaPointerAttributes a;
-  const cudaError_t err = cudaPointerGetAttributes(&a, ptr);
-  if (err != cudaSuccess) {
-    cudaGetLastError();
-    return fail(DV_ERR_INVALID_ARG, "%s: cudaPointerGetAttributes failed", what);
-  }
-  if (a.type != cudaMemoryTypeHost || !a.devicePointer)
-    return fail(DV_ERR_INVALID_ARG, "%s must be pinned, mapped host memory", what);
-  *dev = a.devicePointer;
-  return DV_OK;
 }
 
 enum class Dir { kOut, kIn };
@@ -476,38 +484,6 @@ dv_status do_swap(Dir dir, const dv_cache* c, int32_t l0, int32_t l1, const int3
 
 }  // namespace
 
-namespace dv {
-bool context_id(unsigned long long* id) {
-  using GetCurrentFn = CUresult (*)(CUcontext*);
-  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
-  static const GetCurrentFn get_current =
-      reinterpret_cast<GetCurrentFn>(driver_fn("cuCtxGetCurrent"));
-  static const GetIdFn get_id = reinterpret_cast<GetIdFn>(driver_fn("cuCtxGetId"));
-  if (!get_current || !get_id) return false;
-  CUcontext ctx = nullptr;
-  if (get_current(&ctx) != CUDA_SUCCESS) return false;
-  if (!ctx) {  // setting the current device again makes its primary context current
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) {
-      cudaGetLastError();
-      return false;
-    }
-    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
-  }
-  return get_id(ctx, id) == CUDA_SUCCESS;
-}
-
-dv_status set_error(dv_status st, const char* fmt, ...) {
-  char buf[512];
-  va_list ap;
-  va_start(ap, fmt);
-  vsnprintf(buf, sizeof(buf), fmt, ap);
-  va_end(ap);
-  g_last_error = buf;
-  return st;
-}
-}  // namespace dv
-
 // ---- streamer ----------------------------------------------------------------
 
 struct dv_streamer {
@@ -520,240 +496,6 @@ struct dv_streamer {
   bool used[2];
   int next;
 };
-
-struct dv_fetcher {
-  void* slot[2];
-  size_t slot_bytes;
-  cudaStream_t copy;
-  cudaStream_t unpack;
-  cudaEvent_t copied[2];
-  cudaEvent_t freed[2];
-  bool used[2];
-  int next;
-};
-
-// ---- replica -----------------------------------------------------------------
-
-namespace {
-struct Record {
-  int64_t step;
-  int32_t l0, l1;
-  size_t offset, bytes;
-  size_t ranges;  // index of this record's ranges in dv_replica::ranges (2 * batch ints)
-};
-}  // namespace
-
-struct dv_replica {
-  uint8_t* arena;
-  size_t arena_bytes;
-  size_t used;
-  int32_t batch;
-  std::vector<Record> records;
-  std::vector<int32_t> ranges;
-};
-
-namespace {
-
-// One record of a log: its layers, its ranges (batch starts, then batch ends)
-// and where its staging bytes lie relative to the log's first byte.
-struct LogRec {
-  int32_t l0, l1;
-  const int32_t* ranges;
-  size_t offset, bytes;
-  int64_t step;
-};
-
-// The non-empty records of a log, validated against a cache, and how they go:
-//  - alone: long ranges (the tile kernel's, normally a snapshot), or larger
-//    than a piece, unpacked by themselves;
-//  - run[i] > 1: records i .. i + run[i] - 1 are a run of one-token records
-//    (run_length) at least dv::run_min_records long, unpacked by the run
-//    kernel;
-//  - the others, consecutive and disjoint, by the record kernel.
-struct LogPlan {
-  std::vector<LogRec> todo;
-  std::vector<dv::RecordRanges> recs;
-  std::vector<char> alone;
-  std::vector<int> run;
-  dv::Plan base;  // the cache: geometry, resolved K / V, layers [0, the last record's l1)
-  size_t total = 0;
-
-  // How many records from i on one record-kernel launch takes: consecutive
-  // records neither alone nor the start of a run, whose writes are disjoint,
-  // that fit the parameters and (piece > 0) piece bytes together.
-  int batch_at(int i, size_t piece) const {
-    int n = 0;
-    while (i + n < (int)todo.size() && !alone[i + n] && (n == 0 || run[i + n] <= 1)) ++n;
-    const int k = dv::records_per_launch(base, recs.data() + i, n);
-    size_t bytes = 0;
-    for (int j = 0; j < k; ++j) {
-      if (piece && bytes + todo[i + j].bytes > piece) return j;
-      bytes += todo[i + j].bytes;
-    }
-    return k;
-  }
-
-  // Records per run-kernel launch from a run starting at i (piece > 0: as many
-  // as piece bytes hold).
-  int run_piece(int i, size_t piece) const {
-    int64_t k = dv::run_max_records(base, recs[i]);
-    if (piece) {
-      const int64_t fit = (int64_t)(piece / todo[i].bytes);
-      if (fit < k) k = fit;
-    }
-    return k < 1 ? 1 : (int)k;
-  }
-};
-
-// Validates every record of `all` against `cache` before anything is
-// enqueued and plans the log.  piece > 0: the bytes one copy can carry; a
-// record larger than that goes by itself in groups of layers, so one of its
-// layer slabs must fit.
-dv_status plan_log(const dv_cache* cache, const std::vector<LogRec>& all, size_t piece,
-                   LogPlan* lp) {
-  if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
-  const int32_t B = cache->batch;
-  int32_t l_end = 0;
-  try {
-    dv::Plan q;
-    for (const LogRec& rec : all) {
-      const int32_t* s = rec.ranges;
-      const dv_status st = plan_ranges(cache, rec.l0, rec.l1, s, s + B, &q);
-      if (st != DV_OK) return st;
-      if ((size_t)q.bytes != rec.bytes)
-        return fail(DV_ERR_INVALID_ARG, "record of step %lld does not match this cache geometry",
-                    (long long)rec.step);
-      if (rec.bytes == 0) continue;
-      const bool by_itself = dv::auto_kind(q) == dv::kTile || (piece && rec.bytes > piece);
-      if (by_itself && piece && piece < (size_t)dv::layer_slab_bytes(q))
-        return fail(DV_ERR_BUFFER_TOO_SMALL, "a staging piece of %zu bytes holds less than one "
-                    "layer slab (%lld bytes) of the record of step %lld", piece,
-                    (long long)dv::layer_slab_bytes(q), (long long)rec.step);
-      lp->todo.push_back(rec);
-      lp->recs.push_back(dv::RecordRanges{rec.l0, rec.l1, s, s + B});
-      lp->alone.push_back(by_itself);
-      if (rec.l1 > l_end) l_end = rec.l1;
-      lp->total += rec.bytes;
-    }
-  } catch (...) {
-    return fail(DV_ERR_INVALID_ARG, "out of host memory for the restore plan");
-  }
-  if (lp->todo.empty()) return DV_OK;
-  std::vector<int32_t> zero((size_t)B, 0);
-  dv_status st = plan_ranges(cache, 0, l_end, zero.data(), zero.data(), &lp->base);
-  if (st != DV_OK) return st;
-  if ((st = resolve_cache(cache, &lp->base)) != DV_OK) return st;
-  // Runs of one-token records, greedily from the front, among the records
-  // that do not go alone and lie back to back.
-  const int n = (int)lp->todo.size();
-  const int min_run = dv::run_min_records(lp->base);
-  lp->run.assign((size_t)n, 1);
-  for (int i = 0; i < n;) {
-    if (lp->alone[i]) {
-      ++i;
-      continue;
-    }
-    int m = i + 1;
-    while (m < n && !lp->alone[m] &&
-           lp->todo[m].offset == lp->todo[m - 1].offset + lp->todo[m - 1].bytes)
-      ++m;
-    const int len = dv::run_length(lp->base, lp->recs.data() + i, m - i);
-    if (len >= min_run) {
-      lp->run[i] = len;
-      i += len;
-    } else {
-      ++i;
-    }
-  }
-  return DV_OK;
-}
-
-// The records of `r` with from <= step < upto (no upper limit when upto < 0),
-// planned for `cache`.
-dv_status plan_restore(const dv_replica* r, const dv_cache* cache, int64_t from, int64_t upto,
-                       size_t piece, LogPlan* lp) {
-  if (!r) return fail(DV_ERR_INVALID_ARG, "replica is NULL");
-  if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
-  if (cache->batch != r->batch)
-    return fail(DV_ERR_INVALID_ARG, "cache batch %d differs from the replica's %d", cache->batch,
-                r->batch);
-  std::vector<LogRec> all;
-  try {
-    for (const Record& rec : r->records) {
-      if (upto >= 0 && rec.step >= upto) break;
-      if (rec.step < from) continue;
-      all.push_back(LogRec{rec.l0, rec.l1, r->ranges.data() + rec.ranges, rec.offset, rec.bytes,
-                           rec.step});
-    }
-  } catch (...) {
-    return fail(DV_ERR_INVALID_ARG, "out of host memory for the restore plan");
-  }
-  return plan_log(cache, all, piece, lp);
-}
-
-// Enqueues the unpack of every planned record straight from `src` (the
-// device-visible address of the log's first byte; host memory when
-// `host_side`), on `stream`.
-dv_status unpack_log_direct(const dv_cache* cache, LogPlan& lp, const uint8_t* src,
-                            bool host_side, cudaStream_t stream) {
-  lp.base.host_side = host_side;
-  const int n = (int)lp.todo.size();
-  cudaError_t err = cudaSuccess;
-  for (int i = 0; i < n;) {
-    const LogRec& first = lp.todo[i];
-    if (lp.alone[i]) {
-      dv::Plan q;
-      const dv_status st = plan_ranges(cache, first.l0, first.l1, first.ranges,
-                                       first.ranges + cache->batch, &q);
-      if (st != DV_OK) return st;
-      q.k = lp.base.k;
-      q.v = lp.base.v;
-      q.host_side = host_side;
-      if ((err = dv::launch_unpack(q, src + first.offset, stream, dv::kAuto)) != cudaSuccess)
-        return cuda_fail(err, "log unpack launch");
-      ++i;
-    } else if (lp.run[i] > 1) {
-      const int len = lp.run[i];
-      for (int j = 0; j < len;) {
-        const int k = std::min(lp.run_piece(i + j, 0), len - j);
-        if ((err = dv::launch_unpack_run(lp.base, lp.recs[i + j], k,
-                                         src + lp.todo[i + j].offset, stream)) != cudaSuccess)
-          return cuda_fail(err, "run unpack launch");
-        j += k;
-      }
-      i += len;
-    } else {
-      const int k = lp.batch_at(i, 0);
-      if ((err = dv::launch_unpack_records(lp.base, lp.recs.data() + i, k, src + first.offset,
-                                           stream)) != cudaSuccess)
-        return cuda_fail(err, "record unpack launch");
-      i += k;
-    }
-  }
-  return DV_OK;
-}
-
-// Copies `bytes` from `src` (host memory) into the fetcher's next slot on its
-// copy stream, after that slot's previous unpack, then runs unpack(slot) on
-// its unpack stream after the copy.
-template <typename Unpack>
-cudaError_t fetch_piece(dv_fetcher* h, const void* src, size_t bytes, Unpack&& unpack) {
-  const int i = h->next;
-  cudaError_t err;
-  if (h->used[i] && (err = cudaStreamWaitEvent(h->copy, h->freed[i], 0)) != cudaSuccess)
-    return err;
-  if ((err = cudaMemcpyAsync(h->slot[i], src, bytes, cudaMemcpyDefault, h->copy)) != cudaSuccess)
-    return err;
-  if ((err = cudaEventRecord(h->copied[i], h->copy)) != cudaSuccess) return err;
-  if ((err = cudaStreamWaitEvent(h->unpack, h->copied[i], 0)) != cudaSuccess) return err;
-  if ((err = unpack(h->slot[i])) != cudaSuccess) return err;
-  if ((err = cudaEventRecord(h->freed[i], h->unpack)) != cudaSuccess) return err;
-  h->used[i] = true;
-  h->next = i ^ 1;
-  return cudaSuccess;
-}
-
-}  // namespace
 
 extern "C" {
 
@@ -1063,6 +805,7 @@ dv_status dv_fetch_layer(dv_fetcher* h, const dv_cache* cache, int32_t layer,
   if ((st = resolve_cache(cache, &p)) != DV_OK) return st;
   {
     cudaPointerAttributes a;
+    dv::ensure_context();
     if (cudaPointerGetAttributes(&a, host_src) != cudaSuccess ||
         a.type == cudaMemoryTypeUnregistered) {
       cudaGetLastError();
@@ -1094,558 +837,4 @@ void dv_fetcher_destroy(dv_fetcher* h) {
   cudaEventDestroy(h->freed[1]);
   delete h;
 }
-
-dv_status dv_replica_create(dv_replica** out, void* host_arena, size_t arena_bytes,
-                            int32_t batch) {
-  if (!out) return fail(DV_ERR_INVALID_ARG, "out is NULL");
-  *out = nullptr;
-  if (batch <= 0 || batch > dv::kMaxBatch)
-    return fail(DV_ERR_INVALID_ARG, "batch %d outside [1, %d]", batch, dv::kMaxBatch);
-  void* dev = nullptr;
-  dv_status st = check_host(host_arena, "host_arena", &dev);
-  if (st != DV_OK) return st;
-  dv_replica* r = new (std::nothrow) dv_replica();
-  if (!r) return fail(DV_ERR_INVALID_ARG, "out of host memory for the replica handle");
-  r->arena = static_cast<uint8_t*>(host_arena);
-  r->arena_bytes = arena_bytes;
-  r->used = 0;
-  r->batch = batch;
-  *out = r;
-  return DV_OK;
-}
-
-dv_status dv_replica_append(dv_replica* r, const dv_cache* cache, int32_t l0, int32_t l1,
-                            const int32_t* seq_start, const int32_t* seq_end, int64_t step,
-                            void* staging, size_t staging_bytes, dv_stream stream) {
-  const Trace trace("dv_replica_append");
-  if (!r) return fail(DV_ERR_INVALID_ARG, "replica is NULL");
-  if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
-  if (cache->batch != r->batch)
-    return fail(DV_ERR_INVALID_ARG, "cache batch %d differs from the replica's %d", cache->batch,
-                r->batch);
-  if (!r->records.empty() && step < r->records.back().step)
-    return fail(DV_ERR_INVALID_ARG, "step %lld is before the last record's %lld",
-                (long long)step, (long long)r->records.back().step);
-  size_t bytes = 0;
-  dv_status st = dv_staging_bytes(cache, l0, l1, seq_start, seq_end, &bytes);
-  if (st != DV_OK) return st;
-  const size_t off = r->used;  // records are multiples of 16 bytes
-  if (off + bytes > r->arena_bytes)
-    return fail(DV_ERR_BUFFER_TOO_SMALL, "replica arena full: %zu + %zu > %zu bytes", off, bytes,
-                r->arena_bytes);
-  if (bytes > 0) {
-    st = dv_swap_out(cache, l0, l1, seq_start, seq_end, r->arena + off, bytes, staging,
-                     staging_bytes, stream);
-    if (st != DV_OK) return st;
-  }
-  Record rec{step, l0, l1, off, bytes, r->ranges.size()};
-  try {
-    r->ranges.insert(r->ranges.end(), seq_start, seq_start + r->batch);
-    r->ranges.insert(r->ranges.end(), seq_end, seq_end + r->batch);
-    r->records.push_back(rec);
-  } catch (...) {
-    r->ranges.resize(rec.ranges);
-    return fail(DV_ERR_INVALID_ARG, "out of host memory for the replica index");
-  }
-  r->used = off + bytes;
-  return DV_OK;
-}
-
-dv_status dv_replica_restore(const dv_replica* r, const dv_cache* cache, int64_t upto_step,
-                             void* staging, size_t staging_bytes, dv_stream stream) {
-  const Trace trace("dv_replica_restore");
-  if (!r) return fail(DV_ERR_INVALID_ARG, "replica is NULL");
-  if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
-  if (cache->batch != r->batch)
-    return fail(DV_ERR_INVALID_ARG, "cache batch %d differs from the replica's %d", cache->batch,
-                r->batch);
-  // Validate every record against this cache before enqueuing anything.
-  for (const Record& rec : r->records) {
-    if (upto_step >= 0 && rec.step >= upto_step) break;
-    size_t bytes = 0;
-    const int32_t* s = r->ranges.data() + rec.ranges;
-    const dv_status st = dv_staging_bytes(cache, rec.l0, rec.l1, s, s + r->batch, &bytes);
-    if (st != DV_OK) return st;
-    if (bytes != rec.bytes)
-      return fail(DV_ERR_INVALID_ARG, "record of step %lld does not match this cache geometry",
-                  (long long)rec.step);
-  }
-  for (const Record& rec : r->records) {
-    if (upto_step >= 0 && rec.step >= upto_step) break;
-    if (rec.bytes == 0) continue;
-    const int32_t* s = r->ranges.data() + rec.ranges;
-    const dv_status st = dv_swap_in(cache, rec.l0, rec.l1, s, s + r->batch, r->arena + rec.offset,
-                                    rec.bytes, staging, staging_bytes, stream);
-    if (st != DV_OK) return st;
-  }
-  return DV_OK;
-}
-
-dv_status dv_replica_restore_batched(const dv_replica* r, const dv_cache* cache,
-                                    int64_t upto_step, void* staging, size_t staging_bytes,
-                                    dv_stream stream) {
-  const Trace trace("dv_replica_restore_batched");
-  LogPlan lp;
-  dv_status st = plan_restore(r, cache, INT64_MIN, upto_step, staging ? staging_bytes : 0, &lp);
-  if (st != DV_OK) return st;
-  const int n = (int)lp.todo.size();
-  if (n == 0) return DV_OK;
-  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (!staging) {  // fused: every kernel reads the arena over the host link
-    void* arena_dev = nullptr;
-    if ((st = check_host(r->arena, "replica arena", &arena_dev)) != DV_OK) return st;
-    return unpack_log_direct(cache, lp, static_cast<const uint8_t*>(arena_dev), true, cs);
-  }
-  void* stg = nullptr;
-  const size_t need = lp.total < staging_bytes ? lp.total : staging_bytes;
-  if ((st = resolve(staging, need, false, "staging", &stg)) != DV_OK) return st;
-  uint8_t* sp = static_cast<uint8_t*>(stg);
-  cudaError_t err;
-  for (int i = 0; i < n;) {
-    const LogRec& first = lp.todo[i];
-    if (lp.alone[i]) {
-      const int32_t* s = first.ranges;
-      st = dv_swap_in(cache, first.l0, first.l1, s, s + r->batch, r->arena + first.offset,
-                      first.bytes, staging, staging_bytes, stream);
-      if (st != DV_OK) return st;
-      ++i;
-      continue;
-    }
-    if (lp.run[i] > 1) {  // a run, in pieces of as many records as staging holds
-      const int len = lp.run[i];
-      for (int j = 0; j < len;) {
-        const int k = std::min(lp.run_piece(i + j, staging_bytes), len - j);
-        const LogRec& f = lp.todo[i + j];
-        if ((err = cudaMemcpyAsync(sp, r->arena + f.offset, (size_t)k * f.bytes,
-                                   cudaMemcpyHostToDevice, cs)) != cudaSuccess)
-          return cuda_fail(err, "restore copy");
-        if ((err = dv::launch_unpack_run(lp.base, lp.recs[i + j], k, sp, cs)) != cudaSuccess)
-          return cuda_fail(err, "run restore launch");
-        j += k;
-      }
-      i += len;
-      continue;
-    }
-    const int k = lp.batch_at(i, staging_bytes);
-    size_t bytes = 0;
-    for (int j = 0; j < k; ++j) bytes += lp.todo[i + j].bytes;
-    if ((err = cudaMemcpyAsync(sp, r->arena + first.offset, bytes, cudaMemcpyHostToDevice, cs)) !=
-        cudaSuccess)
-      return cuda_fail(err, "restore copy");
-    if ((err = dv::launch_unpack_records(lp.base, lp.recs.data() + i, k, sp, cs)) != cudaSuccess)
-      return cuda_fail(err, "batched restore launch");
-    i += k;
-  }
-  return DV_OK;
-}
-
-dv_status dv_replica_restore_fetched(const dv_replica* r, const dv_cache* cache,
-                                    int64_t upto_step, dv_fetcher* h) {
-  const Trace trace("dv_replica_restore_fetched");
-  return dv_replica_restore_fetched_steps(r, cache, INT64_MIN, upto_step, h);
-}
-
-dv_status dv_replica_restore_fetched_steps(const dv_replica* r, const dv_cache* cache,
-                                          int64_t from_step, int64_t upto_step, dv_fetcher* h) {
-  const Trace trace("dv_replica_restore_fetched_steps");
-  if (!h) return fail(DV_ERR_INVALID_ARG, "fetcher is NULL");
-  LogPlan lp;
-  dv_status st = plan_restore(r, cache, from_step, upto_step, h->slot_bytes, &lp);
-  if (st != DV_OK) return st;
-  const int n = (int)lp.todo.size();
-  cudaError_t err = cudaSuccess;
-  for (int i = 0; i < n;) {
-    const LogRec& first = lp.todo[i];
-    if (lp.alone[i]) {
-      // Whole layers at a time, as many as a slot holds.
-      const int32_t* s = first.ranges;
-      dv::Plan q;
-      if ((st = plan_ranges(cache, first.l0, first.l1, s, s + r->batch, &q)) != DV_OK) return st;
-      q.k = lp.base.k;
-      q.v = lp.base.v;
-      const int64_t slab = dv::layer_slab_bytes(q);
-      const int64_t fit = (int64_t)(h->slot_bytes / (size_t)slab);
-      const int32_t group = (int32_t)(fit < (int64_t)(q.l1 - q.l0) ? fit : (int64_t)(q.l1 - q.l0));
-      for (int32_t la = first.l0; la < first.l1; la += group) {
-        const int32_t lb = la + group < first.l1 ? la + group : first.l1;
-        dv::Plan g = q;
-        dv::restrict_layers(g, la, lb);
-        const uint8_t* src = r->arena + first.offset + (size_t)(la - first.l0) * (size_t)slab;
-        err = fetch_piece(h, src, (size_t)g.bytes, [&](void* slot) {
-          return dv::launch_unpack(g, slot, h->unpack, dv::kAuto);
-        });
-        if (err != cudaSuccess) return cuda_fail(err, "fetched restore (layers)");
-      }
-      ++i;
-      continue;
-    }
-    if (lp.run[i] > 1) {  // a run, in pieces of as many records as a slot holds
-      const int len = lp.run[i];
-      for (int j = 0; j < len;) {
-        const int k = std::min(lp.run_piece(i + j, h->slot_bytes), len - j);
-        const LogRec& f = lp.todo[i + j];
-        const dv::RecordRanges& fr = lp.recs[i + j];
-        err = fetch_piece(h, r->arena + f.offset, (size_t)k * f.bytes, [&](void* slot) {
-          return dv::launch_unpack_run(lp.base, fr, k, slot, h->unpack);
-        });
-        if (err != cudaSuccess) return cuda_fail(err, "fetched restore (run)");
-        j += k;
-      }
-      i += len;
-      continue;
-    }
-    const int k = lp.batch_at(i, h->slot_bytes);
-    size_t bytes = 0;
-    for (int j = 0; j < k; ++j) bytes += lp.todo[i + j].bytes;
-    err = fetch_piece(h, r->arena + first.offset, bytes, [&](void* slot) {
-      return dv::launch_unpack_records(lp.base, lp.recs.data() + i, k, slot, h->unpack);
-    });
-    if (err != cudaSuccess) return cuda_fail(err, "fetched restore (records)");
-    i += k;
-  }
-  return DV_OK;
-}
-
-dv_status dv_kv_unpack_records(const dv_cache* cache, int32_t num_records,
-                               const int32_t* layers, const int32_t* ranges, const void* src,
-                               size_t src_bytes, dv_stream stream) {
-  const Trace trace("dv_kv_unpack_records");
-  if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
-  if (num_records < 0) return fail(DV_ERR_INVALID_ARG, "num_records %d < 0", num_records);
-  if (num_records > 0 && (!layers || !ranges))
-    return fail(DV_ERR_INVALID_ARG, "layers / ranges is NULL");
-  if (cache->batch <= 0 || cache->batch > dv::kMaxBatch)
-    return fail(DV_ERR_INVALID_ARG, "cache batch %d outside [1, %d]", cache->batch,
-                dv::kMaxBatch);
-  std::vector<LogRec> all;
-  size_t off = 0;
-  try {
-    all.reserve((size_t)num_records);
-    for (int32_t i = 0; i < num_records; ++i) {
-      const int32_t* rg = ranges + (size_t)i * 2 * cache->batch;
-      size_t bytes = 0;
-      const dv_status st = dv_staging_bytes(cache, layers[2 * i], layers[2 * i + 1], rg,
-                                            rg + cache->batch, &bytes);
-      if (st != DV_OK) return st;
-      all.push_back(LogRec{layers[2 * i], layers[2 * i + 1], rg, off, bytes, (int64_t)i});
-      off += bytes;
-    }
-  } catch (...) {
-    return fail(DV_ERR_INVALID_ARG, "out of host memory for the record plan");
-  }
-  if (off == 0) return DV_OK;
-  if (src_bytes < off)
-    return fail(DV_ERR_BUFFER_TOO_SMALL, "the records need %zu bytes, src has %zu", off,
-                src_bytes);
-  LogPlan lp;
-  dv_status st = plan_log(cache, all, 0, &lp);
-  if (st != DV_OK) return st;
-  void* d = nullptr;
-  bool host_side = false;
-  if ((st = resolve(src, off, true, "src", &d, &host_side)) != DV_OK) return st;
-  return unpack_log_direct(cache, lp, static_cast<const uint8_t*>(d), host_side,
-                           static_cast<cudaStream_t>(stream));
-}
-
-dv_status dv_replica_truncate(dv_replica* r, int64_t step) {
-  if (!r) return fail(DV_ERR_INVALID_ARG, "replica is NULL");
-  size_t keep = 0;
-  while (keep < r->records.size() && r->records[keep].step < step) ++keep;
-  if (keep < r->records.size()) {
-    r->used = r->records[keep].offset;
-    r->ranges.resize(r->records[keep].ranges);
-    r->records.resize(keep);
-  }
-  return DV_OK;
-}
-
-dv_status dv_replica_info(const dv_replica* r, int64_t* num_records, size_t* bytes_used) {
-  if (!r) return fail(DV_ERR_INVALID_ARG, "replica is NULL");
-  if (num_records) *num_records = (int64_t)r->records.size();
-  if (bytes_used) *bytes_used = r->used;
-  return DV_OK;
-}
-
-void dv_replica_destroy(dv_replica* r) { delete r; }
-
-// ---- microbatch swapping through two device caches (Fig 9) -------------------
-
-struct dv_swapper {
-  dv_cache slot[2];
-  dv_fetcher* fetcher;
-  cudaStream_t compute;
-  cudaStream_t swap;
-  const dv_replica* holds[2];  // microbatch swapped in to each cache (or on its way)
-  const dv_replica* cur;       // the acquired microbatch, NULL between steps
-  int current;                 // its cache
-  int last;                    // the cache of the last acquire, -1 before the first
-  cudaEvent_t ready[2];        // after a cache's swap-in (fetcher's unpack stream)
-  cudaEvent_t computed[2];     // after a step's compute (compute stream)
-  cudaEvent_t freed[2];        // after a cache's last swap-out (swap stream)
-  bool ready_set[2], freed_set[2];
-};
-
-namespace {
-
-// Swaps `mb` in to cache i on the fetcher's streams, after that cache's
-// previous step and swap-out.
-dv_status swap_in_slot(dv_swapper* sw, int i, const dv_replica* mb) {
-  dv_fetcher* f = sw->fetcher;
-  cudaError_t err;
-  if (sw->freed_set[i]) {
-    if ((err = cudaStreamWaitEvent(f->copy, sw->freed[i], 0)) != cudaSuccess ||
-        (err = cudaStreamWaitEvent(f->unpack, sw->freed[i], 0)) != cudaSuccess)
-      return cuda_fail(err, "swapper: wait for the cache's swap-out");
-  }
-  const dv_status st = dv_replica_restore_fetched(mb, &sw->slot[i], -1, f);
-  if (st != DV_OK) return st;
-  if ((err = cudaEventRecord(sw->ready[i], f->unpack)) != cudaSuccess)
-    return cuda_fail(err, "swapper: record the swap-in");
-  sw->ready_set[i] = true;
-  sw->holds[i] = mb;
-  return DV_OK;
-}
-
-bool same_geometry(const dv_cache& a, const dv_cache& b) {
-  return a.num_layers == b.num_layers && a.batch == b.batch && a.num_heads == b.num_heads &&
-         a.head_dim == b.head_dim && a.max_seq == b.max_seq && a.elem_bytes == b.elem_bytes &&
-         a.layer_stride_elems == b.layer_stride_elems;
-}
-
-}  // namespace
-
-dv_status dv_swapper_create(dv_swapper** out, const dv_cache* slot0, const dv_cache* slot1,
-                            dv_fetcher* fetcher, dv_stream compute_stream, dv_stream swap_stream) {
-  if (!out) return fail(DV_ERR_INVALID_ARG, "out is NULL");
-  *out = nullptr;
-  if (!slot0 || !slot1 || !fetcher)
-    return fail(DV_ERR_INVALID_ARG, "slot0 / slot1 / fetcher is NULL");
-  if (!same_geometry(*slot0, *slot1))
-    return fail(DV_ERR_INVALID_ARG, "the two caches must have the same geometry");
-  if (slot0->k_base == slot1->k_base || slot0->v_base == slot1->v_base)
-    return fail(DV_ERR_INVALID_ARG, "the two caches must not share memory");
-  std::vector<int32_t> zero((size_t)(slot0->batch > 0 ? slot0->batch : 1), 0);
-  for (const dv_cache* c : {slot0, slot1}) {
-    dv::Plan p;
-    dv_status st = plan_ranges(c, 0, c->num_layers, zero.data(), zero.data(), &p);
-    if (st != DV_OK) return st;
-    if ((st = resolve_cache(c, &p)) != DV_OK) return st;
-  }
-  dv_swapper* sw = new (std::nothrow) dv_swapper();
-  if (!sw) return fail(DV_ERR_INVALID_ARG, "out of host memory for the swapper handle");
-  sw->slot[0] = *slot0;
-  sw->slot[1] = *slot1;
-  sw->fetcher = fetcher;
-  sw->compute = compute_stream;
-  sw->swap = swap_stream;
-  sw->holds[0] = sw->holds[1] = nullptr;
-  sw->cur = nullptr;
-  sw->current = -1;
-  sw->last = -1;
-  sw->ready_set[0] = sw->ready_set[1] = sw->freed_set[0] = sw->freed_set[1] = false;
-  cudaEvent_t* evs[6] = {&sw->ready[0], &sw->ready[1], &sw->computed[0], &sw->computed[1],
-                         &sw->freed[0], &sw->freed[1]};
-  int made = 0;
-  cudaError_t err = cudaSuccess;
-  for (; made < 6; ++made)
-    if ((err = cudaEventCreateWithFlags(evs[made], cudaEventDisableTiming)) != cudaSuccess) break;
-  if (made < 6) {
-    for (int i = 0; i < made; ++i) cudaEventDestroy(*evs[i]);
-    delete sw;
-    return cuda_fail(err, "cudaEventCreateWithFlags");
-  }
-  *out = sw;
-  return DV_OK;
-}
-
-dv_status dv_swapper_acquire(dv_swapper* sw, const dv_replica* mb, int32_t* slot) {
-  const Trace trace("dv_swapper_acquire");
-  if (!sw || !mb || !slot) return fail(DV_ERR_INVALID_ARG, "swapper / microbatch / slot is NULL");
-  if (sw->cur) return fail(DV_ERR_INVALID_ARG, "the current microbatch has not been released");
-  if (mb->batch != sw->slot[0].batch)
-    return fail(DV_ERR_INVALID_ARG, "microbatch batch %d differs from the caches' %d", mb->batch,
-                sw->slot[0].batch);
-  int i = sw->holds[0] == mb ? 0 : sw->holds[1] == mb ? 1 : -1;
-  if (i < 0) {  // not swapped in: now, into the cache the last step did not use
-    i = sw->last < 0 ? 0 : 1 - sw->last;
-    const dv_status st = swap_in_slot(sw, i, mb);
-    if (st != DV_OK) return st;
-  }
-  if (sw->ready_set[i]) {
-    const cudaError_t err = cudaStreamWaitEvent(sw->compute, sw->ready[i], 0);
-    if (err != cudaSuccess) return cuda_fail(err, "swapper: wait for the swap-in");
-  }
-  sw->cur = mb;
-  sw->current = i;
-  sw->last = i;
-  *slot = i;
-  return DV_OK;
-}
-
-dv_status dv_swapper_prefetch(dv_swapper* sw, const dv_replica* mb) {
-  const Trace trace("dv_swapper_prefetch");
-  if (!sw || !mb) return fail(DV_ERR_INVALID_ARG, "swapper / microbatch is NULL");
-  if (mb->batch != sw->slot[0].batch)
-    return fail(DV_ERR_INVALID_ARG, "microbatch batch %d differs from the caches' %d", mb->batch,
-                sw->slot[0].batch);
-  if (sw->holds[0] == mb || sw->holds[1] == mb) return DV_OK;  // already there
-  const int j = sw->last < 0 ? 0 : 1 - sw->last;
-  return swap_in_slot(sw, j, mb);
-}
-
-dv_status dv_swapper_release(dv_swapper* sw, dv_replica* mb, int32_t l0, int32_t l1,
-                             const int32_t* seq_start, const int32_t* seq_end, int64_t step) {
-  const Trace trace("dv_swapper_release");
-  if (!sw || !mb) return fail(DV_ERR_INVALID_ARG, "swapper / microbatch is NULL");
-  if (sw->cur != mb) return fail(DV_ERR_INVALID_ARG, "this microbatch is not the acquired one");
-  const int i = sw->current;
-  size_t bytes = 0;
-  dv_status st = dv_staging_bytes(&sw->slot[i], l0, l1, seq_start, seq_end, &bytes);
-  if (st != DV_OK) return st;
-  if (!mb->records.empty() && step < mb->records.back().step)
-    return fail(DV_ERR_INVALID_ARG, "step %lld is before the last record's %lld",
-                (long long)step, (long long)mb->records.back().step);
-  if (mb->used + bytes > mb->arena_bytes)
-    return fail(DV_ERR_BUFFER_TOO_SMALL, "replica arena full: %zu + %zu > %zu bytes", mb->used,
-                bytes, mb->arena_bytes);
-  cudaError_t err;
-  if ((err = cudaEventRecord(sw->computed[i], sw->compute)) != cudaSuccess ||
-      (err = cudaStreamWaitEvent(sw->swap, sw->computed[i], 0)) != cudaSuccess)
-    return cuda_fail(err, "swapper: order the swap-out after the step");
-  if ((st = dv_replica_append(mb, &sw->slot[i], l0, l1, seq_start, seq_end, step, nullptr, 0,
-                              sw->swap)) != DV_OK)
-    return st;
-  if ((err = cudaEventRecord(sw->freed[i], sw->swap)) != cudaSuccess)
-    return cuda_fail(err, "swapper: record the swap-out");
-  sw->freed_set[i] = true;
-  sw->cur = nullptr;
-  return DV_OK;
-}
-
-dv_status dv_swapper_wait(dv_swapper* sw) {
-  if (!sw) return fail(DV_ERR_INVALID_ARG, "swapper is NULL");
-  for (int i = 0; i < 2; ++i) {
-    cudaError_t err = cudaSuccess;
-    if (sw->ready_set[i] && (err = cudaEventSynchronize(sw->ready[i])) != cudaSuccess)
-      return cuda_fail(err, "cudaEventSynchronize");
-    if (sw->freed_set[i] && (err = cudaEventSynchronize(sw->freed[i])) != cudaSuccess)
-      return cuda_fail(err, "cudaEventSynchronize");
-  }
-  return DV_OK;
-}
-
-void dv_swapper_destroy(dv_swapper* sw) {
-  if (!sw) return;
-  for (cudaEvent_t e : {sw->ready[0], sw->ready[1], sw->computed[0], sw->computed[1],
-                        sw->freed[0], sw->freed[1]})
-    cudaEventDestroy(e);
-  delete sw;
-}
-
-// ---- decode deltas streamed beside the compute (Fig 7c) ------------------------
-
-struct dv_delta_streamer {
-  dv_replica* replica;
-  cudaStream_t compute;
-  cudaStream_t side;
-  void* staging;
-  size_t staging_bytes;
-  cudaEvent_t written;   // after a step's writes (compute stream)
-  cudaEvent_t streamed;  // after the last append (side stream)
-  bool any;
-};
-
-dv_status dv_delta_streamer_create(dv_delta_streamer** out, dv_replica* replica,
-                                   dv_stream compute_stream, dv_stream side_stream,
-                                   void* staging, size_t staging_bytes) {
-  if (!out) return fail(DV_ERR_INVALID_ARG, "out is NULL");
-  *out = nullptr;
-  if (!replica) return fail(DV_ERR_INVALID_ARG, "replica is NULL");
-  if (compute_stream == side_stream)
-    return fail(DV_ERR_INVALID_ARG, "the side stream must differ from the compute stream");
-  if (staging) {
-    void* d = nullptr;
-    const dv_status st = resolve(staging, staging_bytes, false, "staging", &d);
-    if (st != DV_OK) return st;
-  }
-  dv_delta_streamer* ds = new (std::nothrow) dv_delta_streamer();
-  if (!ds) return fail(DV_ERR_INVALID_ARG, "out of host memory for the delta streamer handle");
-  ds->replica = replica;
-  ds->compute = compute_stream;
-  ds->side = side_stream;
-  ds->staging = staging;
-  ds->staging_bytes = staging ? staging_bytes : 0;
-  ds->any = false;
-  cudaError_t err = cudaEventCreateWithFlags(&ds->written, cudaEventDisableTiming);
-  if (err == cudaSuccess) {
-    err = cudaEventCreateWithFlags(&ds->streamed, cudaEventDisableTiming);
-    if (err != cudaSuccess) cudaEventDestroy(ds->written);
-  }
-  if (err != cudaSuccess) {
-    delete ds;
-    return cuda_fail(err, "cudaEventCreateWithFlags");
-  }
-  *out = ds;
-  return DV_OK;
-}
-
-dv_status dv_delta_stream(dv_delta_streamer* ds, const dv_cache* cache, int32_t l0, int32_t l1,
-                          const int32_t* seq_start, const int32_t* seq_end, int64_t step) {
-  const Trace trace("dv_delta_stream");
-  if (!ds) return fail(DV_ERR_INVALID_ARG, "delta streamer is NULL");
-  dv_replica* r = ds->replica;
-  if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
-  if (cache->batch != r->batch)
-    return fail(DV_ERR_INVALID_ARG, "cache batch %d differs from the replica's %d", cache->batch,
-                r->batch);
-  size_t bytes = 0;
-  dv_status st = dv_staging_bytes(cache, l0, l1, seq_start, seq_end, &bytes);
-  if (st != DV_OK) return st;
-  if (!r->records.empty() && step < r->records.back().step)
-    return fail(DV_ERR_INVALID_ARG, "step %lld is before the last record's %lld",
-                (long long)step, (long long)r->records.back().step);
-  if (r->used + bytes > r->arena_bytes)
-    return fail(DV_ERR_BUFFER_TOO_SMALL, "replica arena full: %zu + %zu > %zu bytes", r->used,
-                bytes, r->arena_bytes);
-  if (ds->staging && bytes > 0) {
-    dv::Plan p;
-    if ((st = plan_ranges(cache, l0, l1, seq_start, seq_end, &p)) != DV_OK) return st;
-    if ((size_t)dv::layer_slab_bytes(p) > ds->staging_bytes)
-      return fail(DV_ERR_BUFFER_TOO_SMALL, "staging of %zu bytes holds less than one layer slab "
-                  "(%lld bytes)", ds->staging_bytes, (long long)dv::layer_slab_bytes(p));
-  }
-  cudaError_t err;
-  if ((err = cudaEventRecord(ds->written, ds->compute)) != cudaSuccess ||
-      (err = cudaStreamWaitEvent(ds->side, ds->written, 0)) != cudaSuccess)
-    return cuda_fail(err, "delta stream: order the append after the step");
-  if ((st = dv_replica_append(r, cache, l0, l1, seq_start, seq_end, step, ds->staging,
-                              ds->staging_bytes, ds->side)) != DV_OK)
-    return st;
-  if ((err = cudaEventRecord(ds->streamed, ds->side)) != cudaSuccess)
-    return cuda_fail(err, "delta stream: record the append");
-  ds->any = true;
-  return DV_OK;
-}
-
-dv_status dv_delta_streamer_join(dv_delta_streamer* ds) {
-  if (!ds) return fail(DV_ERR_INVALID_ARG, "delta streamer is NULL");
-  if (!ds->any) return DV_OK;
-  const cudaError_t err = cudaStreamWaitEvent(ds->compute, ds->streamed, 0);
-  return err == cudaSuccess ? DV_OK : cuda_fail(err, "delta stream: join");
-}
-
-dv_status dv_delta_streamer_wait(dv_delta_streamer* ds) {
-  if (!ds) return fail(DV_ERR_INVALID_ARG, "delta streamer is NULL");
-  if (!ds->any) return DV_OK;
-  const cudaError_t err = cudaEventSynchronize(ds->streamed);
-  return err == cudaSuccess ? DV_OK : cuda_fail(err, "cudaEventSynchronize");
-}
-
-void dv_delta_streamer_destroy(dv_delta_streamer* ds) {
-  if (!ds) return;
-  cudaEventDestroy(ds->written);
-  cudaEventDestroy(ds->streamed);
-  delete ds;
-}
-
 }  // extern "C"

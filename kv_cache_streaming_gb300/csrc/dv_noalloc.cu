@@ -10,8 +10,7 @@
 #include <utility>
 #include <vector>
 
-#include "../../include/dv.h"
-#include "dv_plan.h"
+#include "dv_host.h"
 
 namespace {
 
@@ -31,7 +30,7 @@ std::vector<std::pair<unsigned long long, void*>> g_addr;  // (context id, addre
 dv_status staging_address(void** out) {
   unsigned long long id = 0;
   if (!dv::context_id(&id))
-    return dv::set_error(DV_ERR_CUDA, "dv_swap_out_noalloc: no current CUDA context");
+    return dv::fail(DV_ERR_CUDA, "dv_swap_out_noalloc: no current CUDA context");
   std::lock_guard<std::mutex> lock(g_mu);
   for (const auto& e : g_addr)
     if (e.first == id) {
@@ -42,13 +41,13 @@ dv_status staging_address(void** out) {
   const cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_staging);
   if (err != cudaSuccess || !p) {
     cudaGetLastError();
-    return dv::set_error(DV_ERR_CUDA, "cudaGetSymbolAddress of the built-in staging buffer: %s",
+    return dv::fail(DV_ERR_CUDA, "cudaGetSymbolAddress of the built-in staging buffer: %s",
                          cudaGetErrorName(err));
   }
   try {
     g_addr.emplace_back(id, p);
   } catch (...) {
-    return dv::set_error(DV_ERR_INVALID_ARG, "out of host memory for the buffer address");
+    return dv::fail(DV_ERR_INVALID_ARG, "out of host memory for the buffer address");
   }
   *out = p;
   return DV_OK;
@@ -65,7 +64,7 @@ extern "C" dv_status dv_swap_out_noalloc(const dv_cache* cache, int32_t l0, int3
   if (total == 0) return DV_OK;
   const size_t slab = total / (size_t)(l1 - l0);  // every layer of the ranges is the same size
   if (slab > (size_t)DV_NOALLOC_STAGING_BYTES)
-    return dv::set_error(DV_ERR_BUFFER_TOO_SMALL,
+    return dv::fail(DV_ERR_BUFFER_TOO_SMALL,
                          "dv_swap_out_noalloc: one layer of these ranges needs %zu staging bytes, "
                          "more than the built-in %zu; use dv_swap_out with a staging buffer",
                          slab, (size_t)DV_NOALLOC_STAGING_BYTES);

@@ -107,12 +107,4 @@ cudaError_t launch_unpack_run(const Plan& cache, const RecordRanges& first, int 
 bool checked_build();
 cudaError_t read_fault(uint64_t* out);
 
-// The unique id of the calling thread's current CUDA context (made current
-// by the runtime if none is); false if it cannot be had.  Keys per-context
-// state: a context that is destroyed and made again gets a new id.
-bool context_id(unsigned long long* id);
-
-// Records a message for dv_last_error() on the calling thread; returns `st`.
-dv_status set_error(dv_status st, const char* fmt, ...);
-
 }  // namespace dv
