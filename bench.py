@@ -19,9 +19,10 @@ bytes read plus bytes written by all its launches, divided by the step time
 (the step runs as one CUDA graph replay on one stream; every buffer is read at
 least 19 GB of traffic after it was written, so L2 serves none of it).  `e2e`
 is the same byte count through the public API with pinned host buffers: the
-snapshot and the deltas appended to a host replica (dv_replica_append, the
-pack writing straight over the host link), then restored into the second
-cache through a fetcher (dv_replica_restore_fetched).  Side sections: the
+snapshot and the deltas appended to a host replica through a layer streamer
+(dv_replica_append_streamed: packs into two device slots, copy engines to the
+host), each part restored into the second cache through a fetcher
+(dv_replica_restore_fetched_steps) while the next goes out.  Side sections: the
 GPT2-1.5B step (layer-by-layer prompt packs + 24 deltas), swap against the
 measured host-link peak, the other workloads, microbatch swapping and decode
 streaming.
@@ -507,7 +508,9 @@ class Bloom:
     # one step through the public API with pinned host buffers
     def setup_e2e(self):
         torch, dv, g = self.torch, self.dv, self.g
-        self.arena = torch.empty(self.total, dtype=torch.uint8, pin_memory=True)
+        # the replica's arena in pinned host memory backed by huge pages
+        # (dv_host_alloc): every pass over it runs at the link rate
+        self.arena = dv.host_empty(self.total)
         self.replica = dv.Replica(self.arena, g.batch)
         slot = dv.dv_staging_bytes(self.cache, 0, 1, self.zs, self.len0)  # one snapshot layer
         self.slots = (torch.empty(slot, dtype=torch.uint8, device="cuda"),
@@ -515,36 +518,46 @@ class Bloom:
         self.in_copy = torch.cuda.Stream()
         self.in_unpack = torch.cuda.Stream()
         self.fetcher = dv.Fetcher(self.slots[0], self.slots[1], self.in_copy, self.in_unpack)
-        # the appends' staging: packs land here and copy engines take them to
-        # the host, so both directions of the link run on copy engines
-        self.out_staging = torch.empty(slot, dtype=torch.uint8, device="cuda")
+        # the appends go through a layer streamer: packs into its two device
+        # slots, copy engines take them to the host, so both directions of
+        # the link run on copy engines and each pack overlaps the previous copy
+        self.out_slots = (torch.empty(slot, dtype=torch.uint8, device="cuda"),
+                          torch.empty(slot, dtype=torch.uint8, device="cuda"))
+        self.out_pack = torch.cuda.Stream()
+        self.out_copy = torch.cuda.Stream()
+        self.streamer = dv.Streamer(self.out_slots[0], self.out_slots[1], self.out_pack,
+                                    self.out_copy)
+
+    E2E_DELTA_CHUNK = 16  # deltas restored as they accumulate, this many at a time
 
     def e2e_step(self):
         """The log through the host replica and back: the snapshot appended
-        layer by layer (each packed into a device buffer and copied to pinned
-        memory by a copy engine), each layer restored into the second cache
-        through the fetcher as soon as it is in host memory (the host-to-device
-        copy of layer l overlaps the device-to-host copy of layer l+1: copy
-        engines both ways), then the 256 deltas appended in decode order, each
-        64 restored (one run of records) while the next 64 go out."""
+        layer by layer through the streamer (each layer packed into a device
+        slot while the previous one is copied to pinned memory by a copy
+        engine), each layer restored into the second cache through the fetcher
+        as soon as it is in host memory (the host-to-device copy of layer l
+        overlaps the device-to-host copy of layer l+1: copy engines both
+        ways), then the 256 deltas appended the same way in decode order, each
+        16 restored (one run of records) while the next 16 go out."""
         g, s = self.g, self.stream
         L = g.num_layers
-        rep = self.replica
+        rep, st = self.replica, self.streamer
         rep.truncate(0)
         self.in_unpack.wait_stream(s)    # the second cache is free
-        stg = self.out_staging
+        self.out_pack.wait_stream(s)     # the first cache is written
         for l in range(L):
-            rep.append(self.cache, l, l + 1, self.zs, self.len0, step=l, staging=stg, stream=s)
-            self.in_copy.wait_stream(s)  # layer l is in host memory
+            rep.append_streamed(st, self.cache, l, l + 1, self.zs, self.len0, step=l)
+            self.in_copy.wait_stream(self.out_copy)  # layer l is in host memory
             rep.restore_fetched(self.cache_b, self.fetcher, upto_step=l + 1, from_step=l)
-        chunk = 64                       # deltas restored as they accumulate
+        chunk = self.E2E_DELTA_CHUNK
         for k0 in range(0, self.nd, chunk):
             for k in range(k0, min(self.nd, k0 + chunk)):
                 a, b = self.deltas[k]
-                rep.append(self.cache, 0, L, a, b, step=L + k, staging=stg, stream=s)
-            self.in_copy.wait_stream(s)  # these deltas are in host memory
+                rep.append_streamed(st, self.cache, 0, L, a, b, step=L + k)
+            self.in_copy.wait_stream(self.out_copy)  # these deltas are in host memory
             rep.restore_fetched(self.cache_b, self.fetcher, upto_step=L + k0 + chunk,
                                 from_step=L + k0)
+        s.wait_stream(self.out_copy)
         s.wait_stream(self.in_unpack)
 
     def timed_e2e(self, steps, warmup, world):
@@ -567,8 +580,9 @@ class Bloom:
 
     def close_e2e(self):
         self.fetcher.close()
+        self.streamer.close()
         self.replica.close()
-        del self.arena, self.slots, self.out_staging
+        del self.arena, self.slots, self.out_slots
 
 
 def link_peaks(torch, nbytes=2 << 30, reps=3):
@@ -608,6 +622,37 @@ def link_peaks(torch, nbytes=2 << 30, reps=3):
     del host, dev, host2, dev2
     torch.cuda.empty_cache()
     return {k: round(v, 2) for k, v in out.items()}
+
+
+def host_memory_passes(torch, dv, dev, passes=6):
+    """Device-to-host copy passes over all of `dev` (in 1 GiB copies) into
+    pinned memory of each kind: torch's pinned allocator (cudaHostAlloc, base
+    pages) and dv_host_alloc (huge pages where the kernel gives them).  GB/s
+    of each pass."""
+    n = dev.numel()
+    s = torch.cuda.Stream()
+    out = {}
+    for kind in ("torch_pinned", "dv_host_alloc"):
+        host = (torch.empty(n, dtype=torch.uint8, pin_memory=True) if kind == "torch_pinned"
+                else dv.host_empty(n))
+        rates = []
+        for r in range(passes + 1):
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s):
+                a.record(s)
+                for o in range(0, n, 1 << 30):
+                    host[o:o + (1 << 30)].copy_(dev[o:o + (1 << 30)], non_blocking=True)
+                b.record(s)
+            torch.cuda.synchronize()
+            if r:
+                rates.append(round(n / (a.elapsed_time(b) / 1e3) / 1e9, 1))
+        out[kind] = {"passes_gbs": rates, "median_gbs": statistics.median(rates),
+                     "min_gbs": min(rates)}
+        del host
+    out["bytes_per_pass"] = n
+    return out
 
 
 class Bench:
@@ -1630,9 +1675,9 @@ def run_mine(args):
     # e2e through the public API with host buffers
     link = link_peaks(torch)
     b.setup_e2e()
-    e2e_steps = max(3, min(args.steps, 10))
+    e2e_steps = max(3, min(args.steps, 20))
     b.clear_b()
-    e2e_ts = b.timed_e2e(e2e_steps, 1, world)
+    e2e_ts = b.timed_e2e(e2e_steps, 2, world)
     e2e_ok = b.verify()
     e2e_med = max_over_ranks(statistics.median(e2e_ts), world)
     e2e_value = whole_job_rate(b.bytes_per_step, 1, e2e_med, world)
@@ -1641,6 +1686,7 @@ def run_mine(args):
     link_bytes = 2 * b.total  # every log byte crosses once each way
     serial_link_s = b.total / (link["d2h_gbs"] * 1e9) + b.total / (link["h2d_gbs"] * 1e9)
     b.close_e2e()
+    hostmem = host_memory_passes(torch, b.dv, b.log) if rank == 0 and not args.no_swap else None
     per_step = {"bytes_per_step": b.bytes_per_step, "log_bytes": b.total,
                 "snapshot_bytes": b.snap, "delta_bytes": b.dsz,
                 "launches_per_step": b.launches_per_step()}
@@ -1709,12 +1755,15 @@ def run_mine(args):
                 "timing": "median step (each step synchronised); over all steps: "
                           f"{e2e_all:.1f} GB/s, slowest step {max(e2e_ts) * 1e3:.1f} ms, "
                           f"fastest {min(e2e_ts) * 1e3:.1f} ms",
-                "path": "dv_replica_append of the snapshot one layer at a time (staged: the "
-                        "pack into a device buffer, a copy engine to the host), each layer "
+                "step_ms": [round(x * 1e3, 1) for x in e2e_ts],
+                "path": "dv_replica_append_streamed of the snapshot one layer at a time "
+                        "(a layer streamer: each pack into one of two device slots while "
+                        "the other is copied to the host by a copy engine), each layer "
                         "restored through a fetcher (dv_replica_restore_fetched_steps) while "
                         "the next goes out; then the 256 deltas appended the same way, each "
-                        "64 restored as a run of records while the next 64 go out "
-                        "(one-layer slots)"},
+                        f"{Bloom.E2E_DELTA_CHUNK} restored as a run of records while the next "
+                        f"{Bloom.E2E_DELTA_CHUNK} go out (one-layer slots)"},
+        "host_memory": hostmem,
         "gpt2_step": gpt2,
         "swap": swap,
         "naive_vs_buffered": naive,

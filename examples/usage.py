@@ -56,6 +56,11 @@ def main():
         st.wait_stream(torch.cuda.current_stream())         # after the calls above
     rep.restore_fetched(cache, fetcher)                     # the same, copies pipelined
     fetcher.wait()
+    rep.truncate(0)                                         # the same log, appended through
+    rep.append_streamed(streamer, cache, 0, 1, s, e, step=0)   # the streamer's slots (a layer
+    for t in range(4):                                         # of the snapshot: one slot)
+        rep.append_streamed(streamer, cache, 0, 1, e + t, e + t + 1, step=1 + t)
+    streamer.wait()
 
     # two microbatches through two device caches (each kept as a replica)
     caches = [dv.Cache(L, B, H, D, S, 2, torch.zeros_like(k), torch.zeros_like(v))

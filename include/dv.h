@@ -151,6 +151,33 @@ dv_status dv_debug_fault(uint64_t* fault);
  * tell (then calls rely on the sizes the caller passes). */
 dv_status dv_allocation_extent(const void* ptr, size_t* bytes_after);
 
+/* ---- pinned host memory (the host side of swaps and replicas) ---------- */
+
+/* Allocates `bytes` of host memory and registers it with CUDA as pinned,
+ * mapped and portable memory (cudaHostRegister), for use wherever a call
+ * takes pinned host memory: a replica's arena, a swap's host buffer, a
+ * streamer's destination.  The memory is anonymous and zeroed, its start is
+ * aligned to the kernel's transparent-huge-page size, and the huge-page-
+ * aligned part of it is marked for huge pages (madvise; the kernel may
+ * decline).  Why: on a GB300 host with 64 KiB base pages, copy-engine passes
+ * over tens of GB of pinned memory made of base pages periodically run at
+ * about half the link rate, where the same passes over huge pages run at the
+ * full rate every time.  Not thread-safe with respect to a concurrent
+ * dv_host_free of the same pointer; otherwise safe from any thread.  Needs a
+ * CUDA device (the registration makes the current device's primary context
+ * current if the thread has none).  Errors: DV_ERR_INVALID_ARG (out is NULL,
+ * bytes is 0, no host memory), DV_ERR_CUDA (the registration failed; nothing
+ * stays allocated).  No counterpart on the pages: they state only that the
+ * host copies live in pinned CPU memory. */
+dv_status dv_host_alloc(size_t bytes, void** out);
+
+/* Unregisters and unmaps memory from dv_host_alloc (NULL: nothing to do).
+ * The caller ensures that no enqueued work still reads or writes it.
+ * DV_ERR_INVALID_ARG for a pointer dv_host_alloc did not return (or already
+ * freed); DV_ERR_CUDA if the unregistration fails (the memory is unmapped
+ * all the same). */
+dv_status dv_host_free(void* ptr);
+
 /* Bytes the staging buffer of (l0, l1, ranges) takes (see the size formula
  * above).  Host only; enqueues nothing.  Pointers in `cache` are not read. */
 dv_status dv_staging_bytes(const dv_cache* cache, int32_t l0, int32_t l1,
@@ -358,6 +385,26 @@ dv_status dv_replica_create(dv_replica** out, void* host_arena, size_t arena_byt
 dv_status dv_replica_append(dv_replica* replica, const dv_cache* cache, int32_t l0, int32_t l1,
                             const int32_t* seq_start, const int32_t* seq_end, int64_t step,
                             void* staging, size_t staging_bytes, dv_stream stream);
+
+/* The append of dv_replica_append through a layer streamer (§3 "Layer-by-
+ * layer prompt cache streaming", Fig 7b, streaming into the replica of Fig
+ * 10): the record's staging bytes are packed into the streamer's next slot on
+ * its pack stream, after that slot's previous copy, and copied into the arena
+ * on its copy stream.  A record larger than a slot goes in groups of whole
+ * layers, one group per slot, the slots taken in turn.  Unlike the staged
+ * dv_replica_append, no stream waits for the copy: the pack of the next
+ * record (or group) runs while the previous one is being copied.  The caller
+ * orders the pack stream after the writes to the record's ranges; an event
+ * recorded on the copy stream after the call marks the record in host
+ * memory.  DV_ERR_BUFFER_TOO_SMALL, before anything is enqueued, when the
+ * arena is full or when one layer of the record is larger than a slot;
+ * otherwise the errors of dv_replica_append.  If a CUDA call fails part-way,
+ * the record is not added (bytes already copied past the last record are
+ * overwritten by the next append). */
+dv_status dv_replica_append_streamed(dv_replica* replica, dv_streamer* streamer,
+                                     const dv_cache* cache, int32_t l0, int32_t l1,
+                                     const int32_t* seq_start, const int32_t* seq_end,
+                                     int64_t step);
 
 /* Unpacks every record with step < upto_step (all records if upto_step < 0),
  * in append order, into `cache` by dv_swap_in.  The cache must have the

@@ -18,11 +18,13 @@ from .dv import (  # noqa: F401
     DV_ERR_MISALIGNED, DV_ERR_CUDA, DV_ERR_TIMEOUT, DV_ERR_UNSUPPORTED,
     DV_VARIANT_AUTO, DV_VARIANT_FLAT, DV_VARIANT_TILE, DV_VARIANT_TOKEN,
     DvError, Cache, Streamer, Fetcher, Replica, lib, library_path,
+    HostBuffer, dv_host_alloc, dv_host_free, host_empty,
     dv_abi_version, dv_allocation_extent, dv_debug_fault, dv_staging_bytes, dv_kv_pack, dv_kv_unpack, dv_kv_unpack_records, dv_naive_gather, dv_swap_out, dv_swap_in,
     dv_swap_out_noalloc, DV_NOALLOC_STAGING_BYTES,
     dv_streamer_create, dv_stream_layer, dv_streamer_wait, dv_streamer_destroy,
     dv_fetcher_create, dv_fetch_layer, dv_fetcher_wait, dv_fetcher_destroy,
-    dv_replica_create, dv_replica_append, dv_replica_restore, dv_replica_restore_batched,
+    dv_replica_create, dv_replica_append, dv_replica_append_streamed, dv_replica_restore,
+    dv_replica_restore_batched,
     dv_replica_restore_fetched, dv_replica_restore_fetched_steps,
     dv_replica_truncate,
     dv_replica_info, dv_replica_destroy,

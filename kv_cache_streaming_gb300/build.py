@@ -26,7 +26,8 @@ CSRC = PKG / "csrc"
 OBJ = PKG / "_build"
 LIB = PKG / "libdv.so"
 LIB_CHECKED = PKG / "libdv_checked.so"  # device-side bounds checks (debugging)
-SOURCES = ["dv_api.cu", "dv_replica.cu", "dv_sched.cu", "dv_kernels.cu", "dv_noalloc.cu"]
+SOURCES = ["dv_api.cu", "dv_replica.cu", "dv_sched.cu", "dv_hostmem.cu", "dv_kernels.cu",
+           "dv_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -484,18 +484,26 @@ dv_status do_swap(Dir dir, const dv_cache* c, int32_t l0, int32_t l1, const int3
 
 }  // namespace
 
-// ---- streamer ----------------------------------------------------------------
+namespace dv {
 
-struct dv_streamer {
-  void* slot[2];
-  size_t slot_bytes;
-  cudaStream_t pack;
-  cudaStream_t copy;
-  cudaEvent_t packed[2];
-  cudaEvent_t freed[2];
-  bool used[2];
-  int next;
-};
+cudaError_t stream_piece(dv_streamer* h, const Plan& p, void* dst) {
+  const int i = h->next;
+  cudaError_t err;
+  if (h->used[i] && (err = cudaStreamWaitEvent(h->pack, h->freed[i], 0)) != cudaSuccess)
+    return err;
+  if ((err = launch_pack(p, h->slot[i], h->pack, kAuto)) != cudaSuccess) return err;
+  if ((err = cudaEventRecord(h->packed[i], h->pack)) != cudaSuccess) return err;
+  if ((err = cudaStreamWaitEvent(h->copy, h->packed[i], 0)) != cudaSuccess) return err;
+  if ((err = cudaMemcpyAsync(dst, h->slot[i], (size_t)p.bytes, cudaMemcpyDefault, h->copy)) !=
+      cudaSuccess)
+    return err;
+  if ((err = cudaEventRecord(h->freed[i], h->copy)) != cudaSuccess) return err;
+  h->used[i] = true;
+  h->next = i ^ 1;
+  return cudaSuccess;
+}
+
+}  // namespace dv
 
 extern "C" {
 
@@ -704,30 +712,15 @@ dv_status dv_stream_layer(dv_streamer* h, const dv_cache* cache, int32_t layer,
   if ((st = resolve_cache(cache, &p)) != DV_OK) return st;
   {
     cudaPointerAttributes a;
+    dv::ensure_context();
     if (cudaPointerGetAttributes(&a, host_dst) != cudaSuccess ||
         a.type == cudaMemoryTypeUnregistered) {
       cudaGetLastError();
       return fail(DV_ERR_INVALID_ARG, "host_dst must be pinned host or device memory");
     }
   }
-  const int i = h->next;
-  cudaError_t err;
-  if (h->used[i] && (err = cudaStreamWaitEvent(h->pack, h->freed[i], 0)) != cudaSuccess)
-    return cuda_fail(err, "cudaStreamWaitEvent(slot free)");
-  if ((err = dv::launch_pack(p, h->slot[i], h->pack, dv::kAuto)) != cudaSuccess)
-    return cuda_fail(err, "stream_layer pack launch");
-  if ((err = cudaEventRecord(h->packed[i], h->pack)) != cudaSuccess)
-    return cuda_fail(err, "cudaEventRecord(packed)");
-  if ((err = cudaStreamWaitEvent(h->copy, h->packed[i], 0)) != cudaSuccess)
-    return cuda_fail(err, "cudaStreamWaitEvent(packed)");
-  if ((err = cudaMemcpyAsync(static_cast<uint8_t*>(host_dst) + off, h->slot[i], (size_t)p.bytes,
-                             cudaMemcpyDefault, h->copy)) != cudaSuccess)
-    return cuda_fail(err, "stream_layer copy");
-  if ((err = cudaEventRecord(h->freed[i], h->copy)) != cudaSuccess)
-    return cuda_fail(err, "cudaEventRecord(freed)");
-  h->used[i] = true;
-  h->next = i ^ 1;
-  return DV_OK;
+  const cudaError_t err = dv::stream_piece(h, p, static_cast<uint8_t*>(host_dst) + off);
+  return err == cudaSuccess ? DV_OK : cuda_fail(err, "stream_layer");
 }
 
 dv_status dv_streamer_wait(dv_streamer* h) {

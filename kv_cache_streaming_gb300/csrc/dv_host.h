@@ -1,7 +1,7 @@
 // Internal to libdv: what the ABI translation units (dv_api.cu, dv_replica.cu,
 // dv_sched.cu, dv_noalloc.cu) share: error reporting, argument validation,
 // pointer resolution, NVTX ranges, and the handles that more than one of them
-// opens (the fetcher and the replica).
+// opens (the streamer, the fetcher and the replica).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -30,6 +30,17 @@ struct Record {
 };
 
 }  // namespace dv
+
+struct dv_streamer {
+  void* slot[2];
+  size_t slot_bytes;
+  cudaStream_t pack;
+  cudaStream_t copy;
+  cudaEvent_t packed[2];
+  cudaEvent_t freed[2];
+  bool used[2];
+  int next;
+};
 
 struct dv_fetcher {
   void* slot[2];
@@ -104,6 +115,11 @@ dv_status resolve_cache(const dv_cache* c, Plan* p);
 
 // The device-visible address of pinned, mapped host memory `ptr`.
 dv_status check_host(const void* ptr, const char* what, void** dev);
+
+// Packs the planned ranges (p's cache bases resolved) into the streamer's
+// next slot on its pack stream, after that slot's previous copy, then copies
+// the p.bytes of the slot to `dst` (host memory) on its copy stream.
+cudaError_t stream_piece(dv_streamer* h, const Plan& p, void* dst);
 
 // Copies `bytes` from `src` (host memory) into the fetcher's next slot on its
 // copy stream, after that slot's previous unpack, then runs unpack(slot) on

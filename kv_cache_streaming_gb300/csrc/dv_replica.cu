@@ -202,6 +202,35 @@ dv_status unpack_log_direct(const dv_cache* cache, LogPlan& lp, const uint8_t* s
   return DV_OK;
 }
 
+// The checks every append makes before it plans anything.
+dv_status check_append(const dv_replica* r, const dv_cache* cache, int64_t step) {
+  if (!r) return fail(DV_ERR_INVALID_ARG, "replica is NULL");
+  if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
+  if (cache->batch != r->batch)
+    return fail(DV_ERR_INVALID_ARG, "cache batch %d differs from the replica's %d", cache->batch,
+                r->batch);
+  if (!r->records.empty() && step < r->records.back().step)
+    return fail(DV_ERR_INVALID_ARG, "step %lld is before the last record's %lld",
+                (long long)step, (long long)r->records.back().step);
+  return DV_OK;
+}
+
+// Adds the record of an append whose bytes were enqueued to r->arena + off.
+dv_status add_record(dv_replica* r, int64_t step, int32_t l0, int32_t l1, size_t off,
+                     size_t bytes, const int32_t* seq_start, const int32_t* seq_end) {
+  Record rec{step, l0, l1, off, bytes, r->ranges.size()};
+  try {
+    r->ranges.insert(r->ranges.end(), seq_start, seq_start + r->batch);
+    r->ranges.insert(r->ranges.end(), seq_end, seq_end + r->batch);
+    r->records.push_back(rec);
+  } catch (...) {
+    r->ranges.resize(rec.ranges);
+    return fail(DV_ERR_INVALID_ARG, "out of host memory for the replica index");
+  }
+  r->used = off + bytes;
+  return DV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -229,17 +258,10 @@ dv_status dv_replica_append(dv_replica* r, const dv_cache* cache, int32_t l0, in
                             const int32_t* seq_start, const int32_t* seq_end, int64_t step,
                             void* staging, size_t staging_bytes, dv_stream stream) {
   const Trace trace("dv_replica_append");
-  if (!r) return fail(DV_ERR_INVALID_ARG, "replica is NULL");
-  if (!cache) return fail(DV_ERR_INVALID_ARG, "cache is NULL");
-  if (cache->batch != r->batch)
-    return fail(DV_ERR_INVALID_ARG, "cache batch %d differs from the replica's %d", cache->batch,
-                r->batch);
-  if (!r->records.empty() && step < r->records.back().step)
-    return fail(DV_ERR_INVALID_ARG, "step %lld is before the last record's %lld",
-                (long long)step, (long long)r->records.back().step);
-  size_t bytes = 0;
-  dv_status st = dv_staging_bytes(cache, l0, l1, seq_start, seq_end, &bytes);
+  dv_status st = check_append(r, cache, step);
   if (st != DV_OK) return st;
+  size_t bytes = 0;
+  if ((st = dv_staging_bytes(cache, l0, l1, seq_start, seq_end, &bytes)) != DV_OK) return st;
   const size_t off = r->used;  // records are multiples of 16 bytes
   if (off + bytes > r->arena_bytes)
     return fail(DV_ERR_BUFFER_TOO_SMALL, "replica arena full: %zu + %zu > %zu bytes", off, bytes,
@@ -249,17 +271,40 @@ dv_status dv_replica_append(dv_replica* r, const dv_cache* cache, int32_t l0, in
                      staging_bytes, stream);
     if (st != DV_OK) return st;
   }
-  Record rec{step, l0, l1, off, bytes, r->ranges.size()};
-  try {
-    r->ranges.insert(r->ranges.end(), seq_start, seq_start + r->batch);
-    r->ranges.insert(r->ranges.end(), seq_end, seq_end + r->batch);
-    r->records.push_back(rec);
-  } catch (...) {
-    r->ranges.resize(rec.ranges);
-    return fail(DV_ERR_INVALID_ARG, "out of host memory for the replica index");
+  return add_record(r, step, l0, l1, off, bytes, seq_start, seq_end);
+}
+
+dv_status dv_replica_append_streamed(dv_replica* r, dv_streamer* streamer, const dv_cache* cache,
+                                     int32_t l0, int32_t l1, const int32_t* seq_start,
+                                     const int32_t* seq_end, int64_t step) {
+  const Trace trace("dv_replica_append_streamed");
+  dv_status st = check_append(r, cache, step);
+  if (st != DV_OK) return st;
+  if (!streamer) return fail(DV_ERR_INVALID_ARG, "streamer is NULL");
+  dv::Plan p;
+  if ((st = plan_ranges(cache, l0, l1, seq_start, seq_end, &p)) != DV_OK) return st;
+  const size_t bytes = (size_t)p.bytes;
+  const size_t off = r->used;
+  if (off + bytes > r->arena_bytes)
+    return fail(DV_ERR_BUFFER_TOO_SMALL, "replica arena full: %zu + %zu > %zu bytes", off, bytes,
+                r->arena_bytes);
+  if (bytes > 0) {
+    // Whole layers per slot: the record goes in groups of layers, each group
+    // a contiguous part of its staging bytes.
+    const size_t slab = (size_t)dv::layer_slab_bytes(p);
+    if (slab > streamer->slot_bytes)
+      return fail(DV_ERR_BUFFER_TOO_SMALL, "a layer slab of %zu bytes exceeds the slots of %zu",
+                  slab, streamer->slot_bytes);
+    if ((st = resolve_cache(cache, &p)) != DV_OK) return st;
+    const int32_t per = (int32_t)std::min<size_t>((size_t)(l1 - l0), streamer->slot_bytes / slab);
+    for (int32_t la = l0; la < l1; la += per) {
+      dv::Plan q = p;
+      dv::restrict_layers(q, la, std::min(l1, la + per));
+      const cudaError_t err = dv::stream_piece(streamer, q, r->arena + off + (la - l0) * slab);
+      if (err != cudaSuccess) return cuda_fail(err, "append_streamed");
+    }
   }
-  r->used = off + bytes;
-  return DV_OK;
+  return add_record(r, step, l0, l1, off, bytes, seq_start, seq_end);
 }
 
 dv_status dv_replica_restore(const dv_replica* r, const dv_cache* cache, int64_t upto_step,

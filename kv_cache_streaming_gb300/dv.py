@@ -61,6 +61,8 @@ _last_error = _sig("dv_last_error", [], ctypes.c_char_p)
 _staging_bytes = _sig("dv_staging_bytes", _RANGE + [ctypes.POINTER(_SZ)])
 _extent = _sig("dv_allocation_extent", [_P, ctypes.POINTER(_SZ)])
 _debug_fault = _sig("dv_debug_fault", [ctypes.POINTER(ctypes.c_uint64)])
+_host_alloc = _sig("dv_host_alloc", [_SZ, ctypes.POINTER(_P)])
+_host_free = _sig("dv_host_free", [_P])
 _pack = _sig("dv_kv_pack_variant", _RANGE + [_P, _SZ, _P, _I32])
 _unpack = _sig("dv_kv_unpack_variant", _RANGE + [_P, _SZ, _P, _I32])
 _swap_out = _sig("dv_swap_out", _RANGE + [_P, _SZ, _P, _SZ, _P])
@@ -79,6 +81,7 @@ _fetcher_wait = _sig("dv_fetcher_wait", [_P])
 _fetcher_destroy = _sig("dv_fetcher_destroy", [_P], None)
 _replica_create = _sig("dv_replica_create", [ctypes.POINTER(_P), _P, _SZ, _I32])
 _replica_append = _sig("dv_replica_append", [_P] + _RANGE + [_I64, _P, _SZ, _P])
+_replica_append_streamed = _sig("dv_replica_append_streamed", [_P, _P] + _RANGE + [_I64])
 _replica_restore = _sig("dv_replica_restore", [_P, _CP, _I64, _P, _SZ, _P])
 _replica_restore_batched = _sig("dv_replica_restore_batched", [_P, _CP, _I64, _P, _SZ, _P])
 _replica_restore_fetched = _sig("dv_replica_restore_fetched", [_P, _CP, _I64, _P])
@@ -124,6 +127,8 @@ def _buf(x, nbytes=None):
         return None, 0
     if isinstance(x, tuple):
         return int(x[0]), int(x[1] if nbytes is None else nbytes)
+    if isinstance(x, HostBuffer):
+        return x.ptr, int(x.nbytes if nbytes is None else nbytes)
     if hasattr(x, "data_ptr"):
         if hasattr(x, "is_contiguous") and not x.is_contiguous():
             raise TypeError("a tensor buffer must be contiguous (its bytes are one range)")
@@ -207,6 +212,51 @@ def dv_debug_fault():
         return None
     _check(st)
     return out.value
+
+
+class HostBuffer:
+    """Pinned, mapped host memory from ``dv_host_alloc`` (huge pages where the
+    kernel gives them).  Pass it wherever a call takes pinned host memory, or
+    view it as a uint8 CPU tensor with ``tensor()``; the memory is freed by
+    ``close()`` or once neither the buffer nor a tensor over it is referenced."""
+
+    def __init__(self, nbytes):
+        p = _P()
+        _check(_host_alloc(int(nbytes), ctypes.byref(p)))
+        self.ptr, self.nbytes = p.value, int(nbytes)
+
+    def tensor(self):
+        import torch
+        if not self.ptr:
+            raise ValueError("the buffer is closed")
+        arr = (ctypes.c_uint8 * self.nbytes).from_address(self.ptr)
+        arr._owner = self  # the tensor keeps the buffer alive
+        return torch.frombuffer(arr, dtype=torch.uint8)
+
+    def close(self):
+        if self.ptr:
+            ptr, self.ptr = self.ptr, None
+            _check(_host_free(ptr))
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def dv_host_alloc(nbytes) -> HostBuffer:
+    return HostBuffer(nbytes)
+
+
+def dv_host_free(buf: HostBuffer) -> None:
+    buf.close()
+
+
+def host_empty(nbytes):
+    """A uint8 CPU tensor of ``nbytes`` over pinned, mapped host memory from
+    ``dv_host_alloc`` (zeroed)."""
+    return HostBuffer(nbytes).tensor()
 
 
 def dv_allocation_extent(ptr):
@@ -421,6 +471,11 @@ class Replica:
         st, sn = _buf(staging)
         _check(_replica_append(self.h, cache.ref, l0, l1, sp, ep, step, st, sn, _stream(stream)))
 
+    def append_streamed(self, streamer: "Streamer", cache: Cache, l0, l1, seq_start, seq_end,
+                        step):
+        s, e, sp, ep = _ranges(seq_start, seq_end, cache.c.batch)
+        _check(_replica_append_streamed(self.h, streamer.h, cache.ref, l0, l1, sp, ep, step))
+
     def restore(self, cache: Cache, upto_step=-1, staging=None, stream=None):
         st, sn = _buf(staging)
         _check(_replica_restore(self.h, cache.ref, upto_step, st, sn, _stream(stream)))
@@ -464,6 +519,11 @@ def dv_replica_create(host_arena, batch) -> Replica:
 def dv_replica_append(replica: Replica, cache: Cache, l0, l1, seq_start, seq_end, step,
                       staging=None, stream=None) -> None:
     replica.append(cache, l0, l1, seq_start, seq_end, step, staging, stream)
+
+
+def dv_replica_append_streamed(replica: Replica, streamer: Streamer, cache: Cache, l0, l1,
+                               seq_start, seq_end, step) -> None:
+    replica.append_streamed(streamer, cache, l0, l1, seq_start, seq_end, step)
 
 
 def dv_replica_restore(replica: Replica, cache: Cache, upto_step=-1, staging=None,

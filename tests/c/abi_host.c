@@ -59,6 +59,13 @@ int main(void) {
   CHECK(dv_replica_restore_fetched(NULL, &c, -1, NULL) == DV_ERR_INVALID_ARG);
   CHECK(dv_replica_truncate(NULL, 0) == DV_ERR_INVALID_ARG);
   CHECK(dv_replica_restore_fetched_steps(NULL, &c, 0, -1, NULL) == DV_ERR_INVALID_ARG);
+  CHECK(dv_replica_append_streamed(NULL, NULL, &c, 0, 48, s, e, 0) == DV_ERR_INVALID_ARG);
+  /* host memory: bad arguments and unknown pointers are refused without CUDA */
+  void* hp = (void*)0x1;
+  CHECK(dv_host_alloc(0, &hp) == DV_ERR_INVALID_ARG && hp == NULL);
+  CHECK(dv_host_alloc(16, NULL) == DV_ERR_INVALID_ARG);
+  CHECK(dv_host_free((void*)0x10000) == DV_ERR_INVALID_ARG);
+  CHECK(dv_host_free(NULL) == DV_OK);
   /* the log scatter: tables, counts and ranges are checked on the host */
   int32_t layers[2] = {0, 48}, ranges[16];
   memcpy(ranges, s, sizeof s);

@@ -156,7 +156,10 @@ int main(void) {
 
   /* A replica of the ranges (snapshot) and one decode token after each range
    * (where it fits), restored record-batched and pipelined through the
-   * fetcher into zeroed caches: both give the selected slices of [s, e + 1). */
+   * fetcher into zeroed caches: both give the selected slices of [s, e + 1).
+   * Then the same log appended again through the streamer (one layer per
+   * slot: the snapshot in L groups), byte for byte the same arena, restored
+   * record-batched. */
   int32_t e1[B];
   for (int b = 0; b < B; ++b) e1[b] = e[b] < S ? e[b] + 1 : e[b];
   size_t delta = 0;
@@ -167,11 +170,23 @@ int main(void) {
   CHECK(dv_replica_create(&rep, arena, bytes + delta, B) == DV_OK);
   CHECK(dv_replica_append(rep, &c, 0, L, s, e, 0, NULL, 0, NULL) == DV_OK);
   CHECK(dv_replica_append(rep, &c, 0, L, e, e1, 1, NULL, 0, NULL) == DV_OK);
-  for (int mode = 0; mode < 2; ++mode) {
+  for (int mode = 0; mode < 3; ++mode) {
+    if (mode == 2) {
+      CHECK(cudaDeviceSynchronize() == cudaSuccess);
+      uint8_t* first = (uint8_t*)malloc(bytes + delta);
+      memcpy(first, arena, bytes + delta);
+      memset(arena, 0, bytes + delta);
+      CHECK(dv_replica_truncate(rep, 0) == DV_OK);
+      CHECK(dv_replica_append_streamed(rep, st, &c, 0, L, s, e, 0) == DV_OK);
+      CHECK(dv_replica_append_streamed(rep, st, &c, 0, L, e, e1, 1) == DV_OK);
+      CHECK(dv_streamer_wait(st) == DV_OK);
+      CHECK(memcmp(first, arena, bytes + delta) == 0);
+      free(first);
+    }
     cudaMemset(yk, 0, n * P);
     cudaMemset(yv, 0, n * P);
     CHECK(cudaDeviceSynchronize() == cudaSuccess);
-    if (mode == 0) {
+    if (mode != 1) {
       CHECK(dv_replica_restore_batched(rep, &y, -1, NULL, 0, NULL) == DV_OK);
     } else {
       CHECK(dv_replica_restore_fetched(rep, &y, -1, ft) == DV_OK);

@@ -263,8 +263,11 @@ def test_fetcher_errors_enqueue_nothing():
     assert (H.to_np(back.k) == 0x11).all() and (H.to_np(back.v) == 0x11).all()
 
 
-@pytest.mark.parametrize("staged", [False, True])
-def test_replica_snapshot_deltas_restore_truncate(staged):
+@pytest.mark.parametrize("mode", ["fused", "staged", "streamed"])
+def test_replica_snapshot_deltas_restore_truncate(mode):
+    """streamed: the appends go through a layer streamer whose slots hold two
+    of the snapshot's layers, so the snapshot goes in two groups (layers 0-1,
+    then 2) and each delta in one."""
     g = Geometry("rep", 3, 4, 2, 128, 64, 2, "bf16")
     kh, vh = H.host_cache(g, 12)
     cache = H.device_cache(g, fill=(kh, vh))
@@ -273,16 +276,31 @@ def test_replica_snapshot_deltas_restore_truncate(staged):
     steps = 6
     total = ORC.staging_bytes(g, 0, g.num_layers, zero, len0 + steps)
     arena = H.pinned(total + 4096)
-    staging = H.device_bytes(total) if staged else None
+    staging = H.device_bytes(total) if mode == "staged" else None
+    streamer = None
+    if mode == "streamed":
+        slot = 2 * ORC.staging_bytes(g, 0, 1, zero, len0)
+        torch.cuda.synchronize()
+        streamer = dv.Streamer(H.device_bytes(slot), H.device_bytes(slot), torch.cuda.Stream(),
+                               torch.cuda.Stream())
     rep = dv.Replica(arena, g.batch)
-    rep.append(cache, 0, g.num_layers, zero, len0, step=0, staging=staging)
+
+    def append(l0, l1, s, e, step):
+        if streamer:
+            rep.append_streamed(streamer, cache, l0, l1, s, e, step=step)
+        else:
+            rep.append(cache, l0, l1, s, e, step=step, staging=staging)
+
+    append(0, g.num_layers, zero, len0, 0)
     pos = len0.copy()
     records = [(0, g.num_layers, zero, len0.copy())]
     for k in range(1, steps + 1):
         act = np.array([1, 1, 1 if k < 3 else 0, 1], np.int32)  # sequence 2 finishes
-        rep.append(cache, 0, g.num_layers, pos, pos + act, step=k, staging=staging)
+        append(0, g.num_layers, pos, pos + act, k)
         records.append((0, g.num_layers, pos.copy(), (pos + act).copy()))
         pos = pos + act
+    if streamer:
+        streamer.wait()
     torch.cuda.synchronize()
     nrec, used = rep.info()
     assert nrec == steps + 1
@@ -304,6 +322,38 @@ def test_replica_snapshot_deltas_restore_truncate(staged):
     kw, vw = ORC.restore(g, [(a, b, s, e, ORC.pack(g, kh, vh, a, b, s, e))
                              for a, b, s, e in records[:4]])
     assert np.array_equal(H.to_np(z2.k), kw) and np.array_equal(H.to_np(z2.v), vw)
+    rep.close()
+    if streamer:
+        streamer.close()
+
+
+def test_replica_append_streamed_errors():
+    g = Geometry("reperr", 3, 4, 2, 128, 64, 2, "bf16")
+    cache = H.device_cache(g, fill=0x21)
+    zero = np.zeros(g.batch, np.int32)
+    len0 = np.array([5, 20, 1, 33], np.int32)
+    slab = ORC.staging_bytes(g, 0, 1, zero, len0)
+    arena = H.pinned(ORC.staging_bytes(g, 0, g.num_layers, zero, len0) + 64)
+    rep = dv.Replica(arena, g.batch)
+    small = dv.Streamer(H.device_bytes(slab - 16), H.device_bytes(slab - 16))
+    # one layer of the record is larger than a slot: refused before anything is enqueued
+    assert _status(lambda: rep.append_streamed(small, cache, 0, 3, zero, len0, step=0)) == \
+        dv.DV_ERR_BUFFER_TOO_SMALL
+    assert rep.info() == (0, 0)
+    ok = dv.Streamer(H.device_bytes(slab), H.device_bytes(slab))
+    rep.append_streamed(ok, cache, 0, 3, zero, len0, step=1)       # three groups of one layer
+    assert _status(lambda: rep.append_streamed(ok, cache, 0, 3, zero, len0, step=2)) == \
+        dv.DV_ERR_BUFFER_TOO_SMALL                                  # the arena is full
+    assert _status(lambda: rep.append_streamed(ok, cache, 0, 1, zero, zero + 1, step=0)) == \
+        dv.DV_ERR_INVALID_ARG                                       # step before the last record's
+    assert _status(lambda: rep.append_streamed(ok, cache, 0, 1, zero, zero + 65, step=3)) == \
+        dv.DV_ERR_RANGE
+    ok.wait()
+    torch.cuda.synchronize()
+    assert rep.info() == (1, 3 * slab)
+    assert (arena.numpy()[:3 * slab] == 0x21).all()               # every byte of the cache is 0x21
+    small.close()
+    ok.close()
     rep.close()
 
 
