@@ -58,7 +58,8 @@ dv_status dv_host_alloc(size_t bytes, void** out) {
   if (!out) return fail(DV_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   if (bytes == 0) return fail(DV_ERR_INVALID_ARG, "bytes is 0");
-  const size_t page = (size_t)sysconf(_SC_PAGESIZE);
+  const long ps = sysconf(_SC_PAGESIZE);
+  const size_t page = ps > 0 ? (size_t)ps : 4096;
   const size_t hp = huge_page_bytes();
   const size_t len = round_up(bytes, page);
   if (len < bytes || len + hp < len) return fail(DV_ERR_INVALID_ARG, "bytes %zu too large", bytes);
