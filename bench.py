@@ -1139,7 +1139,7 @@ class MicrobatchSwapping:
         for m, (p, o) in enumerate(self.mbs):
             seed = seed_of(4) * 10 + m
             cap = int((p.sum() + g.batch * (rounds + 1)) * self.per_token)  # + per_op's
-            arena = torch.empty(cap, dtype=torch.uint8, pin_memory=True)
+            arena = dv.host_empty(cap)
             rep = dv.Replica(arena, g.batch)
             slot = self.slots[0]
             synth_gpu.fill_cache(g, slot.k, slot.v, seed)
@@ -1270,7 +1270,7 @@ class MicrobatchSwapping:
         L = g.num_layers
         slot = self.slots[0]
         big = max(dv.dv_staging_bytes(slot, 0, L, self.zs, ln) for ln in self.lens)
-        host = torch.empty(big, dtype=torch.uint8, pin_memory=True)
+        host = dv.host_empty(big)
 
         def ev_time(fn):
             a = torch.cuda.Event(enable_timing=True)
@@ -1439,7 +1439,7 @@ def workload_section(torch, dv):
     lens = opt13b_lengths()
     zs = np.zeros(g.batch, np.int32)
     n = dv.dv_staging_bytes(c, 0, g.num_layers, zs, lens)
-    host = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    host = dv.host_empty(n)
     stg = torch.empty(4 * (n // g.num_layers), dtype=torch.uint8, device="cuda")
     res = {"payload_bytes": n}
     for name, st in (("fused", None), ("staged", stg)):
@@ -1456,7 +1456,7 @@ def workload_section(torch, dv):
     len0 = bloom_lengths()
     zs = np.zeros(g.batch, np.int32)
     total = dv.dv_staging_bytes(c, 0, g.num_layers, zs, len0 + BLOOM_DECODE_STEPS)
-    arena = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    arena = dv.host_empty(total)
     rep = dv.Replica(arena, g.batch)
     snap = dv.dv_staging_bytes(c, 0, g.num_layers, zs, len0)
 
