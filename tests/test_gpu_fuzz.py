@@ -145,7 +145,9 @@ def test_random_replica_logs_restore_like_the_oracle(block):
     """Random logs (1 to 40 records, each over its own layer range and range
     pattern, the live cache rewritten now and then so that later records
     carry new bytes for slices earlier records wrote) restore to the cache
-    the oracle's in-order restore gives."""
+    the oracle's in-order restore gives; the arena holds the oracle's records
+    end to end, whichever way they were appended."""
+    import torch
     rng = np.random.default_rng(0x5E57 + block)
     for i in range(20):
         g = _geometry(rng, 1000 + 100 * block + i, max_bytes=1 << 20)
@@ -165,14 +167,34 @@ def test_random_replica_logs_restore_like_the_oracle(block):
         total = sum(d.size for *_, d, _ in logs)
         arena = H.pinned(total + 64)
         rep = dv.Replica(arena, g.batch)
-        for step, (l0, l1, s, e, _, c) in enumerate(logs):
-            rep.append(c, l0, l1, s, e, step=step)
         slabs = [d.size // (l1 - l0) for l0, l1, _, _, d, _ in logs if d.size]
         slab = max(slabs) if slabs else 16
+        # appended fused, staged, or through a layer streamer whose slots hold
+        # between one layer slab and the whole log (records split into groups)
+        mode = str(rng.choice(["fused", "staged", "streamed"]))
+        streamer = staging = None
+        if mode == "streamed":
+            slot = (int(rng.integers(slab, max(slab, total) + 1)) + 15) // 16 * 16
+            streamer = dv.Streamer(H.device_bytes(slot), H.device_bytes(slot),
+                                   torch.cuda.current_stream(), torch.cuda.Stream())
+        elif mode == "staged":
+            staging = H.device_bytes(max(total, 16))
+        for step, (l0, l1, s, e, _, c) in enumerate(logs):
+            if streamer:
+                rep.append_streamed(streamer, c, l0, l1, s, e, step=step)
+            else:
+                rep.append(c, l0, l1, s, e, step=step, staging=staging)
+        if streamer:
+            streamer.wait()
+            streamer.close()
+        torch.cuda.synchronize()
+        assert np.array_equal(arena.numpy()[:total],
+                              np.concatenate([d for *_, d, _ in logs]) if total else
+                              np.empty(0, np.uint8)), (g, nrec, mode)
         how = str(rng.choice(["fused", "staged", "fetched"]))
         z = _restore_into_zero(g, rep, how, slab, total, rng)
         kw, vw = ORC.restore(g, [(l0, l1, s, e, d) for l0, l1, s, e, d, _ in logs])
-        where = (g, nrec, how)
+        where = (g, nrec, mode, how)
         assert np.array_equal(H.to_np(z.k), kw), where
         assert np.array_equal(H.to_np(z.v), vw), where
         rep.close()
