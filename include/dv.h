@@ -20,7 +20,9 @@
  *   dv_replica_*     §3 "Fault detection and recovery" (Fig 10) on one GPU:
  *                    per-step decode deltas (§3 "Token computation and
  *                    streaming parallelization", Fig 7c) appended to a
- *                    host-side replica, and the restore of a cache from it.
+ *                    host-side replica, and the restore of a cache from it;
+ *                    dv_replica_append_streamed appends through a layer
+ *                    streamer's two slots (Fig 7b streaming into Fig 10).
  *   dv_kv_unpack_records  the scatter of a whole log of records at once.
  *   dv_swapper_*     §3 "Microbatch swapping" (Fig 9): N microbatches
  *                    through two device caches, the next swapped in while
@@ -28,6 +30,9 @@
  *   dv_delta_*       §3 "Token computation and streaming parallelization"
  *                    (Fig 7c): each step's delta streamed on a side stream
  *                    while the next step computes.
+ *   dv_host_alloc    pinned, mapped host memory on huge pages for replica
+ *                    arenas and swap buffers (the host side of every
+ *                    transfer above).
  *
  * Cache layout (the FasterTransformer-style layout the pages build on).  Per
  * layer, with x = 16 / elem_bytes elements per 16-byte chunk:
@@ -49,7 +54,10 @@
  *    read during the call only; 0 <= s_b <= e_b <= max_seq; an empty range is
  *    legal (a finished sequence).  Layer range: 0 <= l0 <= l1 <= num_layers.
  *  - Ownership: the caller allocates every buffer.  The library allocates no
- *    device or host memory except the small streamer and replica handles.
+ *    device or host memory except its small handles (streamer, fetcher,
+ *    replica, swapper, delta streamer), one copy stream per CUDA context for
+ *    staged swaps, and the pinned host memory dv_host_alloc returns when
+ *    asked (dv_swap_out_noalloc's buffer is static device memory).
  *  - Memory kinds: k_base / v_base and `staging` are device memory of the
  *    current device.  A pack destination or unpack source may be device
  *    memory or pinned (page-locked, mapped) host memory; for host memory the
@@ -162,16 +170,16 @@ dv_status dv_allocation_extent(const void* ptr, size_t* bytes_after);
  * decline).  Why: on a GB300 host with 64 KiB base pages, copy-engine passes
  * over tens of GB of pinned memory made of base pages periodically run at
  * about half the link rate, where the same passes over huge pages run at the
- * full rate every time.  Not thread-safe with respect to a concurrent
- * dv_host_free of the same pointer; otherwise safe from any thread.  Needs a
- * CUDA device (the registration makes the current device's primary context
+ * full rate every time.  Synchronous; safe from any thread.  Needs a CUDA
+ * device (the registration makes the current device's primary context
  * current if the thread has none).  Errors: DV_ERR_INVALID_ARG (out is NULL,
  * bytes is 0, no host memory), DV_ERR_CUDA (the registration failed; nothing
  * stays allocated).  No counterpart on the pages: they state only that the
  * host copies live in pinned CPU memory. */
 dv_status dv_host_alloc(size_t bytes, void** out);
 
-/* Unregisters and unmaps memory from dv_host_alloc (NULL: nothing to do).
+/* Unregisters and unmaps memory from dv_host_alloc (NULL: nothing to do);
+ * synchronous.
  * The caller ensures that no enqueued work still reads or writes it.
  * DV_ERR_INVALID_ARG for a pointer dv_host_alloc did not return (or already
  * freed); DV_ERR_CUDA if the unregistration fails (the memory is unmapped
