@@ -123,8 +123,11 @@ int main(void) {
   CHECK(cudaMalloc(&yk, n * P) == cudaSuccess && cudaMalloc(&yv, n * P) == cudaSuccess);
   cudaMemset(yk, 0, n * P);
   cudaMemset(yv, 0, n * P);
+  /* The host side from dv_host_alloc: pinned, mapped, on huge pages where the
+   * kernel gives them. */
   uint8_t* out = NULL;
-  CHECK(cudaHostAlloc((void**)&out, bytes, cudaHostAllocDefault) == cudaSuccess);
+  CHECK(dv_host_alloc(bytes, (void**)&out) == DV_OK && out != NULL);
+  CHECK(((uintptr_t)out & 15) == 0);
   cudaStream_t ps, cs, fc, fu;
   cudaStreamCreate(&ps);
   cudaStreamCreate(&cs);
@@ -294,6 +297,9 @@ int main(void) {
   dv_fetcher_destroy(ft);
   dv_streamer_destroy(st);
   cudaEventDestroy(out_done);
+  CHECK(cudaDeviceSynchronize() == cudaSuccess);
+  CHECK(dv_host_free(out) == DV_OK);
+  CHECK(dv_host_free(out) == DV_ERR_INVALID_ARG); /* already freed */
   if (failures == 0) printf("gpu_roundtrip: all checks passed\n");
   return failures == 0 ? 0 : 1;
 }
