@@ -185,7 +185,8 @@ def whole_job_rate(bytes_per_step, steps, max_secs, world):
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "temperature.gpu,temperature.memory,clocks.mem")
 
     def __init__(self, local_rank):
         vis = os.environ.get("CUDA_VISIBLE_DEVICES")
@@ -209,6 +210,7 @@ class ClockSampler:
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
         sm, mx, reasons, power = [], [], set(), []
+        extra = {"gpu_temp_c": [], "mem_temp_c": [], "mem_mhz": []}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
@@ -223,10 +225,18 @@ class ClockSampler:
             for nm, val in zip(names, parts[5:9]):
                 if val.lower() == "active":
                     reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None,
-                "power_w_max": max(power) if power else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+            for key, val in zip(extra, parts[9:12]):
+                try:
+                    extra[key].append(float(val))
+                except ValueError:  # "N/A" where the GPU does not report it
+                    pass
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(mx) if mx else None,
+               "power_w_max": max(power) if power else None,
+               "samples": len(sm), "reasons": sorted(reasons)}
+        out.update({k: (max(v) if "temp" in k else statistics.median(v)) if v else None
+                    for k, v in extra.items()})
+        return out
 
 
 # ---- the reference arm: the CPU oracle on a bounded sample --------------------
