@@ -239,6 +239,22 @@ class ClockSampler:
         return out
 
 
+def gpu_identity(local_rank):
+    """Name, VBIOS, ECC mode, power limit and memory size of the GPU the bench
+    runs on (read once; None when nvidia-smi cannot tell)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    index = vis.split(",")[local_rank] if vis else str(local_rank)
+    fields = ["name", "vbios_version", "ecc.mode.current", "power.limit", "memory.total"]
+    try:
+        out = subprocess.run(["nvidia-smi", f"--query-gpu={','.join(fields)}",
+                              "--format=csv,noheader", "-i", index], capture_output=True,
+                             text=True, timeout=20).stdout.strip()
+    except (OSError, subprocess.SubprocessError):
+        return None
+    vals = [v.strip() for v in out.split(",")]
+    return dict(zip(fields, vals)) if len(vals) == len(fields) else None
+
+
 # ---- the reference arm: the CPU oracle on a bounded sample --------------------
 
 def host_cores() -> int:
@@ -1783,6 +1799,7 @@ def run_mine(args):
         "hbm_by_workload": hbm,
         "gpu_launches": per_step["launches_per_step"] * args.steps,
         "clocks": clk,
+        "gpu": gpu_identity(local),
     }
     print(json.dumps(line), flush=True)
 
