@@ -87,7 +87,8 @@ def parse_args():
                              "swap-in", "ragged-pack", "ragged-unpack", "delta-graph-pack",
                              "delta-graph-unpack", "bloom-snapshot-pack",
                              "bloom-snapshot-unpack", "bloom-delta-pack", "bloom-run-restore",
-                             "short-ragged-pack", "short-ragged-unpack", "gpt2-step"],
+                             "short-ragged-pack", "short-ragged-unpack", "group-pack",
+                             "group-unpack", "gpt2-step"],
                     help="run one kernel of the step on an 8-layer cache of the workload's "
                          "shape, 5 launches, and exit (a small case for profilers); "
                          "flat-*: ragged 16..64-token ranges of the OPT-13B-shaped cache, "
@@ -104,6 +105,8 @@ def parse_args():
                          "(snapshot pack / unpack: 3 launches; delta pack: 8 launches, 8 "
                          "tokens apart; run restore: 3 launches of 256 one-token records); "
                          "short-ragged-*: the flat-* ranges under the automatic kernel choice; "
+                         "group-*: ragged 2..32-token ranges of 32 sequences, 40 layers, "
+                         "head_dim 128, all in grouped tiles; "
                          "gpt2-step: the GPT2-1.5B side-section step (one stream), 3 graph "
                          "replays after one eager step")
     return ap.parse_args()
@@ -1820,6 +1823,9 @@ def run_kernel_case(case):
     if case.startswith("flat") or case.startswith("short-ragged"):
         run_flat_case(case, torch, dv, synth_gpu)
         return
+    if case.startswith("group"):
+        run_group_case(case, torch, dv, synth_gpu)
+        return
     if case.startswith("ragged"):
         run_ragged_case(case, torch, dv, synth_gpu)
         return
@@ -1876,7 +1882,8 @@ def run_flat_case(case, torch, dv, synth_gpu):
     """Ragged short ranges: 16..64 tokens at seeded positions of each of the 8
     sequences of the OPT-13B-shaped cache, all 40 layers (about 260 MB of
     staging, more than L2), 5 launches; flat-*: the flat kernel forced,
-    short-ragged-*: the automatic choice (the tile kernel for these ranges)."""
+    short-ragged-*: the automatic choice (the tile kernel for the ranges of
+    more than 32 tokens, grouped tiles in a second launch for the others)."""
     from synth.configs import OPT13B
     g = OPT13B
     k = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
@@ -1895,6 +1902,35 @@ def run_flat_case(case, torch, dv, synth_gpu):
             dv.dv_kv_pack(cache, 0, g.num_layers, s, e, stg, variant=var)
         else:
             dv.dv_kv_unpack(cache, 0, g.num_layers, s, e, stg, variant=var)
+    torch.cuda.synchronize()
+    print(f"{case}: 5 launches of {2 * n} algorithmic bytes each "
+          f"(ranges of {int((e - s).min())}..{int((e - s).max())} tokens)")
+
+
+def run_group_case(case, torch, dv, synth_gpu):
+    """Ragged short ranges in grouped tiles: 2..32 tokens at seeded positions of
+    each of 32 sequences, a cache of 40 layers, 40 heads, head_dim 128 (fp16)
+    and 128 token slots (3.4 GB; about 450 MB of staging, more than L2), every
+    range at most half the tile kernel's token block, so the tile kernel's
+    launch is all grouped tiles (group_kernel); 5 launches."""
+    from synth.configs import Geometry
+    g = Geometry("group-c16", 40, 32, 40, 128, 128, 2, "fp16")
+    k = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+    v = torch.empty(g.tensor_bytes, dtype=torch.uint8, device="cuda")
+    synth_gpu.fill_cache(g, k, v, seed_of(3))
+    cache = dv.Cache.from_geometry(g, k, v)
+    rng = np.random.default_rng(seed_of(3))
+    s = rng.integers(0, g.max_seq - 32, size=g.batch).astype(np.int32)
+    e = (s + rng.integers(2, 33, size=g.batch)).astype(np.int32)
+    n = dv.dv_staging_bytes(cache, 0, g.num_layers, s, e)
+    stg = torch.empty(n, dtype=torch.uint8, device="cuda")
+    tile = dv.DV_VARIANT_TILE
+    dv.dv_kv_pack(cache, 0, g.num_layers, s, e, stg, variant=tile)
+    for _ in range(5):
+        if case.endswith("-pack"):
+            dv.dv_kv_pack(cache, 0, g.num_layers, s, e, stg, variant=tile)
+        else:
+            dv.dv_kv_unpack(cache, 0, g.num_layers, s, e, stg, variant=tile)
     torch.cuda.synchronize()
     print(f"{case}: 5 launches of {2 * n} algorithmic bytes each "
           f"(ranges of {int((e - s).min())}..{int((e - s).max())} tokens)")

@@ -133,9 +133,15 @@ typedef enum {
                           token kernel below 640 16-byte chunks per head and range
                           (80 tokens at head_dim 64, fp16), the tile kernel above;
                           ragged ranges: the flat kernel below a mean of 512 chunks,
-                          the tile kernel above */
+                          the tile kernel above.  At 8 or 16 chunks per token
+                          (head_dim 64 / 128 in 2-byte elements) the unpack takes the
+                          tile kernel from 64 chunks (ragged) and from 128 (equal
+                          lengths above one token), the pack from 300 (ragged, 16
+                          chunks per token) */
   DV_VARIANT_FLAT = 1, /* staging order, each warp a window of 128 chunks */
-  DV_VARIANT_TILE = 2, /* token tiles; K transposed through shared memory */
+  DV_VARIANT_TILE = 2, /* token tiles; K transposed through shared memory; at 8 or
+                          16 chunks per token, ranges of at most half the token block
+                          go several heads to a tile (a second launch) */
   DV_VARIANT_TOKEN = 3 /* every non-empty range equally long: one chunk per thread */
 } dv_variant;
 

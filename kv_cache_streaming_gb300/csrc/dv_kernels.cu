@@ -10,7 +10,7 @@
 // one V row.  Bytes are copied as bit patterns and never pass through
 // floating point.
 //
-// Six kernels, the first three with a pack and an unpack form:
+// Seven kernels, the first four with a pack and an unpack form:
 //  * tile_kernel (long ranges): one CTA of 256 threads moves one tile, up to TB
 //    tokens of one (layer, K|V, sequence, head); TB * C = 1024 chunks (16 KiB)
 //    when C is 8 or 16, four in flight per thread.  A V tile is one contiguous
@@ -22,6 +22,11 @@
 //    fall in 8 distinct 16-byte bank groups.  The grid is persistent (SMs x
 //    resident CTAs) and strides over the tiles in staging order, so at any
 //    moment the whole GPU works on neighbouring tiles.
+//  * group_kernel (grouped tiles, C = 8 or 16): the tile kernel's shape for
+//    ranges of at most half the token block, G = TB / NT heads of one
+//    sequence to a tile (NT = the range length rounded up to a power of two),
+//    so that short ranges fill the tile; a launch with both long and short
+//    ranges runs the tile kernel over the long ones, then this one.
 //  * token_kernel (every non-empty range of one common length: one-token
 //    decode deltas, multi-token deltas): one chunk per thread, its run and
 //    token found with multiply-high divisions by host constants; no shared
@@ -73,6 +78,7 @@ struct KParams {
   int32_t tok_pre[MAXB + 1];
   int32_t tile_pre[MAXB + 1];  // tile kernel: H * sum of ceil(len / TB)
   uint32_t m_len[MAXB];        // flat kernel: ceil(2^32 / seq_len[b]), 0 for length 1
+  uint8_t log2nt[MAXB];        // grouped tile kernel: log2 of token slots per head (LOG2TB: plain tiles)
 };
 
 #ifndef DV_TILE_CPT
@@ -84,6 +90,9 @@ struct KParams {
 #ifndef DV_FLAT_MIN_BLOCKS
 #define DV_FLAT_MIN_BLOCKS 4  // resident CTAs per SM the flat kernel is compiled for
                               // (5 spills: 20-40% slower on 16..64-token unpacks)
+#endif
+#ifndef DV_GROUP_MIN_BLOCKS
+#define DV_GROUP_MIN_BLOCKS 5  // resident CTAs per SM the grouped tile kernel is compiled for
 #endif
 #ifndef DV_LOOKUP_HOST_SCALE
 #define DV_LOOKUP_HOST_SCALE 2  // flat / record kernels on host memory: CTAs per tile-kernel CTA
@@ -706,6 +715,159 @@ tile_kernel(const __grid_constant__ KParams<MAXB> p) {
     copy_tile<PACK, false, LOG2C>(p, decode_tile<LOG2TB>(p, tile, C), smem);
 }
 
+// ---- grouped tiles: short ranges in the tile kernel's shape -------------------
+
+// A tile of several heads of one sequence whose range is at most half the
+// token block: G = TB / NT consecutive heads with NT = 2^log2nt >= n token
+// slots each (n the range's length).  In staging the heads' blocks lie back to
+// back, one span of heads * n * C chunks.  In the cache, K is heads * C rows of
+// n chunks, S apart (head h's rows continue head h - 1's: row r of the tile is
+// row r % C of head r / C), and V one run of n * C chunks per head, S * C
+// apart.
+struct GroupJob {
+  uint4* stg;
+  uint4* cache;    // K: row 0 of the first head at the range start; V: its first token row
+  int32_t n;       // tokens of each head
+  int32_t heads;   // heads in the tile (G; fewer in the sequence's last tile)
+  int32_t log2nt;  // NT = 2^log2nt token slots per head
+  bool is_v;
+};
+
+// Moves one grouped tile.  Its TB * C slots are G heads x NT tokens x C
+// chunks; slot (g, t, c) is live when g < heads and t < n.  Staging and V are
+// walked in token order (g, t, c): head g's block is n * C chunks from
+// g * n * C in staging and from g * S * C in V.  K goes through shared memory
+// ([t][r], odd pitch; r = g * C + c), its cache side walked in row order
+// (r, t) so that consecutive lanes move a row's consecutive tokens.  No
+// division: every index is a shift or a mask.
+template <bool PACK, int LOG2C, typename Params>
+__device__ __forceinline__ void copy_group(const Params& p, const GroupJob& j, uint4* smem) {
+  constexpr int C = 1 << LOG2C;
+  constexpr int LOG2TB = TileShape<LOG2C>::LOG2TB;
+  constexpr int TC = (1 << LOG2TB) * C;  // chunk slots of a tile
+  const int log2nt = j.log2nt;
+  const int ntm = (1 << log2nt) - 1;
+  const int log2hc = log2nt + LOG2C;     // slots of one head
+  const int hcm = (1 << log2hc) - 1;
+  const int RP = (1 << (LOG2TB - log2nt + LOG2C)) | 1;  // row pitch: G * C rows, odd
+  const int n = j.n;
+  const int heads = j.heads;
+  const int rows = heads << LOG2C;
+  uint4* const stg = j.stg;
+  uint4* const cache = j.cache;
+  const int64_t S = p.S;
+  const int64_t vstride = S << LOG2C;   // V chunks from one head's first token row to the next's
+  // staging index of slot (g, t, c), or -1 when the slot is not live
+  const auto slot_stg = [&](int q) -> int {
+    const int g = q >> log2hc, t = (q >> LOG2C) & ntm;
+    return (g < heads && t < n) ? (g * n + t) * C + (q & (C - 1)) : -1;
+  };
+  if (j.is_v) {
+    for (int q0 = threadIdx.x; q0 < TC; q0 += kThreads * kTileUnroll) {
+      uint4 val[kTileUnroll];
+      int sq[kTileUnroll];
+#pragma unroll
+      for (int u = 0; u < kTileUnroll; ++u) {
+        const int q = q0 + u * kThreads;
+        sq[u] = slot_stg(q);
+        uint4* const cp = cache + (q >> log2hc) * vstride + (q & hcm);
+        if (sq[u] >= 0 && !(DV_OK_V(cp, 51) && DV_OK_S(stg + sq[u], 52))) sq[u] = -1;
+        if (sq[u] >= 0) val[u] = PACK ? ld_stream(cp) : ld_stream(stg + sq[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < kTileUnroll; ++u) {
+        const int q = q0 + u * kThreads;
+        if (sq[u] < 0) continue;
+        if (PACK) stg[sq[u]] = val[u];
+        else cache[(q >> log2hc) * vstride + (q & hcm)] = val[u];
+      }
+    }
+  } else if (PACK) {
+    for (int q0 = threadIdx.x; q0 < TC; q0 += kThreads * kTileUnroll) {
+      uint4 val[kTileUnroll];
+#pragma unroll
+      for (int u = 0; u < kTileUnroll; ++u) {
+        const int q = q0 + u * kThreads;
+        const int t = q & ntm, r = q >> log2nt;
+        if (t < n && r < rows && DV_OK_K(cache + (int64_t)r * S + t, 53))
+          val[u] = ld_stream(cache + (int64_t)r * S + t);
+      }
+#pragma unroll
+      for (int u = 0; u < kTileUnroll; ++u) {
+        const int q = q0 + u * kThreads;
+        const int t = q & ntm, r = q >> log2nt;
+        if (t < n && r < rows) smem[t * RP + r] = val[u];
+      }
+    }
+    __syncthreads();
+    for (int q = threadIdx.x; q < TC; q += kThreads) {
+      const int s = slot_stg(q);
+      const int r = ((q >> log2hc) << LOG2C) + (q & (C - 1));
+      if (s >= 0 && DV_OK_S(stg + s, 54)) stg[s] = smem[((q >> LOG2C) & ntm) * RP + r];
+    }
+    __syncthreads();
+  } else {
+    for (int q0 = threadIdx.x; q0 < TC; q0 += kThreads * kTileUnroll) {
+      uint4 val[kTileUnroll];
+      int sq[kTileUnroll];
+#pragma unroll
+      for (int u = 0; u < kTileUnroll; ++u) {
+        sq[u] = slot_stg(q0 + u * kThreads);
+        if (sq[u] >= 0 && !DV_OK_S(stg + sq[u], 55)) sq[u] = -1;
+        if (sq[u] >= 0) val[u] = ld_stream(stg + sq[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < kTileUnroll; ++u) {
+        const int q = q0 + u * kThreads;
+        if (sq[u] < 0) continue;
+        const int r = ((q >> log2hc) << LOG2C) + (q & (C - 1));
+        smem[((q >> LOG2C) & ntm) * RP + r] = val[u];
+      }
+    }
+    __syncthreads();
+    for (int q = threadIdx.x; q < TC; q += kThreads) {
+      const int t = q & ntm, r = q >> log2nt;
+      if (t < n && r < rows && DV_OK_K(cache + (int64_t)r * S + t, 56))
+        cache[(int64_t)r * S + t] = smem[t * RP + r];
+    }
+    __syncthreads();
+  }
+}
+
+// Grouped tiles of the sequences whose range is at most half the token block
+// (log2nt[b] < LOG2TB; the other sequences have no tiles here and go to the
+// tile kernel in a launch of their own).  Tiles in staging order: (layer,
+// K|V), sequence, head group.  C = 8 or 16.
+template <bool PACK, int MAXB, int LOG2C>
+__global__ void __launch_bounds__(kThreads, DV_GROUP_MIN_BLOCKS)
+group_kernel(const __grid_constant__ KParams<MAXB> p) {
+  extern __shared__ uint4 smem[];  // TB rows of (C | 1) chunks
+  constexpr int C = 1 << LOG2C;
+  constexpr int LOG2TB = TileShape<LOG2C>::LOG2TB;
+  int64_t tile = blockIdx.x;
+  if (tile >= p.total) return;
+  pdl_enter();
+  for (; tile < p.total; tile += gridDim.x) {
+    const int64_t lkv = (int64_t)div64_by((uint64_t)tile, (uint64_t)p.tiles_per_lkv, p.m_tpl);
+    const int32_t r = (int32_t)(tile - lkv * p.tiles_per_lkv);
+    const int b = find_seq(p.tile_pre, p.B, r);
+    const int32_t len = p.seq_len[b];
+    const int lg = p.log2nt[b];
+    const int32_t h0 = (r - p.tile_pre[b]) << (LOG2TB - lg);
+    const int64_t l = p.l0 + (lkv >> 1);
+    const int64_t bh0 = (int64_t)b * p.H + h0;
+    GroupJob j;
+    j.n = len;
+    j.heads = min(1 << (LOG2TB - lg), p.H - h0);
+    j.log2nt = lg;
+    j.is_v = (lkv & 1) != 0;
+    j.stg = p.stg + lkv * p.lkv_chunks + ((int64_t)p.H * p.tok_pre[b] + (int64_t)h0 * len) * C;
+    j.cache = j.is_v ? p.v + l * p.layer_chunks + (bh0 * p.S + p.seq_start[b]) * C
+                     : p.k + l * p.layer_chunks + bh0 * C * p.S + p.seq_start[b];
+    copy_group<PACK, LOG2C>(p, j, smem);
+  }
+}
+
 // ---- runs of one-token log records (replica restore) -------------------------
 
 // n consecutive log records over the same layers [l0, l0 + nl) and the same
@@ -1008,16 +1170,33 @@ cudaError_t run_flat(const Plan& p, void* stg, cudaStream_t stream) {
   return launch_kernel(kernel, grid, 0, stream, kp);
 }
 
+// Whether sequence b's range goes in grouped tiles: non-empty and at most half
+// the token block, with C = 8 or 16.
+template <int LOG2C>
+bool grouped_seq(const Plan& p, int b) {
+  return LOG2C >= 0 && p.seq_len[b] > 0 && 2 * p.seq_len[b] <= TileShape<LOG2C>::TB;
+}
+
+// The grouped tiles of a launch (group_kernel): sequences whose range is at
+// most half the token block, G = TB / NT heads per tile, NT the range length
+// rounded up to a power of two.
 template <bool PACK, int MAXB, int LOG2C>
-cudaError_t run_tile(const Plan& p, void* stg, cudaStream_t stream) {
+cudaError_t run_group(const Plan& p, void* stg, cudaStream_t stream) {
   static std::atomic<int64_t> occ_cache{0};
-  constexpr int TB = TileShape<LOG2C>::TB;
+  constexpr int LOG2TB = TileShape<LOG2C>::LOG2TB;
+  constexpr int TB = 1 << LOG2TB;
   KParams<MAXB> kp;
   fill_params(kp, p, stg);
   int32_t acc = 0;
   for (int b = 0; b < p.B; ++b) {
     kp.tile_pre[b] = acc;
-    acc += p.H * ((p.seq_len[b] + TB - 1) / TB);
+    kp.log2nt[b] = (uint8_t)LOG2TB;
+    if (!grouped_seq<LOG2C>(p, b)) continue;
+    int lg = 0;
+    while ((1 << lg) < p.seq_len[b]) ++lg;
+    kp.log2nt[b] = (uint8_t)lg;
+    const int32_t G = TB >> lg;  // heads per tile
+    acc += (p.H + G - 1) / G;
   }
   kp.tile_pre[p.B] = acc;
   kp.tiles_per_lkv = acc;
@@ -1025,10 +1204,48 @@ cudaError_t run_tile(const Plan& p, void* stg, cudaStream_t stream) {
   kp.total = tiles;
   kp.m_tpl = div64_magic((uint64_t)kp.tiles_per_lkv);
   const size_t smem = (size_t)TB * (p.C | 1) * sizeof(uint4);
-  const auto kernel = tile_kernel<PACK, MAXB, LOG2C>;
+  const auto kernel = group_kernel<PACK, MAXB, LOG2C>;
   const int64_t cap = host_cap(p, (int64_t)sm_count() * blocks_per_sm(kernel, smem, occ_cache));
   const unsigned grid = (unsigned)(tiles < cap ? tiles : cap);
   return launch_kernel(kernel, grid, smem, stream, kp);
+}
+
+// The tile kernel's launch over the sequences with long ranges, then (C = 8
+// or 16) the grouped tiles of the short ones in a second launch.
+template <bool PACK, int MAXB, int LOG2C>
+cudaError_t run_tile(const Plan& p, void* stg, cudaStream_t stream) {
+  static std::atomic<int64_t> occ_cache{0};
+  constexpr int TB = TileShape<LOG2C>::TB;
+  KParams<MAXB> kp;
+  fill_params(kp, p, stg);
+  bool grouped = false;
+  int32_t acc = 0;
+  for (int b = 0; b < p.B; ++b) {
+    kp.tile_pre[b] = acc;
+    if (grouped_seq<LOG2C>(p, b)) {
+      grouped = true;  // no tiles here
+      continue;
+    }
+    acc += p.H * ((p.seq_len[b] + TB - 1) / TB);
+  }
+  kp.tile_pre[p.B] = acc;
+  if (acc > 0) {
+    kp.tiles_per_lkv = acc;
+    const int64_t tiles = 2 * (int64_t)(p.l1 - p.l0) * acc;
+    kp.total = tiles;
+    kp.m_tpl = div64_magic((uint64_t)kp.tiles_per_lkv);
+    const size_t smem = (size_t)TB * (p.C | 1) * sizeof(uint4);
+    const auto kernel = tile_kernel<PACK, MAXB, LOG2C>;
+    const int64_t cap =
+        host_cap(p, (int64_t)sm_count() * blocks_per_sm(kernel, smem, occ_cache));
+    const unsigned grid = (unsigned)(tiles < cap ? tiles : cap);
+    const cudaError_t err = launch_kernel(kernel, grid, smem, stream, kp);
+    if (err != cudaSuccess) return err;
+  }
+  if constexpr (LOG2C >= 0) {
+    if (grouped) return run_group<PACK, MAXB, LOG2C>(p, stg, stream);
+  }
+  return cudaSuccess;
 }
 
 template <bool PACK, int MAXB, int LOG2C>
@@ -1085,7 +1302,7 @@ template <bool PACK>
 cudaError_t launch(const Plan& p, void* stg, cudaStream_t stream, int variant) {
   if (p.bytes == 0) return cudaSuccess;
   int kind = variant;
-  if (variant == kAuto) kind = auto_kind(p);
+  if (variant == kAuto) kind = auto_kind(p, PACK);
   if (p.B <= kSmallBatch) return dispatch_c<PACK, kSmallBatch>(p, stg, stream, kind);
   return dispatch_c<PACK, kMaxBatch>(p, stg, stream, kind);
 }
@@ -1239,25 +1456,38 @@ bool token_supported(const Plan& p) {
          2 * (int64_t)(p.l1 - p.l0) * p.H * p.tokens * p.C < ((int64_t)1 << 31);
 }
 
-int auto_kind(const Plan& p) {
+int auto_kind(const Plan& p, bool pack) {
   // Equal-length ranges: the token kernel up to about 640 chunks per run
   // (measured on GB300: between 64 and 96 tokens at head_dim 64, between 32
-  // and 48 at 128 in fp16), the tile kernel beyond.  Ragged ranges: the flat
-  // kernel below the tile kernel's crossover (auto_uses_tile).
-  if (token_supported(p))
-    return tile_supported(p) && (int64_t)p.max_len * p.C >= 640 ? kTile : kToken;
-  return auto_uses_tile(p) ? kTile : kFlat;
+  // and 48 at 128 in fp16), the tile kernel beyond.  With grouped tiles (C = 8
+  // or 16) the unpack takes the tile kernel from 128 chunks per run (8 tokens
+  // at head_dim 128, 16 at 64; one-token deltas stay with the token kernel):
+  // its K stores cover each row's tokens together, 7-26% faster at batch 32.
+  // Ragged ranges: the flat kernel below the tile kernel's crossover
+  // (auto_uses_tile).
+  if (token_supported(p)) {
+    if (!tile_supported(p)) return kToken;
+    const int64_t run = (int64_t)p.max_len * p.C;  // chunks per (layer, K|V, sequence, head)
+    if (!pack && (p.C == 8 || p.C == 16) && p.max_len > 1) return run >= 128 ? kTile : kToken;
+    return run >= 640 ? kTile : kToken;
+  }
+  return auto_uses_tile(p, pack) ? kTile : kFlat;
 }
 
-bool auto_uses_tile(const Plan& p) {
+bool auto_uses_tile(const Plan& p, bool pack) {
   if (!tile_supported(p) || p.active == 0) return false;
   // Tiles pay once a (layer, K|V, sequence, head) run holds about 512 chunks
-  // (8 KiB) on average, for pack and unpack alike: measured on GB300 with
-  // ragged ranges over all layers, the flat kernel wins at 292 chunks per
-  // run for head_dim 128 and at 477 for 64 in fp16, the tile kernel at 648
-  // and 712 for 128 (unpack 0.77-0.79 of the copy peak against 0.66) and at
-  // 770 for 64.
-  return p.tokens * p.C >= (int64_t)512 * p.active;
+  // (8 KiB) on average, for pack and unpack alike (measured on GB300 with
+  // ragged ranges over all layers: the flat kernel wins at 292 chunks per run
+  // for head_dim 128 and at 477 for 64 in fp16, the tile kernel at 648 and 712
+  // for 128 and at 770 for 64).  With grouped tiles (C = 8 or 16; ranges of at
+  // most half the token block go several heads to a tile) the unpack wins
+  // from about 64 chunks per run (10-16% on 2..32- and 8..24-token ranges,
+  // batch 8 and 32) and the pack at head_dim 128 from about 300.
+  int64_t per_run = 512;
+  if (p.C == 16) per_run = pack ? 300 : 64;
+  if (p.C == 8 && !pack) per_run = 64;
+  return p.tokens * p.C >= per_run * p.active;
 }
 
 bool checked_build() { return DV_CHECKED != 0; }

@@ -46,10 +46,10 @@ inline int64_t layer_slab_bytes(const Plan& p) { return 2 * p.lkv_chunks * 16; }
 
 enum Variant { kAuto = 0, kFlat = 1, kTile = 2, kToken = 3 };
 
-// Kernel choice of kAuto.
-int auto_kind(const Plan& p);
+// Kernel choice of kAuto for a pack (pack = true) or an unpack.
+int auto_kind(const Plan& p, bool pack);
 // For ragged ranges: whether the tile kernel beats the flat kernel.
-bool auto_uses_tile(const Plan& p);
+bool auto_uses_tile(const Plan& p, bool pack);
 // Whether the tile kernel handles this geometry (C <= 64).
 bool tile_supported(const Plan& p);
 // Whether the token kernel handles these ranges (every non-empty range the

@@ -93,7 +93,7 @@ dv_status plan_log(const dv_cache* cache, const std::vector<LogRec>& all, size_t
         return fail(DV_ERR_INVALID_ARG, "record of step %lld does not match this cache geometry",
                     (long long)rec.step);
       if (rec.bytes == 0) continue;
-      const bool by_itself = dv::auto_kind(q) == dv::kTile || (piece && rec.bytes > piece);
+      const bool by_itself = dv::auto_kind(q, false) == dv::kTile || (piece && rec.bytes > piece);
       if (by_itself && piece && piece < (size_t)dv::layer_slab_bytes(q))
         return fail(DV_ERR_BUFFER_TOO_SMALL, "a staging piece of %zu bytes holds less than one "
                     "layer slab (%lld bytes) of the record of step %lld", piece,
