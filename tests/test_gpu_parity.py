@@ -120,6 +120,31 @@ def test_pack_unpack_geometries(g):
                 check_pack_unpack(g, cache, kh, vh, l0, l1, s, e, variant)
 
 
+@pytest.mark.parametrize("g, lens", [
+    (Geometry("grp16", 2, 12, 37, 128, 160, 2, "fp16"),      # C = 16: 64-token block
+     [1, 2, 3, 31, 32, 33, 63, 64, 65, 0, 17, 129]),
+    (Geometry("grp8", 2, 10, 37, 64, 300, 2, "bf16"),        # C = 8: 128-token block
+     [1, 5, 63, 64, 65, 127, 128, 129, 0, 257]),
+], ids=["c16", "c8"])
+def test_grouped_tiles_at_the_block_edges(g, lens):
+    """The tile variant with ranges around half the token block (grouped tiles up
+    to it, the tile kernel's one-head tiles beyond, both in one call) and 37
+    heads (no group size divides it: every sequence's last group is partial)."""
+    kh, vh = H.host_cache(g, 4321)
+    cache = H.device_cache(g, fill=(kh, vh))
+    rng = np.random.default_rng(55)
+    ln = np.array(lens, np.int32)
+    s = np.array([rng.integers(0, g.max_seq - n + 1) for n in ln], np.int32)
+    e = (s + ln).astype(np.int32)
+    for l0, l1 in ((0, g.num_layers), (1, 2)):
+        check_pack_unpack(g, cache, kh, vh, l0, l1, s, e, dv.DV_VARIANT_TILE)
+        check_pack_unpack(g, cache, kh, vh, l0, l1, s, e, dv.DV_VARIANT_AUTO)
+    # every range short: a launch of grouped tiles alone
+    short = np.minimum(ln, 16).astype(np.int32)
+    check_pack_unpack(g, cache, kh, vh, 0, g.num_layers, s, (s + short).astype(np.int32),
+                      dv.DV_VARIANT_TILE)
+
+
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_pack_to_and_unpack_from_pinned_host(variant):
     g = GEOMS[0]
