@@ -117,6 +117,52 @@ def test_random_pack_unpack_matches_oracle(block):
         del cache, back, dst, src
 
 
+def test_random_grouped_tiles_match_oracle():
+    """Grouped tiles (C = 8 or 16): random head counts (1..80, so the last group of
+    a sequence is often partial), ranges mostly shorter than half the token block
+    mixed with longer ones, through the tile variant and the automatic choice,
+    to and from device or pinned host memory."""
+    rng = np.random.default_rng(0x6A0)
+    for i in range(40):
+        C = int(rng.choice([8, 16]))
+        tb = 1024 // C
+        nh = int(rng.integers(1, 81))
+        B = int(rng.choice([1, 3, 8, 33]))
+        S = int(rng.choice([tb // 2, tb, 2 * tb + 5]))
+        L = int(rng.integers(1, 4))
+        g = Geometry(f"gz{i}", L, B, nh, C * 8, S, 2, "fp16")
+        if g.tensor_bytes > (24 << 20):
+            continue
+        kh, vh = H.host_cache(g, 7700 + i)
+        cache = H.device_cache(g, fill=(kh, vh))
+        short = rng.random(B) < 0.75
+        lens = np.where(short, rng.integers(0, tb // 2 + 1, size=B),
+                        rng.integers(0, S + 1, size=B))
+        lens = np.minimum(lens, S)
+        s = np.array([rng.integers(0, S - n + 1) for n in lens], np.int32)
+        e = (s + lens).astype(np.int32)
+        l0 = int(rng.integers(0, L))
+        l1 = int(rng.integers(l0 + 1, L + 1))
+        variant = int(rng.choice([dv.DV_VARIANT_TILE, dv.DV_VARIANT_AUTO]))
+        host = bool(rng.random() < 0.25)
+        where = (g, l0, l1, s.tolist(), e.tolist(), variant, host)
+        n = ORC.staging_bytes(g, l0, l1, s, e)
+        want = ORC.pack(g, kh, vh, l0, l1, s, e)
+        dst = _buffer(n + 48, host, 0xEE)
+        dv.dv_kv_pack(cache, l0, l1, s, e, dst, variant=variant)
+        got = H.to_np(dst)
+        assert np.array_equal(got[:n], want), where
+        assert (got[n:] == 0xEE).all(), where
+        back = H.device_cache(g, fill=0x5A)
+        dv.dv_kv_unpack(back, l0, l1, s, e, dst, variant=variant, src_bytes=n)
+        kw = np.full(g.tensor_bytes, 0x5A, np.uint8)
+        vw = np.full(g.tensor_bytes, 0x5A, np.uint8)
+        ORC.unpack(g, kw, vw, l0, l1, s, e, want)
+        assert np.array_equal(H.to_np(back.k), kw), where
+        assert np.array_equal(H.to_np(back.v), vw), where
+        del cache, back, dst
+
+
 def _restore_into_zero(g, rep, how, slab, total, rng):
     """A zeroed cache after restoring the replica: record-batched fused or
     staged (a staging buffer between the largest layer slab and the whole
