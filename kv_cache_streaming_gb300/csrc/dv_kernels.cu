@@ -1205,7 +1205,11 @@ cudaError_t run_group(const Plan& p, void* stg, cudaStream_t stream) {
   kp.m_tpl = div64_magic((uint64_t)kp.tiles_per_lkv);
   const size_t smem = (size_t)TB * (p.C | 1) * sizeof(uint4);
   const auto kernel = group_kernel<PACK, MAXB, LOG2C>;
-  const int64_t cap = host_cap(p, (int64_t)sm_count() * blocks_per_sm(kernel, smem, occ_cache));
+  // On host memory, twice the tile kernel's CTAs: a grouped tile is 50-100% live,
+  // and at 1x its transfers carried 90-93% of the link (2..32-token ranges, batch
+  // 32), at 2x 99-100%.
+  const int64_t cap =
+      host_cap(p, (int64_t)sm_count() * blocks_per_sm(kernel, smem, occ_cache), 2);
   const unsigned grid = (unsigned)(tiles < cap ? tiles : cap);
   return launch_kernel(kernel, grid, smem, stream, kp);
 }
