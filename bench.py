@@ -614,13 +614,17 @@ class Bloom:
         del self.arena, self.slots, self.out_slots
 
 
-def link_peaks(torch, nbytes=2 << 30, reps=3):
+def link_peaks(torch, nbytes=2 << 30, reps=5):
     """The host link measured in this run: large pinned cudaMemcpyAsync each
-    way alone and both ways at once (GB/s, median of `reps`)."""
+    way alone and both ways at once (GB/s, median of `reps`).  The host
+    buffers come from dv_host_alloc (huge pages), whose passes run at the link
+    rate every time (torch's pinned buffers showed slow passes on some boxes,
+    which once put the both-ways figure at 231 GB/s)."""
+    import kv_cache_streaming_gb300 as dv
     s = torch.cuda.Stream()
-    host = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    host = dv.host_empty(nbytes)
     dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-    host2 = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    host2 = dv.host_empty(nbytes)
     dev2 = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     s2 = torch.cuda.Stream()
 
