@@ -918,7 +918,7 @@ class Bench:
         zs = np.zeros(g.batch, np.int32)
         full = np.full(g.batch, g.max_seq, np.int32)
         n = dv.dv_staging_bytes(self.cache, 0, g.num_layers, zs, full)
-        host = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+        host = dv.host_empty(n)  # huge-page pinned memory: every pass at the link rate
         dev = torch.empty(n, dtype=torch.uint8, device="cuda")
         staging = torch.empty(4 * (n // g.num_layers), dtype=torch.uint8, device="cuda")
 
@@ -939,7 +939,7 @@ class Bench:
         res = {"payload_bytes": n}
         res["link_d2h_gbs"] = n / timed(lambda: host.copy_(dev, non_blocking=True)) / 1e9
         res["link_h2d_gbs"] = n / timed(lambda: dev.copy_(host, non_blocking=True)) / 1e9
-        host2 = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+        host2 = dv.host_empty(n)
         dev2 = torch.empty(n, dtype=torch.uint8, device="cuda")
         s2 = torch.cuda.Stream()
 
