@@ -89,3 +89,43 @@ def test_replica_in_host_alloc_memory():
     assert np.array_equal(H.to_np(z.k), kw) and np.array_equal(H.to_np(z.v), vw)
     rep.close()
     arena.close()
+
+
+def test_alloc_and_free_from_many_threads():
+    """Eight threads allocate, write, check and free buffers of their own at
+    once: every call succeeds and no two live buffers overlap."""
+    import threading
+    torch.cuda.synchronize()
+    errors, spans, lock = [], [], threading.Lock()
+
+    def work(i):
+        try:
+            for r in range(6):
+                n = (i + 1) * 4096 + r * 16
+                buf = dv.HostBuffer(n)
+                with lock:
+                    spans.append((buf.ptr, buf.ptr + n, True))
+                t = buf.tensor()
+                t.fill_(i)
+                assert int(t.sum()) == i * n
+                with lock:
+                    spans.remove((buf.ptr, buf.ptr + n, True))
+                del t
+                buf.close()
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append(repr(e))
+
+    def check_overlap():
+        with lock:
+            live = sorted(spans)
+        for (a0, a1, _), (b0, b1, _) in zip(live, live[1:]):
+            assert a1 <= b0
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(8)]
+    for th in threads:
+        th.start()
+    for _ in range(20):
+        check_overlap()
+    for th in threads:
+        th.join()
+    assert not errors, errors
