@@ -43,7 +43,7 @@ def main():
     fetcher.wait()
 
     delta = dv.dv_staging_bytes(cache, 0, L, e, e + 1)      # one decode token
-    arena = torch.empty(n + 8 * delta, dtype=torch.uint8, pin_memory=True)
+    arena = dv.host_empty(n + 8 * delta)                   # pinned host memory on huge pages
     rep = dv.Replica(arena, B)
     rep.append(cache, 0, L, s, e, step=0)                   # snapshot
     ds = dv.DeltaStreamer(rep, torch.cuda.current_stream(), torch.cuda.Stream())
