@@ -474,7 +474,11 @@ dv_status dv_replica_restore_fetched_steps(const dv_replica* replica, const dv_c
                                           int64_t from_step, int64_t upto_step,
                                           dv_fetcher* fetcher);
 
-/* Drops every record with step >= step (the acknowledged prefix is kept). */
+/* Drops every record with step >= step (the acknowledged prefix is kept);
+ * their arena bytes are reused by the next appends.  Host-side only: copies
+ * of dropped records still in flight are not waited for, so an append that
+ * reuses their bytes must be ordered after them (the same stream, the same
+ * streamer, or an event). */
 dv_status dv_replica_truncate(dv_replica* replica, int64_t step);
 
 dv_status dv_replica_info(const dv_replica* replica, int64_t* num_records, size_t* bytes_used);
