@@ -133,11 +133,13 @@ typedef enum {
                           token kernel below 640 16-byte chunks per head and range
                           (80 tokens at head_dim 64, fp16), the tile kernel above;
                           ragged ranges: the flat kernel below a mean of 512 chunks,
-                          the tile kernel above.  At 8 or 16 chunks per token
-                          (head_dim 64 / 128 in 2-byte elements) the unpack takes the
-                          tile kernel from 64 chunks (ragged) and from 128 (equal
-                          lengths above one token), the pack from 300 (ragged, 16
-                          chunks per token) */
+                          the tile kernel above.  With grouped tiles (8 or 16 chunks
+                          per token: head_dim 64 / 128 in 2-byte elements) the tile
+                          kernel from fewer chunks: the unpack of ragged ranges at any
+                          length (8 chunks per token) or from 64 (16), of equal ranges
+                          of more than one token from 32 (8) or 128 (16); the pack of
+                          ragged ranges from 300 (8) or 64 (16), of equal ranges from
+                          512 (16) */
   DV_VARIANT_FLAT = 1, /* staging order, each warp a window of 128 chunks */
   DV_VARIANT_TILE = 2, /* token tiles; K transposed through shared memory; at 8 or
                           16 chunks per token, ranges of at most half the token block

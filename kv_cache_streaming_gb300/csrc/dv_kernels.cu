@@ -91,8 +91,12 @@ struct KParams {
 #define DV_FLAT_MIN_BLOCKS 4  // resident CTAs per SM the flat kernel is compiled for
                               // (5 spills: 20-40% slower on 16..64-token unpacks)
 #endif
-#ifndef DV_GROUP_MIN_BLOCKS
-#define DV_GROUP_MIN_BLOCKS 5  // resident CTAs per SM the grouped tile kernel is compiled for
+#ifndef DV_GROUP_MIN_BLOCKS_PACK
+#define DV_GROUP_MIN_BLOCKS_PACK 4    // resident CTAs per SM of the grouped tile kernel's pack:
+                                      // 64 registers, 4-10% faster than 5 CTAs at 48
+#endif
+#ifndef DV_GROUP_MIN_BLOCKS_UNPACK
+#define DV_GROUP_MIN_BLOCKS_UNPACK 5  // ... and of its unpack (at 4: up to 6% slower)
 #endif
 #ifndef DV_LOOKUP_HOST_SCALE
 #define DV_LOOKUP_HOST_SCALE 2  // flat / record kernels on host memory: CTAs per tile-kernel CTA
@@ -839,7 +843,8 @@ __device__ __forceinline__ void copy_group(const Params& p, const GroupJob& j, u
 // tile kernel in a launch of their own).  Tiles in staging order: (layer,
 // K|V), sequence, head group.  C = 8 or 16.
 template <bool PACK, int MAXB, int LOG2C>
-__global__ void __launch_bounds__(kThreads, DV_GROUP_MIN_BLOCKS)
+__global__ void __launch_bounds__(kThreads,
+                                  PACK ? DV_GROUP_MIN_BLOCKS_PACK : DV_GROUP_MIN_BLOCKS_UNPACK)
 group_kernel(const __grid_constant__ KParams<MAXB> p) {
   extern __shared__ uint4 smem[];  // TB rows of (C | 1) chunks
   constexpr int C = 1 << LOG2C;
@@ -1466,14 +1471,16 @@ int auto_kind(const Plan& p, bool pack) {
   // and 48 at 128 in fp16), the tile kernel beyond.  With grouped tiles (C = 8
   // or 16) the unpack takes the tile kernel from 128 chunks per run (8 tokens
   // at head_dim 128, 16 at 64; one-token deltas stay with the token kernel):
-  // its K stores cover each row's tokens together, 7-26% faster at batch 32.
-  // Ragged ranges: the flat kernel below the tile kernel's crossover
-  // (auto_uses_tile).
+  // its K stores cover each row's tokens together, 7-26% faster at batch 32
+  // (at head_dim 64 from 4 tokens, 32 chunks); the pack at head_dim 128 from
+  // 512 chunks.  Ragged ranges: the flat kernel
+  // below the tile kernel's crossover (auto_uses_tile).
   if (token_supported(p)) {
     if (!tile_supported(p)) return kToken;
     const int64_t run = (int64_t)p.max_len * p.C;  // chunks per (layer, K|V, sequence, head)
-    if (!pack && (p.C == 8 || p.C == 16) && p.max_len > 1) return run >= 128 ? kTile : kToken;
-    return run >= 640 ? kTile : kToken;
+    if (!pack && (p.C == 8 || p.C == 16) && p.max_len > 1)
+      return run >= (p.C == 8 ? 32 : 128) ? kTile : kToken;
+    return run >= (pack && p.C == 16 ? 512 : 640) ? kTile : kToken;
   }
   return auto_uses_tile(p, pack) ? kTile : kFlat;
 }
@@ -1485,12 +1492,14 @@ bool auto_uses_tile(const Plan& p, bool pack) {
   // ragged ranges over all layers: the flat kernel wins at 292 chunks per run
   // for head_dim 128 and at 477 for 64 in fp16, the tile kernel at 648 and 712
   // for 128 and at 770 for 64).  With grouped tiles (C = 8 or 16; ranges of at
-  // most half the token block go several heads to a tile) the unpack wins
-  // from about 64 chunks per run (10-16% on 2..32- and 8..24-token ranges,
-  // batch 8 and 32) and the pack at head_dim 128 from about 300.
+  // most half the token block go several heads to a tile) the tile variant
+  // wins from about 64 chunks per run for the unpack and for the pack at
+  // head_dim 128 (4-13% on 4..16- to 16..32-token ranges, batch 8 and 32), at
+  // any length for the unpack at head_dim 64 (1..8-token ranges: 6-16%), and
+  // for the pack at head_dim 64 from about 300.
   int64_t per_run = 512;
-  if (p.C == 16) per_run = pack ? 300 : 64;
-  if (p.C == 8 && !pack) per_run = 64;
+  if (p.C == 16) per_run = 64;
+  if (p.C == 8) per_run = pack ? 300 : 0;  // the unpack at head_dim 64: tiles at any length
   return p.tokens * p.C >= per_run * p.active;
 }
 
