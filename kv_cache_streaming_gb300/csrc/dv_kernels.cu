@@ -87,6 +87,13 @@ struct KParams {
 #ifndef DV_TILE_MIN_BLOCKS
 #define DV_TILE_MIN_BLOCKS 5  // resident CTAs per SM the tile kernel is compiled for
 #endif
+#ifndef DV_TILE_MIN_BLOCKS_BIG
+#define DV_TILE_MIN_BLOCKS_BIG 4  // ... for launches of many rounds of tiles (64 registers)
+#endif
+// Launches of at least this many rounds of a 4-CTA-per-SM grid take the
+// 64-register form: 2-3% faster on gigabyte launches (snapshot pack 0.950
+// against 0.925 of the copy peak), 2.5% slower on 51 MB ones, level at 150 MB.
+constexpr int kBigLaunchRounds = 16;
 #ifndef DV_FLAT_MIN_BLOCKS
 #define DV_FLAT_MIN_BLOCKS 4  // resident CTAs per SM the flat kernel is compiled for
                               // (5 spills: 20-40% slower on 16..64-token unpacks)
@@ -702,8 +709,8 @@ __device__ __forceinline__ void copy_tile(const Params& p, const TileJob& job, u
   }
 }
 
-template <bool PACK, int MAXB, int LOG2C>
-__global__ void __launch_bounds__(kThreads, DV_TILE_MIN_BLOCKS)
+template <bool PACK, int MAXB, int LOG2C, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
 tile_kernel(const __grid_constant__ KParams<MAXB> p) {
   extern __shared__ uint4 smem[];  // TB rows of (C | 1) chunks
   constexpr int LOG2TB = TileShape<LOG2C>::LOG2TB;
@@ -938,8 +945,8 @@ __device__ __forceinline__ TileJob decode_run_tile(const RunParams<MAXB>& p, int
 // transpose.  A restore of one record at a time, or of records in staging
 // order, writes each K chunk alone into a half-filled sector; here the tokens
 // that share a K sector or line are written together.
-template <int MAXB, int LOG2C>
-__global__ void __launch_bounds__(kThreads, DV_TILE_MIN_BLOCKS)
+template <int MAXB, int LOG2C, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
 run_unpack_kernel(const __grid_constant__ RunParams<MAXB> p) {
   extern __shared__ uint4 smem[];  // TB rows of (C | 1) chunks
   constexpr int LOG2TB = TileShape<LOG2C>::LOG2TB;
@@ -1224,6 +1231,7 @@ cudaError_t run_group(const Plan& p, void* stg, cudaStream_t stream) {
 template <bool PACK, int MAXB, int LOG2C>
 cudaError_t run_tile(const Plan& p, void* stg, cudaStream_t stream) {
   static std::atomic<int64_t> occ_cache{0};
+  static std::atomic<int64_t> occ_big{0};
   constexpr int TB = TileShape<LOG2C>::TB;
   KParams<MAXB> kp;
   fill_params(kp, p, stg);
@@ -1244,9 +1252,12 @@ cudaError_t run_tile(const Plan& p, void* stg, cudaStream_t stream) {
     kp.total = tiles;
     kp.m_tpl = div64_magic((uint64_t)kp.tiles_per_lkv);
     const size_t smem = (size_t)TB * (p.C | 1) * sizeof(uint4);
-    const auto kernel = tile_kernel<PACK, MAXB, LOG2C>;
-    const int64_t cap =
-        host_cap(p, (int64_t)sm_count() * blocks_per_sm(kernel, smem, occ_cache));
+    const bool big = !p.host_side && tiles >= (int64_t)kBigLaunchRounds *
+                                                 DV_TILE_MIN_BLOCKS_BIG * sm_count();
+    const auto kernel = big ? tile_kernel<PACK, MAXB, LOG2C, DV_TILE_MIN_BLOCKS_BIG>
+                            : tile_kernel<PACK, MAXB, LOG2C, DV_TILE_MIN_BLOCKS>;
+    const int64_t cap = host_cap(
+        p, (int64_t)sm_count() * blocks_per_sm(kernel, smem, big ? occ_big : occ_cache));
     const unsigned grid = (unsigned)(tiles < cap ? tiles : cap);
     const cudaError_t err = launch_kernel(kernel, grid, smem, stream, kp);
     if (err != cudaSuccess) return err;
@@ -1374,6 +1385,7 @@ template <int MAXB, int LOG2C>
 cudaError_t run_run(const Plan& cache, const RecordRanges& first, int n, const void* src,
                     cudaStream_t stream) {
   static std::atomic<int64_t> occ_cache{0};
+  static std::atomic<int64_t> occ_big{0};
   constexpr int TB = TileShape<LOG2C>::TB;
   RunParams<MAXB> kp;
   kp.k = static_cast<uint4*>(cache.k);
@@ -1427,13 +1439,17 @@ cudaError_t run_run(const Plan& cache, const RecordRanges& first, int n, const v
   kp.tiles_per_lkv = ah * nblk;
   kp.total = 2 * (int64_t)nl * kp.tiles_per_lkv;
   kp.m_tpl = div64_magic((uint64_t)kp.tiles_per_lkv);
-  const auto kernel = run_unpack_kernel<MAXB, LOG2C>;
+  const bool big = !cache.host_side && kp.total >= (int64_t)kBigLaunchRounds *
+                                                       DV_TILE_MIN_BLOCKS_BIG * sm_count();
+  const auto kernel = big ? run_unpack_kernel<MAXB, LOG2C, DV_TILE_MIN_BLOCKS_BIG>
+                          : run_unpack_kernel<MAXB, LOG2C, DV_TILE_MIN_BLOCKS>;
   // From host memory, a run shorter than the token block leaves each tile
   // (and so each CTA's bytes in flight over the link) that much emptier than
   // a full one: scale the CTA cap up to match, at most 8x.
   const int64_t fill = n < TB ? (TB + n - 1) / n : 1;
-  const int64_t cap = host_cap(cache, (int64_t)sm_count() * blocks_per_sm(kernel, smem, occ_cache),
-                               fill < 8 ? fill : 8);
+  const int64_t cap = host_cap(
+      cache, (int64_t)sm_count() * blocks_per_sm(kernel, smem, big ? occ_big : occ_cache),
+      fill < 8 ? fill : 8);
   const unsigned grid = (unsigned)(kp.total < cap ? kp.total : cap);
   return launch_kernel(kernel, grid, smem, stream, kp);
 }
