@@ -118,15 +118,15 @@ def parse_args():
 # it moves (traffic grows in proportion).  None until captured, and set back to
 # None whenever the kernel changes.
 TRAFFIC_PER_LAUNCH = {
-    # bloom-snapshot-pack: 2.868 GB per launch of the cut x 19.137 / 1.463 GB
-    "pack snapshot (tile kernel)": 2.8685e9 * 19136724992 / 1463074816,
+    # bloom-snapshot-pack: 2.870 GB per launch of the cut x 19.137 / 1.463 GB
+    "pack snapshot (tile kernel)": 2.8696e9 * 19136724992 / 1463074816,
     # bloom-delta-pack: 4.594 MB of reads per launch of the cut (its 1.8 MB of
     # staging writes are still in L2 when it ends) x 14
     "pack one-token delta (token kernel)": 4.594e6 * 14,
     # bloom-snapshot-unpack: 2.866 GB per launch of the cut
-    "unpack snapshot (tile kernel)": 2.8657e9 * 19136724992 / 1463074816,
-    # bloom-run-restore: 0.884 GB per launch of the cut (256 records) x 14
-    "unpack 256 one-token deltas (run kernel)": 0.8838e9 * 14,
+    "unpack snapshot (tile kernel)": 2.8659e9 * 19136724992 / 1463074816,
+    # bloom-run-restore: 0.885 GB per launch of the cut (256 records) x 14
+    "unpack 256 one-token deltas (run kernel)": 0.8851e9 * 14,
 }
 
 
