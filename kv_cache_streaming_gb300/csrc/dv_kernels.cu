@@ -21,7 +21,9 @@
 //    odd (C | 1 chunks), so the column-wise accesses of 8 consecutive tokens
 //    fall in 8 distinct 16-byte bank groups.  The grid is persistent (SMs x
 //    resident CTAs) and strides over the tiles in staging order, so at any
-//    moment the whole GPU works on neighbouring tiles.
+//    moment the whole GPU works on neighbouring tiles.  Two occupancy forms:
+//    4 CTAs per SM (more registers) for launches of many rounds of tiles, 5
+//    for smaller ones (kBigLaunchRounds).
 //  * group_kernel (grouped tiles, C = 8 or 16): the tile kernel's shape for
 //    ranges of at most half the token block, G = TB / NT heads of one
 //    sequence to a tile (NT = the range length rounded up to a power of two),
