@@ -27,6 +27,21 @@ def test_every_declared_symbol_is_exported():
         assert hasattr(dv.lib, name), name
 
 
+def test_only_the_c_abi_is_exported():
+    """The library's dynamic symbol table holds the functions of dv.h and nothing
+    else (no C++ internals, no statically linked CUDA runtime)."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", str(dv.library_path)],
+                         capture_output=True, text=True, check=True).stdout
+    exported = sorted({line.split()[-1] for line in out.splitlines()
+                       if len(line.split()) >= 3 and line.split()[1] in "TtWwDdBbRrVv"})
+    assert exported == declared_functions(), set(exported) ^ set(declared_functions())
+
+
 def test_abi_version():
     assert dv.dv_abi_version() == 1
 
