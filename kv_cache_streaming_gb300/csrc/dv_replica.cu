@@ -33,8 +33,9 @@ struct LogRec {
 };
 
 // The non-empty records of a log, validated against a cache, and how they go:
-//  - alone: long ranges (the tile kernel's, normally a snapshot), or larger
-//    than a piece, unpacked by themselves;
+//  - alone: records of at least kAloneMinBytes that the unpack gives the tile
+//    kernel (normally a snapshot), or larger than a piece, unpacked by
+//    themselves;
 //  - run[i] > 1: records i .. i + run[i] - 1 are a run of one-token records
 //    (run_length) at least dv::run_min_records long, unpacked by the run
 //    kernel;
@@ -74,6 +75,8 @@ struct LogPlan {
   }
 };
 
+constexpr size_t kAloneMinBytes = (size_t)4 << 20;  // smallest record unpacked by itself
+
 // Validates every record of `all` against `cache` before anything is
 // enqueued and plans the log.  piece > 0: the bytes one copy can carry; a
 // record larger than that goes by itself in groups of layers, so one of its
@@ -93,7 +96,12 @@ dv_status plan_log(const dv_cache* cache, const std::vector<LogRec>& all, size_t
         return fail(DV_ERR_INVALID_ARG, "record of step %lld does not match this cache geometry",
                     (long long)rec.step);
       if (rec.bytes == 0) continue;
-      const bool by_itself = dv::auto_kind(q, false) == dv::kTile || (piece && rec.bytes > piece);
+      // A record the unpack would give the tile kernel goes by itself, unless it
+      // is small enough for its own launch to cost more than its share of a
+      // record-kernel launch (64 ragged 0.16 MB records: 203 us alone, 68 us
+      // batched; from 6 MB on the same either way).
+      const bool tile = dv::auto_kind(q, false) == dv::kTile && rec.bytes >= kAloneMinBytes;
+      const bool by_itself = tile || (piece && rec.bytes > piece);
       if (by_itself && piece && piece < (size_t)dv::layer_slab_bytes(q))
         return fail(DV_ERR_BUFFER_TOO_SMALL, "a staging piece of %zu bytes holds less than one "
                     "layer slab (%lld bytes) of the record of step %lld", piece,
