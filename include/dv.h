@@ -134,8 +134,9 @@ typedef enum {
                           (80 tokens at head_dim 64, fp16), the tile kernel above;
                           ragged ranges: the flat kernel below a mean of 512 chunks,
                           the tile kernel above.  With grouped tiles (8 or 16 chunks
-                          per token: head_dim 64 / 128 in 2-byte elements) the tile
-                          kernel from fewer chunks: the unpack of ragged ranges at any
+                          per token: head_dim 64 / 128 in 2-byte elements), for
+                          transfers of at least 4 MiB, the tile kernel from fewer
+                          chunks: the unpack of ragged ranges at any
                           length (8 chunks per token) or from 64 (16), of equal ranges
                           of more than one token from 32 (8) or 128 (16); the pack of
                           ragged ranges from 300 (8) or 64 (16), of equal ranges from

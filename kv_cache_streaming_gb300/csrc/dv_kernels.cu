@@ -1483,6 +1483,14 @@ bool token_supported(const Plan& p) {
          2 * (int64_t)(p.l1 - p.l0) * p.H * p.tokens * p.C < ((int64_t)1 << 31);
 }
 
+// Whether the lower crossovers of grouped tiles apply: C = 8 or 16, and a
+// transfer of at least 4 MiB (below that a launch costs about its start, and
+// the token or flat kernel's single launch is the cheaper one: a 150 KB
+// unpack took 1.9 us in grouped tiles against 1.3 in the token kernel).
+static bool grouped_pays(const Plan& p) {
+  return (p.C == 8 || p.C == 16) && p.bytes >= ((int64_t)4 << 20);
+}
+
 int auto_kind(const Plan& p, bool pack) {
   // Equal-length ranges: the token kernel up to about 640 chunks per run
   // (measured on GB300: between 64 and 96 tokens at head_dim 64, between 32
@@ -1496,9 +1504,9 @@ int auto_kind(const Plan& p, bool pack) {
   if (token_supported(p)) {
     if (!tile_supported(p)) return kToken;
     const int64_t run = (int64_t)p.max_len * p.C;  // chunks per (layer, K|V, sequence, head)
-    if (!pack && (p.C == 8 || p.C == 16) && p.max_len > 1)
+    if (grouped_pays(p) && !pack && p.max_len > 1)
       return run >= (p.C == 8 ? 32 : 128) ? kTile : kToken;
-    return run >= (pack && p.C == 16 ? 512 : 640) ? kTile : kToken;
+    return run >= (grouped_pays(p) && pack && p.C == 16 ? 512 : 640) ? kTile : kToken;
   }
   return auto_uses_tile(p, pack) ? kTile : kFlat;
 }
@@ -1516,8 +1524,8 @@ bool auto_uses_tile(const Plan& p, bool pack) {
   // any length for the unpack at head_dim 64 (1..8-token ranges: 6-16%), and
   // for the pack at head_dim 64 from about 300.
   int64_t per_run = 512;
-  if (p.C == 16) per_run = 64;
-  if (p.C == 8) per_run = pack ? 300 : 0;  // the unpack at head_dim 64: tiles at any length
+  if (grouped_pays(p) && p.C == 16) per_run = 64;
+  if (grouped_pays(p) && p.C == 8) per_run = pack ? 300 : 0;  // the unpack at head_dim 64: any
   return p.tokens * p.C >= per_run * p.active;
 }
 
